@@ -1,0 +1,345 @@
+#!/usr/bin/env python
+"""Throughput of the routed NVFP4 MoE expert block on GB300.
+
+One step = the whole hot path over one batch: routing metadata, NVFP4 input
+quantization into permuted order, GEMM1 with the fused SwiGLU + requant
+epilogue, GEMM2, and the post-expert finalize -- five kernel launches through
+the C ABI, inputs resident in HBM. The default workload is the b = 8 decode
+batch (T = 8, H = 5120, I = 2048, E = 128, top-8, uniform routing).
+
+Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
+the launching stream, bracketed by a barrier and a device synchronize; the
+layer's prepared weights rotate over several copies whose total exceeds L2,
+so no step reads the previous step's weights from L2. The GEMM1 launches are
+bracketed by their own events for the roofline. `e2e` repeats the
+measurement through the public layer call with host (pinned) inputs and
+outputs, the copies inside the timed region.
+
+Multi-GPU: replicas only -- each rank runs its own copy of the layer on its
+own batch; the value is all ranks' tokens over the slowest rank's time.
+
+`--impl reference` times the CPU oracle (numpy) on a bounded sample of the
+same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at 1 GB300 and % of HBM (decode) / FP4 tensor (prefill) roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            with open(self.file.name) as f:
+                for ln in f:
+                    parts = [p.strip() for p in ln.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.file.name)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def _max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(w, raw, batch, a1, a2, tokens: int) -> dict:
+    """Time the CPU oracle on the first `tokens` tokens of the batch."""
+    from oracle import layer as olayer
+
+    t0 = time.perf_counter()
+    olayer.moe_layer(batch["x"][:tokens], batch["topk_ids"][:tokens], batch["topk_weights"][:tokens], raw, a1, a2,
+                     raw["gamma"], 1e-6, w.tile_m)
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{tokens} of {w.T} tokens of {w.name} ({tokens * w.K} routes), exact fp64/int oracle, "
+                      f"numpy BLAS on the host's default thread count, {dt:.2f} s"}
+
+
+def run_reference(args, w) -> None:
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from nvfp4_mixture_experts_route_gb300 import inputs
+
+    raw = inputs.make_layer(w)
+    batch = inputs.make_batch(w)
+    a1, a2 = inputs.global_scales(w)
+    tokens = 1
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, raw, batch, a1, a2, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_sample(w, raw, batch, a1, a2, tokens)
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{tokens} token ({w.K} routes) of {w.name} per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w) -> dict:
+    return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "top_k": w.K, "routing": w.routing,
+            "tile_m": w.tile_m, "parallelism": "replicas"}
+
+
+def run_ours(args, w) -> None:
+    import numpy as np
+    import torch
+
+    from nvfp4_mixture_experts_route_gb300 import binding as B
+    from nvfp4_mixture_experts_route_gb300 import inputs
+    from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+
+    raw = inputs.make_layer(w)
+    batch = inputs.make_batch(w, seed=rank)
+    a1, a2 = inputs.global_scales(w)
+    T, K, E, H, I, tile = w.T, w.K, w.E, w.H, w.I, w.tile_m
+
+    # Prepared weight copies, rotated so that every step streams from HBM.
+    moe = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=tile, device=dev)
+    copies = [moe.weights]
+    keep = [moe.prepared]
+    layer_bytes = sum(t.numel() for t in moe.prepared.values())
+    n_copies = max(1, args.copies)
+    for _ in range(n_copies - 1):
+        p = {k: v.clone() for k, v in moe.prepared.items()}
+        keep.append(p)
+        copies.append(B.weights_struct(p, moe.g1_alphas, moe.g1_scale_c, moe.g2_alphas))
+
+    x = torch.from_numpy(batch["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+    ids = torch.from_numpy(batch["topk_ids"]).to(dev)
+    tw = torch.from_numpy(batch["topk_weights"]).to(dev)
+    bufs = moe.buffers(T, K)
+    route, ws, rows, out, status = bufs["route"], bufs["ws"], bufs["rows"], bufs["out"], bufs["status"]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        wts = copies[i % len(copies)]
+        B.route_permute(ids, E, tile, route=route, status=status)
+        B.experts_quantize(route, ws, x=x, a1_gscale=moe.a1_gscale, T=T, H=H, I=I, E=E, K=K, status=status)
+        if ev is not None:
+            ev[0].record(stream)
+        B.experts_gemm1(wts, route, ws, a2_gscale=moe.a2_gscale, T=T, H=H, I=I, E=E, K=K, status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        B.experts_gemm2(wts, route, ws, rows, T=T, H=H, I=I, E=E, K=K, status=status)
+        if ev is not None:
+            ev[2].record(stream)
+        B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out)
+
+    launches_per_step = 5
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = _max_over_ranks(world, start.elapsed_time(end))
+    gemm1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    gemm2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} in the timed region")
+
+    # e2e: the public layer call with pinned host buffers, copies timed.
+    x_h = torch.from_numpy(batch["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_h = torch.from_numpy(batch["topk_ids"]).pin_memory()
+    tw_h = torch.from_numpy(batch["topk_weights"]).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d, ids_d, tw_d = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(tw)
+
+    def e2e_step(i):
+        moe.weights = copies[i % len(copies)]
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        tw_d.copy_(tw_h, non_blocking=True)
+        o, _ = moe.forward(x_d, ids_d, tw_d)
+        out_h.copy_(o, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
+    moe.weights = copies[0]
+
+    if rank != 0:
+        return
+    touched = np.unique(batch["topk_ids"][batch["topk_ids"] >= 0])
+    n_touch = len(touched)
+    w13_bytes = 2 * I * (H // 2) + 2 * I * (H // 16)
+    w2_bytes = H * (I // 2) + H * (I // 16)
+    peak, peak_kind = _peaks()
+    gemm1_gbs = n_touch * w13_bytes / (gemm1_ms * 1e-3) / 1e9
+    tokens_total = T * args.steps * world
+    value = tokens_total / (total_ms * 1e-3)
+    step_ms = total_ms / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1xue4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {**_config(w), "l2": f"{len(copies)} rotating prepared weight copies "
+                                        f"({len(copies) * layer_bytes / 1e9:.2f} GB > L2)"},
+        "roofline": {"bound": "hbm", "kernel": "grouped_gemm_kernel<1> (GEMM1 + SwiGLU + requant)",
+                     "achieved": gemm1_gbs, "peak": peak, "unit": "GB/s", "frac": gemm1_gbs / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "algorithmic_bytes": n_touch * w13_bytes, "launch_ms": gemm1_ms},
+        "step_roofline": {"bytes": n_touch * (w13_bytes + w2_bytes), "touched_experts": int(n_touch),
+                          "achieved_gbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9,
+                          "frac_of_measured": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9 / peak,
+                          "frac_of_8tbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 8e12,
+                          "gemm2_ms": gemm2_ms},
+        "clocks": clocks.summary(),
+        "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * 4 + tw_h.numel() * 4,
+                "d2h_bytes_per_step": out_h.numel() * 2},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, raw, batch, a1, a2, tokens=args.cpu_tokens)
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_b8")
+    ap.add_argument("--copies", type=int, default=4)
+    ap.add_argument("--cpu-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from nvfp4_mixture_experts_route_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_nvfp4.so: the routed NVFP4 mixture-of-experts
+ * expert block with the MuseSpark1x post-expert finalize, for GB300 (sm_103a).
+ *
+ * The block (vLLM "muse_moe_runner" page: MuseSparkTrtLlmNvFp4Experts
+ * .apply_routed and MusePostExpertFinalize; "flashinfer_ops" page:
+ * FlashInferOps.slot / nvfp4_arguments / gemm2_rows; "expert_tp" page:
+ * StockNvfp4 and the module docstring; "model" page: MuseSpark1xMoE):
+ *
+ *   a1  a    = NVFP4(x) with the fp32 global scale a1_gscale
+ *   a2  routing metadata: per-expert histogram, permuted and padded rows
+ *   a3  acc  = a . w13[e]^T  (block-scaled FP4, fp32 accumulate)
+ *       gate = g1_alphas[e] * acc[:, 0:I],  up = g1_scale_c[e] * acc[:, I:2I]
+ *   a4  h    = SiLU(gate) * up
+ *   a5  hq   = NVFP4(h) with a2_gscale
+ *   a6  rows = bf16(g2_alphas[e] * hq . w2[e]^T)
+ *   a7  out[t] = bf16( sum_k w[t,k] * RMSNorm(rows[p(t,k)]) ), fp32 norm
+ *       output and fp32 sum; zero-centred gamma (weight 1 + gamma)
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device memory owned by the caller unless stated; scalar
+ *     arguments (sizes, eps, flags) are host values.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Every call only enqueues work on it: no allocation, no host
+ *     synchronisation, no host read of device data.
+ *   - The return value is MOE_OK or a negative MOE_ERR_* code for errors
+ *     found on the host (arguments, sizes, a failed launch); nothing is
+ *     enqueued when a call returns an error. moe_last_error() then gives the
+ *     reason (thread-local, valid until the next failing call).
+ *   - Data-dependent errors found on the device (an expert id out of range,
+ *     a bounded wait that gave up) are recorded in the optional caller-owned
+ *     `int32_t* status` word: the first error code wins (atomic
+ *     compare-and-swap from 0). The library never clears it: zero it before
+ *     the calls and read it after synchronising. A kernel that records an
+ *     error leaves the outputs it could not compute unspecified.
+ *   - No kernel traps, asserts or waits without a bound.
+ *
+ * Number formats: e2m1 values packed two per byte, the even element in the
+ * low nibble; e4m3 ("fn") block scales, one per 16 consecutive elements along
+ * K; bf16 activations; fp32 scalars.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misaligned buffer */
+  MOE_ERR_UNSUPPORTED = -2,   /* shape the layout/kernels cannot hold      */
+  MOE_ERR_WORKSPACE = -3,     /* workspace smaller than the size query     */
+  MOE_ERR_CUDA = -4,          /* a CUDA runtime / driver call failed       */
+  MOE_ERR_TIMEOUT = -5,       /* device: a bounded wait gave up            */
+  MOE_ERR_INVALID_ROUTE = -6, /* device: topk id >= E or < -1              */
+};
+
+/* Reason for the last error returned on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* ABI version, bumped on any incompatible change. */
+int moe_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * Weight preparation (runs once per layer, at load).
+ *
+ * Raw weights (the expert_tp page, StockNvfp4 shapes, block scales
+ * unswizzled):
+ *   w13    uint8 [E, 2I, H/2]   rows [0, I) gate (w1), rows [I, 2I) up (w3)
+ *   w13_sf e4m3  [E, 2I, H/16]
+ *   w2     uint8 [E, H, I/2]
+ *   w2_sf  e4m3  [E, H, I/16]
+ *
+ * Prepared layout written by moe_prepare_weights (this library's own, not
+ * the pages' TRT-LLM layout):
+ *   p_w13    uint8 [E, 2I, H/2]: prepared row r holds raw row
+ *              16*(r/32) + r%32           if r%32 < 16  (gate)
+ *              I + 16*(r/32) + r%32 - 16  otherwise     (up)
+ *            so every 32-row group holds the gate and up rows of the same
+ *            16 intermediate columns (the GEMM1 epilogue pairs them in one
+ *            warp). Bytes inside a row are unchanged.
+ *   p_w13_sf uint8 [E, 2I/128, H/64, 512]: scale atoms. Byte
+ *              (e, mt, kc, 16*m0 + 4*m1 + c), m0 < 32, m1 < 4, c < 4,
+ *            holds the scale of prepared row 128*mt + 32*m1 + m0 for the
+ *            16-element block 4*kc + c. One atom is what one tcgen05.cp
+ *            (32x128b, warpx4) moves into tensor memory for one K=64 MMA of
+ *            128 rows.
+ *   p_w2     uint8 [E, H, I/2]: w2 unchanged.
+ *   p_w2_sf  uint8 [E, H/128, I/64, 512]: the same atoms over w2_sf.
+ *
+ * Layout identity (the expert_tp page's requirement for free TP cuts): for
+ * tp with I' = I/tp, I' % 64 == 0 and H % 128 == 0, intermediate slice r of
+ * the prepared tensors -- p_w13 rows [2rI', 2(r+1)I'), p_w13_sf row tiles
+ * [2rI'/128, 2(r+1)I'/128), p_w2 bytes [rI'/2, (r+1)I'/2) of every row,
+ * p_w2_sf k-atoms [rI'/64, (r+1)I'/64) -- is byte for byte
+ * moe_prepare_weights of the raw slice.
+ *
+ * Requires H % 128 == 0 and I % 64 == 0 (else MOE_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the four prepared tensors: {p_w13, p_w13_sf, p_w2, p_w2_sf}. */
+int moe_prepared_sizes(int E, int H, int I, size_t out_bytes[4]);
+
+/* Write the prepared layout. Inputs and outputs must not overlap; every
+ * pointer 16-byte aligned. */
+int moe_prepare_weights(const void* w13, const void* w13_sf, const void* w2,
+                        const void* w2_sf, int E, int H, int I, void* p_w13,
+                        void* p_w13_sf, void* p_w2, void* p_w2_sf,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
+ * Routing metadata (step a2; the flashinfer_ops page, FlashInferOps.slot).
+ *
+ * R = T*K routes, route j = t*K + k. tile_m in {32, 64, 128, 256}; E in
+ * [1, 1024].
+ *   expert_counts[E]        routes per expert
+ *   expert_offsets[E+1]     exclusive prefix of the padded counts
+ *                           ceil(count/tile_m)*tile_m; [E] = total padded
+ *   expanded_to_permuted[R] permuted row of route j; -1 if topk_ids[j] == -1
+ *   permuted_to_token[P]    token of a permuted row; -1 on padding rows and
+ *                           on every row past the total
+ *   tile_expert[MT]         expert of tile tau (rows [tau*tile_m,
+ *                           (tau+1)*tile_m)); -1 past the live tiles
+ *   tile_row_limit[MT]      offsets[e] + counts[e] of that expert; -1 past
+ *   totals[2]               {live tiles, total padded rows}
+ * with P = max_padded_rows = tile_m*(F + (R-F)/tile_m), F = min(E, R) (the
+ * flashinfer_ops page's gemm2_rows bound) and MT = max_tiles = P/tile_m.
+ * Inside an expert, routes take rows in ascending j: the result is unique
+ * and deterministic. topk_ids of -1 mean "not routed" (expert parallel marks
+ * remote experts so); ids < -1 or >= E record MOE_ERR_INVALID_ROUTE in
+ * *status and leave the metadata unspecified. T == 0 is valid.
+ * ---------------------------------------------------------------------- */
+
+int moe_route_sizes(int T, int K, int E, int tile_m, int* max_padded_rows,
+                    int* max_tiles);
+
+int moe_route_permute(const int32_t* topk_ids, int T, int K, int E,
+                      int tile_m, int32_t* expert_counts,
+                      int32_t* expert_offsets, int32_t* expanded_to_permuted,
+                      int32_t* permuted_to_token, int32_t* tile_expert,
+                      int32_t* tile_row_limit, int32_t* totals,
+                      int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Experts (steps a1, a3-a6; the muse_moe_runner page, apply_routed with
+ * do_finalize=False, and the flashinfer_ops page, nvfp4_arguments).
+ * ---------------------------------------------------------------------- */
+
+typedef struct moe_weights {
+  const void* w13;         /* prepared uint8 [E, 2I, H/2]            */
+  const void* w13_sf;      /* prepared uint8 [E, 2I/128, H/64, 512]  */
+  const void* w2;          /* prepared uint8 [E, H, I/2]             */
+  const void* w2_sf;       /* prepared uint8 [E, H/128, I/64, 512]   */
+  const float* g1_alphas;  /* fp32 [E]: gate scale ("output1_scale_gate_scalar") */
+  const float* g1_scale_c; /* fp32 [E]: up scale ("output1_scale_scalar"); holds
+                              no 1/a2 -- the requant applies a2_gscale */
+  const float* g2_alphas;  /* fp32 [E]: GEMM2 scale ("output2_scale_scalar") */
+} moe_weights;
+
+typedef struct moe_route {
+  const int32_t* permuted_to_token; /* [max_padded_rows] */
+  const int32_t* tile_expert;       /* [max_tiles] */
+  const int32_t* tile_row_limit;    /* [max_tiles] */
+  const int32_t* totals;            /* [2] */
+} moe_route;
+
+/* Workspace bytes moe_nvfp4_experts needs (the permuted NVFP4 activations
+ * and the quantized intermediate; contents opaque). */
+int moe_experts_workspace_size(int T, int K, int E, int H, int I, int tile_m,
+                               size_t* ws_bytes);
+
+/* The whole expert body: a1 quantization into permuted order, GEMM1 with
+ * the SwiGLU + NVFP4 requant epilogue, GEMM2. Give either x (bf16 [T, H]) or
+ * a pre-quantized a (uint8 [T, H/2]) with a_sf (e4m3 [T, H/16], row-major,
+ * as scaled_fp4_quant(..., is_sf_swizzled_layout=False) returns it) and
+ * pass NULL for the other. a1_gscale, a2_gscale: device fp32 [1].
+ * gemm2_rows: bf16 [max_padded_rows, H]; only rows < totals[1] that carry a
+ * route are written (the flashinfer_ops page trims to gemm2_rows; padding
+ * rows are never read by the finalize). Requires H % 128 == 0,
+ * I % 128 == 0, tile_m in {32, 64, 128, 256}; every device pointer 16-byte
+ * aligned; ws at least moe_experts_workspace_size bytes, 1024-byte
+ * aligned. */
+int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a,
+                      const void* a_sf, const float* a1_gscale,
+                      const float* a2_gscale, const moe_route* r, int T,
+                      int H, int I, int E, int K, int tile_m,
+                      void* gemm2_rows, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream);
+
+/* The same body in its three launches, for timing one step alone. Called
+ * in this order on one stream they equal moe_nvfp4_experts. */
+int moe_experts_quantize(const void* x, const void* a, const void* a_sf,
+                         const float* a1_gscale, const moe_route* r, int T,
+                         int H, int I, int E, int K, int tile_m, void* ws,
+                         size_t ws_bytes, int32_t* status, void* stream);
+int moe_experts_gemm1(const moe_weights* w, const float* a2_gscale,
+                      const moe_route* r, int T, int H, int I, int E, int K,
+                      int tile_m, void* ws, size_t ws_bytes, int32_t* status,
+                      void* stream);
+int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H,
+                      int I, int E, int K, int tile_m, void* gemm2_rows,
+                      void* ws, size_t ws_bytes, int32_t* status,
+                      void* stream);
+
+/* Copy a quantized operand out of / into the workspace, in permuted row
+ * order with row-major scales: which = 0 for the activations a (codes
+ * uint8 [max_padded_rows, H/2], scales e4m3 [max_padded_rows, H/16]),
+ * which = 1 for the intermediate hq ([max_padded_rows, I/2] and
+ * [max_padded_rows, I/16]). moe_experts_import followed by
+ * moe_experts_gemm2 runs GEMM2 on a given intermediate. */
+int moe_experts_export(int which, const void* ws, size_t ws_bytes, int T,
+                       int H, int I, int E, int K, int tile_m, void* codes,
+                       void* scales, void* stream);
+int moe_experts_import(int which, const void* codes, const void* scales,
+                       int T, int H, int I, int E, int K, int tile_m,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Post-expert finalize (step a7; the muse_moe_runner page,
+ * MusePostExpertFinalize.__call__(unfinalized, out), _finalize_native,
+ * _finalize_chunk, _effective_weight; the model page's post_expert_norm).
+ *
+ *   out[t] = bf16( sum_{k < K} w[t,k] * N(rows[p(t,k)]) ),  p = -1 adds 0
+ *   g = 1 + float(gamma)            (gain centre added in fp32)
+ *   weight_before_norm != 0:  u = g*r,  N = u * rsqrt(mean(u^2) + eps)
+ *   weight_before_norm == 0:  N = g * r * rsqrt(mean(r^2) + eps)
+ * all in fp32 over the full hidden size H, summed over k in order 0..K-1.
+ * rows: bf16 [*, H] (GEMM2 rows); expanded_to_permuted int32 [T, K];
+ * topk_weights fp32 [T, K]; gamma bf16 [H]; out bf16 [T, H] (caller-owned,
+ * may not alias rows). H % 8 == 0, H <= 16384; T == 0 is valid.
+ * ---------------------------------------------------------------------- */
+int moe_post_expert_finalize(const void* rows,
+                             const int32_t* expanded_to_permuted,
+                             const float* topk_weights, const void* gamma,
+                             float eps, int weight_before_norm, int T, int K,
+                             int H, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

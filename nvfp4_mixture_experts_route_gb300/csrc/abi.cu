@@ -1,0 +1,346 @@
+// The extern "C" entry points of libmoe_nvfp4.so (declared and documented in
+// include/moe_nvfp4.h): host-side argument checks, the workspace layout, and
+// the kernel launches on the caller's stream.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "common.cuh"
+#include "layout.cuh"
+
+namespace moe {
+cudaError_t launch_route_permute(const int32_t*, int, int, int, int, int, int, int32_t*, int32_t*,
+                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
+                                 cudaStream_t);
+size_t route_smem_bytes(int E);
+cudaError_t launch_quantize_permute(const void*, const void*, const void*, const float*,
+                                    const int32_t*, const int32_t*, int, int, int, uint8_t*,
+                                    uint8_t*, cudaStream_t);
+cudaError_t launch_act_scales_io(int, uint8_t*, uint8_t*, int, int, int, cudaStream_t);
+cudaError_t launch_prepare_weights(const void*, const void*, const void*, const void*, int, int,
+                                   int, void*, void*, void*, void*, cudaStream_t);
+cudaError_t launch_finalize(const void*, const int32_t*, const float*, const void*, float, int,
+                            int, int, int, void*, cudaStream_t);
+int launch_gemm1(const void*, const void*, const float*, const float*, const float*,
+                 const int32_t*, const int32_t*, const int32_t*, const uint8_t*, const uint8_t*,
+                 uint8_t*, uint8_t*, int, int, int, int, int, int, int32_t*, cudaStream_t,
+                 const char**);
+int launch_gemm2(const void*, const void*, const float*, const int32_t*, const int32_t*,
+                 const int32_t*, const uint8_t*, const uint8_t*, void*, int, int, int, int, int,
+                 int, int32_t*, cudaStream_t, const char**);
+}  // namespace moe
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_tile(int tile_m) {
+  return tile_m == 32 || tile_m == 64 || tile_m == 128 || tile_m == 256;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct RouteDims {
+  int P = 0, MT = 0;
+};
+
+int route_dims(int T, int K, int E, int tile_m, RouteDims* d) {
+  if (T < 0 || K < 1 || K > 64 || E < 1 || E > 1024)
+    return fail(MOE_ERR_INVALID_ARG, "bad routing shape T=%d K=%d E=%d", T, K, E);
+  if (!valid_tile(tile_m)) return fail(MOE_ERR_UNSUPPORTED, "tile_m %d not in {32,64,128,256}", tile_m);
+  const long long R = (long long)T * K;
+  if (R > (1ll << 24)) return fail(MOE_ERR_UNSUPPORTED, "too many routes (%lld)", R);
+  const long long F = R < E ? R : E;
+  const long long P = (long long)tile_m * (F + (R - F) / tile_m);
+  d->P = (int)P;
+  d->MT = (int)(P / tile_m);
+  return MOE_OK;
+}
+
+// Workspace of the expert body: permuted NVFP4 activations and the quantized
+// intermediate (codes row-major, scales as per-tile atoms; see quant.cu).
+struct WsLayout {
+  size_t a_codes = 0, a_sf = 0, h_codes = 0, h_sf = 0, total = 0;
+  int P = 0, MT = 0, S = 0;
+};
+
+int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
+  RouteDims d;
+  int rc = route_dims(T, K, E, tile_m, &d);
+  if (rc) return rc;
+  if (H < 128 || I < 128 || H % 128 || I % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "hidden %d and intermediate %d must be multiples of 128", H, I);
+  w->P = d.P;
+  w->MT = d.MT;
+  w->S = moe::sf_atoms_per_tile(tile_m);
+  size_t off = 0;
+  w->a_codes = off;
+  off = round_up(off + (size_t)d.P * (H / 2), 1024);
+  w->a_sf = off;
+  off = round_up(off + (size_t)d.MT * (H / 64) * w->S * moe::kAtomBytes, 1024);
+  w->h_codes = off;
+  off = round_up(off + (size_t)d.P * (I / 2), 1024);
+  w->h_sf = off;
+  off = round_up(off + (size_t)d.MT * (I / 64) * w->S * moe::kAtomBytes, 1024);
+  w->total = off;
+  return MOE_OK;
+}
+
+int check_ws(const void* ws, size_t ws_bytes, const WsLayout& L) {
+  if (L.total && ws == nullptr) return fail(MOE_ERR_INVALID_ARG, "workspace is null");
+  if (!aligned(ws, 1024)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 1024-byte aligned");
+  if (ws_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  return MOE_OK;
+}
+
+int check_route(const moe_route* r) {
+  if (!r || !r->permuted_to_token || !r->tile_expert || !r->tile_row_limit || !r->totals)
+    return fail(MOE_ERR_INVALID_ARG, "routing metadata pointer is null");
+  return MOE_OK;
+}
+
+int check_weights(const moe_weights* w, bool gemm1) {
+  if (!w) return fail(MOE_ERR_INVALID_ARG, "weights are null");
+  if (gemm1) {
+    if (!w->w13 || !w->w13_sf || !w->g1_alphas || !w->g1_scale_c)
+      return fail(MOE_ERR_INVALID_ARG, "GEMM1 weight pointer is null");
+    if (!aligned(w->w13, 16) || !aligned(w->w13_sf, 16))
+      return fail(MOE_ERR_INVALID_ARG, "w13 / w13_sf must be 16-byte aligned");
+  } else {
+    if (!w->w2 || !w->w2_sf || !w->g2_alphas)
+      return fail(MOE_ERR_INVALID_ARG, "GEMM2 weight pointer is null");
+    if (!aligned(w->w2, 16) || !aligned(w->w2_sf, 16))
+      return fail(MOE_ERR_INVALID_ARG, "w2 / w2_sf must be 16-byte aligned");
+  }
+  return MOE_OK;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+int moe_abi_version(void) { return 1; }
+
+int moe_prepared_sizes(int E, int H, int I, size_t out_bytes[4]) {
+  if (!out_bytes) return fail(MOE_ERR_INVALID_ARG, "out_bytes is null");
+  if (E < 1 || H < 1 || I < 1) return fail(MOE_ERR_INVALID_ARG, "bad shape E=%d H=%d I=%d", E, H, I);
+  if (H % 128 || I % 64)
+    return fail(MOE_ERR_UNSUPPORTED, "hidden %d and intermediate %d must be multiples of 128 and 64",
+                H, I);
+  out_bytes[0] = (size_t)E * 2 * I * (H / 2);
+  out_bytes[1] = (size_t)E * 2 * I * (H / 16);
+  out_bytes[2] = (size_t)E * H * (I / 2);
+  out_bytes[3] = (size_t)E * H * (I / 16);
+  return MOE_OK;
+}
+
+int moe_prepare_weights(const void* w13, const void* w13_sf, const void* w2, const void* w2_sf,
+                        int E, int H, int I, void* p_w13, void* p_w13_sf, void* p_w2,
+                        void* p_w2_sf, void* stream) {
+  size_t sz[4];
+  int rc = moe_prepared_sizes(E, H, I, sz);
+  if (rc) return rc;
+  const void* ptrs[8] = {w13, w13_sf, w2, w2_sf, p_w13, p_w13_sf, p_w2, p_w2_sf};
+  for (const void* p : ptrs) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "weight pointer is null");
+    if (!aligned(p, 16)) return fail(MOE_ERR_INVALID_ARG, "weight pointers must be 16-byte aligned");
+  }
+  cudaError_t err = moe::launch_prepare_weights(w13, w13_sf, w2, w2_sf, E, H, I, p_w13, p_w13_sf,
+                                                p_w2, p_w2_sf, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_prepare_weights");
+}
+
+int moe_route_sizes(int T, int K, int E, int tile_m, int* max_padded_rows, int* max_tiles) {
+  RouteDims d;
+  int rc = route_dims(T, K, E, tile_m, &d);
+  if (rc) return rc;
+  if (max_padded_rows) *max_padded_rows = d.P;
+  if (max_tiles) *max_tiles = d.MT;
+  return MOE_OK;
+}
+
+int moe_route_permute(const int32_t* topk_ids, int T, int K, int E, int tile_m,
+                      int32_t* expert_counts, int32_t* expert_offsets,
+                      int32_t* expanded_to_permuted, int32_t* permuted_to_token,
+                      int32_t* tile_expert, int32_t* tile_row_limit, int32_t* totals,
+                      int32_t* status, void* stream) {
+  RouteDims d;
+  int rc = route_dims(T, K, E, tile_m, &d);
+  if (rc) return rc;
+  if (!expert_counts || !expert_offsets || !totals || (T > 0 && (!topk_ids || !expanded_to_permuted)) ||
+      (d.P > 0 && (!permuted_to_token || !tile_expert || !tile_row_limit)))
+    return fail(MOE_ERR_INVALID_ARG, "routing buffer is null");
+  cudaError_t err = moe::launch_route_permute(topk_ids, T, K, E, tile_m, d.P, d.MT, expert_counts,
+                                              expert_offsets, expanded_to_permuted,
+                                              permuted_to_token, tile_expert, tile_row_limit,
+                                              totals, status, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route_permute");
+}
+
+int moe_experts_workspace_size(int T, int K, int E, int H, int I, int tile_m, size_t* ws_bytes) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if (!ws_bytes) return fail(MOE_ERR_INVALID_ARG, "ws_bytes is null");
+  *ws_bytes = L.total;
+  return MOE_OK;
+}
+
+int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const float* a1_gscale,
+                         const moe_route* r, int T, int H, int I, int E, int K, int tile_m,
+                         void* ws, size_t ws_bytes, int32_t* status, void* stream) {
+  (void)status;
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L)) || (rc = check_route(r))) return rc;
+  if (L.P == 0) return MOE_OK;
+  if (x) {
+    if (!a1_gscale) return fail(MOE_ERR_INVALID_ARG, "a1_gscale is null");
+    if (!aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  } else {
+    if (!a || !a_sf) return fail(MOE_ERR_INVALID_ARG, "give x, or a and a_sf");
+    if (!aligned(a, 8)) return fail(MOE_ERR_INVALID_ARG, "a must be 8-byte aligned");
+  }
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  cudaError_t err = moe::launch_quantize_permute(x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale,
+                                                 r->permuted_to_token, r->totals, H, tile_m, L.P,
+                                                 base + L.a_codes, base + L.a_sf, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
+}
+
+int moe_experts_gemm1(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T,
+                      int H, int I, int E, int K, int tile_m, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L)) || (rc = check_route(r)) || (rc = check_weights(w, true)))
+    return rc;
+  if (!a2_gscale) return fail(MOE_ERR_INVALID_ARG, "a2_gscale is null");
+  if (L.P == 0) return MOE_OK;
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  const char* why = "";
+  rc = moe::launch_gemm1(w->w13, w->w13_sf, w->g1_alphas, w->g1_scale_c, a2_gscale, r->tile_expert,
+                         r->tile_row_limit, r->totals, base + L.a_codes, base + L.a_sf,
+                         base + L.h_codes, base + L.h_sf, E, H, I, tile_m, L.P, L.MT, status,
+                         as_stream(stream), &why);
+  return rc ? fail(rc, "%s", why) : MOE_OK;
+}
+
+int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E, int K,
+                      int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes, int32_t* status,
+                      void* stream) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L)) || (rc = check_route(r)) || (rc = check_weights(w, false)))
+    return rc;
+  if (L.P == 0) return MOE_OK;
+  if (!gemm2_rows || !aligned(gemm2_rows, 16))
+    return fail(MOE_ERR_INVALID_ARG, "gemm2_rows must be non-null and 16-byte aligned");
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  const char* why = "";
+  rc = moe::launch_gemm2(w->w2, w->w2_sf, w->g2_alphas, r->tile_expert, r->tile_row_limit,
+                         r->totals, base + L.h_codes, base + L.h_sf, gemm2_rows, E, H, I, tile_m,
+                         L.P, L.MT, status, as_stream(stream), &why);
+  return rc ? fail(rc, "%s", why) : MOE_OK;
+}
+
+int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const void* a_sf,
+                      const float* a1_gscale, const float* a2_gscale, const moe_route* r, int T,
+                      int H, int I, int E, int K, int tile_m, void* gemm2_rows, void* ws,
+                      size_t ws_bytes, int32_t* status, void* stream) {
+  int rc = check_weights(w, true);
+  if (rc || (rc = check_weights(w, false))) return rc;
+  rc = moe_experts_quantize(x, a, a_sf, a1_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status,
+                            stream);
+  if (rc) return rc;
+  rc = moe_experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream);
+  if (rc) return rc;
+  return moe_experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream);
+}
+
+int moe_experts_export(int which, const void* ws, size_t ws_bytes, int T, int H, int I, int E,
+                       int K, int tile_m, void* codes, void* scales, void* stream) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  if (which != 0 && which != 1) return fail(MOE_ERR_INVALID_ARG, "which must be 0 or 1");
+  if (L.P == 0) return MOE_OK;
+  if (!codes || !scales) return fail(MOE_ERR_INVALID_ARG, "codes / scales are null");
+  // Every one of the max_padded_rows rows is copied; rows past totals[1]
+  // hold whatever the workspace held.
+  uint8_t* base = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(ws));
+  const int Kc = which ? I : H;
+  cudaError_t err = cudaMemcpyAsync(codes, base + (which ? L.h_codes : L.a_codes),
+                                    (size_t)L.P * (Kc / 2), cudaMemcpyDeviceToDevice,
+                                    as_stream(stream));
+  if (err == cudaSuccess)
+    err = moe::launch_act_scales_io(1, base + (which ? L.h_sf : L.a_sf),
+                                    reinterpret_cast<uint8_t*>(scales), Kc, tile_m, L.P,
+                                    as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_export");
+}
+
+int moe_experts_import(int which, const void* codes, const void* scales, int T, int H, int I,
+                       int E, int K, int tile_m, void* ws, size_t ws_bytes, void* stream) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  if (which != 0 && which != 1) return fail(MOE_ERR_INVALID_ARG, "which must be 0 or 1");
+  if (L.P == 0) return MOE_OK;
+  if (!codes || !scales) return fail(MOE_ERR_INVALID_ARG, "codes / scales are null");
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  const int Kc = which ? I : H;
+  cudaError_t err = cudaMemcpyAsync(base + (which ? L.h_codes : L.a_codes), codes,
+                                    (size_t)L.P * (Kc / 2), cudaMemcpyDeviceToDevice,
+                                    as_stream(stream));
+  if (err == cudaSuccess)
+    err = moe::launch_act_scales_io(0, base + (which ? L.h_sf : L.a_sf),
+                                    const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(scales)),
+                                    Kc, tile_m, L.P, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_import");
+}
+
+int moe_post_expert_finalize(const void* rows, const int32_t* expanded_to_permuted,
+                             const float* topk_weights, const void* gamma, float eps,
+                             int weight_before_norm, int T, int K, int H, void* out,
+                             void* stream) {
+  if (T < 0 || K < 1 || H < 8 || H % 8 || H > 16384)
+    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d", T, K, H);
+  if (T == 0) return MOE_OK;
+  if (!rows || !expanded_to_permuted || !topk_weights || !gamma || !out)
+    return fail(MOE_ERR_INVALID_ARG, "finalize pointer is null");
+  if (!aligned(rows, 16) || !aligned(gamma, 16) || !aligned(out, 16))
+    return fail(MOE_ERR_INVALID_ARG, "rows / gamma / out must be 16-byte aligned");
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  cudaError_t err = moe::launch_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps,
+                                         weight_before_norm, T, K, H, out, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize");
+}
+
+}  // extern "C"

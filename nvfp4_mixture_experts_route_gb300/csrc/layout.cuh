@@ -1,0 +1,41 @@
+// Index arithmetic of the library's layouts (prepared weights, workspace).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kAtomRows = 128;   // rows of one scale atom
+constexpr int kAtomBytes = 512;  // 32 x 16 bytes
+
+__host__ __device__ __forceinline__ int sf_atoms_per_tile(int tile_m) {
+  return (tile_m + kAtomRows - 1) / kAtomRows;
+}
+
+// Byte of scale (row r, 16-element block b) inside an atom.
+__host__ __device__ __forceinline__ int atom_byte(int r, int b) {
+  return 16 * (r & 31) + 4 * ((r & 127) >> 5) + (b & 3);
+}
+
+// Workspace activations / intermediate: scales of permuted row p, block b.
+__host__ __device__ __forceinline__ size_t act_sf_offset(int p, int b, int tile_m, int kc, int S) {
+  const int tau = p / tile_m, i = p - tau * tile_m;
+  return ((size_t)((size_t)tau * kc + (b >> 2)) * S + (i >> 7)) * kAtomBytes + atom_byte(i, b);
+}
+
+// Prepared weights: scales of (expert e, prepared row r, block b) for a
+// tensor with `rows` rows per expert and kc = K/64 atoms along K.
+__host__ __device__ __forceinline__ size_t weight_sf_offset(int e, int r, int b, int rows,
+                                                            int kc) {
+  return ((size_t)((size_t)e * (rows / kAtomRows) + (r >> 7)) * kc + (b >> 2)) * kAtomBytes +
+         atom_byte(r, b);
+}
+
+// Raw w13 row feeding prepared row r (gate/up alternate in 16-row granules).
+__host__ __device__ __forceinline__ int w13_source_row(int r, int I) {
+  const int g = r >> 5, j = r & 31;
+  return j < 16 ? 16 * g + j : I + 16 * g + (j - 16);
+}
+
+}  // namespace moe

@@ -1,0 +1,152 @@
+// Routing metadata (step a2): per-expert histogram, padded offsets, the
+// stable expanded->permuted map, permuted->token, and the tile tables.
+//
+// What is computed follows the flashinfer_ops page (FlashInferOps.slot names
+// the tensors; gemm2_rows bounds the padded rows): counts[e], offsets as the
+// exclusive prefix of ceil(counts/tile)*tile, routes of one expert in
+// ascending expanded index j = t*K + k, tiles enumerated by (expert, index).
+//
+// One CTA of 1024 threads does it all, deterministically and without global
+// atomics: warp w owns a contiguous segment of the routes, so the order of
+// its routes is the order of j. Pass 1 builds a warp-private histogram
+// hist[w][e] (warp __match_any_sync groups equal experts in a 32-route chunk;
+// the group leader adds the group size). A per-expert scan over the warps and
+// a block scan over the experts turn it into each warp's first row per
+// expert. Pass 2 walks the segment again and hands out rows in order (rank
+// inside the chunk = peers below the lane).
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_permute_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int tile_m,
+                         int P, int MT, int32_t* __restrict__ expert_counts,
+                         int32_t* __restrict__ expert_offsets,
+                         int32_t* __restrict__ expanded_to_permuted,
+                         int32_t* __restrict__ permuted_to_token, int32_t* __restrict__ tile_expert,
+                         int32_t* __restrict__ tile_row_limit, int32_t* __restrict__ totals,
+                         int32_t* status) {
+  extern __shared__ int32_t hist[];  // [kRouteWarps][E]
+  __shared__ int32_t warp_sums[kRouteWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = T * K;
+  const int seg = (R + kRouteWarps - 1) / kRouteWarps;
+  const int beg = min(R, warp * seg), end = min(R, beg + seg);
+
+  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
+  for (int i = tid; i < P; i += kRouteThreads) permuted_to_token[i] = -1;
+  for (int i = tid; i < MT; i += kRouteThreads) {
+    tile_expert[i] = -1;
+    tile_row_limit[i] = -1;
+  }
+  __syncthreads();
+
+  // Pass 1: warp-private histogram.
+  int32_t* my = hist + warp * E;
+  bool bad = false;
+  for (int base = beg; base < end; base += 32) {
+    const int j = base + lane;
+    int e = (j < end) ? topk_ids[j] : -1;
+    if (e < -1 || e >= E) {
+      bad = true;
+      e = -1;
+    }
+    // Lanes without a route get a key no expert uses, unique per lane.
+    const int key = (e >= 0) ? e : -2 - lane;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) record_status(status, MOE_ERR_INVALID_ROUTE);
+  __syncthreads();
+
+  // Per expert: scan over warps (warp-relative starts) and the padded count.
+  int padded = 0, count = 0;
+  if (tid < E) {
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int c = hist[w * E + tid];
+      hist[w * E + tid] = count;
+      count += c;
+    }
+    padded = (count + tile_m - 1) / tile_m * tile_m;
+  }
+  // Block-wide exclusive scan of padded over the experts (E <= 1024).
+  int incl = padded;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, s, d);
+      if (lane >= d) s += v;
+    }
+    warp_sums[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int offset = incl - padded + (warp > 0 ? warp_sums[warp - 1] : 0);
+  const int total = warp_sums[kRouteWarps - 1];
+  if (tid < E) {
+    expert_counts[tid] = count;
+    expert_offsets[tid] = offset;
+    for (int w = 0; w < kRouteWarps; ++w) hist[w * E + tid] += offset;
+    // Tiles of this expert: [offset/tile_m, (offset+padded)/tile_m).
+    const int t0 = offset / tile_m, nt = padded / tile_m;
+    for (int i = 0; i < nt; ++i) {
+      tile_expert[t0 + i] = tid;
+      tile_row_limit[t0 + i] = offset + count;
+    }
+  }
+  if (tid == 0) {
+    expert_offsets[E] = total;
+    totals[0] = total / tile_m;
+    totals[1] = total;
+  }
+  __syncthreads();
+
+  // Pass 2: hand out rows in ascending j.
+  for (int base = beg; base < end; base += 32) {
+    const int j = base + lane;
+    int e = (j < end) ? topk_ids[j] : -1;
+    if (e < -1 || e >= E) e = -1;
+    const int key = (e >= 0) ? e : -2 - lane;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (e >= 0) {
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int p = my[e] + rank;
+      expanded_to_permuted[j] = p;
+      permuted_to_token[p] = j / K;
+    } else if (j < end) {
+      expanded_to_permuted[j] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+size_t route_smem_bytes(int E) { return sizeof(int32_t) * kRouteWarps * (size_t)E; }
+
+cudaError_t launch_route_permute(const int32_t* topk_ids, int T, int K, int E, int tile_m, int P,
+                                 int MT, int32_t* counts, int32_t* offsets, int32_t* e2p,
+                                 int32_t* p2t, int32_t* tile_expert, int32_t* tile_row_limit,
+                                 int32_t* totals, int32_t* status, cudaStream_t stream) {
+  const size_t smem = route_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(route_permute_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  route_permute_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, T, K, E, tile_m, P, MT,
+                                                            counts, offsets, e2p, p2t, tile_expert,
+                                                            tile_row_limit, totals, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,74 @@
+"""The routed NVFP4 expert block as one object over the C ABI.
+
+``NvFp4MoE`` holds one layer's prepared weights and scalars on the device and
+runs the four entry points in order on the current stream: routing metadata,
+the expert body (input quantization, GEMM1 + SwiGLU + requant, GEMM2), and
+the post-expert finalize. It only allocates (once, then reuses) and passes
+pointers; the work is the library's.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+class NvFp4MoE:
+    def __init__(self, raw: dict, a1_gscale: float, a2_gscale: float, gamma_bits, eps: float = 1e-6,
+                 tile_m: int = 32, weight_before_norm: bool = True, device="cuda"):
+        """``raw``: numpy or torch uint8 w13 [E,2I,H/2], w13_sf [E,2I,H/16],
+        w2 [E,H,I/2], w2_sf [E,H,I/16]; fp32 g1_alphas, g1_scale_c, g2_alphas
+        [E]. ``gamma_bits``: bf16 bit patterns [H] (uint16) or a bf16 tensor."""
+        dev = torch.device(device)
+        t = {k: torch.as_tensor(raw[k]).to(dev) for k in ("w13", "w13_sf", "w2", "w2_sf")}
+        self.E, twoI, half_h = t["w13"].shape
+        self.I, self.H = twoI // 2, 2 * half_h
+        self.prepared = B.prepare_weights(t["w13"], t["w13_sf"], t["w2"], t["w2_sf"])
+        del t
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.g1_alphas = torch.as_tensor(raw["g1_alphas"]).to(**f32).contiguous()
+        self.g1_scale_c = torch.as_tensor(raw["g1_scale_c"]).to(**f32).contiguous()
+        self.g2_alphas = torch.as_tensor(raw["g2_alphas"]).to(**f32).contiguous()
+        self.a1_gscale = torch.tensor([a1_gscale], **f32)
+        self.a2_gscale = torch.tensor([a2_gscale], **f32)
+        if isinstance(gamma_bits, torch.Tensor) and gamma_bits.dtype == torch.bfloat16:
+            g = gamma_bits
+        else:
+            g = torch.from_numpy(np.asarray(gamma_bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+        self.gamma = g.to(dev).contiguous()
+        self.eps = float(eps)
+        self.tile_m = tile_m
+        self.weight_before_norm = weight_before_norm
+        self.device = dev
+        self.weights = B.weights_struct(self.prepared, self.g1_alphas, self.g1_scale_c, self.g2_alphas)
+        self._buffers: dict = {}
+
+    def buffers(self, T: int, K: int) -> dict:
+        """Per-(T, K) metadata, workspace and output buffers, made once."""
+        key = (T, K)
+        if key not in self._buffers:
+            P, _ = B.route_sizes(T, K, self.E, self.tile_m)
+            self._buffers[key] = {
+                "route": B.alloc_route(T, K, self.E, self.tile_m, self.device),
+                "ws": B.alloc_workspace(T, K, self.E, self.H, self.I, self.tile_m, self.device),
+                "rows": torch.empty((max(P, 1), self.H), dtype=torch.bfloat16, device=self.device),
+                "out": torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device),
+                "status": torch.zeros(1, dtype=torch.int32, device=self.device),
+            }
+        return self._buffers[key]
+
+    def forward(self, x, topk_ids, topk_weights, out=None, status=None):
+        """x bf16 [T, H], topk_ids int32 [T, K], topk_weights fp32 [T, K] ->
+        bf16 [T, H]. Returns (out, buffers) ; buffers hold the metadata and the
+        GEMM2 rows of this call."""
+        T, K = topk_ids.shape
+        b = self.buffers(T, K)
+        st = b["status"] if status is None else status
+        B.route_permute(topk_ids, self.E, self.tile_m, route=b["route"], status=st)
+        B.nvfp4_experts(self.weights, b["route"], x=x, a1_gscale=self.a1_gscale, a2_gscale=self.a2_gscale,
+                        T=T, H=self.H, I=self.I, E=self.E, K=K, gemm2_rows=b["rows"], ws=b["ws"], status=st)
+        o = b["out"] if out is None else out
+        B.post_expert_finalize(b["rows"], b["route"].expanded_to_permuted, topk_weights, self.gamma, self.eps,
+                               self.weight_before_norm, out=o)
+        return o, b

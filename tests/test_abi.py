@@ -1,0 +1,78 @@
+"""The C-ABI library loads, exports every declared entry point, and checks
+its arguments on the host (no GPU calls)."""
+import ctypes as C
+
+import pytest
+
+from nvfp4_mixture_experts_route_gb300 import binding as B
+from nvfp4_mixture_experts_route_gb300 import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = B.declared_symbols()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(B._SIGNATURES) == set(names)
+
+
+def test_version_and_sizes(lib):
+    assert lib.moe_abi_version() == 1
+    assert B.prepared_sizes(128, 5120, 2048) == [
+        128 * 4096 * 2560, 128 * 4096 * 320, 128 * 5120 * 1024, 128 * 5120 * 128]
+    assert B.route_sizes(8, 8, 128, 32) == (2048, 64)
+    assert B.route_sizes(8192, 8, 128, 128) == (128 * (128 + (65536 - 128) // 128), 128 + (65536 - 128) // 128)
+    assert B.route_sizes(0, 8, 128, 32) == (0, 0)
+
+
+def test_workspace_size_formula(lib):
+    T, K, E, H, I, tm = 8, 8, 128, 5120, 2048, 32
+    P, MT = B.route_sizes(T, K, E, tm)
+
+    def up(v):
+        return (v + 1023) // 1024 * 1024
+
+    want = up(P * H // 2) + up(MT * (H // 64) * 512) + up(P * I // 2) + up(MT * (I // 64) * 512)
+    assert B.experts_workspace_size(T, K, E, H, I, tm) == want
+
+
+@pytest.mark.parametrize("call,code", [
+    (lambda: B.prepared_sizes(8, 192, 128), "MOE_ERR_UNSUPPORTED"),
+    (lambda: B.prepared_sizes(8, 256, 96), "MOE_ERR_UNSUPPORTED"),
+    (lambda: B.route_sizes(4, 2, 8, 48), "MOE_ERR_UNSUPPORTED"),
+    (lambda: B.route_sizes(4, 2, 0, 32), "MOE_ERR_INVALID_ARG"),
+    (lambda: B.experts_workspace_size(4, 2, 8, 256, 64, 32), "MOE_ERR_UNSUPPORTED"),
+])
+def test_host_refusals(lib, call, code):
+    with pytest.raises(B.MoeError) as ei:
+        call()
+    assert code in str(ei.value)
+    assert lib.moe_last_error()
+
+
+def test_null_pointers_refused_before_any_launch(lib):
+    rc = lib.moe_route_permute(None, 4, 2, 8, 32, None, None, None, None, None, None, None, None, None)
+    assert rc == -1 and b"null" in lib.moe_last_error()
+    rc = lib.moe_post_expert_finalize(None, None, None, None, 1e-6, 1, 4, 2, 256, None, None)
+    assert rc == -1
+    rc = lib.moe_post_expert_finalize(None, None, None, None, 1e-6, 1, 4, 2, 250, None, None)
+    assert rc == -1 and b"shape" in lib.moe_last_error()
+    w = B.MoeWeights()
+    r = B.MoeRoute()
+    rc = lib.moe_nvfp4_experts(C.byref(w), None, None, None, None, None, C.byref(r), 4, 256, 128, 8, 2, 32,
+                               None, None, 0, None, None)
+    assert rc == -1
+    # misaligned workspace
+    w = B.MoeWeights(*([16] * 7))
+    r = B.MoeRoute(16, 16, 16, 16)
+    rc = lib.moe_experts_gemm2(C.byref(w), C.byref(r), 4, 256, 128, 8, 2, 32, 16, 1040, 1 << 20, None, None)
+    assert rc == -1 and b"aligned" in lib.moe_last_error()
+    # undersized workspace
+    rc = lib.moe_experts_gemm2(C.byref(w), C.byref(r), 4, 256, 128, 8, 2, 32, 16, 1024, 16, None, None)
+    assert rc == -3

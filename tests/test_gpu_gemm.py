@@ -1,0 +1,269 @@
+"""GPU parity of the tcgen05 grouped GEMMs and of the whole expert block
+against the CPU oracle, through the C ABI.
+
+Bars: GEMM2 rows on identical quantized operands within rel-L2 2e-3; final
+output within rel-L2 1e-2 (the intermediate requant may flip FP4 codes at
+rounding boundaries because h is fp32 on the GPU and fp64 in the oracle);
+routing metadata bit-exact (test_gpu_kernels)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import codecs, layer as olayer, layout as olayout
+from nvfp4_mixture_experts_route_gb300 import binding as B
+from nvfp4_mixture_experts_route_gb300 import inputs
+
+from _util import bf16_dev, bf16_host_f64, canon_codes, finite_summary, layer_for, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+GEMM2_BAR = 2e-3
+OUT_BAR = 1e-2
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(DEV) if dtype is None else t.to(DEV, dtype)
+
+
+class Prepared:
+    """A layer uploaded and prepared once."""
+
+    def __init__(self, raw):
+        t = {k: _dev(raw[k]) for k in ("w13", "w13_sf", "w2", "w2_sf")}
+        self.E, twoI, hh = raw["w13"].shape
+        self.I, self.H = twoI // 2, 2 * hh
+        self.p = B.prepare_weights(t["w13"], t["w13_sf"], t["w2"], t["w2_sf"])
+        del t
+        self.g1a = _dev(raw["g1_alphas"])
+        self.g1c = _dev(raw["g1_scale_c"])
+        self.g2a = _dev(raw["g2_alphas"])
+        self.gamma = bf16_dev(raw["gamma"])
+        self.w = B.weights_struct(self.p, self.g1a, self.g1c, self.g2a)
+
+
+def run_gpu(prep: Prepared, batch, tile, a1, a2, *, hq_override=None, wbn=True, export=True):
+    """Routing, quantize, GEMM1, [import hq], GEMM2, finalize. Returns numpy
+    views of what the tests compare."""
+    E, H, I = prep.E, prep.H, prep.I
+    ids = _dev(batch["topk_ids"].astype(np.int32))
+    T, K = ids.shape
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r = B.route_permute(ids, E, tile, status=status)
+    ws = B.alloc_workspace(T, K, E, H, I, tile, DEV)
+    g1 = torch.tensor([a1], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([a2], dtype=torch.float32, device=DEV)
+    B.experts_quantize(r, ws, x=bf16_dev(batch["x"]), a1_gscale=g1, T=T, H=H, I=I, E=E, K=K, status=status)
+    B.experts_gemm1(prep.w, r, ws, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K, status=status)
+    out = {}
+    if export:
+        hc, hs = B.experts_export(1, ws, T=T, H=H, I=I, E=E, K=K, tile_m=tile)
+        out["hq_codes"], out["hq_sf"] = hc.cpu().numpy(), hs.cpu().numpy()
+    if hq_override is not None:
+        B.experts_import(1, _dev(hq_override[0]), _dev(hq_override[1]), ws, T=T, H=H, I=I, E=E, K=K, tile_m=tile)
+    P, _ = B.route_sizes(T, K, E, tile)
+    rows = torch.zeros((max(P, 1), H), dtype=torch.bfloat16, device=DEV)
+    B.experts_gemm2(prep.w, r, ws, rows, T=T, H=H, I=I, E=E, K=K, status=status)
+    fin = B.post_expert_finalize(rows, r.expanded_to_permuted, _dev(batch["topk_weights"]), prep.gamma, 1e-6, wbn)
+    torch.cuda.synchronize()
+    out.update(
+        status=int(status.item()),
+        e2p=r.expanded_to_permuted.cpu().numpy(),
+        p2t=r.permuted_to_token.cpu().numpy(),
+        rows=bf16_host_f64(rows),
+        out=bf16_host_f64(fin),
+    )
+    return out
+
+
+def oracle_hq_permuted(er, e2p, P, I):
+    """The oracle's quantized intermediate placed at the permuted rows."""
+    codes = np.zeros((P, I // 2), np.uint8)
+    sf = np.zeros((P, I // 16), np.uint8)
+    flat = e2p.reshape(-1)
+    live = flat >= 0
+    codes[flat[live]] = codecs.pack_nibbles(er["hq_codes"][live])
+    sf[flat[live]] = er["hq_sf"][live]
+    return codes, sf
+
+
+def _workload(T, H, I, E, K, routing="uniform", tile=32):
+    return inputs.Workload(f"t{T}h{H}i{I}e{E}k{K}", T=T, H=H, I=I, E=E, K=K, routing=routing, tile_m=tile)
+
+
+SMALL = [
+    # (T, H, I, E, K, routing, tile, a1, a2)
+    (4, 256, 128, 8, 2, "uniform", 32, 1.0, 1.0),           # the tiny workload
+    (37, 512, 256, 8, 4, "uniform", 32, 4.0, 1e-3),        # several tiles, ragged tail
+    (29, 640, 384, 4, 3, "zipf", 64, 4.0, 1e-3),           # ragged K (2.5 and 1.5 stages)
+    (70, 512, 256, 4, 4, "zipf", 128, 4.0, 1e-3),          # tile 128
+    (150, 256, 256, 4, 4, "uniform", 256, 4.0, 1e-3),      # tile 256: two scale atoms per tile
+]
+
+
+@pytest.fixture(scope="module")
+def small_cases():
+    out = []
+    for T, H, I, E, K, routing, tile, a1, a2 in SMALL:
+        w = _workload(T, H, I, E, K, routing, tile)
+        raw = inputs.make_layer(w)
+        batch = inputs.make_batch(w)
+        out.append((w, raw, batch, tile, a1, a2))
+    return out
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+def test_gemm2_on_identical_operands(small_cases, idx):
+    w, raw, batch, tile, a1, a2 = small_cases[idx]
+    er = olayer.expert_rows(batch["x"], batch["topk_ids"], raw, a1, a2, return_intermediate=True)
+    prep = Prepared(raw)
+    P, _ = B.route_sizes(w.T, w.K, w.E, tile)
+    first = run_gpu(prep, batch, tile, a1, a2, export=False)
+    hq = oracle_hq_permuted(er, first["e2p"], P, w.I)
+    got = run_gpu(prep, batch, tile, a1, a2, hq_override=hq, export=False)
+    assert got["status"] == 0
+    e2p = got["e2p"].reshape(-1)
+    live = e2p >= 0
+    rows = got["rows"][e2p[live]]
+    want = er["rows_bf16"][live]
+    err = rel_l2(rows, want)
+    assert err < GEMM2_BAR, f"rel-L2 {err:.3g}; gpu {finite_summary(rows)}"
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+def test_gemm1_intermediate_and_end_to_end(small_cases, idx):
+    w, raw, batch, tile, a1, a2 = small_cases[idx]
+    ref = olayer.moe_layer(batch["x"], batch["topk_ids"], batch["topk_weights"], raw, a1, a2, raw["gamma"],
+                           1e-6, tile, return_intermediate=True)
+    prep = Prepared(raw)
+    got = run_gpu(prep, batch, tile, a1, a2)
+    assert got["status"] == 0
+    assert np.array_equal(got["e2p"], ref["meta"]["expanded_to_permuted"])
+    e2p = got["e2p"].reshape(-1)
+    live = e2p >= 0
+    # the requantized intermediate: scales and codes agree except at rare
+    # rounding-boundary flips
+    g_sf = got["hq_sf"][e2p[live]]
+    g_codes = canon_codes(codecs.unpack_nibbles(got["hq_codes"][e2p[live]]))
+    w_codes = canon_codes(ref["routes"]["hq_codes"][live])
+    sf_match = np.mean(g_sf == ref["routes"]["hq_sf"][live])
+    code_match = np.mean(g_codes == w_codes)
+    assert sf_match > 0.99 and code_match > 0.99, (sf_match, code_match)
+    err_rows = rel_l2(got["rows"][e2p[live]], ref["routes"]["rows_bf16"][live])
+    assert err_rows < OUT_BAR, err_rows
+    err = rel_l2(got["out"], ref["out"])
+    assert err < OUT_BAR, f"out rel-L2 {err:.3g}; gpu {finite_summary(got['out'])}"
+
+
+def test_weight_before_norm_reading_end_to_end(small_cases):
+    w, raw, batch, tile, a1, a2 = small_cases[1]
+    raw = dict(raw)
+    raw["gamma"] = inputs._to_bf16_bits(np.random.default_rng(0).standard_normal(w.H))
+    prep = Prepared(raw)
+    for wbn in (True, False):
+        ref = olayer.moe_layer(batch["x"], batch["topk_ids"], batch["topk_weights"], raw, a1, a2, raw["gamma"],
+                               1e-6, tile, weight_before_norm=wbn)
+        got = run_gpu(prep, batch, tile, a1, a2, wbn=wbn, export=False)
+        assert rel_l2(got["out"], ref["out"]) < OUT_BAR
+
+
+def test_determinism(small_cases):
+    w, raw, batch, tile, a1, a2 = small_cases[2]
+    prep = Prepared(raw)
+    a = run_gpu(prep, batch, tile, a1, a2)
+    b = run_gpu(prep, batch, tile, a1, a2)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["hq_codes"], b["hq_codes"])
+
+
+def test_unrouted_routes_contribute_nothing(small_cases):
+    w, raw, batch, tile, a1, a2 = small_cases[1]
+    batch = dict(batch)
+    ids = batch["topk_ids"].copy()
+    ids[::2, 0] = -1
+    batch["topk_ids"] = ids
+    ref = olayer.moe_layer(batch["x"], ids, batch["topk_weights"], raw, a1, a2, raw["gamma"], 1e-6, tile)
+    got = run_gpu(Prepared(raw), batch, tile, a1, a2, export=False)
+    assert rel_l2(got["out"], ref["out"]) < OUT_BAR
+
+
+# ---------------------------------------------------------------------------
+# Full-size layer (H = 5120, I = 2048, E = 128): decode, TP slices, prefill
+# ---------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def full():
+    raw = layer_for("decode_b8")
+    return raw, Prepared(raw)
+
+
+def test_decode_b8_full_size(full):
+    raw, prep = full
+    w = inputs.WORKLOADS["decode_b8"]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    ref = olayer.moe_layer(batch["x"], batch["topk_ids"], batch["topk_weights"], raw, a1, a2, raw["gamma"],
+                           1e-6, w.tile_m, return_intermediate=True)
+    got = run_gpu(prep, batch, w.tile_m, a1, a2)
+    assert got["status"] == 0
+    e2p = got["e2p"].reshape(-1)
+    err_rows = rel_l2(got["rows"][e2p], ref["routes"]["rows_bf16"])
+    err = rel_l2(got["out"], ref["out"])
+    assert err < OUT_BAR and err_rows < OUT_BAR, (err, err_rows)
+    # GEMM2 alone on the oracle's intermediate
+    P, _ = B.route_sizes(w.T, w.K, w.E, w.tile_m)
+    hq = oracle_hq_permuted(ref["routes"], got["e2p"], P, w.I)
+    same = run_gpu(prep, batch, w.tile_m, a1, a2, hq_override=hq, export=False)
+    assert rel_l2(same["rows"][e2p], ref["routes"]["rows_bf16"]) < GEMM2_BAR
+
+
+def test_decode_b64_zipf_full_size_sampled(full):
+    raw, prep = full
+    w = inputs.WORKLOADS["decode_b64_zipf"]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    got = run_gpu(prep, batch, w.tile_m, a1, a2, export=False)
+    assert got["status"] == 0
+    pick = np.array([0, 17, 63])
+    ref = olayer.moe_layer(batch["x"][pick], batch["topk_ids"][pick], batch["topk_weights"][pick], raw, a1, a2,
+                           raw["gamma"], 1e-6, w.tile_m)
+    assert rel_l2(got["out"][pick], ref["out"]) < OUT_BAR
+
+
+def test_expert_tp_identity(full):
+    """The expert_tp page: the K-partial GEMM2 rows of the tp = 8
+    intermediate slices (I' = 256), run one after another on this GPU and
+    summed in fp32 with one bf16 rounding, equal the full-width rows."""
+    raw, prep = full
+    w = inputs.WORKLOADS["tp8_slice_b32"]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    full_run = run_gpu(prep, batch, w.tile_m, a1, a2, export=False)
+    e2p = full_run["e2p"].reshape(-1)
+    acc = np.zeros((len(e2p), w.H), dtype=np.float32)
+    for r in range(w.tp):
+        sl = olayout.raw_slice(raw, r, w.tp)
+        part = run_gpu(Prepared(sl), batch, w.tile_m, a1, a2, export=False)
+        assert np.array_equal(part["e2p"], full_run["e2p"])
+        acc += part["rows"][e2p].astype(np.float32)
+        torch.cuda.empty_cache()
+    summed = codecs.round_to_bf16(acc.astype(np.float64))
+    assert rel_l2(summed, full_run["rows"][e2p]) < GEMM2_BAR
+    pick = np.array([0, 31])
+    ref = olayer.expert_rows(batch["x"][pick], batch["topk_ids"][pick], raw, a1, a2)
+    sel = (np.arange(w.T * w.K) // w.K)
+    mask = np.isin(sel, pick)
+    assert rel_l2(summed[mask], ref["rows_bf16"]) < OUT_BAR
+
+
+def test_prefill_t8192_sampled(full):
+    raw, prep = full
+    w = inputs.WORKLOADS["prefill_t8192_zipf"]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    got = run_gpu(prep, batch, w.tile_m, a1, a2, export=False)
+    assert got["status"] == 0
+    assert np.isfinite(got["out"]).all()
+    pick = np.array([0, 4095, 8191])
+    ref = olayer.moe_layer(batch["x"][pick], batch["topk_ids"][pick], batch["topk_weights"][pick], raw, a1, a2,
+                           raw["gamma"], 1e-6, w.tile_m)
+    assert rel_l2(got["out"][pick], ref["out"]) < OUT_BAR
