@@ -9,9 +9,29 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "../../include/moe_nvfp4.h"
 
 namespace moe {
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
+// that later launches (including ones recorded into a CUDA graph) make no
+// attribute call.
+inline cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done.insert({func, dev});
+  return err;
+}
 
 // ---------------------------------------------------------------------------
 // Status word: the first device-side error wins.

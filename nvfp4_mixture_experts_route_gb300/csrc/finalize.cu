@@ -4,37 +4,29 @@
 // marked -1 add nothing).
 //
 // One CTA per token. Each thread owns 8-element (16-byte) vectors of the
-// hidden dimension; for every route k the CTA loads the GEMM2 row, reduces
-// the sum of squares across the block, and adds w * u / rms into fp32
-// registers. HBM traffic: K rows of H bf16 in, one row out.
+// hidden dimension. Routes are taken in chunks of up to kFinChunk: the CTA
+// first issues the loads of every row of the chunk (so their latencies
+// overlap), then reduces all of the chunk's sums of squares in one block
+// reduction, then adds w * u / rms into fp32 registers. HBM traffic: K rows
+// of H bf16 in, one row out.
 #include "common.cuh"
 
 namespace moe {
 
 constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kFinChunk = 8;  // most routes per chunk (fewer for wide rows)
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();  // red[] free from the previous use
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float s = 0.f;
-#pragma unroll
-  for (int w = 0; w < kFinThreads / 32; ++w) s += red[w];  // fixed order
-  return s;
-}
-
-// VPT: 8-element vectors per thread (ceil(H / 8 / 256)), a template so that
-// the per-thread arrays stay in registers.
-template <int VPT>
+// VPT: 8-element vectors per thread (ceil(H / 8 / 256)) and CH: routes per
+// chunk, templates so that the per-thread arrays stay in registers.
+template <int VPT, int CH>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ e2p,
     const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
     int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out) {
-  __shared__ float red[kFinThreads / 32];
+  __shared__ float red[kFinWarps][CH];
   const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = H / 8;
   float g[VPT][8];
   float acc[VPT][8];
@@ -58,42 +50,64 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     }
   }
   const float inv_h = 1.0f / (float)H;
-  for (int k = 0; k < K; ++k) {
-    const int p = e2p[(size_t)t * K + k];
-    if (p < 0) continue;  // uniform across the block
-    const float wk = topk_w[(size_t)t * K + k];
-    float u[VPT][8];
-    float ss = 0.f;
+  for (int k0 = 0; k0 < K; k0 += CH) {
+    const int kc = min(CH, K - k0);
+    int pr[CH];
+    uint4 raw[CH][VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = threadIdx.x + i * kFinThreads;
+    for (int c = 0; c < CH; ++c) {
+      pr[c] = c < kc ? e2p[(size_t)t * K + k0 + c] : -1;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) u[i][q] = 0.f;
-      if (v < nvec) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(rows + (size_t)p * H + 8 * v);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      for (int i = 0; i < VPT; ++i) {
+        const int v = threadIdx.x + i * kFinThreads;
+        raw[c][i] = (pr[c] >= 0 && v < nvec)
+                        ? *reinterpret_cast<const uint4*>(rows + (size_t)pr[c] * H + 8 * v)
+                        : make_uint4(0, 0, 0, 0);
+      }
+    }
+    float ss[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      ss[c] = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[c][i]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float2 f = __bfloat1622float2(h[q]);
-          u[i][2 * q] = f.x;
-          u[i][2 * q + 1] = f.y;
+          const float a = weight_before_norm ? f.x * g[i][2 * q] : f.x;
+          const float b = weight_before_norm ? f.y * g[i][2 * q + 1] : f.y;
+          ss[c] = fmaf(a, a, ss[c]);
+          ss[c] = fmaf(b, b, ss[c]);
         }
-        if (weight_before_norm) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) u[i][q] *= g[i][q];
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) ss = fmaf(u[i][q], u[i][q], ss);
       }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) ss[c] += __shfl_xor_sync(0xffffffffu, ss[c], d);
     }
-    const float total = block_sum(ss, red);
-    const float c = wk / sqrtf(total * inv_h + eps);
+    __syncthreads();  // red[] is free from the previous chunk
+    if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
+      for (int c = 0; c < CH; ++c) red[warp][c] = ss[c];
+    }
+    __syncthreads();
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float n = weight_before_norm ? u[i][q] * c : (u[i][q] * c) * g[i][q];
-        acc[i][q] += n;
+    for (int c = 0; c < CH; ++c) {
+      if (pr[c] < 0) continue;  // uniform across the block
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kFinWarps; ++w) total += red[w][c];  // fixed order
+      const float coef = topk_w[(size_t)t * K + k0 + c] / sqrtf(total * inv_h + eps);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[c][i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(h[q]);
+          // (r * g) * coef in both readings; the reading only moves g inside
+          // or outside the mean of squares above.
+          acc[i][2 * q] += (f.x * g[i][2 * q]) * coef;
+          acc[i][2 * q + 1] += (f.y * g[i][2 * q + 1]) * coef;
+        }
       }
     }
   }
@@ -120,8 +134,8 @@ cudaError_t launch_finalize(const void* rows, const int32_t* e2p, const float* w
   auto op = reinterpret_cast<__nv_bfloat16*>(out);
 #define MOE_FIN_CASE(n)                                                                     \
   case n:                                                                                   \
-    finalize_kernel<n><<<T, kFinThreads, 0, stream>>>(rp, e2p, w, gp, eps, weight_before_norm, \
-                                                      K, H, op);                              \
+    finalize_kernel<n, (n <= 2 ? 8 : n <= 4 ? 4 : 2)><<<T, kFinThreads, 0, stream>>>(           \
+        rp, e2p, w, gp, eps, weight_before_norm, K, H, op);                                  \
     break;
   switch (vpt) {
     MOE_FIN_CASE(1)

@@ -10,30 +10,39 @@
 //   GEMM2  rows[r, :] = bf16(g2_alphas[e] * sum_i hq[r, i] w2[e][:, i])
 //
 // Tiling ("swap AB"): the MMA's M = 128 rows are weight rows, its N = tile_m
-// rows are permuted route rows of one routing tile (all of one expert). One
-// CTA computes one (route tile tau, weight tile mt) pair over the whole K:
-//   - warp 0 / lane 0: TMA producer. Per pipeline stage (K = 256 elements =
-//     128 bytes per row): the 128 x 128 B weight box, the tile_m x 128 B
-//     route box (both 128-byte swizzled), and the stage's scale atoms for both
-//     operands with plain bulk copies; one mbarrier with a transaction count.
-//   - warp 1 / lane 0: MMA issuer. Copies the stage's scale atoms into tensor
-//     memory (tcgen05.cp 32x128b.warpx4; each stage has its own columns, so a
-//     refill can never race an MMA still reading them), issues 4 MMAs of
-//     K = 64 accumulating into TMEM columns [0, tile_m), and commits the stage
-//     back to the producer.
-//   - all 4 warps: epilogue. Warp w reads TMEM lanes [32w, 32w+32) (weight
-//     rows) for every route column.
-// The grid is (route tiles, weight tiles) with route tiles fastest, so the
-// CTAs that share an expert's weight tile run side by side and the second
-// reads it from L2. Tiles past the live count (totals[0]) exit at once.
+// rows are permuted route rows of one routing tile (all of one expert). A
+// work unit is one (route tile tau, weight tile mt) pair over the whole K.
 //
-// The prepared w13 interleaves gate and up rows in 16-row granules, so a
-// warp's 32 lanes hold gate (lanes 0-15) and up (lanes 16-31) of the same 16
-// intermediate columns: SwiGLU is one shuffle, the NVFP4 block amax four.
+// Persistent, warp-specialised kernel, one CTA per SM, 6 warps:
+//   - warp 0 / lane 0: TMA producer. Walks this CTA's units in order and, per
+//     pipeline stage (K = 256 elements = 128 bytes per row), loads the
+//     128 x 128 B weight box and the tile_m x 128 B route box (both 128-byte
+//     swizzled) and the stage's scale atoms for both operands (plain bulk
+//     copies), all completing one mbarrier. The ring of ST stages runs across
+//     unit boundaries, so HBM streaming never stops between units.
+//   - warp 1 / lane 0: MMA issuer. Copies each stage's scale atoms into that
+//     stage's own tensor-memory columns (tcgen05.cp 32x128b.warpx4), issues
+//     4 MMAs of K = 64 into the unit's accumulator buffer, and commits the
+//     stage back to the producer; after a unit's last stage it commits the
+//     accumulator to the epilogue.
+//   - warps 2-5: epilogue. Warp w reads TMEM lane quadrant w % 4 (32 weight
+//     rows) of the finished accumulator, then hands the buffer back. Two
+//     accumulator buffers (one for tile_m = 256) let the epilogue of unit i
+//     run while unit i+1 streams.
+// Units are ordered with the weight tile fastest (u -> mt = u % tiles_w,
+// tau = u / tiles_w) and dealt round-robin, so the CTAs working at the same
+// time share route tiles (and, for experts with many tiles, weight tiles) in
+// L2. Tiles past the live count (totals[0]) are not units at all.
+//
+// GEMM1's epilogue: the prepared w13 puts the gate (16 rows) and up (16 rows)
+// of 16 intermediate columns in one 32-row quadrant, so warp w stages
+// scale * acc for its 32 rows x 32 route columns in shared memory and then
+// each lane takes one route column: SwiGLU of 16 elements and one NVFP4
+// block, no shuffles.
 //
 // Every mbarrier wait is bounded (1 s); on a timeout the CTA records
-// MOE_ERR_TIMEOUT, drains its own copies and MMAs (bounded again), frees its
-// tensor memory and exits.
+// MOE_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs (bounded
+// again), frees its tensor memory and exits.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -43,9 +52,14 @@ namespace moe {
 
 constexpr int kStageK = 256;                   // K elements per pipeline stage
 constexpr int kStageRowBytes = kStageK / 2;    // 128
-constexpr int kWTile = 128;                    // weight rows per CTA (MMA M)
+constexpr int kWTile = 128;                    // weight rows per unit (MMA M)
 constexpr uint32_t kABytes = kWTile * kStageRowBytes;  // 16 KiB
 constexpr uint32_t kSfStageBytes = 4 * kAtomBytes;     // 4 K=64 steps
+constexpr int kMaxStages = 8;
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
+constexpr uint32_t kEpiBytes = kEpiWarps * 32 * kEpiStride * 4;
 
 struct GemmParams {
   const uint8_t* w_sf;  // prepared scale atoms [E][rows_w/128][K/64][512]
@@ -60,95 +74,114 @@ struct GemmParams {
   uint8_t* hq_sf;          // GEMM1: intermediate scale atoms [tiles][I/64][S][512]
   __nv_bfloat16* rows;     // GEMM2: [P][H]
   int32_t* status;
-  int E, rows_w, K, tile_m, S, out_cols;
+  int E, rows_w, K, tile_m, S, out_cols, stages, acc_bufs;
 };
 
-__host__ __device__ constexpr uint32_t tmem_cols_for(int tile_m, int S, int stages) {
-  const int need = tile_m + stages * 16 * (1 + S);
+// Pipeline depth and accumulator buffers per route-tile size (1 CTA per SM).
+__host__ __device__ constexpr int stages_for(int tile_m) {
+  return tile_m <= 32 ? 8 : tile_m <= 64 ? 6 : tile_m <= 128 ? 5 : 3;
+}
+__host__ __device__ constexpr int acc_bufs_for(int tile_m) { return tile_m <= 128 ? 2 : 1; }
+
+__host__ __device__ constexpr uint32_t stage_bytes(int tile_m, int S) {
+  return kABytes + (uint32_t)tile_m * kStageRowBytes + kSfStageBytes * (uint32_t)(1 + S);
+}
+
+__host__ __device__ constexpr uint32_t tmem_cols_for(int tile_m, int S, int stages, int bufs) {
+  const int need = bufs * tile_m + stages * 16 * (1 + S);
   uint32_t c = 32;
   while ((int)c < need) c <<= 1;
   return c;
 }
 
-__host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m, int S, int stages) {
-  return 1024 + (size_t)stages * (kABytes + (size_t)tile_m * kStageRowBytes +
-                                  kSfStageBytes * (size_t)(1 + S));
+__host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m, int S) {
+  return 1024 + (size_t)stages_for(tile_m) * stage_bytes(tile_m, S) + kEpiBytes;
 }
 
-// SwiGLU + NVFP4 requant of one route column; lanes 0-15 carry the gate and
-// lanes 16-31 the up rows of 16 intermediate columns.
-__device__ __forceinline__ void gemm1_column(float v, float sc, float a2g, int lane, uint8_t* hq_row,
-                                             uint8_t* hq_sf_byte) {
-  const float x = v * sc;
-  const float o = __shfl_xor_sync(0xffffffffu, x, 16);
-  const float gate = lane < 16 ? x : o;
-  const float up = lane < 16 ? o : x;
-  const float h = gate / (1.0f + expf(-gate)) * up;
-  float a = fabsf(h);
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-  const float s = (a * a2g) / 6.0f;
-  const uint32_t sfc = f32_to_e4m3(s);
-  const float sfv = e4m3_to_f32(sfc);
-  const float inv = sfv > 0.f ? a2g / sfv : 0.f;
-  const float t = h * inv;
-  const float tn = __shfl_down_sync(0xffffffffu, t, 1);
-  uint32_t byte = f32x2_to_e2m1x2(t, tn);
-  if (!(sfv > 0.f)) byte = 0;
-  const bool even = !(lane & 1);
-  uint32_t lo = (even && lane < 8) ? byte << (8 * (lane >> 1)) : 0u;
-  uint32_t hi = (even && lane >= 8 && lane < 16) ? byte << (8 * ((lane - 8) >> 1)) : 0u;
-  lo |= __shfl_xor_sync(0xffffffffu, lo, 2);
-  hi |= __shfl_xor_sync(0xffffffffu, hi, 2);
-  lo |= __shfl_xor_sync(0xffffffffu, lo, 4);
-  hi |= __shfl_xor_sync(0xffffffffu, hi, 4);
-  lo |= __shfl_xor_sync(0xffffffffu, lo, 8);
-  hi |= __shfl_xor_sync(0xffffffffu, hi, 8);
-  if (lane == 0) {
-    *reinterpret_cast<uint2*>(hq_row) = make_uint2(lo, hi);
-    *hq_sf_byte = static_cast<uint8_t>(sfc);
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 lanes x 32 bit, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// NVFP4 of one 16-element block with global scale g; same arithmetic as the
+// input quantization (s = amax*g/6, sf = e4m3(s), q = e2m1(v * g/sf)).
+__device__ __forceinline__ void quant16(const float (&v)[16], float g, uint2& codes,
+                                        uint32_t& sf_code) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  sf_code = f32_to_e4m3((amax * g) / 6.0f);
+  const float sfv = e4m3_to_f32(sf_code);
+  uint32_t lo = 0, hi = 0;
+  if (sfv > 0.f) {
+    const float inv = g / sfv;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) lo |= f32x2_to_e2m1x2(v[i] * inv, v[i + 1] * inv) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+      hi |= f32x2_to_e2m1x2(v[8 + i] * inv, v[9 + i] * inv) << (4 * i);
   }
+  codes = make_uint2(lo, hi);
 }
 
-template <int KIND, int ST>
-__global__ void __launch_bounds__(128, 1)
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t dsmem[];
-  __shared__ __align__(8) uint64_t full_bar[ST];
-  __shared__ __align__(8) uint64_t empty_bar[ST];
-  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tau = blockIdx.x, mt = blockIdx.y;
-  if (tau >= p.totals[0]) return;
-  const int e = p.tile_expert[tau];
-  if (e < 0 || e >= p.E) {
-    if (tid == 0) record_status(p.status, MOE_ERR_INVALID_ROUTE);
-    return;
-  }
+  const int ntiles = p.totals[0];
+  const int tiles_w = p.rows_w / kWTile;
+  const int n_units = ntiles * tiles_w;
+  if ((int)blockIdx.x >= n_units) return;
 
-  const int tile_m = p.tile_m, S = p.S;
+  const int tile_m = p.tile_m, S = p.S, ST = p.stages, NB = p.acc_bufs;
   const uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;
   const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sA = sbase;
   const uint32_t sB = sA + ST * kABytes;
   const uint32_t sSFA = sB + ST * b_bytes;
   const uint32_t sSFB = sSFA + ST * kSfStageBytes;
+  const uint32_t sEpi = sSFB + ST * kSfStageBytes * S;
   const int KC = p.K / 64;
   const int nks = (KC + 3) / 4;
-  const uint32_t ncols = tmem_cols_for(tile_m, S, ST);
+  const uint32_t ncols = tmem_cols_for(tile_m, S, ST, NB);
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    mbar_init(smem_u32(&acc_bar), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&accf_bar[b]), 1);
+      mbar_init(smem_u32(&acce_bar[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
     abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -162,108 +195,156 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t t_sfa = tmem + (uint32_t)tile_m;
+  const uint32_t t_sfa = tmem + (uint32_t)(NB * tile_m);
   const uint32_t t_sfb = t_sfa + ST * 16;
 
   if (warp == 0) {
+    // ------------------------------ producer ------------------------------
     if (lane == 0) {
-      const int a_row = e * p.rows_w + mt * kWTile;
-      const uint8_t* wsf = p.w_sf + ((size_t)e * (p.rows_w / kWTile) + mt) * KC * kAtomBytes;
-      const uint8_t* bsf = p.b_sf + (size_t)tau * KC * S * kAtomBytes;
-      int issued = 0;
-      for (int ks = 0; ks < nks; ++ks) {
-        const int s = ks % ST, round = ks / ST;
-        if (round > 0 &&
-            !mbar_wait(smem_u32(&empty_bar[s]), (round - 1) & 1, &abort_flag, p.status))
-          break;
-        const int kk = min(4, KC - 4 * ks);
-        const uint32_t fb = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, kABytes + b_bytes + (uint32_t)kk * kAtomBytes * (1 + S));
-        tma_load_2d(sA + s * kABytes, &tmA, fb, ks * kStageRowBytes, a_row);
-        tma_load_2d(sB + s * b_bytes, &tmB, fb, ks * kStageRowBytes, tau * tile_m);
-        bulk_load(sSFA + s * kSfStageBytes, wsf + (size_t)4 * ks * kAtomBytes,
-                  (uint32_t)kk * kAtomBytes, fb);
-        bulk_load(sSFB + s * kSfStageBytes * S, bsf + (size_t)4 * ks * S * kAtomBytes,
-                  (uint32_t)kk * S * kAtomBytes, fb);
-        ++issued;
+      int it = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const int mt = u % tiles_w, tau = u / tiles_w;
+        const int e = p.tile_expert[tau];
+        const int a_row = e * p.rows_w + mt * kWTile;
+        const uint8_t* wsf = p.w_sf + ((size_t)e * tiles_w + mt) * KC * kAtomBytes;
+        const uint8_t* bsf = p.b_sf + (size_t)tau * KC * S * kAtomBytes;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % ST, round = it / ST;
+          if (round > 0 &&
+              !mbar_wait(smem_u32(&empty_bar[s]), (round - 1) & 1, &abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
+          const int kk = min(4, KC - 4 * ks);
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          mbar_arrive_expect_tx(fb, kABytes + b_bytes + (uint32_t)kk * kAtomBytes * (1 + S));
+          tma_load_2d(sA + s * kABytes, &tmA, fb, ks * kStageRowBytes, a_row);
+          tma_load_2d(sB + s * b_bytes, &tmB, fb, ks * kStageRowBytes, tau * tile_m);
+          bulk_load(sSFA + s * kSfStageBytes, wsf + (size_t)4 * ks * kAtomBytes,
+                    (uint32_t)kk * kAtomBytes, fb);
+          bulk_load(sSFB + s * kSfStageBytes * S, bsf + (size_t)4 * ks * S * kAtomBytes,
+                    (uint32_t)kk * S * kAtomBytes, fb);
+        }
       }
-      // Wait for the copies still in flight (normally all landed already).
-      for (int ks = max(0, issued - ST); ks < issued; ++ks)
-        mbar_wait_cleanup(smem_u32(&full_bar[ks % ST]), (ks / ST) & 1);
+      // Wait for the copies still in flight (normally all consumed already).
+      for (int j = max(0, it - ST); j < it; ++j)
+        mbar_wait_cleanup(smem_u32(&full_bar[j % ST]), (j / ST) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------ MMA issuer ----------------------------
     if (lane == 0) {
       const uint32_t idesc = idesc_nvf4(kWTile, (uint32_t)tile_m);
-      for (int ks = 0; ks < nks; ++ks) {
-        const int s = ks % ST, round = ks / ST;
-        if (!mbar_wait(smem_u32(&full_bar[s]), round & 1, &abort_flag, p.status)) break;
+      int it = 0, uc = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++uc) {
+        const int b = uc % NB, use = uc / NB;
+        if (use > 0 &&
+            !mbar_wait(smem_u32(&acce_bar[b]), (use - 1) & 1, &abort_flag, p.status))
+          break;
         tc_fence_after();
-        const int kk = min(4, KC - 4 * ks);
-        const uint32_t fa = t_sfa + s * 16, fbc = t_sfb + s * 16 * S;
-        const uint32_t sfa_smem = sSFA + s * kSfStageBytes;
-        const uint32_t sfb_smem = sSFB + s * kSfStageBytes * S;
-        for (int j = 0; j < kk; ++j) {
-          tc_copy_scale_atom(fa + 4 * j, smem_desc(sfa_smem + j * kAtomBytes, 0, 128, 0));
-          for (int sub = 0; sub < S; ++sub)
-            tc_copy_scale_atom(fbc + 4 * (j * S + sub),
-                               smem_desc(sfb_smem + (j * S + sub) * kAtomBytes, 0, 128, 0));
+        const uint32_t dacc = tmem + (uint32_t)(b * tile_m);
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % ST, round = it / ST;
+          if (!mbar_wait(smem_u32(&full_bar[s]), round & 1, &abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const int kk = min(4, KC - 4 * ks);
+          const uint32_t fa = t_sfa + s * 16, fbc = t_sfb + s * 16 * S;
+          const uint32_t sfa_smem = sSFA + s * kSfStageBytes;
+          const uint32_t sfb_smem = sSFB + s * kSfStageBytes * S;
+          for (int j = 0; j < kk; ++j) {
+            tc_copy_scale_atom(fa + 4 * j, smem_desc(sfa_smem + j * kAtomBytes, 0, 128, 0));
+            for (int sub = 0; sub < S; ++sub)
+              tc_copy_scale_atom(fbc + 4 * (j * S + sub),
+                                 smem_desc(sfb_smem + (j * S + sub) * kAtomBytes, 0, 128, 0));
+          }
+          for (int j = 0; j < kk; ++j) {
+            const uint64_t ad = smem_desc(sA + s * kABytes + 32 * j, 16, 1024, 2);
+            const uint64_t bd = smem_desc(sB + s * b_bytes + 32 * j, 16, 1024, 2);
+            tc_mma_nvf4(dacc, ad, bd, idesc, fa + 4 * j, fbc + 4 * j * S, (ks | j) != 0);
+          }
+          tc_commit(smem_u32(&empty_bar[s]));
         }
-        for (int j = 0; j < kk; ++j) {
-          const uint64_t ad = smem_desc(sA + s * kABytes + 32 * j, 16, 1024, 2);
-          const uint64_t bd = smem_desc(sB + s * b_bytes + 32 * j, 16, 1024, 2);
-          tc_mma_nvf4(tmem, ad, bd, idesc, fa + 4 * j, fbc + 4 * j * S, (ks | j) != 0);
-        }
-        tc_commit(smem_u32(&empty_bar[s]));
+        tc_commit(smem_u32(&accf_bar[b]));
       }
-      tc_commit(smem_u32(&acc_bar));
     }
     __syncwarp();
-  }
-
-  // ---------------- epilogue: TMEM -> registers -> global ----------------
-  const bool ok = mbar_wait(smem_u32(&acc_bar), 0, &abort_flag, p.status);
-  __syncwarp();  // the tcgen05.ld below are warp-collective
-  tc_fence_after();
-  if (ok && !abort_flag) {
-    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
-    const int row0 = tau * tile_m;
-    if (KIND == 1) {
-      const float sc = lane < 16 ? p.s0[e] : p.s1[e];
-      const float a2g = *p.a2_gscale;
-      const int I = p.out_cols, kco = I / 64;
-      const int kb = 4 * mt + warp;  // intermediate 16-block of this warp
-      for (int c0 = 0; c0 < tile_m; c0 += 16) {
-        float v[16];
-        tmem_ld16(taddr + c0, v);
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
+                   (warp - 2) * 32 * kEpiStride;
+    int uc = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+      const int b = uc % NB, use = uc / NB;
+      const bool ok = mbar_wait(smem_u32(&accf_bar[b]), use & 1, &abort_flag, p.status);
+      __syncwarp();
+      if (!ok) break;
+      tc_fence_after();
+      const int mt = u % tiles_w, tau = u / tiles_w;
+      const int e = p.tile_expert[tau];
+      const int row0 = tau * tile_m;
+      const uint32_t taddr = tmem + (uint32_t)(b * tile_m) + ((uint32_t)(32 * q) << 16);
+      if (KIND == 1) {
+        const float sc = lane < 16 ? p.s0[e] : p.s1[e];
+        const float a2g = *p.a2_gscale;
+        const int I = p.out_cols, kco = I / 64;
+        const int kb = 4 * mt + q;  // this quadrant's intermediate 16-block
+        for (int c0 = 0; c0 < tile_m; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + c0, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = row0 + c0 + i;
-          gemm1_column(v[i], sc, a2g, lane, p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * warp,
-                       p.hq_sf + act_sf_offset(r, kb, tile_m, kco, S));
+          for (int i = 0; i < 32; ++i) stage[i * kEpiStride + lane] = v[i] * sc;
+          __syncwarp();
+          // lane = route column: 16 gate values, then the 16 matching up values
+          float h[16];
+          const float* col = stage + lane * kEpiStride;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g = col[j], up = col[16 + j];
+            h[j] = g / (1.0f + expf(-g)) * up;
+          }
+          uint2 codes;
+          uint32_t sfc;
+          quant16(h, a2g, codes, sfc);
+          const int r = row0 + c0 + lane;
+          *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * q) = codes;
+          p.hq_sf[act_sf_offset(r, kb, tile_m, kco, S)] = static_cast<uint8_t>(sfc);
+          __syncwarp();
+        }
+      } else {
+        const float g2 = p.s0[e];
+        const int limit = p.tile_row_limit[tau];
+        const int colx = mt * kWTile + 32 * q + lane;
+        for (int c0 = 0; c0 < tile_m; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int r = row0 + c0 + i;
+            if (r < limit) p.rows[(size_t)r * p.out_cols + colx] = __float2bfloat16_rn(v[i] * g2);
+          }
         }
       }
-    } else {
-      const float g2 = p.s0[e];
-      const int limit = p.tile_row_limit[tau];
-      const int col = mt * kWTile + 32 * warp + lane;
-      for (int c0 = 0; c0 < tile_m; c0 += 16) {
-        float v[16];
-        tmem_ld16(taddr + c0, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = row0 + c0 + i;
-          if (r < limit) p.rows[(size_t)r * p.out_cols + col] = __float2bfloat16_rn(v[i] * g2);
-        }
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce_bar[b]));
     }
   }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    // Every MMA this CTA issued has completed once acc_bar has (it tracks all
-    // of them); normally this returns at once.
-    mbar_wait_cleanup(smem_u32(&acc_bar), 0);
+    // One more commit from the MMA thread tracks every tcgen05 op it issued
+    // (on a timeout too); once it lands no MMA or copy still uses TMEM.
+    if (lane == 0) {
+      tc_commit(smem_u32(&drain_bar));
+      mbar_wait_cleanup(smem_u32(&drain_bar), 0);
+    }
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
@@ -302,18 +383,32 @@ static CUresult encode_rows_map(CUtensorMap* map, const void* base, uint64_t row
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-constexpr int kStages = 4;
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 148;
+  return n;
+}
 
 template <int KIND>
-static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
                               int max_tiles, cudaStream_t stream) {
-  const size_t smem = gemm_smem_bytes(p.tile_m, p.S, kStages);
-  auto kern = grouped_gemm_kernel<KIND, kStages>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  p.stages = stages_for(p.tile_m);
+  p.acc_bufs = acc_bufs_for(p.tile_m);
+  const size_t smem = gemm_smem_bytes(p.tile_m, p.S);
+  auto kern = grouped_gemm_kernel<KIND>;
+  size_t most = 0;
+  for (int t : {32, 64, 128, 256}) {
+    const size_t b = gemm_smem_bytes(t, sf_atoms_per_tile(t));
+    most = b > most ? b : most;
+  }
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)most);
   if (err != cudaSuccess) return err;
-  dim3 grid(max_tiles, p.rows_w / kWTile);
-  kern<<<grid, 128, smem, stream>>>(ta, tb, p);
+  // One CTA per SM; CTAs past the live unit count exit at once.
+  const long long units = (long long)max_tiles * (p.rows_w / kWTile);
+  const int grid = (int)(units < sm_count() ? units : sm_count());
+  kern<<<grid, kThreads, smem, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }
 

@@ -140,8 +140,8 @@ cudaError_t launch_route_permute(const int32_t* topk_ids, int T, int K, int E, i
                                  int32_t* p2t, int32_t* tile_expert, int32_t* tile_row_limit,
                                  int32_t* totals, int32_t* status, cudaStream_t stream) {
   const size_t smem = route_smem_bytes(E);
-  cudaError_t err = cudaFuncSetAttribute(route_permute_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(route_permute_kernel),
+                                      (int)route_smem_bytes(1024));
   if (err != cudaSuccess) return err;
   route_permute_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, T, K, E, tile_m, P, MT,
                                                             counts, offsets, e2p, p2t, tile_expert,

@@ -10,6 +10,8 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
+    # measured errors are recorded as junit properties
+    config.option.junit_family = "xunit1"
 
 
 def pytest_collection_modifyitems(config, items):

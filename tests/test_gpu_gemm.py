@@ -114,7 +114,7 @@ def small_cases():
 
 
 @pytest.mark.parametrize("idx", range(len(SMALL)))
-def test_gemm2_on_identical_operands(small_cases, idx):
+def test_gemm2_on_identical_operands(small_cases, idx, record_property):
     w, raw, batch, tile, a1, a2 = small_cases[idx]
     er = olayer.expert_rows(batch["x"], batch["topk_ids"], raw, a1, a2, return_intermediate=True)
     prep = Prepared(raw)
@@ -128,11 +128,12 @@ def test_gemm2_on_identical_operands(small_cases, idx):
     rows = got["rows"][e2p[live]]
     want = er["rows_bf16"][live]
     err = rel_l2(rows, want)
+    record_property("gemm2_rel_l2", err)
     assert err < GEMM2_BAR, f"rel-L2 {err:.3g}; gpu {finite_summary(rows)}"
 
 
 @pytest.mark.parametrize("idx", range(len(SMALL)))
-def test_gemm1_intermediate_and_end_to_end(small_cases, idx):
+def test_gemm1_intermediate_and_end_to_end(small_cases, idx, record_property):
     w, raw, batch, tile, a1, a2 = small_cases[idx]
     ref = olayer.moe_layer(batch["x"], batch["topk_ids"], batch["topk_weights"], raw, a1, a2, raw["gamma"],
                            1e-6, tile, return_intermediate=True)
@@ -153,6 +154,8 @@ def test_gemm1_intermediate_and_end_to_end(small_cases, idx):
     err_rows = rel_l2(got["rows"][e2p[live]], ref["routes"]["rows_bf16"][live])
     assert err_rows < OUT_BAR, err_rows
     err = rel_l2(got["out"], ref["out"])
+    for k, v in (("sf_match", sf_match), ("code_match", code_match), ("rows_rel_l2", err_rows), ("out_rel_l2", err)):
+        record_property(k, float(v))
     assert err < OUT_BAR, f"out rel-L2 {err:.3g}; gpu {finite_summary(got['out'])}"
 
 
@@ -196,7 +199,7 @@ def full():
     return raw, Prepared(raw)
 
 
-def test_decode_b8_full_size(full):
+def test_decode_b8_full_size(full, record_property):
     raw, prep = full
     w = inputs.WORKLOADS["decode_b8"]
     a1, a2 = inputs.global_scales(w)
@@ -208,15 +211,19 @@ def test_decode_b8_full_size(full):
     e2p = got["e2p"].reshape(-1)
     err_rows = rel_l2(got["rows"][e2p], ref["routes"]["rows_bf16"])
     err = rel_l2(got["out"], ref["out"])
+    record_property("out_rel_l2", err)
+    record_property("rows_rel_l2", err_rows)
     assert err < OUT_BAR and err_rows < OUT_BAR, (err, err_rows)
     # GEMM2 alone on the oracle's intermediate
     P, _ = B.route_sizes(w.T, w.K, w.E, w.tile_m)
     hq = oracle_hq_permuted(ref["routes"], got["e2p"], P, w.I)
     same = run_gpu(prep, batch, w.tile_m, a1, a2, hq_override=hq, export=False)
-    assert rel_l2(same["rows"][e2p], ref["routes"]["rows_bf16"]) < GEMM2_BAR
+    err2 = rel_l2(same["rows"][e2p], ref["routes"]["rows_bf16"])
+    record_property("gemm2_rel_l2", err2)
+    assert err2 < GEMM2_BAR
 
 
-def test_decode_b64_zipf_full_size_sampled(full):
+def test_decode_b64_zipf_full_size_sampled(full, record_property):
     raw, prep = full
     w = inputs.WORKLOADS["decode_b64_zipf"]
     a1, a2 = inputs.global_scales(w)
@@ -226,36 +233,60 @@ def test_decode_b64_zipf_full_size_sampled(full):
     pick = np.array([0, 17, 63])
     ref = olayer.moe_layer(batch["x"][pick], batch["topk_ids"][pick], batch["topk_weights"][pick], raw, a1, a2,
                            raw["gamma"], 1e-6, w.tile_m)
-    assert rel_l2(got["out"][pick], ref["out"]) < OUT_BAR
+    err = rel_l2(got["out"][pick], ref["out"])
+    record_property("out_rel_l2", err)
+    assert err < OUT_BAR
 
 
-def test_expert_tp_identity(full):
-    """The expert_tp page: the K-partial GEMM2 rows of the tp = 8
-    intermediate slices (I' = 256), run one after another on this GPU and
-    summed in fp32 with one bf16 rounding, equal the full-width rows."""
+def test_expert_tp_identity(full, record_property):
+    """The expert_tp page: the GEMM2 rows of the tp = 8 intermediate slices
+    (I' = 256) are K-partials whose sum is the full-width row.
+
+    Exact part: with I' % 16 == 0 every requant block lies inside a slice, so
+    each slice's quantized intermediate (GEMM1 + SwiGLU + requant on the
+    slice's own prepared weights) equals, bit for bit, the same columns of
+    the full-width run's.
+
+    Rows part: the slices run one after another on this GPU and their bf16
+    partial rows are summed in fp32 with one bf16 rounding (the page's
+    probe_rel_l2). Each partial and the full-width row were rounded to bf16
+    once, so the difference is a sum of independent roundings of relative
+    size at most 2^-9 (RMS 2^-9/sqrt(3)); the bar is three times the RMS this
+    predicts from the rows themselves, and never above 1e-2."""
     raw, prep = full
     w = inputs.WORKLOADS["tp8_slice_b32"]
     a1, a2 = inputs.global_scales(w)
     batch = inputs.make_batch(w)
-    full_run = run_gpu(prep, batch, w.tile_m, a1, a2, export=False)
+    full_run = run_gpu(prep, batch, w.tile_m, a1, a2)
     e2p = full_run["e2p"].reshape(-1)
+    s = w.I // w.tp
     acc = np.zeros((len(e2p), w.H), dtype=np.float32)
+    sq_parts = 0.0
     for r in range(w.tp):
         sl = olayout.raw_slice(raw, r, w.tp)
-        part = run_gpu(Prepared(sl), batch, w.tile_m, a1, a2, export=False)
+        part = run_gpu(Prepared(sl), batch, w.tile_m, a1, a2)
         assert np.array_equal(part["e2p"], full_run["e2p"])
-        acc += part["rows"][e2p].astype(np.float32)
+        assert np.array_equal(part["hq_codes"][e2p], full_run["hq_codes"][e2p][:, r * s // 2:(r + 1) * s // 2])
+        assert np.array_equal(part["hq_sf"][e2p], full_run["hq_sf"][e2p][:, r * s // 16:(r + 1) * s // 16])
+        rows_r = part["rows"][e2p]
+        acc += rows_r.astype(np.float32)
+        sq_parts += float(np.sum(rows_r ** 2))
         torch.cuda.empty_cache()
     summed = codecs.round_to_bf16(acc.astype(np.float64))
-    assert rel_l2(summed, full_run["rows"][e2p]) < GEMM2_BAR
+    want = full_run["rows"][e2p]
+    sq_full = float(np.sum(want ** 2))
+    predicted = np.sqrt((sq_parts + 2.0 * sq_full) * 2.0**-18 / 3.0 / sq_full)
+    err = rel_l2(summed, want)
+    record_property("tp_sum_rel_l2", err)
+    record_property("tp_predicted_rms", float(predicted))
+    assert err < min(3.0 * predicted, OUT_BAR), (err, predicted)
     pick = np.array([0, 31])
     ref = olayer.expert_rows(batch["x"][pick], batch["topk_ids"][pick], raw, a1, a2)
-    sel = (np.arange(w.T * w.K) // w.K)
-    mask = np.isin(sel, pick)
+    mask = np.isin(np.arange(w.T * w.K) // w.K, pick)
     assert rel_l2(summed[mask], ref["rows_bf16"]) < OUT_BAR
 
 
-def test_prefill_t8192_sampled(full):
+def test_prefill_t8192_sampled(full, record_property):
     raw, prep = full
     w = inputs.WORKLOADS["prefill_t8192_zipf"]
     a1, a2 = inputs.global_scales(w)
@@ -266,4 +297,6 @@ def test_prefill_t8192_sampled(full):
     pick = np.array([0, 4095, 8191])
     ref = olayer.moe_layer(batch["x"][pick], batch["topk_ids"][pick], batch["topk_weights"][pick], raw, a1, a2,
                            raw["gamma"], 1e-6, w.tile_m)
-    assert rel_l2(got["out"][pick], ref["out"]) < OUT_BAR
+    err = rel_l2(got["out"][pick], ref["out"])
+    record_property("out_rel_l2", err)
+    assert err < OUT_BAR
