@@ -219,6 +219,40 @@ int moe_experts_import(int which, const void* codes, const void* scales,
                        int T, int H, int I, int E, int K, int tile_m,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* moe_nvfp4_experts without a workspace argument: it allocates nothing.
+ *
+ * The pages have no counterpart of this entry point. It exists for callers
+ * that cannot allocate device memory at the point of the call: code
+ * recorded into a CUDA graph capture (cudaMalloc is not allowed while a
+ * stream is being captured), latency-critical serving loops that must not
+ * reach the allocator (a cudaMalloc may synchronise the device), and
+ * plug-ins whose host framework owns all device memory and hands them
+ * none. Instead of a caller buffer it uses one fixed array of
+ * moe_noalloc_scratch_bytes() bytes (32 MiB) that the library defines in
+ * device memory; every GPU that loads the library holds that array until
+ * the process exits. Shapes whose workspace (moe_experts_workspace_size)
+ * is larger are refused with MOE_ERR_WORKSPACE before anything is enqueued;
+ * at H = 5120, I = 2048, E = 128, top-8, tile_m = 32 that admits up to 64
+ * tokens.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture. Every other argument, the outputs
+ * and the status word behave as in moe_nvfp4_experts, and the caller still
+ * owns x / a / a_sf, the routing metadata and gemm2_rows. All calls share
+ * the one array: two calls whose work overlaps on the GPU (different
+ * streams without ordering between them) race and give undefined results.
+ * Nothing in the array has to start at zero: every byte a call reads has
+ * been written earlier in the same call. */
+int moe_nvfp4_experts_noalloc(const moe_weights* w, const void* x, const void* a,
+                              const void* a_sf, const float* a1_gscale,
+                              const float* a2_gscale, const moe_route* r, int T,
+                              int H, int I, int E, int K, int tile_m,
+                              void* gemm2_rows, int32_t* status, void* stream);
+
+/* Size in bytes of the array moe_nvfp4_experts_noalloc uses. */
+size_t moe_noalloc_scratch_bytes(void);
+
 /* ------------------------------------------------------------------------
  * Post-expert finalize (step a7; the muse_moe_runner page,
  * MusePostExpertFinalize.__call__(unfinalized, out), _finalize_native,

@@ -86,6 +86,11 @@ _SIGNATURES = {
     "moe_experts_export": ([_I, _P, C.c_size_t, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_experts_import": ([_I, _P, _P, _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P], _I),
     "moe_post_expert_finalize": ([_P, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P], _I),
+    "moe_nvfp4_experts_noalloc": (
+        [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _P],
+        _I,
+    ),
+    "moe_noalloc_scratch_bytes": ([], C.c_size_t),
 }
 
 _lib = None
@@ -114,7 +119,7 @@ def declared_symbols() -> list[str]:
 
     with open(HEADER) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
 
 
 def _check(rc: int) -> None:
@@ -283,6 +288,26 @@ def experts_export(which: int, ws, *, T, H, I, E, K, tile_m, stream=None):
 def experts_import(which: int, codes, scales, ws, *, T, H, I, E, K, tile_m, stream=None):
     _check(load().moe_experts_import(which, _ptr(codes), _ptr(scales), T, H, I, E, K, tile_m, _ptr(ws),
                                      ws.numel(), _stream(stream)))
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load().moe_noalloc_scratch_bytes())
+
+
+def nvfp4_experts_noalloc(w: MoeWeights, route: Route, *, x=None, a=None, a_sf=None, a1_gscale, a2_gscale,
+                          T, H, I, E, K, gemm2_rows=None, status=None, stream=None):
+    """moe_nvfp4_experts on the library's own fixed device scratch array (no
+    workspace argument, nothing allocated by the call itself)."""
+    import torch
+
+    P, _ = route_sizes(T, K, E, route.tile_m)
+    if gemm2_rows is None:
+        gemm2_rows = torch.empty((max(P, 1), H), dtype=torch.bfloat16, device=route.totals.device)
+    rs = route.struct()
+    _check(load().moe_nvfp4_experts_noalloc(
+        C.byref(w), _ptr(x), _ptr(a), _ptr(a_sf), _ptr(a1_gscale), _ptr(a2_gscale), C.byref(rs),
+        T, H, I, E, K, route.tile_m, _ptr(gemm2_rows), _ptr(status), _stream(stream)))
+    return gemm2_rows
 
 
 def post_expert_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps: float,

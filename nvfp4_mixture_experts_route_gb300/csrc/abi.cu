@@ -136,6 +136,19 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace moe {
+// Record an error for moe_last_error() from another translation unit.
+int report_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
