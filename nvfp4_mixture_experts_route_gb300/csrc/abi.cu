@@ -77,7 +77,7 @@ int route_dims(int T, int K, int E, int tile_m, RouteDims* d) {
 // intermediate (codes row-major, scales as per-tile atoms; see quant.cu).
 struct WsLayout {
   size_t a_codes = 0, a_sf = 0, h_codes = 0, h_sf = 0, total = 0;
-  int P = 0, MT = 0, S = 0;
+  int P = 0, MT = 0;
 };
 
 int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
@@ -88,16 +88,16 @@ int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
     return fail(MOE_ERR_UNSUPPORTED, "hidden %d and intermediate %d must be multiples of 128", H, I);
   w->P = d.P;
   w->MT = d.MT;
-  w->S = moe::sf_atoms_per_tile(tile_m);
+  const size_t S = (size_t)moe::sf_atoms_per_tile(tile_m);
   size_t off = 0;
   w->a_codes = off;
   off = round_up(off + (size_t)d.P * (H / 2), 1024);
   w->a_sf = off;
-  off = round_up(off + (size_t)d.MT * (H / 64) * w->S * moe::kAtomBytes, 1024);
+  off = round_up(off + (size_t)d.MT * (H / 64) * S * moe::kAtomBytes, 1024);
   w->h_codes = off;
   off = round_up(off + (size_t)d.P * (I / 2), 1024);
   w->h_sf = off;
-  off = round_up(off + (size_t)d.MT * (I / 64) * w->S * moe::kAtomBytes, 1024);
+  off = round_up(off + (size_t)d.MT * (I / 64) * S * moe::kAtomBytes, 1024);
   w->total = off;
   return MOE_OK;
 }

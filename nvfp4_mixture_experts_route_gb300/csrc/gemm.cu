@@ -58,8 +58,9 @@ constexpr uint32_t kSfStageBytes = 4 * kAtomBytes;     // 4 K=64 steps
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
+constexpr int kEpiCols = 16;    // route columns per GEMM1 epilogue chunk
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
-constexpr uint32_t kEpiBytes = kEpiWarps * 32 * kEpiStride * 4;
+constexpr uint32_t kEpiBytes = kEpiWarps * kEpiCols * kEpiStride * 4;
 
 struct GemmParams {
   const uint8_t* w_sf;  // prepared scale atoms [E][rows_w/128][K/64][512]
@@ -77,26 +78,54 @@ struct GemmParams {
   int E, rows_w, K, tile_m, S, out_cols, stages, acc_bufs;
 };
 
-// Pipeline depth and accumulator buffers per route-tile size (1 CTA per SM).
-__host__ __device__ constexpr int stages_for(int tile_m) {
-  return tile_m <= 32 ? 8 : tile_m <= 64 ? 6 : tile_m <= 128 ? 5 : 3;
-}
+// Launch shape per route-tile size. Tiles of up to 64 rows run two CTAs per
+// SM: each CTA's tcgen05 copies and MMAs execute in order, and a second,
+// independent CTA fills the gaps (measured: about 1.8x on the b = 8 decode).
+// The pipeline depth is what the shared memory left for the CTA holds, and
+// tensor memory is split between the CTAs of an SM.
+__host__ __device__ constexpr int ctas_per_sm(int tile_m) { return tile_m <= 64 ? 2 : 1; }
 __host__ __device__ constexpr int acc_bufs_for(int tile_m) { return tile_m <= 128 ? 2 : 1; }
 
-__host__ __device__ constexpr uint32_t stage_bytes(int tile_m, int S) {
-  return kABytes + (uint32_t)tile_m * kStageRowBytes + kSfStageBytes * (uint32_t)(1 + S);
+__host__ __device__ constexpr int sf_atoms_for(int tile_m) { return (tile_m + 127) / 128; }
+
+__host__ __device__ constexpr uint32_t stage_bytes(int tile_m) {
+  return kABytes + (uint32_t)tile_m * kStageRowBytes +
+         kSfStageBytes * (uint32_t)(1 + sf_atoms_for(tile_m));
 }
 
-__host__ __device__ constexpr uint32_t tmem_cols_for(int tile_m, int S, int stages, int bufs) {
-  const int need = bufs * tile_m + stages * 16 * (1 + S);
+// Dynamic shared memory a CTA may take: 227 KB alone, or half of the SM's
+// 228 KB less the per-CTA reserve and static storage when two share an SM.
+constexpr int kSmemOneCta = 232448;
+constexpr int kSmemTwoCtas = 115456;
+
+__host__ __device__ constexpr int stages_for(int tile_m) {
+  const int budget = (ctas_per_sm(tile_m) == 2 ? kSmemTwoCtas : kSmemOneCta) - 1024 - (int)kEpiBytes;
+  const int st = budget / (int)stage_bytes(tile_m);
+  return st > kMaxStages ? kMaxStages : st;
+}
+
+__host__ __device__ constexpr uint32_t tmem_cols_for(int tile_m, int stages, int bufs) {
+  const int need = bufs * tile_m + stages * 16 * (1 + sf_atoms_for(tile_m));
   uint32_t c = 32;
   while ((int)c < need) c <<= 1;
   return c;
 }
 
-__host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m, int S) {
-  return 1024 + (size_t)stages_for(tile_m) * stage_bytes(tile_m, S) + kEpiBytes;
+__host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m) {
+  return 1024 + (size_t)stages_for(tile_m) * stage_bytes(tile_m) + kEpiBytes;
 }
+
+static_assert(stages_for(32) >= 4 && stages_for(64) >= 3 && stages_for(128) >= 5 &&
+                  stages_for(256) >= 3,
+              "pipeline too shallow");
+static_assert(tmem_cols_for(32, stages_for(32), 2) <= 256 &&
+                  tmem_cols_for(64, stages_for(64), 2) <= 256 &&
+                  tmem_cols_for(128, stages_for(128), 2) <= 512 &&
+                  tmem_cols_for(256, stages_for(256), 1) <= 512,
+              "tensor memory over budget");
+static_assert(gemm_smem_bytes(32) <= kSmemTwoCtas && gemm_smem_bytes(64) <= kSmemTwoCtas &&
+                  gemm_smem_bytes(128) <= kSmemOneCta && gemm_smem_bytes(256) <= kSmemOneCta,
+              "shared memory over budget");
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -170,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sEpi = sSFB + ST * kSfStageBytes * S;
   const int KC = p.K / 64;
   const int nks = (KC + 3) / 4;
-  const uint32_t ncols = tmem_cols_for(tile_m, S, ST, NB);
+  const uint32_t ncols = tmem_cols_for(tile_m, ST, NB);
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -253,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const int kk = min(4, KC - 4 * ks);
+          // Scale-factor addresses of the MMA must be 4-column aligned: each
+          // K=64 step gets its own 4-column group per operand.
           const uint32_t fa = t_sfa + s * 16, fbc = t_sfb + s * 16 * S;
           const uint32_t sfa_smem = sSFA + s * kSfStageBytes;
           const uint32_t sfb_smem = sSFB + s * kSfStageBytes * S;
@@ -277,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;  // TMEM lane quadrant of this warp
     float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
-                   (warp - 2) * 32 * kEpiStride;
+                   (warp - 2) * kEpiCols * kEpiStride;
     int uc = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
       const int b = uc % NB, use = uc / NB;
@@ -294,26 +325,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float a2g = *p.a2_gscale;
         const int I = p.out_cols, kco = I / 64;
         const int kb = 4 * mt + q;  // this quadrant's intermediate 16-block
-        for (int c0 = 0; c0 < tile_m; c0 += 32) {
-          float v[32];
-          tmem_ld32(taddr + c0, v);
+        for (int c0 = 0; c0 < tile_m; c0 += kEpiCols) {
+          float v[kEpiCols];
+          tmem_ld16(taddr + c0, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) stage[i * kEpiStride + lane] = v[i] * sc;
+          for (int i = 0; i < kEpiCols; ++i) stage[i * kEpiStride + lane] = v[i] * sc;
           __syncwarp();
-          // lane = route column: 16 gate values, then the 16 matching up values
-          float h[16];
-          const float* col = stage + lane * kEpiStride;
+          if (lane < kEpiCols) {
+            // lane = route column: 16 gate values, then the 16 matching up values
+            float h[16];
+            const float* col = stage + lane * kEpiStride;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g = col[j], up = col[16 + j];
-            h[j] = g / (1.0f + expf(-g)) * up;
+            for (int j = 0; j < 16; ++j) {
+              const float g = col[j], up = col[16 + j];
+              h[j] = g / (1.0f + expf(-g)) * up;
+            }
+            uint2 codes;
+            uint32_t sfc;
+            quant16(h, a2g, codes, sfc);
+            const int r = row0 + c0 + lane;
+            *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * q) = codes;
+            p.hq_sf[act_sf_offset(r, kb, tile_m, kco, S)] = static_cast<uint8_t>(sfc);
           }
-          uint2 codes;
-          uint32_t sfc;
-          quant16(h, a2g, codes, sfc);
-          const int r = row0 + c0 + lane;
-          *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * q) = codes;
-          p.hq_sf[act_sf_offset(r, kb, tile_m, kco, S)] = static_cast<uint8_t>(sfc);
           __syncwarp();
         }
       } else {
@@ -396,18 +429,19 @@ static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
                               int max_tiles, cudaStream_t stream) {
   p.stages = stages_for(p.tile_m);
   p.acc_bufs = acc_bufs_for(p.tile_m);
-  const size_t smem = gemm_smem_bytes(p.tile_m, p.S);
+  const size_t smem = gemm_smem_bytes(p.tile_m);
   auto kern = grouped_gemm_kernel<KIND>;
   size_t most = 0;
   for (int t : {32, 64, 128, 256}) {
-    const size_t b = gemm_smem_bytes(t, sf_atoms_per_tile(t));
+    const size_t b = gemm_smem_bytes(t);
     most = b > most ? b : most;
   }
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)most);
   if (err != cudaSuccess) return err;
-  // One CTA per SM; CTAs past the live unit count exit at once.
+  // ctas_per_sm CTAs per SM; CTAs past the live unit count exit at once.
   const long long units = (long long)max_tiles * (p.rows_w / kWTile);
-  const int grid = (int)(units < sm_count() ? units : sm_count());
+  const long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
+  const int grid = (int)(units < slots ? units : slots);
   kern<<<grid, kThreads, smem, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }

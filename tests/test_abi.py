@@ -38,6 +38,7 @@ def test_workspace_size_formula(lib):
     def up(v):
         return (v + 1023) // 1024 * 1024
 
+    # codes row-major; scales as one 512-byte atom per K=64 step per 128 rows of a tile
     want = up(P * H // 2) + up(MT * (H // 64) * 512) + up(P * I // 2) + up(MT * (I // 64) * 512)
     assert B.experts_workspace_size(T, K, E, H, I, tm) == want
 
