@@ -211,7 +211,10 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H,
  * uint8 [max_padded_rows, H/2], scales e4m3 [max_padded_rows, H/16]),
  * which = 1 for the intermediate hq ([max_padded_rows, I/2] and
  * [max_padded_rows, I/16]). moe_experts_import followed by
- * moe_experts_gemm2 runs GEMM2 on a given intermediate. */
+ * moe_experts_gemm2 runs GEMM2 on a given intermediate. In the activations,
+ * padding rows (permuted_to_token == -1) have zero scales and unspecified
+ * codes, which contribute exactly zero to every product; rows past
+ * totals[1] are unspecified. */
 int moe_experts_export(int which, const void* ws, size_t ws_bytes, int T,
                        int H, int I, int E, int K, int tile_m, void* codes,
                        void* scales, void* stream);
@@ -272,6 +275,56 @@ int moe_post_expert_finalize(const void* rows,
                              const float* topk_weights, const void* gamma,
                              float eps, int weight_before_norm, int T, int K,
                              int H, void* out, void* stream);
+
+/* Expert-TP tail (the expert_tp page: with expert tensor parallelism every
+ * rank computes K-partial GEMM2 rows over its intermediate slice, and they
+ * are summed -- "FP32 sum, one BF16 rounding" -- before the per-route norm;
+ * the muse_moe_runner page's TP finalize fuses that sum into the norm).
+ * rows_parts is a HOST array of nparts (1..16) device pointers to bf16
+ * [*, H] row buffers indexed alike; each route's row is
+ * bf16(sum_r float(part_r[p])) and then finalized exactly as
+ * moe_post_expert_finalize does. With nparts = 1 it equals
+ * moe_post_expert_finalize. */
+int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts,
+                                const int32_t* expanded_to_permuted,
+                                const float* topk_weights, const void* gamma,
+                                float eps, int weight_before_norm, int T, int K,
+                                int H, void* out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Steps that feed the block (the model page, MuseSpark1xMoE).
+ * ---------------------------------------------------------------------- */
+
+/* MuseSpark1x routing from fp32 router logits [T, E] (fused_musespark1x_routing:
+ * sigmoid scores, an fp32 expert bias [E] that only steers the choice,
+ * sum-renormalised weights with division eps, route_scale; no groups):
+ *   s = sigmoid(logits); chosen = the K largest s + bias, the lower expert
+ *   index first on equal values; w = s[chosen] / (sum + eps) * route_scale.
+ * topk_ids int32 [T, K] in choice order, topk_weights fp32 [T, K]. Tokens
+ * with is_padding[t] != 0 (optional uint8 [T]) get ids -1 and weights 0.
+ * E <= 1024, K <= min(32, E). */
+int moe_musespark1x_routing(const float* logits, const float* expert_bias,
+                            const uint8_t* is_padding, int T, int E, int K,
+                            float route_scale, float eps, int32_t* topk_ids,
+                            float* topk_weights, void* stream);
+
+/* Pre-expert RMSNorm fused into the NVFP4 input quantization
+ * (norm_quant_trtllm_nvfp4; the norm's weight applied after normalising):
+ *   y = x / sqrt(mean(x^2) + eps) * (1 + gamma),  (a, a_sf) = NVFP4(y, gscale)
+ * x bf16 [T, H], gamma bf16 [H] (zero-centred), gscale device fp32 [1];
+ * y stays fp32 and is quantized like moe_experts_quantize. Outputs a uint8
+ * [T, H/2] and a_sf e4m3 [T, H/16] row-major (scaled_fp4_quant's layout). */
+int moe_rmsnorm_nvfp4_quant(const void* x, const void* gamma, float eps,
+                            const float* gscale, int T, int H, void* a,
+                            void* a_sf, void* stream);
+
+/* The same, written straight into the expert body's workspace in permuted
+ * order: a drop-in replacement for moe_experts_quantize when the block's
+ * input is the pooled, not yet normalised activation. */
+int moe_experts_norm_quantize(const void* x, const void* gamma, float eps,
+                              const float* a1_gscale, const moe_route* r, int T,
+                              int H, int I, int E, int K, int tile_m, void* ws,
+                              size_t ws_bytes, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

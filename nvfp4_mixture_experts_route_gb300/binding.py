@@ -91,6 +91,12 @@ _SIGNATURES = {
         _I,
     ),
     "moe_noalloc_scratch_bytes": ([], C.c_size_t),
+    "moe_post_expert_finalize_tp": (
+        [C.POINTER(C.c_void_p), _I, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P], _I),
+    "moe_musespark1x_routing": ([_P, _P, _P, _I, _I, _I, C.c_float, C.c_float, _P, _P, _P], _I),
+    "moe_rmsnorm_nvfp4_quant": ([_P, _P, C.c_float, _P, _I, _I, _P, _P, _P], _I),
+    "moe_experts_norm_quantize": (
+        [_P, _P, C.c_float, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P], _I),
 }
 
 _lib = None
@@ -322,3 +328,54 @@ def post_expert_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps: f
         _ptr(rows), _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
         1 if weight_before_norm else 0, T, K, H, _ptr(out), _stream(stream)))
     return out
+
+
+def post_expert_finalize_tp(row_parts, expanded_to_permuted, topk_weights, gamma, eps: float,
+                            weight_before_norm: bool = True, out=None, stream=None):
+    """Finalize from tp K-partial row buffers (summed in fp32, one bf16
+    rounding, before the norm)."""
+    import torch
+
+    T, K = expanded_to_permuted.shape
+    H = gamma.numel()
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=gamma.device)
+    arr = (C.c_void_p * len(row_parts))(*[r.data_ptr() for r in row_parts])
+    _check(load().moe_post_expert_finalize_tp(
+        arr, len(row_parts), _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
+        1 if weight_before_norm else 0, T, K, H, _ptr(out), _stream(stream)))
+    return out
+
+
+def musespark1x_routing(logits, expert_bias, top_k: int, route_scale: float = 1.0, eps: float = 1e-15,
+                        is_padding=None, topk_ids=None, topk_weights=None, stream=None):
+    import torch
+
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    _check(load().moe_musespark1x_routing(_ptr(logits), _ptr(expert_bias), _ptr(is_padding), T, E, top_k,
+                                          float(route_scale), float(eps), _ptr(topk_ids), _ptr(topk_weights),
+                                          _stream(stream)))
+    return topk_ids, topk_weights
+
+
+def rmsnorm_nvfp4_quant(x, gamma, eps: float, gscale, stream=None):
+    import torch
+
+    T, H = x.shape
+    a = torch.empty((T, H // 2), dtype=torch.uint8, device=x.device)
+    a_sf = torch.empty((T, H // 16), dtype=torch.uint8, device=x.device)
+    _check(load().moe_rmsnorm_nvfp4_quant(_ptr(x), _ptr(gamma), float(eps), _ptr(gscale), T, H, _ptr(a),
+                                          _ptr(a_sf), _stream(stream)))
+    return a, a_sf
+
+
+def experts_norm_quantize(route: Route, ws, *, x, gamma, eps: float, a1_gscale, T, H, I, E, K, status=None,
+                          stream=None):
+    rs = route.struct()
+    _check(load().moe_experts_norm_quantize(_ptr(x), _ptr(gamma), float(eps), _ptr(a1_gscale), C.byref(rs), T,
+                                            H, I, E, K, route.tile_m, _ptr(ws), ws.numel(), _ptr(status),
+                                            _stream(stream)))

@@ -21,6 +21,14 @@ cudaError_t launch_prepare_weights(const void*, const void*, const void*, const 
                                    int, void*, void*, void*, void*, cudaStream_t);
 cudaError_t launch_finalize(const void*, const int32_t*, const float*, const void*, float, int,
                             int, int, int, void*, cudaStream_t);
+cudaError_t launch_finalize_parts(const void* const*, int, const int32_t*, const float*, const void*,
+                                  float, int, int, int, int, void*, cudaStream_t);
+cudaError_t launch_musespark1x_routing(const float*, const float*, const uint8_t*, int, int, int, float,
+                                       float, int32_t*, float*, cudaStream_t);
+cudaError_t launch_rmsnorm_nvfp4(const void*, const void*, float, const float*, int, int, void*, void*,
+                                 cudaStream_t);
+cudaError_t launch_rmsnorm_nvfp4_permuted(const void*, const void*, float, const float*, const int32_t*,
+                                          const int32_t*, int, int, int, uint8_t*, uint8_t*, cudaStream_t);
 int launch_gemm1(const void*, const void*, const float*, const float*, const float*,
                  const int32_t*, const int32_t*, const int32_t*, const uint8_t*, const uint8_t*,
                  uint8_t*, uint8_t*, int, int, int, int, int, int, int32_t*, cudaStream_t,
@@ -354,6 +362,74 @@ int moe_post_expert_finalize(const void* rows, const int32_t* expanded_to_permut
   cudaError_t err = moe::launch_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps,
                                          weight_before_norm, T, K, H, out, as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize");
+}
+
+int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts,
+                                const int32_t* expanded_to_permuted, const float* topk_weights,
+                                const void* gamma, float eps, int weight_before_norm, int T, int K,
+                                int H, void* out, void* stream) {
+  if (T < 0 || K < 1 || H < 8 || H % 8 || H > 16384)
+    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d", T, K, H);
+  if (nparts < 1 || nparts > 16) return fail(MOE_ERR_UNSUPPORTED, "nparts %d not in [1, 16]", nparts);
+  if (T == 0) return MOE_OK;
+  if (!rows_parts || !expanded_to_permuted || !topk_weights || !gamma || !out)
+    return fail(MOE_ERR_INVALID_ARG, "finalize pointer is null");
+  for (int i = 0; i < nparts; ++i)
+    if (!rows_parts[i] || !aligned(rows_parts[i], 16))
+      return fail(MOE_ERR_INVALID_ARG, "row part %d is null or not 16-byte aligned", i);
+  if (!aligned(gamma, 16) || !aligned(out, 16))
+    return fail(MOE_ERR_INVALID_ARG, "gamma / out must be 16-byte aligned");
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  cudaError_t err = moe::launch_finalize_parts(rows_parts, nparts, expanded_to_permuted, topk_weights, gamma,
+                                               eps, weight_before_norm, T, K, H, out, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize_tp");
+}
+
+int moe_musespark1x_routing(const float* logits, const float* expert_bias, const uint8_t* is_padding, int T,
+                            int E, int K, float route_scale, float eps, int32_t* topk_ids,
+                            float* topk_weights, void* stream) {
+  if (T < 0 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E)
+    return fail(MOE_ERR_INVALID_ARG, "bad routing shape T=%d E=%d K=%d (E <= 1024, K <= min(32, E))", T,
+                E, K);
+  if (T == 0) return MOE_OK;
+  if (!logits || !expert_bias || !topk_ids || !topk_weights)
+    return fail(MOE_ERR_INVALID_ARG, "routing pointer is null");
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  cudaError_t err = moe::launch_musespark1x_routing(logits, expert_bias, is_padding, T, E, K, route_scale, eps,
+                                                    topk_ids, topk_weights, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_musespark1x_routing");
+}
+
+int moe_rmsnorm_nvfp4_quant(const void* x, const void* gamma, float eps, const float* gscale, int T, int H,
+                            void* a, void* a_sf, void* stream) {
+  if (T < 0 || H < 16 || H % 16) return fail(MOE_ERR_INVALID_ARG, "bad shape T=%d H=%d", T, H);
+  if (T == 0) return MOE_OK;
+  if (!x || !gamma || !gscale || !a || !a_sf) return fail(MOE_ERR_INVALID_ARG, "pointer is null");
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(a, 8))
+    return fail(MOE_ERR_INVALID_ARG, "x / gamma must be 16-byte and a 8-byte aligned");
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  cudaError_t err = moe::launch_rmsnorm_nvfp4(x, gamma, eps, gscale, T, H, a, a_sf, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_rmsnorm_nvfp4_quant");
+}
+
+int moe_experts_norm_quantize(const void* x, const void* gamma, float eps, const float* a1_gscale,
+                              const moe_route* r, int T, int H, int I, int E, int K, int tile_m, void* ws,
+                              size_t ws_bytes, int32_t* status, void* stream) {
+  (void)status;
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L)) || (rc = check_route(r))) return rc;
+  if (L.P == 0) return MOE_OK;
+  if (!x || !gamma || !a1_gscale) return fail(MOE_ERR_INVALID_ARG, "x / gamma / a1_gscale is null");
+  if (!aligned(x, 16) || !aligned(gamma, 16))
+    return fail(MOE_ERR_INVALID_ARG, "x and gamma must be 16-byte aligned");
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  cudaError_t err = moe::launch_rmsnorm_nvfp4_permuted(x, gamma, eps, a1_gscale, r->permuted_to_token,
+                                                       r->totals, H, tile_m, L.P, base + L.a_codes,
+                                                       base + L.a_sf, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_norm_quantize");
 }
 
 }  // extern "C"

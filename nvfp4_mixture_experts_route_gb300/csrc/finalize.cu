@@ -16,12 +16,43 @@ namespace moe {
 constexpr int kFinThreads = 256;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kFinChunk = 8;  // most routes per chunk (fewer for wide rows)
+constexpr int kMaxParts = 16;  // K-partial row buffers the expert-TP tail sums
+
+// The GEMM2 rows, or the expert-TP tail's tp K-partial row buffers: a row is
+// bf16(sum over parts, in fp32) -- the expert_tp page's "FP32 sum, one BF16
+// rounding" -- before the norm; with one part it is read as is.
+struct RowParts {
+  const __nv_bfloat16* p[kMaxParts];
+  int n;
+};
+
+__device__ __forceinline__ uint4 load_row_vec(const RowParts& parts, size_t off) {
+  if (parts.n == 1) return *reinterpret_cast<const uint4*>(parts.p[0] + off);
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+  for (int r = 0; r < parts.n; ++r) {
+    const uint4 u = *reinterpret_cast<const uint4*>(parts.p[r] + off);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      acc[2 * q] += f.x;
+      acc[2 * q + 1] += f.y;
+    }
+  }
+  uint4 o;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+  return o;
+}
 
 // VPT: 8-element vectors per thread (ceil(H / 8 / 256)) and CH: routes per
 // chunk, templates so that the per-thread arrays stay in registers.
 template <int VPT, int CH>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
-    const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ e2p,
+    const RowParts rows, const int32_t* __restrict__ e2p,
     const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
     int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out) {
   __shared__ float red[kFinWarps][CH];
@@ -60,9 +91,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = threadIdx.x + i * kFinThreads;
-        raw[c][i] = (pr[c] >= 0 && v < nvec)
-                        ? *reinterpret_cast<const uint4*>(rows + (size_t)pr[c] * H + 8 * v)
-                        : make_uint4(0, 0, 0, 0);
+        raw[c][i] = (pr[c] >= 0 && v < nvec) ? load_row_vec(rows, (size_t)pr[c] * H + 8 * v)
+                                              : make_uint4(0, 0, 0, 0);
       }
     }
     float ss[CH];
@@ -124,12 +154,16 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
   }
 }
 
-cudaError_t launch_finalize(const void* rows, const int32_t* e2p, const float* w,
-                            const void* gamma, float eps, int weight_before_norm, int T, int K,
-                            int H, void* out, cudaStream_t stream) {
+cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const int32_t* e2p,
+                                  const float* w, const void* gamma, float eps,
+                                  int weight_before_norm, int T, int K, int H, void* out,
+                                  cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
+  if (nparts < 1 || nparts > kMaxParts) return cudaErrorInvalidValue;
+  RowParts rp{};
+  rp.n = nparts;
+  for (int i = 0; i < nparts; ++i) rp.p[i] = reinterpret_cast<const __nv_bfloat16*>(parts[i]);
   const int vpt = ceil_div(H / 8, kFinThreads);
-  auto rp = reinterpret_cast<const __nv_bfloat16*>(rows);
   auto gp = reinterpret_cast<const __nv_bfloat16*>(gamma);
   auto op = reinterpret_cast<__nv_bfloat16*>(out);
 #define MOE_FIN_CASE(n)                                                                     \
@@ -153,4 +187,13 @@ cudaError_t launch_finalize(const void* rows, const int32_t* e2p, const float* w
   return cudaGetLastError();
 }
 
+}  // namespace moe
+
+namespace moe {
+cudaError_t launch_finalize(const void* rows, const int32_t* e2p, const float* w, const void* gamma,
+                            float eps, int weight_before_norm, int T, int K, int H, void* out,
+                            cudaStream_t stream) {
+  const void* parts[1] = {rows};
+  return launch_finalize_parts(parts, 1, e2p, w, gamma, eps, weight_before_norm, T, K, H, out, stream);
+}
 }  // namespace moe

@@ -58,9 +58,13 @@ constexpr uint32_t kSfStageBytes = 4 * kAtomBytes;     // 4 K=64 steps
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
-constexpr int kEpiCols = 16;    // route columns per GEMM1 epilogue chunk
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
-constexpr uint32_t kEpiBytes = kEpiWarps * kEpiCols * kEpiStride * 4;
+// GEMM1 epilogue staging: route columns per chunk (32 when a CTA has the SM
+// to itself, 16 when two share it) and the shared memory it takes.
+__host__ __device__ constexpr int epi_cols_for(int ctas) { return ctas == 2 ? 16 : 32; }
+__host__ __device__ constexpr uint32_t epi_bytes_for(int cols) {
+  return kEpiWarps * cols * kEpiStride * 4;
+}
 
 struct GemmParams {
   const uint8_t* w_sf;  // prepared scale atoms [E][rows_w/128][K/64][512]
@@ -99,7 +103,8 @@ constexpr int kSmemOneCta = 232448;
 constexpr int kSmemTwoCtas = 115456;
 
 __host__ __device__ constexpr int stages_for(int tile_m) {
-  const int budget = (ctas_per_sm(tile_m) == 2 ? kSmemTwoCtas : kSmemOneCta) - 1024 - (int)kEpiBytes;
+  const int budget = (ctas_per_sm(tile_m) == 2 ? kSmemTwoCtas : kSmemOneCta) - 1024 -
+                     (int)epi_bytes_for(epi_cols_for(ctas_per_sm(tile_m)));
   const int st = budget / (int)stage_bytes(tile_m);
   return st > kMaxStages ? kMaxStages : st;
 }
@@ -112,7 +117,8 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int tile_m, int stages, int
 }
 
 __host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m) {
-  return 1024 + (size_t)stages_for(tile_m) * stage_bytes(tile_m) + kEpiBytes;
+  return 1024 + (size_t)stages_for(tile_m) * stage_bytes(tile_m) +
+         epi_bytes_for(epi_cols_for(ctas_per_sm(tile_m)));
 }
 
 static_assert(stages_for(32) >= 4 && stages_for(64) >= 3 && stages_for(128) >= 5 &&
@@ -168,6 +174,40 @@ __device__ __forceinline__ void quant16(const float (&v)[16], float g, uint2& co
       hi |= f32x2_to_e2m1x2(v[8 + i] * inv, v[9 + i] * inv) << (4 * i);
   }
   codes = make_uint2(lo, hi);
+}
+
+// GEMM1 epilogue for COLS route columns of one accumulator: lanes write
+// scale * acc (gate rows 0-15, up rows 16-31 of this quadrant) to the warp's
+// staging rows, then each of the first COLS lanes takes one route column:
+// SwiGLU over its 16 intermediate columns and one NVFP4 block.
+template <int COLS>
+__device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stage, int lane, float sc,
+                                                     float a2g, int r0, int I, int mt, int q,
+                                                     int tile_m, int S, uint8_t* hq, uint8_t* hq_sf) {
+  float v[COLS];
+  if (COLS == 32)
+    tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(v));
+  else
+    tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(v));
+#pragma unroll
+  for (int i = 0; i < COLS; ++i) stage[i * kEpiStride + lane] = v[i] * sc;
+  __syncwarp();
+  if (lane < COLS) {
+    float h[16];
+    const float* col = stage + lane * kEpiStride;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = col[j], up = col[16 + j];
+      h[j] = g / (1.0f + expf(-g)) * up;
+    }
+    uint2 codes;
+    uint32_t sfc;
+    quant16(h, a2g, codes, sfc);
+    const int r = r0 + lane;
+    *reinterpret_cast<uint2*>(hq + (size_t)r * (I / 2) + 32 * mt + 8 * q) = codes;
+    hq_sf[act_sf_offset(r, 4 * mt + q, tile_m, I / 64, S)] = static_cast<uint8_t>(sfc);
+  }
+  __syncwarp();
 }
 
 template <int KIND>
@@ -307,8 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;  // TMEM lane quadrant of this warp
+    // this warp's staging rows: epi_cols_for(...) route columns of 33 floats
     float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
-                   (warp - 2) * kEpiCols * kEpiStride;
+                   (warp - 2) * epi_cols_for(ctas_per_sm(tile_m)) * kEpiStride;
     int uc = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
       const int b = uc % NB, use = uc / NB;
@@ -323,31 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (KIND == 1) {
         const float sc = lane < 16 ? p.s0[e] : p.s1[e];
         const float a2g = *p.a2_gscale;
-        const int I = p.out_cols, kco = I / 64;
-        const int kb = 4 * mt + q;  // this quadrant's intermediate 16-block
-        for (int c0 = 0; c0 < tile_m; c0 += kEpiCols) {
-          float v[kEpiCols];
-          tmem_ld16(taddr + c0, v);
-#pragma unroll
-          for (int i = 0; i < kEpiCols; ++i) stage[i * kEpiStride + lane] = v[i] * sc;
-          __syncwarp();
-          if (lane < kEpiCols) {
-            // lane = route column: 16 gate values, then the 16 matching up values
-            float h[16];
-            const float* col = stage + lane * kEpiStride;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g = col[j], up = col[16 + j];
-              h[j] = g / (1.0f + expf(-g)) * up;
-            }
-            uint2 codes;
-            uint32_t sfc;
-            quant16(h, a2g, codes, sfc);
-            const int r = row0 + c0 + lane;
-            *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * q) = codes;
-            p.hq_sf[act_sf_offset(r, kb, tile_m, kco, S)] = static_cast<uint8_t>(sfc);
-          }
-          __syncwarp();
+        const int I = p.out_cols;
+        const int cols = epi_cols_for(ctas_per_sm(tile_m));
+        for (int c0 = 0; c0 < tile_m; c0 += cols) {
+          if (cols == 32)
+            gemm1_epilogue_chunk<32>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
+                                     p.hq, p.hq_sf);
+          else
+            gemm1_epilogue_chunk<16>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
+                                     p.hq, p.hq_sf);
         }
       } else {
         const float g2 = p.s0[e];

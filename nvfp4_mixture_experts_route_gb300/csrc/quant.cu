@@ -39,7 +39,9 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
 }
 
 // One thread per (permuted row, 16-element block); rows past totals[1] are
-// left alone, padding rows get zero codes and scales.
+// left alone. Padding rows only get zero scales: with a zero block scale the
+// codes (always finite e2m1 values) contribute exactly 0 to every product,
+// so their bytes need not be written.
 __global__ void __launch_bounds__(256) quantize_permute_kernel(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
         sfc = a_sf_in[(size_t)t * nb + b];
       }
     }
-    *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = make_uint2(lo, hi);
+    if (t >= 0) *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = make_uint2(lo, hi);
     scales[act_sf_offset(p, b, tile_m, H / 64, S)] = static_cast<uint8_t>(sfc);
   }
 }

@@ -138,7 +138,7 @@ def test_quantize_permute_bit_exact(T, H, E, K, tile, g, scale):
     pad = np.nonzero(p2t[:total] < 0)[0]
     assert np.array_equal(scales[live], want_sf[p2t[live]])
     assert np.array_equal(canon_packed(codes[live]), canon_packed(want_packed[p2t[live]]))
-    assert not codes[pad].any() and not scales[pad].any()
+    assert not scales[pad].any()  # padding rows: zero scales (their codes are not written)
 
 
 def test_quantize_prequantized_input_is_a_gather():
