@@ -387,12 +387,17 @@ def main() -> None:
     ap.add_argument("--copies", type=int, default=4)
     ap.add_argument("--cpu-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-m", type=int, default=0, help="route tile rows (default: the workload's)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps one by one instead of replaying CUDA graphs")
     args = ap.parse_args()
     from nvfp4_mixture_experts_route_gb300 import inputs
 
     w = inputs.WORKLOADS[args.workload]
+    if args.tile_m:
+        import dataclasses
+
+        w = dataclasses.replace(w, tile_m=args.tile_m)
     if args.impl == "reference":
         run_reference(args, w)
     else:
