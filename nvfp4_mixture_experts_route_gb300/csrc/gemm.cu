@@ -61,7 +61,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
 // GEMM1 epilogue staging: route columns per chunk (32 when a CTA has the SM
 // to itself, 16 when two share it) and the shared memory it takes.
-__host__ __device__ constexpr int epi_cols_for(int ctas) { return ctas == 2 ? 16 : 32; }
+__host__ __device__ constexpr int epi_cols_for(int ctas) { return ctas >= 2 ? 16 : 32; }
 __host__ __device__ constexpr uint32_t epi_bytes_for(int cols) {
   return kEpiWarps * cols * kEpiStride * 4;
 }
@@ -82,12 +82,16 @@ struct GemmParams {
   int E, rows_w, K, tile_m, S, out_cols, stages, acc_bufs;
 };
 
-// Launch shape per route-tile size. Tiles of up to 64 rows run two CTAs per
-// SM: each CTA's tcgen05 copies and MMAs execute in order, and a second,
-// independent CTA fills the gaps (measured: about 1.8x on the b = 8 decode).
-// The pipeline depth is what the shared memory left for the CTA holds, and
-// tensor memory is split between the CTAs of an SM.
-__host__ __device__ constexpr int ctas_per_sm(int tile_m) { return tile_m <= 64 ? 2 : 1; }
+// Launch shape per route-tile size. Each CTA's tcgen05 scale copies and MMAs
+// execute in order, so several independent CTAs per SM overlap their streams:
+// 32-row tiles (decode) run three CTAs per SM, 64-row tiles two, larger tiles
+// one (measured on the b = 8 decode: GEMM1 254 us with one CTA per SM, 136 us
+// with two, about 14% less again with three). The pipeline depth is what the
+// shared memory left for the CTA holds, and tensor memory is split between
+// the CTAs of an SM.
+__host__ __device__ constexpr int ctas_per_sm(int tile_m) {
+  return tile_m <= 32 ? 3 : tile_m <= 64 ? 2 : 1;
+}
 __host__ __device__ constexpr int acc_bufs_for(int tile_m) { return tile_m <= 128 ? 2 : 1; }
 
 __host__ __device__ constexpr int sf_atoms_for(int tile_m) { return (tile_m + 127) / 128; }
@@ -97,13 +101,16 @@ __host__ __device__ constexpr uint32_t stage_bytes(int tile_m) {
          kSfStageBytes * (uint32_t)(1 + sf_atoms_for(tile_m));
 }
 
-// Dynamic shared memory a CTA may take: 227 KB alone, or half of the SM's
-// 228 KB less the per-CTA reserve and static storage when two share an SM.
-constexpr int kSmemOneCta = 232448;
-constexpr int kSmemTwoCtas = 115456;
+// Dynamic shared memory a CTA may take: 227 KB alone, otherwise its share of
+// the SM's 228 KB less the per-CTA reserve and static storage. Tensor-memory
+// columns a CTA may allocate: 512 / CTAs per SM, a power of two.
+__host__ __device__ constexpr int smem_budget(int ctas) {
+  return ctas == 1 ? 232448 : ctas == 2 ? 115456 : 76400;
+}
+__host__ __device__ constexpr int tmem_budget(int ctas) { return ctas == 1 ? 512 : ctas == 2 ? 256 : 128; }
 
 __host__ __device__ constexpr int stages_for(int tile_m) {
-  const int budget = (ctas_per_sm(tile_m) == 2 ? kSmemTwoCtas : kSmemOneCta) - 1024 -
+  const int budget = smem_budget(ctas_per_sm(tile_m)) - 1024 -
                      (int)epi_bytes_for(epi_cols_for(ctas_per_sm(tile_m)));
   const int st = budget / (int)stage_bytes(tile_m);
   return st > kMaxStages ? kMaxStages : st;
@@ -121,16 +128,18 @@ __host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m) {
          epi_bytes_for(epi_cols_for(ctas_per_sm(tile_m)));
 }
 
-static_assert(stages_for(32) >= 4 && stages_for(64) >= 3 && stages_for(128) >= 5 &&
+static_assert(stages_for(32) >= 2 && stages_for(64) >= 3 && stages_for(128) >= 5 &&
                   stages_for(256) >= 3,
               "pipeline too shallow");
-static_assert(tmem_cols_for(32, stages_for(32), 2) <= 256 &&
-                  tmem_cols_for(64, stages_for(64), 2) <= 256 &&
-                  tmem_cols_for(128, stages_for(128), 2) <= 512 &&
-                  tmem_cols_for(256, stages_for(256), 1) <= 512,
+static_assert(tmem_cols_for(32, stages_for(32), 2) <= tmem_budget(ctas_per_sm(32)) &&
+                  tmem_cols_for(64, stages_for(64), 2) <= tmem_budget(ctas_per_sm(64)) &&
+                  tmem_cols_for(128, stages_for(128), 2) <= tmem_budget(ctas_per_sm(128)) &&
+                  tmem_cols_for(256, stages_for(256), 1) <= tmem_budget(ctas_per_sm(256)),
               "tensor memory over budget");
-static_assert(gemm_smem_bytes(32) <= kSmemTwoCtas && gemm_smem_bytes(64) <= kSmemTwoCtas &&
-                  gemm_smem_bytes(128) <= kSmemOneCta && gemm_smem_bytes(256) <= kSmemOneCta,
+static_assert(gemm_smem_bytes(32) <= smem_budget(ctas_per_sm(32)) &&
+                  gemm_smem_bytes(64) <= smem_budget(ctas_per_sm(64)) &&
+                  gemm_smem_bytes(128) <= smem_budget(ctas_per_sm(128)) &&
+                  gemm_smem_bytes(256) <= smem_budget(ctas_per_sm(256)),
               "shared memory over budget");
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
