@@ -244,14 +244,20 @@ def run_ours(args, w) -> None:
     def step(i, ev=None):
         wts = copies[i % len(copies)]
         B.route_permute(ids, E, tile, route=route, status=status)
-        B.experts_quantize(route, ws, x=x, a1_gscale=moe.a1_gscale, T=T, H=H, I=I, E=E, K=K, status=status)
-        if ev is not None:
+        if ev is None:
+            # The expert body as one call: its GEMMs start as programmatic
+            # dependents of the kernel before them.
+            B.nvfp4_experts(wts, route, x=x, a1_gscale=moe.a1_gscale, a2_gscale=moe.a2_gscale, T=T, H=H,
+                            I=I, E=E, K=K, gemm2_rows=rows, ws=ws, status=status)
+        else:
+            # The same kernels through the split entry points (plain launches),
+            # with events between them for the per-kernel durations.
+            B.experts_quantize(route, ws, x=x, a1_gscale=moe.a1_gscale, T=T, H=H, I=I, E=E, K=K,
+                               status=status)
             ev[0].record(stream)
-        B.experts_gemm1(wts, route, ws, a2_gscale=moe.a2_gscale, T=T, H=H, I=I, E=E, K=K, status=status)
-        if ev is not None:
+            B.experts_gemm1(wts, route, ws, a2_gscale=moe.a2_gscale, T=T, H=H, I=I, E=E, K=K, status=status)
             ev[1].record(stream)
-        B.experts_gemm2(wts, route, ws, rows, T=T, H=H, I=I, E=E, K=K, status=status)
-        if ev is not None:
+            B.experts_gemm2(wts, route, ws, rows, T=T, H=H, I=I, E=E, K=K, status=status)
             ev[2].record(stream)
         B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out)
 

@@ -31,11 +31,11 @@ cudaError_t launch_rmsnorm_nvfp4_permuted(const void*, const void*, float, const
                                           const int32_t*, int, int, int, uint8_t*, uint8_t*, cudaStream_t);
 int launch_gemm1(const void*, const void*, const float*, const float*, const float*,
                  const int32_t*, const int32_t*, const int32_t*, const uint8_t*, const uint8_t*,
-                 uint8_t*, uint8_t*, int, int, int, int, int, int, int32_t*, cudaStream_t,
+                 uint8_t*, uint8_t*, int, int, int, int, int, int, int32_t*, cudaStream_t, bool,
                  const char**);
 int launch_gemm2(const void*, const void*, const float*, const int32_t*, const int32_t*,
                  const int32_t*, const uint8_t*, const uint8_t*, void*, int, int, int, int, int,
-                 int, int32_t*, cudaStream_t, const char**);
+                 int, int32_t*, cudaStream_t, bool, const char**);
 }  // namespace moe
 
 namespace {
@@ -251,9 +251,12 @@ int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const f
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
 }
 
-int moe_experts_gemm1(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T,
-                      int H, int I, int E, int K, int tile_m, void* ws, size_t ws_bytes,
-                      int32_t* status, void* stream) {
+// pdl: launch the GEMM as a programmatic dependent of the kernel before it,
+// which must be this library's own step kernel launched in the same call
+// (the GEMM then loads weights before that kernel has completed).
+static int experts_gemm1(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T,
+                         int H, int I, int E, int K, int tile_m, void* ws, size_t ws_bytes,
+                         int32_t* status, void* stream, bool pdl) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -266,13 +269,19 @@ int moe_experts_gemm1(const moe_weights* w, const float* a2_gscale, const moe_ro
   rc = moe::launch_gemm1(w->w13, w->w13_sf, w->g1_alphas, w->g1_scale_c, a2_gscale, r->tile_expert,
                          r->tile_row_limit, r->totals, base + L.a_codes, base + L.a_sf,
                          base + L.h_codes, base + L.h_sf, E, H, I, tile_m, L.P, L.MT, status,
-                         as_stream(stream), &why);
+                         as_stream(stream), pdl, &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
 }
 
-int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E, int K,
-                      int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes, int32_t* status,
-                      void* stream) {
+int moe_experts_gemm1(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T,
+                      int H, int I, int E, int K, int tile_m, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream) {
+  return experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream, false);
+}
+
+static int experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E,
+                         int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
+                         int32_t* status, void* stream, bool pdl) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -285,8 +294,14 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, in
   const char* why = "";
   rc = moe::launch_gemm2(w->w2, w->w2_sf, w->g2_alphas, r->tile_expert, r->tile_row_limit,
                          r->totals, base + L.h_codes, base + L.h_sf, gemm2_rows, E, H, I, tile_m,
-                         L.P, L.MT, status, as_stream(stream), &why);
+                         L.P, L.MT, status, as_stream(stream), pdl, &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
+}
+
+int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E, int K,
+                      int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes, int32_t* status,
+                      void* stream) {
+  return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, false);
 }
 
 int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const void* a_sf,
@@ -298,9 +313,12 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const 
   rc = moe_experts_quantize(x, a, a_sf, a1_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status,
                             stream);
   if (rc) return rc;
-  rc = moe_experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream);
+  // The two GEMMs follow the quantizer and each other as programmatic
+  // dependents: each starts streaming its first weight stages while the
+  // kernel before it drains.
+  rc = experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream, true);
   if (rc) return rc;
-  return moe_experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream);
+  return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true);
 }
 
 int moe_experts_export(int which, const void* ws, size_t ws_bytes, int T, int H, int I, int E,

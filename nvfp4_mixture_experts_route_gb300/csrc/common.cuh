@@ -41,6 +41,40 @@ __device__ __forceinline__ void record_status(int32_t* status, int32_t code) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel on the
+// stream drains; it must call pdl_wait() before it touches anything that
+// kernel writes (or reads and this kernel overwrites). pdl_wait() returns once
+// the previous kernel has completed and its memory is visible; without the
+// attribute it returns at once. pdl_trigger() lets the next kernel be
+// scheduled early; this library calls it only after its own pdl_wait(), so
+// that everything before the previous kernel is complete when the next one
+// starts.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kern` on `stream`, with the programmatic stream-serialization
+// attribute when `pdl` is set.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -84,21 +118,24 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 // Wait for phase `parity` of an mbarrier. Returns false (after recording
 // MOE_ERR_TIMEOUT and raising *abort) if the wait ran out or another thread
-// of the CTA already gave up.
+// of the CTA already gave up. try_wait itself suspends the thread until the
+// phase completes or a short hardware time limit passes, so the loop re-polls
+// without sleeping (a sleep would delay the wake-up on the pipeline's
+// critical path); the abort flag and the clock are read every 16 polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           int32_t* status) {
-  for (int i = 0; i < 64; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      record_status(status, MOE_ERR_TIMEOUT);
-      *abort = 1;
-      return false;
+    if ((n & 15u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, MOE_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
     }
-    __nanosleep(128);
   }
 }
 

@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
     int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out) {
   __shared__ float red[kFinWarps][CH];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = H / 8;
@@ -168,9 +170,11 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
   auto op = reinterpret_cast<__nv_bfloat16*>(out);
 #define MOE_FIN_CASE(n)                                                                     \
   case n:                                                                                   \
-    finalize_kernel<n, (n <= 2 ? 8 : n <= 4 ? 4 : 2)><<<T, kFinThreads, 0, stream>>>(           \
-        rp, e2p, w, gp, eps, weight_before_norm, K, H, op);                                  \
+    err = launch_kernel(finalize_kernel<n, (n <= 2 ? kFinChunk : n <= 4 ? 4 : 2)>, dim3(T),            \
+                        dim3(kFinThreads), 0, stream, true, rp, e2p, w, gp, eps,                 \
+                        weight_before_norm, K, H, op);                                           \
     break;
+  cudaError_t err = cudaSuccess;
   switch (vpt) {
     MOE_FIN_CASE(1)
     MOE_FIN_CASE(2)
@@ -184,7 +188,7 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
       return cudaErrorInvalidValue;
   }
 #undef MOE_FIN_CASE
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace moe

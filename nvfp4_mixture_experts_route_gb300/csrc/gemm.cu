@@ -13,7 +13,7 @@
 // rows are permuted route rows of one routing tile (all of one expert). A
 // work unit is one (route tile tau, weight tile mt) pair over the whole K.
 //
-// Persistent, warp-specialised kernel, one CTA per SM, 6 warps:
+// Persistent, warp-specialised kernel, one to three CTAs per SM, 6 warps:
 //   - warp 0 / lane 0: TMA producer. Walks this CTA's units in order and, per
 //     pipeline stage (K = 256 elements = 128 bytes per row), loads the
 //     128 x 128 B weight box and the tile_m x 128 B route box (both 128-byte
@@ -80,6 +80,11 @@ struct GemmParams {
   __nv_bfloat16* rows;     // GEMM2: [P][H]
   int32_t* status;
   int E, rows_w, K, tile_m, S, out_cols, stages, acc_bufs;
+  // Set when the launch follows this library's previous step kernel with
+  // programmatic dependent launch: the producer then loads the weights of its
+  // first stages before waiting for that kernel (the weights and the routing
+  // metadata are complete by then; only the route operand is not).
+  int prefetch;
 };
 
 // Launch shape per route-tile size. Each CTA's tcgen05 scale copies and MMAs
@@ -233,10 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ntiles = p.totals[0];
+  if (!p.prefetch) {
+    pdl_wait();
+    if (tid == 0) pdl_trigger();
+  }
+  const int ntiles = __ldcg(p.totals);
   const int tiles_w = p.rows_w / kWTile;
   const int n_units = ntiles * tiles_w;
-  if ((int)blockIdx.x >= n_units) return;
+  if ((int)blockIdx.x >= n_units) {
+    // Even an idle CTA must not let this grid complete before its
+    // predecessor: the kernels after it rely on that ordering.
+    if (p.prefetch) pdl_wait();
+    return;
+  }
 
   const int tile_m = p.tile_m, S = p.S, ST = p.stages, NB = p.acc_bufs;
   const uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;
@@ -281,30 +295,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool stop = false;
+      // With p.prefetch the route-operand half of the first stages (at most
+      // ST of them) is held back until the previous kernel has completed.
+      bool waited = !p.prefetch;
+      int held = 0;
+      int held_s[kMaxStages], held_ks[kMaxStages], held_tau[kMaxStages], held_kk[kMaxStages];
+      auto load_route_half = [&](int s, int ks, int tau, int kk) {
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        const uint8_t* bsf = p.b_sf + (size_t)tau * KC * S * kAtomBytes;
+        tma_load_2d(sB + s * b_bytes, &tmB, fb, ks * kStageRowBytes, tau * tile_m);
+        bulk_load(sSFB + s * kSfStageBytes * S, bsf + (size_t)4 * ks * S * kAtomBytes,
+                  (uint32_t)kk * S * kAtomBytes, fb);
+      };
+      auto release_held = [&]() {
+        pdl_wait();
+        pdl_trigger();
+        for (int h = 0; h < held; ++h) load_route_half(held_s[h], held_ks[h], held_tau[h], held_kk[h]);
+        held = 0;
+        waited = true;
+      };
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
         const int mt = u % tiles_w, tau = u / tiles_w;
-        const int e = p.tile_expert[tau];
+        const int e = __ldcg(p.tile_expert + tau);
         const int a_row = e * p.rows_w + mt * kWTile;
         const uint8_t* wsf = p.w_sf + ((size_t)e * tiles_w + mt) * KC * kAtomBytes;
-        const uint8_t* bsf = p.b_sf + (size_t)tau * KC * S * kAtomBytes;
         for (int ks = 0; ks < nks; ++ks, ++it) {
           const int s = it % ST, round = it / ST;
-          if (round > 0 &&
-              !mbar_wait(smem_u32(&empty_bar[s]), (round - 1) & 1, &abort_flag, p.status)) {
-            stop = true;
-            break;
+          if (round > 0) {
+            if (!waited) release_held();
+            if (!mbar_wait(smem_u32(&empty_bar[s]), (round - 1) & 1, &abort_flag, p.status)) {
+              stop = true;
+              break;
+            }
           }
           const int kk = min(4, KC - 4 * ks);
           const uint32_t fb = smem_u32(&full_bar[s]);
           mbar_arrive_expect_tx(fb, kABytes + b_bytes + (uint32_t)kk * kAtomBytes * (1 + S));
           tma_load_2d(sA + s * kABytes, &tmA, fb, ks * kStageRowBytes, a_row);
-          tma_load_2d(sB + s * b_bytes, &tmB, fb, ks * kStageRowBytes, tau * tile_m);
           bulk_load(sSFA + s * kSfStageBytes, wsf + (size_t)4 * ks * kAtomBytes,
                     (uint32_t)kk * kAtomBytes, fb);
-          bulk_load(sSFB + s * kSfStageBytes * S, bsf + (size_t)4 * ks * S * kAtomBytes,
-                    (uint32_t)kk * S * kAtomBytes, fb);
+          if (waited) {
+            load_route_half(s, ks, tau, kk);
+          } else {
+            held_s[held] = s;
+            held_ks[held] = ks;
+            held_tau[held] = tau;
+            held_kk[held] = kk;
+            ++held;
+          }
         }
       }
+      if (!waited) release_held();
       // Wait for the copies still in flight (normally all consumed already).
       for (int j = max(0, it - ST); j < it; ++j)
         mbar_wait_cleanup(smem_u32(&full_bar[j % ST]), (j / ST) & 1);
@@ -460,7 +501,8 @@ static int sm_count() {
 
 template <int KIND>
 static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
-                              int max_tiles, cudaStream_t stream) {
+                              int max_tiles, cudaStream_t stream, bool pdl) {
+  p.prefetch = pdl ? 1 : 0;
   p.stages = stages_for(p.tile_m);
   p.acc_bufs = acc_bufs_for(p.tile_m);
   const size_t smem = gemm_smem_bytes(p.tile_m);
@@ -476,8 +518,7 @@ static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
   const long long units = (long long)max_tiles * (p.rows_w / kWTile);
   const long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
   const int grid = (int)(units < slots ? units : slots);
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, p);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, stream, pdl, ta, tb, p);
 }
 
 // GEMM1: weights p_w13 [E*2I, H/2], route rows a [P, H/2]; writes hq.
@@ -485,7 +526,7 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
                  const float* g1_scale_c, const float* a2_gscale, const int32_t* tile_expert,
                  const int32_t* tile_row_limit, const int32_t* totals, const uint8_t* a_codes,
                  const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, int E, int H, int I,
-                 int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream,
+                 int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream, bool pdl,
                  const char** why) {
   CUtensorMap ta, tb;
   if (encode_rows_map(&ta, p_w13, H / 2, (uint64_t)E * 2 * I, kWTile) != CUDA_SUCCESS ||
@@ -511,7 +552,7 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
   p.tile_m = tile_m;
   p.S = sf_atoms_per_tile(tile_m);
   p.out_cols = I;
-  if (launch_one<1>(ta, tb, p, max_tiles, stream) != cudaSuccess) {
+  if (launch_one<1>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM1 launch failed";
     return MOE_ERR_CUDA;
   }
@@ -522,7 +563,7 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
 int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
                  const int32_t* tile_expert, const int32_t* tile_row_limit, const int32_t* totals,
                  const uint8_t* h_codes, const uint8_t* h_sf, void* rows, int E, int H, int I,
-                 int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream,
+                 int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream, bool pdl,
                  const char** why) {
   CUtensorMap ta, tb;
   if (encode_rows_map(&ta, p_w2, I / 2, (uint64_t)E * H, kWTile) != CUDA_SUCCESS ||
@@ -545,7 +586,7 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
   p.tile_m = tile_m;
   p.S = sf_atoms_per_tile(tile_m);
   p.out_cols = H;
-  if (launch_one<2>(ta, tb, p, max_tiles, stream) != cudaSuccess) {
+  if (launch_one<2>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM2 launch failed";
     return MOE_ERR_CUDA;
   }

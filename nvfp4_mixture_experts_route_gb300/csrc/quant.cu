@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
     const int32_t* __restrict__ permuted_to_token, const int32_t* __restrict__ totals, int H,
     int tile_m, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_trigger();
   const int nb = H / 16;
   const int rows = totals[1];
   const float g = (x != nullptr) ? *gscale : 0.f;
@@ -113,10 +115,10 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                                     const int32_t* totals, int H, int tile_m, int P, uint8_t* codes,
                                     uint8_t* scales, cudaStream_t stream) {
   const int grid = grid_for((long long)P * (H / 16), 256);
-  quantize_permute_kernel<<<grid, 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
-      reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, p2t, totals, H, tile_m, codes, scales);
-  return cudaGetLastError();
+  return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
+                       reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
+                       reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, p2t, totals, H, tile_m, codes,
+                       scales);
 }
 
 cudaError_t launch_act_scales_io(int to_linear, uint8_t* atoms, uint8_t* linear, int K,

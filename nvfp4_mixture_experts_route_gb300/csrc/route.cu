@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   extern __shared__ int32_t hist[];  // [kRouteWarps][E]
   __shared__ int32_t warp_sums[kRouteWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Launched in plain stream order; the kernels after it wait for it to
+  // complete before they read what it writes.
+  pdl_trigger();
   const int R = T * K;
   const int seg = (R + kRouteWarps - 1) / kRouteWarps;
   const int beg = min(R, warp * seg), end = min(R, beg + seg);

@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kNqThreads)
                          const int32_t* __restrict__ totals, int T, int H, int tile_m,
                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   __shared__ float red[kNqThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int nb = H / 16;
   const int rows = PERMUTED ? totals[1] : T;
   const float g = *gscale;
@@ -215,19 +217,18 @@ static int nq_grid(int rows) {
 cudaError_t launch_rmsnorm_nvfp4(const void* x, const void* gamma, float eps, const float* gscale, int T,
                                  int H, void* a, void* a_sf, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_nvfp4_kernel<false><<<nq_grid(T), kNqThreads, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gamma), eps, gscale,
-      nullptr, nullptr, T, H, 32, reinterpret_cast<uint8_t*>(a), reinterpret_cast<uint8_t*>(a_sf));
-  return cudaGetLastError();
+  return launch_kernel(rmsnorm_nvfp4_kernel<false>, dim3(nq_grid(T)), dim3(kNqThreads), 0, stream, true,
+                       reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gamma),
+                       eps, gscale, (const int32_t*)nullptr, (const int32_t*)nullptr, T, H, 32,
+                       reinterpret_cast<uint8_t*>(a), reinterpret_cast<uint8_t*>(a_sf));
 }
 
 cudaError_t launch_rmsnorm_nvfp4_permuted(const void* x, const void* gamma, float eps, const float* gscale,
                                           const int32_t* p2t, const int32_t* totals, int H, int tile_m, int P,
                                           uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
-  rmsnorm_nvfp4_kernel<true><<<nq_grid(P), kNqThreads, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gamma), eps, gscale,
-      p2t, totals, 0, H, tile_m, codes, scales);
-  return cudaGetLastError();
+  return launch_kernel(rmsnorm_nvfp4_kernel<true>, dim3(nq_grid(P)), dim3(kNqThreads), 0, stream, true,
+                       reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(gamma),
+                       eps, gscale, p2t, totals, 0, H, tile_m, codes, scales);
 }
 
 }  // namespace moe
