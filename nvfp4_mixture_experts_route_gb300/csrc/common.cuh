@@ -29,6 +29,11 @@ inline cudaError_t ensure_smem_limit(const void* func, int bytes) {
   std::lock_guard<std::mutex> lock(mu);
   if (done.count({func, dev})) return cudaSuccess;
   err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // Ask for the largest shared-memory carveout: the kernels that come here
+  // size their CTAs per SM from the whole 228 KB.
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
   if (err == cudaSuccess) done.insert({func, dev});
   return err;
 }

@@ -13,22 +13,25 @@
 // rows are permuted route rows of one routing tile (all of one expert). A
 // work unit is one (route tile tau, weight tile mt) pair over the whole K.
 //
-// Persistent, warp-specialised kernel, one to three CTAs per SM, 6 warps:
+// Persistent, warp-specialised kernel, one to three CTAs per SM (tile_cfg
+// below), 2 + 4 or 2 + 8 warps:
 //   - warp 0 / lane 0: TMA producer. Walks this CTA's units in order and, per
-//     pipeline stage (K = 256 elements = 128 bytes per row), loads the
-//     128 x 128 B weight box and the tile_m x 128 B route box (both 128-byte
-//     swizzled) and the stage's scale atoms for both operands (plain bulk
-//     copies), all completing one mbarrier. The ring of ST stages runs across
-//     unit boundaries, so HBM streaming never stops between units.
+//     pipeline stage (K = 256 elements = 128 bytes per row per chunk), loads
+//     the 128 x 128 B weight box and the tile_m x 128 B route box (both
+//     128-byte swizzled) and the stage's scale atoms for both operands (plain
+//     bulk copies), all completing one mbarrier. The ring of ST stages runs
+//     across unit boundaries, so HBM streaming never stops between units.
 //   - warp 1 / lane 0: MMA issuer. Copies each stage's scale atoms into that
 //     stage's own tensor-memory columns (tcgen05.cp 32x128b.warpx4), issues
-//     4 MMAs of K = 64 into the unit's accumulator buffer, and commits the
-//     stage back to the producer; after a unit's last stage it commits the
-//     accumulator to the epilogue.
-//   - warps 2-5: epilogue. Warp w reads TMEM lane quadrant w % 4 (32 weight
-//     rows) of the finished accumulator, then hands the buffer back. Two
-//     accumulator buffers (one for tile_m = 256) let the epilogue of unit i
-//     run while unit i+1 streams.
+//     the stage's MMAs of K = 64 into the unit's accumulator buffer, and
+//     commits the stage back to the producer; after a unit's last stage it
+//     commits the accumulator to the epilogue.
+//   - warps 2..: epilogue. Warp w reads TMEM lane quadrant w % 4 (32 weight
+//     rows) of the finished accumulator (with 8 warps, two per quadrant split
+//     the route columns), then hands the buffer back. With two accumulator
+//     buffers the epilogue of unit i runs while unit i+1 streams; with one
+//     (the larger tiles, whose tensor memory is split between two CTAs or
+//     taken by one wide accumulator) the other CTA on the SM fills the gap.
 // Units are ordered with the weight tile fastest (u -> mt = u % tiles_w,
 // tau = u / tiles_w) and dealt round-robin, so the CTAs working at the same
 // time share route tiles (and, for experts with many tiles, weight tiles) in
@@ -56,15 +59,7 @@ constexpr int kWTile = 128;                    // weight rows per unit (MMA M)
 constexpr uint32_t kABytes = kWTile * kStageRowBytes;  // 16 KiB
 constexpr uint32_t kSfStageBytes = 4 * kAtomBytes;     // 4 K=64 steps
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
-// GEMM1 epilogue staging: route columns per chunk (32 when a CTA has the SM
-// to itself, 16 when two share it) and the shared memory it takes.
-__host__ __device__ constexpr int epi_cols_for(int ctas) { return ctas >= 2 ? 16 : 32; }
-__host__ __device__ constexpr uint32_t epi_bytes_for(int cols) {
-  return kEpiWarps * cols * kEpiStride * 4;
-}
 
 struct GemmParams {
   const uint8_t* w_sf;  // prepared scale atoms [E][rows_w/128][K/64][512]
@@ -80,6 +75,7 @@ struct GemmParams {
   __nv_bfloat16* rows;     // GEMM2: [P][H]
   int32_t* status;
   int E, rows_w, K, tile_m, S, out_cols, stages, acc_bufs;
+  int chunks;  // K = 256 chunks per pipeline stage
   // Set when the launch follows this library's previous step kernel with
   // programmatic dependent launch: the producer then loads the weights of its
   // first stages before waiting for that kernel (the weights and the routing
@@ -87,23 +83,45 @@ struct GemmParams {
   int prefetch;
 };
 
-// Launch shape per route-tile size. Each CTA's tcgen05 scale copies and MMAs
-// execute in order, so several independent CTAs per SM overlap their streams:
-// 32-row tiles (decode) run three CTAs per SM, 64-row tiles two, larger tiles
-// one (measured on the b = 8 decode: GEMM1 254 us with one CTA per SM, 136 us
-// with two, about 14% less again with three). The pipeline depth is what the
-// shared memory left for the CTA holds, and tensor memory is split between
-// the CTAs of an SM.
-__host__ __device__ constexpr int ctas_per_sm(int tile_m) {
-  return tile_m <= 32 ? 3 : tile_m <= 64 ? 2 : 1;
+// Launch shape per route-tile size: CTAs per SM, accumulator buffers, K=256
+// chunks per pipeline stage, epilogue warps and GEMM1 epilogue staging
+// columns. One thread per CTA issues all of its tcgen05 copies and MMAs, and
+// each instruction occupies that thread for a fixed time whatever its size
+// (measured with a pipe probe: about 26 ns per copy or MMA and 175 ns per
+// commit), so the tensor core is fed by several CTAs per SM wherever tensor
+// memory and shared memory allow; the decode tiles (32 rows) run three CTAs
+// per SM (GEMM1 on the b = 8 decode: 254 us with one CTA per SM, 136 us with
+// two, 121 us with three). Each epilogue warp works through its accumulator
+// columns as one dependent instruction stream, so the larger tiles take two
+// warps per TMEM lane quadrant (8 in all) that split the route columns.
+struct TileCfg {
+  int ctas, acc_bufs, chunks, epi_warps, epi_cols;
+};
+__host__ __device__ constexpr TileCfg tile_cfg(int tile_m) {
+  return tile_m <= 32    ? TileCfg{3, 2, 1, 4, 16}
+         : tile_m <= 64  ? TileCfg{2, 2, 1, 4, 16}
+         : tile_m <= 128 ? TileCfg{2, 1, 1, 8, 32}
+                         : TileCfg{1, 1, 1, 8, 32};
 }
-__host__ __device__ constexpr int acc_bufs_for(int tile_m) { return tile_m <= 128 ? 2 : 1; }
+__host__ __device__ constexpr int ctas_per_sm(int tile_m) { return tile_cfg(tile_m).ctas; }
+__host__ __device__ constexpr int acc_bufs_for(int tile_m) { return tile_cfg(tile_m).acc_bufs; }
+__host__ __device__ constexpr int chunks_for(int tile_m) { return tile_cfg(tile_m).chunks; }
+__host__ __device__ constexpr int epi_warps_for(int tile_m) { return tile_cfg(tile_m).epi_warps; }
+__host__ __device__ constexpr int epi_cols_for(int tile_m) { return tile_cfg(tile_m).epi_cols; }
+// Only GEMM1's epilogue stages through shared memory (its SwiGLU pairs rows
+// of two lanes); GEMM2's ring takes the room instead.
+__host__ __device__ constexpr uint32_t epi_bytes_for(int tile_m, int kind) {
+  return kind == 1 ? (uint32_t)(epi_warps_for(tile_m) * epi_cols_for(tile_m) * kEpiStride * 4) : 0u;
+}
 
 __host__ __device__ constexpr int sf_atoms_for(int tile_m) { return (tile_m + 127) / 128; }
 
+// Bytes of one pipeline stage: chunks_for(tile_m) K = 256 chunks of the
+// weight box, the route box and both operands' scale atoms.
 __host__ __device__ constexpr uint32_t stage_bytes(int tile_m) {
-  return kABytes + (uint32_t)tile_m * kStageRowBytes +
-         kSfStageBytes * (uint32_t)(1 + sf_atoms_for(tile_m));
+  return (uint32_t)chunks_for(tile_m) *
+         (kABytes + (uint32_t)tile_m * kStageRowBytes +
+          kSfStageBytes * (uint32_t)(1 + sf_atoms_for(tile_m)));
 }
 
 // Dynamic shared memory a CTA may take: 227 KB alone, otherwise its share of
@@ -114,38 +132,39 @@ __host__ __device__ constexpr int smem_budget(int ctas) {
 }
 __host__ __device__ constexpr int tmem_budget(int ctas) { return ctas == 1 ? 512 : ctas == 2 ? 256 : 128; }
 
-__host__ __device__ constexpr int stages_for(int tile_m) {
-  const int budget = smem_budget(ctas_per_sm(tile_m)) - 1024 -
-                     (int)epi_bytes_for(epi_cols_for(ctas_per_sm(tile_m)));
-  const int st = budget / (int)stage_bytes(tile_m);
-  return st > kMaxStages ? kMaxStages : st;
-}
-
 __host__ __device__ constexpr uint32_t tmem_cols_for(int tile_m, int stages, int bufs) {
-  const int need = bufs * tile_m + stages * 16 * (1 + sf_atoms_for(tile_m));
+  const int need = bufs * tile_m + stages * 16 * chunks_for(tile_m) * (1 + sf_atoms_for(tile_m));
   uint32_t c = 32;
   while ((int)c < need) c <<= 1;
   return c;
 }
 
-__host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m) {
-  return 1024 + (size_t)stages_for(tile_m) * stage_bytes(tile_m) +
-         epi_bytes_for(epi_cols_for(ctas_per_sm(tile_m)));
+// Pipeline depth: as many stages as the shared memory left after the
+// epilogue staging holds and the CTA's tensor-memory share can give scale
+// columns to.
+__host__ __device__ constexpr int stages_for(int tile_m, int kind) {
+  const int budget = smem_budget(ctas_per_sm(tile_m)) - 1024 - (int)epi_bytes_for(tile_m, kind);
+  int st = budget / (int)stage_bytes(tile_m);
+  st = st > kMaxStages ? kMaxStages : st;
+  while (st > 1 && tmem_cols_for(tile_m, st, acc_bufs_for(tile_m)) >
+                       (uint32_t)tmem_budget(ctas_per_sm(tile_m)))
+    --st;
+  return st;
 }
 
-static_assert(stages_for(32) >= 2 && stages_for(64) >= 3 && stages_for(128) >= 5 &&
-                  stages_for(256) >= 3,
-              "pipeline too shallow");
-static_assert(tmem_cols_for(32, stages_for(32), 2) <= tmem_budget(ctas_per_sm(32)) &&
-                  tmem_cols_for(64, stages_for(64), 2) <= tmem_budget(ctas_per_sm(64)) &&
-                  tmem_cols_for(128, stages_for(128), 2) <= tmem_budget(ctas_per_sm(128)) &&
-                  tmem_cols_for(256, stages_for(256), 1) <= tmem_budget(ctas_per_sm(256)),
-              "tensor memory over budget");
-static_assert(gemm_smem_bytes(32) <= smem_budget(ctas_per_sm(32)) &&
-                  gemm_smem_bytes(64) <= smem_budget(ctas_per_sm(64)) &&
-                  gemm_smem_bytes(128) <= smem_budget(ctas_per_sm(128)) &&
-                  gemm_smem_bytes(256) <= smem_budget(ctas_per_sm(256)),
-              "shared memory over budget");
+__host__ __device__ constexpr size_t gemm_smem_bytes(int tile_m, int kind) {
+  return 1024 + (size_t)stages_for(tile_m, kind) * stage_bytes(tile_m) + epi_bytes_for(tile_m, kind);
+}
+
+__host__ __device__ constexpr bool tile_fits(int t, int kind) {
+  return stages_for(t, kind) >= 2 &&
+         tmem_cols_for(t, stages_for(t, kind), acc_bufs_for(t)) <=
+             (uint32_t)tmem_budget(ctas_per_sm(t)) &&
+         gemm_smem_bytes(t, kind) <= (size_t)smem_budget(ctas_per_sm(t));
+}
+static_assert(tile_fits(32, 1) && tile_fits(64, 1) && tile_fits(128, 1) && tile_fits(256, 1) &&
+                  tile_fits(32, 2) && tile_fits(64, 2) && tile_fits(128, 2) && tile_fits(256, 2),
+              "a route-tile shape overflows its pipeline, tensor memory or shared memory budget");
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -212,7 +231,7 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const float g = col[j], up = col[16 + j];
-      h[j] = g / (1.0f + expf(-g)) * up;
+      h[j] = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
     }
     uint2 codes;
     uint32_t sfc;
@@ -224,8 +243,8 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
   __syncwarp();
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KIND, int EPW, int CTAS>
+__global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t dsmem[];
@@ -252,16 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  const int tile_m = p.tile_m, S = p.S, ST = p.stages, NB = p.acc_bufs;
-  const uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;
+  const int tile_m = p.tile_m, S = p.S, ST = p.stages, NB = p.acc_bufs, CH = p.chunks;
+  // Per stage: CH chunks of K = 256, i.e. up to 4 * CH MMA steps of K = 64.
+  const uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;  // one chunk of the route box
+  const uint32_t a_stage = CH * kABytes, b_stage = CH * b_bytes;
+  const uint32_t sfa_stage = CH * kSfStageBytes, sfb_stage = CH * kSfStageBytes * S;
   const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sA = sbase;
-  const uint32_t sB = sA + ST * kABytes;
-  const uint32_t sSFA = sB + ST * b_bytes;
-  const uint32_t sSFB = sSFA + ST * kSfStageBytes;
-  const uint32_t sEpi = sSFB + ST * kSfStageBytes * S;
+  const uint32_t sB = sA + ST * a_stage;
+  const uint32_t sSFA = sB + ST * b_stage;
+  const uint32_t sSFB = sSFA + ST * sfa_stage;
+  const uint32_t sEpi = sSFB + ST * sfb_stage;
   const int KC = p.K / 64;
-  const int nks = (KC + 3) / 4;
+  const int steps_per_stage = 4 * CH;
+  const int nks = (KC + steps_per_stage - 1) / steps_per_stage;
   const uint32_t ncols = tmem_cols_for(tile_m, ST, NB);
 
   if (tid == 0) {
@@ -271,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&accf_bar[b]), 1);
-      mbar_init(smem_u32(&acce_bar[b]), kEpiWarps);
+      mbar_init(smem_u32(&acce_bar[b]), EPW);
     }
     mbar_init(smem_u32(&drain_bar), 1);
     abort_flag = 0;
@@ -288,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const uint32_t t_sfa = tmem + (uint32_t)(NB * tile_m);
-  const uint32_t t_sfb = t_sfa + ST * 16;
+  const uint32_t t_sfb = t_sfa + ST * 16 * CH;
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
@@ -303,8 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_route_half = [&](int s, int ks, int tau, int kk) {
         const uint32_t fb = smem_u32(&full_bar[s]);
         const uint8_t* bsf = p.b_sf + (size_t)tau * KC * S * kAtomBytes;
-        tma_load_2d(sB + s * b_bytes, &tmB, fb, ks * kStageRowBytes, tau * tile_m);
-        bulk_load(sSFB + s * kSfStageBytes * S, bsf + (size_t)4 * ks * S * kAtomBytes,
+        for (int c = 0; 4 * c < kk; ++c)
+          tma_load_2d(sB + s * b_stage + c * b_bytes, &tmB, fb, (ks * CH + c) * kStageRowBytes,
+                      tau * tile_m);
+        bulk_load(sSFB + s * sfb_stage, bsf + (size_t)steps_per_stage * ks * S * kAtomBytes,
                   (uint32_t)kk * S * kAtomBytes, fb);
       };
       auto release_held = [&]() {
@@ -328,11 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          const int kk = min(4, KC - 4 * ks);
+          const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
+          const uint32_t nc = (uint32_t)(kk + 3) / 4;  // chunks in this stage
           const uint32_t fb = smem_u32(&full_bar[s]);
-          mbar_arrive_expect_tx(fb, kABytes + b_bytes + (uint32_t)kk * kAtomBytes * (1 + S));
-          tma_load_2d(sA + s * kABytes, &tmA, fb, ks * kStageRowBytes, a_row);
-          bulk_load(sSFA + s * kSfStageBytes, wsf + (size_t)4 * ks * kAtomBytes,
+          mbar_arrive_expect_tx(fb, nc * (kABytes + b_bytes) + (uint32_t)kk * kAtomBytes * (1 + S));
+          for (int c = 0; c < (int)nc; ++c)
+            tma_load_2d(sA + s * a_stage + c * kABytes, &tmA, fb, (ks * CH + c) * kStageRowBytes,
+                        a_row);
+          bulk_load(sSFA + s * sfa_stage, wsf + (size_t)steps_per_stage * ks * kAtomBytes,
                     (uint32_t)kk * kAtomBytes, fb);
           if (waited) {
             load_route_half(s, ks, tau, kk);
@@ -371,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int kk = min(4, KC - 4 * ks);
+          const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
           // Scale-factor addresses of the MMA must be 4-column aligned: each
           // K=64 step gets its own 4-column group per operand.
-          const uint32_t fa = t_sfa + s * 16, fbc = t_sfb + s * 16 * S;
-          const uint32_t sfa_smem = sSFA + s * kSfStageBytes;
-          const uint32_t sfb_smem = sSFB + s * kSfStageBytes * S;
+          const uint32_t fa = t_sfa + s * 16 * CH, fbc = t_sfb + s * 16 * CH * S;
+          const uint32_t sfa_smem = sSFA + s * sfa_stage;
+          const uint32_t sfb_smem = sSFB + s * sfb_stage;
           for (int j = 0; j < kk; ++j) {
             tc_copy_scale_atom(fa + 4 * j, smem_desc(sfa_smem + j * kAtomBytes, 0, 128, 0));
             for (int sub = 0; sub < S; ++sub)
@@ -384,8 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  smem_desc(sfb_smem + (j * S + sub) * kAtomBytes, 0, 128, 0));
           }
           for (int j = 0; j < kk; ++j) {
-            const uint64_t ad = smem_desc(sA + s * kABytes + 32 * j, 16, 1024, 2);
-            const uint64_t bd = smem_desc(sB + s * b_bytes + 32 * j, 16, 1024, 2);
+            // step j: chunk j / 4 of the stage, 32 bytes (K = 64) per step in it
+            const uint64_t ad =
+                smem_desc(sA + s * a_stage + (j >> 2) * kABytes + 32 * (j & 3), 16, 1024, 2);
+            const uint64_t bd =
+                smem_desc(sB + s * b_stage + (j >> 2) * b_bytes + 32 * (j & 3), 16, 1024, 2);
             tc_mma_nvf4(dacc, ad, bd, idesc, fa + 4 * j, fbc + 4 * j * S, (ks | j) != 0);
           }
           tc_commit(smem_u32(&empty_bar[s]));
@@ -396,10 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------ epilogue ------------------------------
-    const int q = warp & 3;  // TMEM lane quadrant of this warp
-    // this warp's staging rows: epi_cols_for(...) route columns of 33 floats
+    const int q = warp & 3;         // TMEM lane quadrant of this warp
+    const int half = (warp - 2) >> 2;  // which of the quadrant's warps (EPW = 8)
+    constexpr int kSplit = EPW / 4;    // warps per quadrant
+    // this warp's staging rows: epi_cols_for(tile_m) route columns of 33 floats
     float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
-                   (warp - 2) * epi_cols_for(ctas_per_sm(tile_m)) * kEpiStride;
+                   (warp - 2) * epi_cols_for(tile_m) * kEpiStride;
     int uc = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
       const int b = uc % NB, use = uc / NB;
@@ -415,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = lane < 16 ? p.s0[e] : p.s1[e];
         const float a2g = *p.a2_gscale;
         const int I = p.out_cols;
-        const int cols = epi_cols_for(ctas_per_sm(tile_m));
-        for (int c0 = 0; c0 < tile_m; c0 += cols) {
+        const int cols = epi_cols_for(tile_m);
+        for (int c0 = half * cols; c0 < tile_m; c0 += kSplit * cols) {
           if (cols == 32)
             gemm1_epilogue_chunk<32>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
                                      p.hq, p.hq_sf);
@@ -428,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float g2 = p.s0[e];
         const int limit = p.tile_row_limit[tau];
         const int colx = mt * kWTile + 32 * q + lane;
-        for (int c0 = 0; c0 < tile_m; c0 += 32) {
+        for (int c0 = half * 32; c0 < tile_m; c0 += kSplit * 32) {
           float v[32];
           tmem_ld32(taddr + c0, v);
 #pragma unroll
@@ -499,17 +532,18 @@ static int sm_count() {
   return n;
 }
 
-template <int KIND>
+template <int KIND, int EPW, int CTAS>
 static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
                               int max_tiles, cudaStream_t stream, bool pdl) {
   p.prefetch = pdl ? 1 : 0;
-  p.stages = stages_for(p.tile_m);
+  p.stages = stages_for(p.tile_m, KIND);
   p.acc_bufs = acc_bufs_for(p.tile_m);
-  const size_t smem = gemm_smem_bytes(p.tile_m);
-  auto kern = grouped_gemm_kernel<KIND>;
+  p.chunks = chunks_for(p.tile_m);
+  const size_t smem = gemm_smem_bytes(p.tile_m, KIND);
+  auto kern = grouped_gemm_kernel<KIND, EPW, CTAS>;
   size_t most = 0;
   for (int t : {32, 64, 128, 256}) {
-    const size_t b = gemm_smem_bytes(t);
+    const size_t b = gemm_smem_bytes(t, KIND);
     most = b > most ? b : most;
   }
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)most);
@@ -518,7 +552,23 @@ static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
   const long long units = (long long)max_tiles * (p.rows_w / kWTile);
   const long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
   const int grid = (int)(units < slots ? units : slots);
-  return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, stream, pdl, ta, tb, p);
+  return launch_kernel(kern, dim3(grid), dim3(64 + 32 * EPW), smem, stream, pdl, ta, tb, p);
+}
+
+template <int KIND>
+static cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
+                               int max_tiles, cudaStream_t stream, bool pdl) {
+  constexpr TileCfg c32 = tile_cfg(32), c64 = tile_cfg(64), c128 = tile_cfg(128), c256 = tile_cfg(256);
+  switch (p.tile_m) {
+    case 32:
+      return launch_one<KIND, c32.epi_warps, c32.ctas>(ta, tb, p, max_tiles, stream, pdl);
+    case 64:
+      return launch_one<KIND, c64.epi_warps, c64.ctas>(ta, tb, p, max_tiles, stream, pdl);
+    case 128:
+      return launch_one<KIND, c128.epi_warps, c128.ctas>(ta, tb, p, max_tiles, stream, pdl);
+    default:
+      return launch_one<KIND, c256.epi_warps, c256.ctas>(ta, tb, p, max_tiles, stream, pdl);
+  }
 }
 
 // GEMM1: weights p_w13 [E*2I, H/2], route rows a [P, H/2]; writes hq.
@@ -552,7 +602,7 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
   p.tile_m = tile_m;
   p.S = sf_atoms_per_tile(tile_m);
   p.out_cols = I;
-  if (launch_one<1>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
+  if (launch_kind<1>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM1 launch failed";
     return MOE_ERR_CUDA;
   }
@@ -586,7 +636,7 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
   p.tile_m = tile_m;
   p.S = sf_atoms_per_tile(tile_m);
   p.out_cols = H;
-  if (launch_one<2>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
+  if (launch_kind<2>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM2 launch failed";
     return MOE_ERR_CUDA;
   }
