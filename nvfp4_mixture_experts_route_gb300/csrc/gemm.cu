@@ -74,8 +74,7 @@ struct GemmParams {
   uint8_t* hq_sf;          // GEMM1: intermediate scale atoms [tiles][I/64][S][512]
   __nv_bfloat16* rows;     // GEMM2: [P][H]
   int32_t* status;
-  int E, rows_w, K, tile_m, S, out_cols, stages, acc_bufs;
-  int chunks;  // K = 256 chunks per pipeline stage
+  int E, rows_w, K, tile_m, out_cols;
   // Set when the launch follows this library's previous step kernel with
   // programmatic dependent launch: the producer then loads the weights of its
   // first stages before waiting for that kernel (the weights and the routing
@@ -243,8 +242,11 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
   __syncwarp();
 }
 
-template <int KIND, int EPW, int CTAS>
-__global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
+// One instantiation per (GEMM, route-tile size): the tile's launch shape,
+// pipeline depth and scale-atom count are compile-time, so the MMA issuer's
+// per-stage loops unroll and its descriptors are base + constant.
+template <int KIND, int TILE>
+__global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(TILE).ctas)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t dsmem[];
@@ -271,11 +273,12 @@ __global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
     return;
   }
 
-  const int tile_m = p.tile_m, S = p.S, ST = p.stages, NB = p.acc_bufs, CH = p.chunks;
+  constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, KIND);
+  constexpr int NB = acc_bufs_for(TILE), CH = chunks_for(TILE), EPW = epi_warps_for(TILE);
   // Per stage: CH chunks of K = 256, i.e. up to 4 * CH MMA steps of K = 64.
-  const uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;  // one chunk of the route box
-  const uint32_t a_stage = CH * kABytes, b_stage = CH * b_bytes;
-  const uint32_t sfa_stage = CH * kSfStageBytes, sfb_stage = CH * kSfStageBytes * S;
+  constexpr uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;  // one chunk of the route box
+  constexpr uint32_t a_stage = CH * kABytes, b_stage = CH * b_bytes;
+  constexpr uint32_t sfa_stage = CH * kSfStageBytes, sfb_stage = CH * kSfStageBytes * S;
   const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sA = sbase;
   const uint32_t sB = sA + ST * a_stage;
@@ -283,9 +286,9 @@ __global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
   const uint32_t sSFB = sSFA + ST * sfa_stage;
   const uint32_t sEpi = sSFB + ST * sfb_stage;
   const int KC = p.K / 64;
-  const int steps_per_stage = 4 * CH;
+  constexpr int steps_per_stage = 4 * CH;
   const int nks = (KC + steps_per_stage - 1) / steps_per_stage;
-  const uint32_t ncols = tmem_cols_for(tile_m, ST, NB);
+  constexpr uint32_t ncols = tmem_cols_for(tile_m, ST, NB);
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -382,8 +385,16 @@ __global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_nvf4(kWTile, (uint32_t)tile_m);
-      int it = 0, uc = 0;
+      constexpr uint32_t idesc = idesc_nvf4(kWTile, (uint32_t)tile_m);
+      // Descriptors of stage 0's first K = 64 step; another stage or step adds
+      // its byte offset >> 4 to the start-address field (shared-memory
+      // addresses are below 2^18, so the 14-bit field never carries).
+      const uint64_t a_desc0 = smem_desc(sA, 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(sB, 16, 1024, 2);
+      const uint64_t sfa_desc0 = smem_desc(sSFA, 0, 128, 0);
+      const uint64_t sfb_desc0 = smem_desc(sSFB, 0, 128, 0);
+      int s = 0, uc = 0;
+      uint32_t phase = 0;  // ring position: stage s, its current full phase
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++uc) {
         const int b = uc % NB, use = uc / NB;
@@ -392,9 +403,8 @@ __global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
           break;
         tc_fence_after();
         const uint32_t dacc = tmem + (uint32_t)(b * tile_m);
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % ST, round = it / ST;
-          if (!mbar_wait(smem_u32(&full_bar[s]), round & 1, &abort_flag, p.status)) {
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait(smem_u32(&full_bar[s]), phase, &abort_flag, p.status)) {
             stop = true;
             break;
           }
@@ -403,24 +413,35 @@ __global__ void __launch_bounds__(64 + 32 * EPW, CTAS)
           // Scale-factor addresses of the MMA must be 4-column aligned: each
           // K=64 step gets its own 4-column group per operand.
           const uint32_t fa = t_sfa + s * 16 * CH, fbc = t_sfb + s * 16 * CH * S;
-          const uint32_t sfa_smem = sSFA + s * sfa_stage;
-          const uint32_t sfb_smem = sSFB + s * sfb_stage;
-          for (int j = 0; j < kk; ++j) {
-            tc_copy_scale_atom(fa + 4 * j, smem_desc(sfa_smem + j * kAtomBytes, 0, 128, 0));
-            for (int sub = 0; sub < S; ++sub)
-              tc_copy_scale_atom(fbc + 4 * (j * S + sub),
-                                 smem_desc(sfb_smem + (j * S + sub) * kAtomBytes, 0, 128, 0));
+          const uint64_t ad = a_desc0 + ((s * a_stage) >> 4), bd = b_desc0 + ((s * b_stage) >> 4);
+          const uint64_t sad = sfa_desc0 + ((s * sfa_stage) >> 4);
+          const uint64_t sbd = sfb_desc0 + ((s * sfb_stage) >> 4);
+#pragma unroll
+          for (int j = 0; j < steps_per_stage; ++j) {
+            if (j < kk) {
+              tc_copy_scale_atom(fa + 4 * j, sad + j * (kAtomBytes >> 4));
+#pragma unroll
+              for (int sub = 0; sub < S; ++sub)
+                tc_copy_scale_atom(fbc + 4 * (j * S + sub), sbd + (j * S + sub) * (kAtomBytes >> 4));
+            }
           }
-          for (int j = 0; j < kk; ++j) {
-            // step j: chunk j / 4 of the stage, 32 bytes (K = 64) per step in it
-            const uint64_t ad =
-                smem_desc(sA + s * a_stage + (j >> 2) * kABytes + 32 * (j & 3), 16, 1024, 2);
-            const uint64_t bd =
-                smem_desc(sB + s * b_stage + (j >> 2) * b_bytes + 32 * (j & 3), 16, 1024, 2);
-            tc_mma_nvf4(dacc, ad, bd, idesc, fa + 4 * j, fbc + 4 * j * S, (ks | j) != 0);
+#pragma unroll
+          for (int j = 0; j < steps_per_stage; ++j) {
+            if (j < kk) {
+              // step j: chunk j / 4 of the stage, 32 bytes (K = 64) per step in it
+              const uint32_t a_off = ((j >> 2) * kABytes + 32 * (j & 3)) >> 4;
+              const uint32_t b_off = ((j >> 2) * b_bytes + 32 * (j & 3)) >> 4;
+              tc_mma_nvf4(dacc, ad + a_off, bd + b_off, idesc, fa + 4 * j, fbc + 4 * j * S,
+                          (ks | j) != 0);
+            }
           }
           tc_commit(smem_u32(&empty_bar[s]));
+          if (++s == ST) {
+            s = 0;
+            phase ^= 1u;
+          }
         }
+        if (stop) break;
         tc_commit(smem_u32(&accf_bar[b]));
       }
     }
@@ -532,42 +553,34 @@ static int sm_count() {
   return n;
 }
 
-template <int KIND, int EPW, int CTAS>
+template <int KIND, int TILE>
 static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
                               int max_tiles, cudaStream_t stream, bool pdl) {
   p.prefetch = pdl ? 1 : 0;
-  p.stages = stages_for(p.tile_m, KIND);
-  p.acc_bufs = acc_bufs_for(p.tile_m);
-  p.chunks = chunks_for(p.tile_m);
-  const size_t smem = gemm_smem_bytes(p.tile_m, KIND);
-  auto kern = grouped_gemm_kernel<KIND, EPW, CTAS>;
-  size_t most = 0;
-  for (int t : {32, 64, 128, 256}) {
-    const size_t b = gemm_smem_bytes(t, KIND);
-    most = b > most ? b : most;
-  }
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)most);
+  constexpr size_t smem = gemm_smem_bytes(TILE, KIND);
+  auto kern = grouped_gemm_kernel<KIND, TILE>;
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (err != cudaSuccess) return err;
   // ctas_per_sm CTAs per SM; CTAs past the live unit count exit at once.
   const long long units = (long long)max_tiles * (p.rows_w / kWTile);
   const long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
   const int grid = (int)(units < slots ? units : slots);
-  return launch_kernel(kern, dim3(grid), dim3(64 + 32 * EPW), smem, stream, pdl, ta, tb, p);
+  return launch_kernel(kern, dim3(grid), dim3(64 + 32 * epi_warps_for(TILE)), smem, stream, pdl, ta,
+                       tb, p);
 }
 
 template <int KIND>
 static cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
                                int max_tiles, cudaStream_t stream, bool pdl) {
-  constexpr TileCfg c32 = tile_cfg(32), c64 = tile_cfg(64), c128 = tile_cfg(128), c256 = tile_cfg(256);
   switch (p.tile_m) {
     case 32:
-      return launch_one<KIND, c32.epi_warps, c32.ctas>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<KIND, 32>(ta, tb, p, max_tiles, stream, pdl);
     case 64:
-      return launch_one<KIND, c64.epi_warps, c64.ctas>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<KIND, 64>(ta, tb, p, max_tiles, stream, pdl);
     case 128:
-      return launch_one<KIND, c128.epi_warps, c128.ctas>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<KIND, 128>(ta, tb, p, max_tiles, stream, pdl);
     default:
-      return launch_one<KIND, c256.epi_warps, c256.ctas>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<KIND, 256>(ta, tb, p, max_tiles, stream, pdl);
   }
 }
 
@@ -600,7 +613,6 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
   p.rows_w = 2 * I;
   p.K = H;
   p.tile_m = tile_m;
-  p.S = sf_atoms_per_tile(tile_m);
   p.out_cols = I;
   if (launch_kind<1>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM1 launch failed";
@@ -634,7 +646,6 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
   p.rows_w = H;
   p.K = I;
   p.tile_m = tile_m;
-  p.S = sf_atoms_per_tile(tile_m);
   p.out_cols = H;
   if (launch_kind<2>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM2 launch failed";
