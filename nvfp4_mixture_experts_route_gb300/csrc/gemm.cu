@@ -93,24 +93,34 @@ struct GemmParams {
 // two, 121 us with three). Each epilogue warp works through its accumulator
 // columns as one dependent instruction stream, so the larger tiles take two
 // warps per TMEM lane quadrant (8 in all) that split the route columns.
+//
+// route_m: the MMA's M = 128 rows are the route tile itself and N = 128 its
+// weight rows (128-row tiles only; M = 128 is the MMA's full-rate shape and
+// smaller route tiles need the swapped form). A lane of the accumulator is
+// then a route row holding gate and up of the same intermediate columns, so
+// GEMM1's epilogue needs no transposing staging buffer (its shared memory
+// goes to the ring) and GEMM2 stores each route row contiguously.
 struct TileCfg {
   int ctas, acc_bufs, chunks, epi_warps, epi_cols;
+  bool route_m;
 };
 __host__ __device__ constexpr TileCfg tile_cfg(int tile_m) {
-  return tile_m <= 32    ? TileCfg{3, 2, 1, 4, 16}
-         : tile_m <= 64  ? TileCfg{2, 2, 1, 4, 16}
-         : tile_m <= 128 ? TileCfg{2, 1, 1, 8, 32}
-                         : TileCfg{1, 1, 1, 8, 32};
+  return tile_m <= 32    ? TileCfg{3, 2, 1, 4, 16, false}
+         : tile_m <= 64  ? TileCfg{2, 2, 1, 4, 16, false}
+         : tile_m <= 128 ? TileCfg{2, 1, 1, 8, 32, true}
+                         : TileCfg{1, 1, 1, 8, 32, false};
 }
 __host__ __device__ constexpr int ctas_per_sm(int tile_m) { return tile_cfg(tile_m).ctas; }
 __host__ __device__ constexpr int acc_bufs_for(int tile_m) { return tile_cfg(tile_m).acc_bufs; }
 __host__ __device__ constexpr int chunks_for(int tile_m) { return tile_cfg(tile_m).chunks; }
 __host__ __device__ constexpr int epi_warps_for(int tile_m) { return tile_cfg(tile_m).epi_warps; }
 __host__ __device__ constexpr int epi_cols_for(int tile_m) { return tile_cfg(tile_m).epi_cols; }
-// Only GEMM1's epilogue stages through shared memory (its SwiGLU pairs rows
-// of two lanes); GEMM2's ring takes the room instead.
+// Only GEMM1's swapped-form epilogue stages through shared memory (its
+// SwiGLU pairs rows of two lanes); elsewhere the ring takes the room.
 __host__ __device__ constexpr uint32_t epi_bytes_for(int tile_m, int kind) {
-  return kind == 1 ? (uint32_t)(epi_warps_for(tile_m) * epi_cols_for(tile_m) * kEpiStride * 4) : 0u;
+  return kind == 1 && !tile_cfg(tile_m).route_m
+             ? (uint32_t)(epi_warps_for(tile_m) * epi_cols_for(tile_m) * kEpiStride * 4)
+             : 0u;
 }
 
 __host__ __device__ constexpr int sf_atoms_for(int tile_m) { return (tile_m + 127) / 128; }
@@ -185,6 +195,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The same load without the wait: the registers are valid only after
+// tmem_wait_ld(), which lets one warp have several loads in flight.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // NVFP4 of one 16-element block with global scale g; same arithmetic as the
@@ -275,6 +303,7 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
 
   constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, KIND);
   constexpr int NB = acc_bufs_for(TILE), CH = chunks_for(TILE), EPW = epi_warps_for(TILE);
+  constexpr bool kRouteM = tile_cfg(TILE).route_m;
   // Per stage: CH chunks of K = 256, i.e. up to 4 * CH MMA steps of K = 64.
   constexpr uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;  // one chunk of the route box
   constexpr uint32_t a_stage = CH * kABytes, b_stage = CH * b_bytes;
@@ -431,8 +460,12 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
               // step j: chunk j / 4 of the stage, 32 bytes (K = 64) per step in it
               const uint32_t a_off = ((j >> 2) * kABytes + 32 * (j & 3)) >> 4;
               const uint32_t b_off = ((j >> 2) * b_bytes + 32 * (j & 3)) >> 4;
-              tc_mma_nvf4(dacc, ad + a_off, bd + b_off, idesc, fa + 4 * j, fbc + 4 * j * S,
-                          (ks | j) != 0);
+              if constexpr (kRouteM)  // A = route rows, B = weight rows
+                tc_mma_nvf4(dacc, bd + b_off, ad + a_off, idesc, fbc + 4 * j * S, fa + 4 * j,
+                            (ks | j) != 0);
+              else  // A = weight rows, B = route rows
+                tc_mma_nvf4(dacc, ad + a_off, bd + b_off, idesc, fa + 4 * j, fbc + 4 * j * S,
+                            (ks | j) != 0);
             }
           }
           tc_commit(smem_u32(&empty_bar[s]));
@@ -465,7 +498,63 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
       const int e = p.tile_expert[tau];
       const int row0 = tau * tile_m;
       const uint32_t taddr = tmem + (uint32_t)(b * tile_m) + ((uint32_t)(32 * q) << 16);
-      if (KIND == 1) {
+      if constexpr (kRouteM) {
+        // lane = route row r; accumulator column c = weight row mt * 128 + c.
+        // This warp takes column groups cc = half and half + 2 (32 columns
+        // each): both are read out of TMEM, the buffer goes back to the MMA
+        // issuer, and only then are they converted and stored.
+        static_assert(EPW == 8, "the route-rows-on-M epilogue takes two warps per quadrant");
+        const int r = row0 + 32 * q + lane;
+        uint32_t acc[2][32];
+        tmem_ld32_async(taddr + 32 * half, acc[0]);
+        tmem_ld32_async(taddr + 32 * (half + 2), acc[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&acce_bar[b]));
+        if constexpr (KIND == 1) {
+          // columns 32cc..32cc+31: gate and up of intermediate columns
+          // 16 (4 mt + cc) + 0..15 (the prepared w13 granules)
+          const float s0 = p.s0[e], s1 = p.s1[e], a2g = *p.a2_gscale;
+          const int I = p.out_cols;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int cc = half + 2 * k;
+            float h[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g = s0 * __uint_as_float(acc[k][i]);
+              const float up = s1 * __uint_as_float(acc[k][16 + i]);
+              h[i] = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
+            }
+            uint2 codes;
+            uint32_t sfc;
+            quant16(h, a2g, codes, sfc);
+            *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * cc) = codes;
+            p.hq_sf[act_sf_offset(r, 4 * mt + cc, tile_m, I / 64, S)] = static_cast<uint8_t>(sfc);
+          }
+        } else {
+          const float g2 = p.s0[e];
+          if (r < p.tile_row_limit[tau]) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int cc = half + 2 * k;
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(acc[k][2 * i]) * g2,
+                                                                __uint_as_float(acc[k][2 * i + 1]) * g2);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(p.rows + (size_t)r * p.out_cols + mt * kWTile + 32 * cc);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+          }
+        }
+        continue;  // the buffer went back above
+      } else if (KIND == 1) {
         const float sc = lane < 16 ? p.s0[e] : p.s1[e];
         const float a2g = *p.a2_gscale;
         const int I = p.out_cols;
