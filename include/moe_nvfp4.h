@@ -162,10 +162,13 @@ typedef struct moe_weights {
 } moe_weights;
 
 typedef struct moe_route {
-  const int32_t* permuted_to_token; /* [max_padded_rows] */
-  const int32_t* tile_expert;       /* [max_tiles] */
-  const int32_t* tile_row_limit;    /* [max_tiles] */
-  const int32_t* totals;            /* [2] */
+  const int32_t* permuted_to_token;    /* [max_padded_rows] */
+  const int32_t* tile_expert;          /* [max_tiles] */
+  const int32_t* tile_row_limit;       /* [max_tiles] */
+  const int32_t* totals;               /* [2] */
+  const int32_t* expanded_to_permuted; /* [T, K]; read by the input quantizer, which
+                                          quantizes each token once and writes it to
+                                          the rows of its routes */
 } moe_route;
 
 /* Workspace bytes moe_nvfp4_experts needs (the permuted NVFP4 activations

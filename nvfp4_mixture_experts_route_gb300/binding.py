@@ -53,6 +53,7 @@ class MoeRoute(C.Structure):
         ("tile_expert", C.c_void_p),
         ("tile_row_limit", C.c_void_p),
         ("totals", C.c_void_p),
+        ("expanded_to_permuted", C.c_void_p),
     ]
 
 
@@ -195,7 +196,7 @@ class Route:
 
     def struct(self) -> MoeRoute:
         return MoeRoute(_ptr(self.permuted_to_token), _ptr(self.tile_expert), _ptr(self.tile_row_limit),
-                        _ptr(self.totals))
+                        _ptr(self.totals), _ptr(self.expanded_to_permuted))
 
 
 def alloc_route(T: int, K: int, E: int, tile_m: int, device) -> Route:

@@ -14,8 +14,8 @@ cudaError_t launch_route_permute(const int32_t*, int, int, int, int, int, int, i
                                  cudaStream_t);
 size_t route_smem_bytes(int E);
 cudaError_t launch_quantize_permute(const void*, const void*, const void*, const float*,
-                                    const int32_t*, const int32_t*, int, int, int, uint8_t*,
-                                    uint8_t*, cudaStream_t);
+                                    const int32_t*, const int32_t*, const int32_t*, int, int, int,
+                                    int, int, int, uint8_t*, uint8_t*, cudaStream_t);
 cudaError_t launch_act_scales_io(int, uint8_t*, uint8_t*, int, int, int, cudaStream_t);
 cudaError_t launch_prepare_weights(const void*, const void*, const void*, const void*, int, int,
                                    int, void*, void*, void*, void*, cudaStream_t);
@@ -161,7 +161,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-int moe_abi_version(void) { return 1; }
+int moe_abi_version(void) { return 2; }
 
 int moe_prepared_sizes(int E, int H, int I, size_t out_bytes[4]) {
   if (!out_bytes) return fail(MOE_ERR_INVALID_ARG, "out_bytes is null");
@@ -242,12 +242,14 @@ int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const f
     if (!aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
   } else {
     if (!a || !a_sf) return fail(MOE_ERR_INVALID_ARG, "give x, or a and a_sf");
-    if (!aligned(a, 8)) return fail(MOE_ERR_INVALID_ARG, "a must be 8-byte aligned");
+    if (!aligned(a, 16) || !aligned(a_sf, 4))
+      return fail(MOE_ERR_INVALID_ARG, "a must be 16-byte and a_sf 4-byte aligned");
   }
+  if (!r->expanded_to_permuted) return fail(MOE_ERR_INVALID_ARG, "route expanded_to_permuted is null");
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
-  cudaError_t err = moe::launch_quantize_permute(x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale,
-                                                 r->permuted_to_token, r->totals, H, tile_m, L.P,
-                                                 base + L.a_codes, base + L.a_sf, as_stream(stream));
+  cudaError_t err = moe::launch_quantize_permute(
+      x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, r->expanded_to_permuted, r->tile_row_limit,
+      r->totals, T, K, H, tile_m, L.P, L.MT, base + L.a_codes, base + L.a_sf, as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
 }
 

@@ -38,52 +38,78 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
   }
 }
 
-// One thread per (permuted row, 16-element block); rows past totals[1] are
-// left alone. Padding rows only get zero scales: with a zero block scale the
-// codes (always finite e2m1 values) contribute exactly 0 to every product,
-// so their bytes need not be written.
+// Work item (token t, group c of four 16-element blocks): the group is
+// quantized once and its 32 code bytes and 4 scale bytes (contiguous in the
+// scale atom) are written to the row of each of the token's routes, found
+// through expanded_to_permuted. Items past the tokens zero the scales of the
+// padding rows of each live tile (rows tile_row_limit .. the tile's end):
+// with a zero block scale the codes, always finite e2m1 values, contribute
+// exactly 0 to every product, so padding-row codes are never written.
+// Reads x once; writes each route row once.
 __global__ void __launch_bounds__(256) quantize_permute_kernel(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
-    const int32_t* __restrict__ permuted_to_token, const int32_t* __restrict__ totals, int H,
-    int tile_m, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
+    const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales) {
   pdl_wait();
   pdl_trigger();
+  const int ng = H / 64;  // four-block groups per row
   const int nb = H / 16;
-  const int rows = totals[1];
+  const long long n_tok = (long long)T * ng;
+  const long long n_all = n_tok + (long long)totals[0] * ng;
   const float g = (x != nullptr) ? *gscale : 0.f;
   const int S = sf_atoms_per_tile(tile_m);
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-       idx < (long long)rows * nb; idx += (long long)gridDim.x * blockDim.x) {
-    const int p = (int)(idx / nb), b = (int)(idx % nb);
-    const int t = permuted_to_token[p];
-    uint32_t lo = 0, hi = 0, sfc = 0;
-    if (t >= 0) {
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n_all;
+       idx += (long long)gridDim.x * blockDim.x) {
+    if (idx < n_tok) {
+      const int t = (int)(idx / ng), c = (int)(idx % ng);
+      uint4 q0, q1;  // 32 code bytes: blocks 4c .. 4c+3
+      uint32_t sf4;  // their 4 scale bytes, block 4c in the low byte
       if (x != nullptr) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 16 * b);
-        const uint4 u0 = src[0], u1 = src[1];
-        const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
-        const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
-        float v[16];
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 64 * c);
+        uint32_t lo[4], hi[4], sfc[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f0 = __bfloat1622float2(h0[i]);
-          const float2 f1 = __bfloat1622float2(h1[i]);
-          v[2 * i] = f0.x;
-          v[2 * i + 1] = f0.y;
-          v[8 + 2 * i] = f1.x;
-          v[8 + 2 * i + 1] = f1.y;
+        for (int bq = 0; bq < 4; ++bq) {
+          const uint4 u0 = src[2 * bq], u1 = src[2 * bq + 1];
+          const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
+          const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f0 = __bfloat1622float2(h0[i]);
+            const float2 f1 = __bfloat1622float2(h1[i]);
+            v[2 * i] = f0.x;
+            v[2 * i + 1] = f0.y;
+            v[8 + 2 * i] = f1.x;
+            v[8 + 2 * i + 1] = f1.y;
+          }
+          quantize_block16(v, g, lo[bq], hi[bq], sfc[bq]);
         }
-        quantize_block16(v, g, lo, hi, sfc);
+        q0 = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+        q1 = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+        sf4 = sfc[0] | (sfc[1] << 8) | (sfc[2] << 16) | (sfc[3] << 24);
       } else {
-        const uint2 c = *reinterpret_cast<const uint2*>(a_in + (size_t)t * (H / 2) + 8 * b);
-        lo = c.x;
-        hi = c.y;
-        sfc = a_sf_in[(size_t)t * nb + b];
+        const uint4* src = reinterpret_cast<const uint4*>(a_in + (size_t)t * (H / 2) + 32 * c);
+        q0 = src[0];
+        q1 = src[1];
+        sf4 = *reinterpret_cast<const uint32_t*>(a_sf_in + (size_t)t * nb + 4 * c);
       }
+      for (int k = 0; k < K; ++k) {
+        const int p = e2p[(size_t)t * K + k];
+        if (p < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)p * (H / 2) + 32 * c);
+        dst[0] = q0;
+        dst[1] = q1;
+        *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = sf4;
+      }
+    } else {
+      const long long i2 = idx - n_tok;
+      const int tau = (int)(i2 / ng), c = (int)(i2 % ng);
+      const int end = (tau + 1) * tile_m;
+      for (int p = tile_row_limit[tau]; p < end; ++p)
+        *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = 0u;
     }
-    if (t >= 0) *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = make_uint2(lo, hi);
-    scales[act_sf_offset(p, b, tile_m, H / 64, S)] = static_cast<uint8_t>(sfc);
   }
 }
 
@@ -111,14 +137,16 @@ static int grid_for(long long work, int threads) {
 }
 
 cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_sf,
-                                    const float* a1_gscale, const int32_t* p2t,
-                                    const int32_t* totals, int H, int tile_m, int P, uint8_t* codes,
+                                    const float* a1_gscale, const int32_t* e2p,
+                                    const int32_t* tile_row_limit, const int32_t* totals, int T,
+                                    int K, int H, int tile_m, int P, int MT, uint8_t* codes,
                                     uint8_t* scales, cudaStream_t stream) {
-  const int grid = grid_for((long long)P * (H / 16), 256);
+  (void)P;
+  const int grid = grid_for((long long)(T + MT) * (H / 64), 256);
   return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
-                       reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, p2t, totals, H, tile_m, codes,
-                       scales);
+                       reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, e2p, tile_row_limit, totals,
+                       T, K, H, tile_m, codes, scales);
 }
 
 cudaError_t launch_act_scales_io(int to_linear, uint8_t* atoms, uint8_t* linear, int K,

@@ -79,6 +79,35 @@ def test_route_permute_edge_cases(tile):
         _assert_route_equal(_route_np(_route_gpu(ids, E, tile)), want)
 
 
+@pytest.mark.parametrize("tile", [32, 128])
+def test_route_permute_many_routes_edge_cases(tile):
+    """Route counts that take the segmented (count / scan / scatter) path:
+    exactly two segments, a short last segment, everything on one expert,
+    nothing routed, E = 1024 with ragged segments, and -1 holes."""
+    rng = np.random.default_rng(11)
+    cases = [
+        (inputs.draw_topk(rng, 512, 64, 8, "uniform"), 64),     # R = 4096: two segments
+        (inputs.draw_topk(rng, 1531, 128, 8, "zipf"), 128),     # R = 12248: short tail
+        (np.full((6000, 1), 7, np.int32), 8),                   # one expert takes all
+        (-np.ones((4100, 2), np.int32), 16),                    # nothing routed
+        (inputs.draw_topk(rng, 2047, 1024, 3, "zipf"), 1024),   # E = 1024, ragged
+    ]
+    holes = inputs.draw_topk(rng, 3000, 32, 4, "uniform")
+    holes[::5, 2] = -1
+    cases.append((holes, 32))
+    for ids, E in cases:
+        want = orouting.route_metadata(ids, E, tile)
+        _assert_route_equal(_route_np(_route_gpu(ids, E, tile)), want)
+
+
+def test_route_permute_many_routes_refuses_bad_ids():
+    ids = inputs.draw_topk(np.random.default_rng(12), 2048, 64, 4, "uniform")
+    ids[1500, 3] = 64
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _route_gpu(ids, 64, 32, status=status)
+    assert int(status.item()) == -6
+
+
 def test_route_permute_refuses_bad_ids():
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     _route_gpu(np.array([[0, 8], [1, 2]], np.int32), 8, 32, status=status)
