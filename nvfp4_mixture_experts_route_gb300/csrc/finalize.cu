@@ -157,12 +157,15 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
 }
 
 // The same finalize with the token's K rows staged in shared memory by bulk
-// copies (one thread issues them all on one mbarrier): the HBM reads of a
-// whole token are in flight at once without holding registers, so two CTAs
-// per SM keep 2 x K x H x 2 bytes in flight. One CTA per token; each thread
-// owns VPT 8-element vectors of the hidden dimension, reads them from the
-// staged rows twice (sum of squares, then the weighted sum) and writes the
-// output row once. Used when K * H * 2 bytes fit kFinStagedMaxBytes.
+// copies, one mbarrier per route: one thread issues them all up front, and
+// the CTA normalises route k as soon as its row has landed while the later
+// rows are still in flight (a route's coefficient needs only its own sum of
+// squares). Two CTAs per SM keep two tokens' rows in flight without holding
+// registers. One CTA per token; each thread owns VPT 8-element vectors of
+// the hidden dimension, converts each of its row elements once, and applies
+// the gain to the weighted sum at the end (both readings apply g to the
+// normalised row: out = g * sum_k coef_k r_k). Used when K * H * 2 bytes fit
+// kFinStagedMaxBytes.
 constexpr int kFinStagedMaxBytes = 100 * 1024;
 constexpr int kFinMaxK = 64;
 
@@ -172,10 +175,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
     const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
     int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t staged[];  // K rows of H bf16
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ float red[kFinWarps][kFinMaxK];
+  __shared__ __align__(8) uint64_t bar[kFinMaxK];
+  __shared__ float red[2][kFinWarps];
   __shared__ int32_t rowp[kFinMaxK];
-  __shared__ float coef[kFinMaxK];
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -183,27 +185,28 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
   const int nvec = H / 8;
   const uint32_t row_bytes = (uint32_t)H * 2;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar), 1);
+    for (int k = 0; k < K; ++k) mbar_init(smem_u32(&bar[k]), 1);
     fence_barrier_init();
-    uint32_t bytes = 0;
     for (int k = 0; k < K; ++k) {
       const int p = e2p[(size_t)t * K + k];
       rowp[k] = p;
-      if (p >= 0) bytes += row_bytes;
+      if (p >= 0) {
+        mbar_arrive_expect_tx(smem_u32(&bar[k]), row_bytes);
+        bulk_load(smem_u32(staged) + k * row_bytes, rows + (size_t)p * H, row_bytes,
+                  smem_u32(&bar[k]));
+      }
     }
-    mbar_arrive_expect_tx(smem_u32(&bar), bytes);
-    for (int k = 0; k < K; ++k)
-      if (rowp[k] >= 0)
-        bulk_load(smem_u32(staged) + k * row_bytes, rows + (size_t)rowp[k] * H, row_bytes,
-                  smem_u32(&bar));
   }
   // gain g = 1 + gamma (fp32) while the rows arrive
-  float g[VPT][8];
+  float g[VPT][8], acc[VPT][8];
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = threadIdx.x + i * kFinThreads;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) g[i][q] = 1.f;
+    for (int q = 0; q < 8; ++q) {
+      g[i][q] = 1.f;
+      acc[i][q] = 0.f;
+    }
     if (v < nvec) {
       const uint4 u = *reinterpret_cast<const uint4*>(gamma + 8 * v);
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -215,77 +218,62 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
       }
     }
   }
-  __syncthreads();  // rowp[] and the barrier's initialisation are visible
-  // Bounded wait for the bulk copies (they read valid rows and always land;
-  // the limit only keeps a broken launch from spinning forever). A CTA that
-  // gives up waits once more, bounded, so that no copy into its shared
-  // memory is in flight when it exits, and writes no output.
-  {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(smem_u32(&bar), 0)) {
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        mbar_wait_cleanup(smem_u32(&bar), 0);
+  __syncthreads();  // rowp[] and the barriers' initialisation are visible
+  const __nv_bfloat16* srow = reinterpret_cast<const __nv_bfloat16*>(staged);
+  const float inv_h = 1.0f / (float)H;
+  for (int k = 0; k < K; ++k) {
+    if (rowp[k] < 0) continue;  // uniform across the block
+    // Bounded wait for route k's row (a bulk copy of a valid row always
+    // lands; the limit only keeps a broken launch from spinning forever).
+    // A CTA that gives up waits, bounded, for its other copies and exits
+    // without writing output.
+    {
+      const uint64_t t0 = global_timer_ns();
+      bool ok = true;
+      while (!mbar_try_wait(smem_u32(&bar[k]), 0)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) {
+        for (int j = k; j < K; ++j)
+          if (rowp[j] >= 0) mbar_wait_cleanup(smem_u32(&bar[j]), 0);
         return;
       }
     }
-  }
-  const __nv_bfloat16* srow = reinterpret_cast<const __nv_bfloat16*>(staged);
-  // Sums of squares of every route, one block reduction for all of them.
-  for (int k = 0; k < K; ++k) {
+    float f[VPT][8];  // route k's row, converted once
     float ss = 0.f;
-    if (rowp[k] >= 0) {
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int v = threadIdx.x + i * kFinThreads;
-        if (v < nvec) {
-          const uint4 u = *reinterpret_cast<const uint4*>(srow + (size_t)k * H + 8 * v);
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kFinThreads;
+      const uint4 u = v < nvec ? *reinterpret_cast<const uint4*>(srow + (size_t)k * H + 8 * v)
+                               : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = __bfloat1622float2(h[q]);
-            const float a = weight_before_norm ? f.x * g[i][2 * q] : f.x;
-            const float b = weight_before_norm ? f.y * g[i][2 * q + 1] : f.y;
-            ss = fmaf(a, a, ss);
-            ss = fmaf(b, b, ss);
-          }
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float2 x = __bfloat1622float2(h[q]);
+        f[i][2 * q] = x.x;
+        f[i][2 * q + 1] = x.y;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float a = weight_before_norm ? f[i][q] * g[i][q] : f[i][q];
+        ss = fmaf(a, a, ss);
       }
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
-    if (lane == 0) red[warp][k] = ss;
-  }
-  __syncthreads();
-  if (threadIdx.x < K) {
-    const int k = threadIdx.x;
+    if (lane == 0) red[k & 1][warp] = ss;  // two buffers: one barrier per route
+    __syncthreads();
     float total = 0.f;
 #pragma unroll
-    for (int w = 0; w < kFinWarps; ++w) total += red[w][k];  // fixed order
-    coef[k] = rowp[k] >= 0 ? topk_w[(size_t)t * K + k] / sqrtf(total / (float)H + eps) : 0.f;
-  }
-  __syncthreads();
-  float acc[VPT][8];
+    for (int w = 0; w < kFinWarps; ++w) total += red[k & 1][w];  // fixed order
+    const float ck = topk_w[(size_t)t * K + k] / sqrtf(total * inv_h + eps);
 #pragma unroll
-  for (int i = 0; i < VPT; ++i)
+    for (int i = 0; i < VPT; ++i)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
-  for (int k = 0; k < K; ++k) {
-    if (rowp[k] < 0) continue;  // uniform across the block
-    const float ck = coef[k];
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = threadIdx.x + i * kFinThreads;
-      if (v < nvec) {
-        const uint4 u = *reinterpret_cast<const uint4*>(srow + (size_t)k * H + 8 * v);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(h[q]);
-          acc[i][2 * q] += (f.x * g[i][2 * q]) * ck;
-          acc[i][2 * q + 1] += (f.y * g[i][2 * q + 1]) * ck;
-        }
-      }
-    }
+      for (int q = 0; q < 8; ++q) acc[i][q] = fmaf(f[i][q], ck, acc[i][q]);
   }
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
@@ -294,7 +282,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
       uint4 o;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(acc[i][2 * q], acc[i][2 * q + 1]);
+      for (int q = 0; q < 4; ++q)
+        h[q] = __floats2bfloat162_rn(acc[i][2 * q] * g[i][2 * q], acc[i][2 * q + 1] * g[i][2 * q + 1]);
       *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * v) = o;
     }
   }
@@ -314,7 +303,7 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
   auto op = reinterpret_cast<__nv_bfloat16*>(out);
   cudaError_t err = cudaSuccess;
   const size_t staged = (size_t)K * H * 2;
-  if (nparts == 1 && K <= kFinMaxK && staged <= (size_t)kFinStagedMaxBytes && vpt <= 8) {
+  if (nparts == 1 && K <= kFinMaxK && staged <= (size_t)kFinStagedMaxBytes && vpt <= 5) {
     auto rows = reinterpret_cast<const __nv_bfloat16*>(parts[0]);
 #define MOE_FIN_STAGED(n)                                                                       \
   case n:                                                                                       \
@@ -330,9 +319,6 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
       MOE_FIN_STAGED(3)
       MOE_FIN_STAGED(4)
       MOE_FIN_STAGED(5)
-      MOE_FIN_STAGED(6)
-      MOE_FIN_STAGED(7)
-      MOE_FIN_STAGED(8)
       default:
         return cudaErrorInvalidValue;
     }

@@ -41,12 +41,13 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
 // Work item (token t, group c of four 16-element blocks): the group is
 // quantized once and its 32 code bytes and 4 scale bytes (contiguous in the
 // scale atom) are written to the row of each of the token's routes, found
-// through expanded_to_permuted. Items past the tokens zero the scales of the
-// padding rows of each live tile (rows tile_row_limit .. the tile's end):
+// through expanded_to_permuted. The first items (they loop over rows, so
+// they start first) zero the scales of the padding rows of each live tile
+// (rows tile_row_limit .. the tile's end):
 // with a zero block scale the codes, always finite e2m1 values, contribute
 // exactly 0 to every product, so padding-row codes are never written.
 // Reads x once; writes each route row once.
-__global__ void __launch_bounds__(256) quantize_permute_kernel(
+__global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
     const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
@@ -56,14 +57,15 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
   pdl_trigger();
   const int ng = H / 64;  // four-block groups per row
   const int nb = H / 16;
-  const long long n_tok = (long long)T * ng;
-  const long long n_all = n_tok + (long long)totals[0] * ng;
+  const long long n_pad = (long long)totals[0] * ng;
+  const long long n_all = n_pad + (long long)T * ng;
   const float g = (x != nullptr) ? *gscale : 0.f;
   const int S = sf_atoms_per_tile(tile_m);
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n_all;
        idx += (long long)gridDim.x * blockDim.x) {
-    if (idx < n_tok) {
-      const int t = (int)(idx / ng), c = (int)(idx % ng);
+    if (idx >= n_pad) {
+      const long long i2 = idx - n_pad;
+      const int t = (int)(i2 / ng), c = (int)(i2 % ng);
       uint4 q0, q1;  // 32 code bytes: blocks 4c .. 4c+3
       uint32_t sf4;  // their 4 scale bytes, block 4c in the low byte
       if (x != nullptr) {
@@ -104,8 +106,7 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
         *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = sf4;
       }
     } else {
-      const long long i2 = idx - n_tok;
-      const int tau = (int)(i2 / ng), c = (int)(i2 % ng);
+      const int tau = (int)(idx / ng), c = (int)(idx % ng);
       const int end = (tau + 1) * tile_m;
       for (int p = tile_row_limit[tau]; p < end; ++p)
         *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = 0u;
