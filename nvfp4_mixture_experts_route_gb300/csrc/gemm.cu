@@ -175,9 +175,6 @@ static_assert(tile_fits(32, 1) && tile_fits(64, 1) && tile_fits(128, 1) && tile_
                   tile_fits(32, 2) && tile_fits(64, 2) && tile_fits(128, 2) && tile_fits(256, 2),
               "a route-tile shape overflows its pipeline, tensor memory or shared memory budget");
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 // 32 lanes x 32 bit, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
