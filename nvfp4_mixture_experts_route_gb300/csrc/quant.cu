@@ -38,15 +38,16 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
   }
 }
 
-// Work item (token t, group c of four 16-element blocks): the group is
-// quantized once and its 32 code bytes and 4 scale bytes (contiguous in the
-// scale atom) are written to the row of each of the token's routes, found
-// through expanded_to_permuted. The first items (they loop over rows, so
-// they start first) zero the scales of the padding rows of each live tile
-// (rows tile_row_limit .. the tile's end):
-// with a zero block scale the codes, always finite e2m1 values, contribute
-// exactly 0 to every product, so padding-row codes are never written.
-// Reads x once; writes each route row once.
+// Token work item (token t, 16-element block b): the block is quantized once
+// and its 8 code bytes are written to the row of each of the token's routes,
+// found through expanded_to_permuted; the first thread of each quad writes
+// the quad's 4 scale bytes (contiguous in the scale atom). Padding work item (a warp, tile tau, group c):
+// lane i zeroes the 4 scale bytes of rows 32j + i (j < tile_m / 32) of the
+// tile that lie past its row limit; with a zero block scale the codes, always
+// finite e2m1 values, contribute exactly 0 to every product, so padding-row
+// codes are never written. The padding items come first (warp-granular: each
+// warp takes a whole item), then the token items. Reads x once; writes each
+// route row once.
 __global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
@@ -57,59 +58,65 @@ __global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
   pdl_trigger();
   const int ng = H / 64;  // four-block groups per row
   const int nb = H / 16;
-  const long long n_pad = (long long)totals[0] * ng;
-  const long long n_all = n_pad + (long long)T * ng;
   const float g = (x != nullptr) ? *gscale : 0.f;
   const int S = sf_atoms_per_tile(tile_m);
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n_all;
+  // Padding: one warp per (tile, group).
+  {
+    const int lane = threadIdx.x & 31;
+    const long long n_pad = (long long)totals[0] * ng;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+    for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_pad;
+         w += nwarps) {
+      const int tau = (int)(w / ng), c = (int)(w % ng);
+      const int limit = tile_row_limit[tau];
+      for (int j = 0; j < tile_m; j += 32) {
+        const int p = tau * tile_m + j + lane;
+        if (p >= limit)
+          *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = 0u;
+      }
+    }
+  }
+  // Tokens: one thread per (token, 16-element block); the four threads of a
+  // quad hold the four blocks whose scale bytes are contiguous in the atom
+  // (nb is a multiple of 8, so quads never straddle a token or the end).
+  const int lane = threadIdx.x & 31;
+  const unsigned quad = 0xFu << (lane & ~3);
+  const long long n_tok = (long long)T * nb;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n_tok;
        idx += (long long)gridDim.x * blockDim.x) {
-    if (idx >= n_pad) {
-      const long long i2 = idx - n_pad;
-      const int t = (int)(i2 / ng), c = (int)(i2 % ng);
-      uint4 q0, q1;  // 32 code bytes: blocks 4c .. 4c+3
-      uint32_t sf4;  // their 4 scale bytes, block 4c in the low byte
-      if (x != nullptr) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 64 * c);
-        uint32_t lo[4], hi[4], sfc[4];
+    const int t = (int)(idx / nb), b = (int)(idx % nb);
+    uint2 q;
+    uint32_t sfc;
+    if (x != nullptr) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 16 * b);
+      const uint4 u0 = src[0], u1 = src[1];
+      const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
+      const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
+      float v[16];
 #pragma unroll
-        for (int bq = 0; bq < 4; ++bq) {
-          const uint4 u0 = src[2 * bq], u1 = src[2 * bq + 1];
-          const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
-          const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f0 = __bfloat1622float2(h0[i]);
-            const float2 f1 = __bfloat1622float2(h1[i]);
-            v[2 * i] = f0.x;
-            v[2 * i + 1] = f0.y;
-            v[8 + 2 * i] = f1.x;
-            v[8 + 2 * i + 1] = f1.y;
-          }
-          quantize_block16(v, g, lo[bq], hi[bq], sfc[bq]);
-        }
-        q0 = make_uint4(lo[0], hi[0], lo[1], hi[1]);
-        q1 = make_uint4(lo[2], hi[2], lo[3], hi[3]);
-        sf4 = sfc[0] | (sfc[1] << 8) | (sfc[2] << 16) | (sfc[3] << 24);
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(a_in + (size_t)t * (H / 2) + 32 * c);
-        q0 = src[0];
-        q1 = src[1];
-        sf4 = *reinterpret_cast<const uint32_t*>(a_sf_in + (size_t)t * nb + 4 * c);
+      for (int i = 0; i < 4; ++i) {
+        const float2 f0 = __bfloat1622float2(h0[i]);
+        const float2 f1 = __bfloat1622float2(h1[i]);
+        v[2 * i] = f0.x;
+        v[2 * i + 1] = f0.y;
+        v[8 + 2 * i] = f1.x;
+        v[8 + 2 * i + 1] = f1.y;
       }
-      for (int k = 0; k < K; ++k) {
-        const int p = e2p[(size_t)t * K + k];
-        if (p < 0) continue;
-        uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)p * (H / 2) + 32 * c);
-        dst[0] = q0;
-        dst[1] = q1;
-        *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = sf4;
-      }
+      quantize_block16(v, g, q.x, q.y, sfc);
     } else {
-      const int tau = (int)(idx / ng), c = (int)(idx % ng);
-      const int end = (tau + 1) * tile_m;
-      for (int p = tile_row_limit[tau]; p < end; ++p)
-        *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = 0u;
+      q = *reinterpret_cast<const uint2*>(a_in + (size_t)t * (H / 2) + 8 * b);
+      sfc = a_sf_in[(size_t)t * nb + b];
+    }
+    // the quad's four scale bytes, block 4 * (b / 4) in the low byte
+    const int base = lane & ~3;
+    const uint32_t sf4 = __shfl_sync(quad, sfc, base) | (__shfl_sync(quad, sfc, base + 1) << 8) |
+                         (__shfl_sync(quad, sfc, base + 2) << 16) | (__shfl_sync(quad, sfc, base + 3) << 24);
+    for (int k = 0; k < K; ++k) {
+      const int p = e2p[(size_t)t * K + k];
+      if (p < 0) continue;
+      *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = q;
+      if ((b & 3) == 0)
+        *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, b, tile_m, H / 64, S)) = sf4;
     }
   }
 }
@@ -143,7 +150,10 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                                     int K, int H, int tile_m, int P, int MT, uint8_t* codes,
                                     uint8_t* scales, cudaStream_t stream) {
   (void)P;
-  const int grid = grid_for((long long)(T + MT) * (H / 64), 256);
+  // enough warps for one padding item each (one global read then one store
+  // per lane), and threads for the token items
+  const long long pad_threads = (long long)MT * (H / 64) * 32, tok_threads = (long long)T * (H / 16);
+  const int grid = grid_for(pad_threads > tok_threads ? pad_threads : tok_threads, 256);
   return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
                        reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, e2p, tile_row_limit, totals,
