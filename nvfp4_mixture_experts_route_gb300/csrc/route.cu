@@ -21,7 +21,11 @@ namespace moe {
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
-__global__ void __launch_bounds__(kRouteThreads, 1)
+// NT threads (E <= NT): 1024 in general, 256 for few routes and experts,
+// where the per-expert scans over the warps and the block barriers are the
+// latency.
+template <int NT>
+__global__ void __launch_bounds__(NT, 1)
     route_permute_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int tile_m,
                          int P, int MT, int32_t* __restrict__ expert_counts,
                          int32_t* __restrict__ expert_offsets,
@@ -29,19 +33,20 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
                          int32_t* __restrict__ permuted_to_token, int32_t* __restrict__ tile_expert,
                          int32_t* __restrict__ tile_row_limit, int32_t* __restrict__ totals,
                          int32_t* status) {
-  extern __shared__ int32_t hist[];  // [kRouteWarps][E]
-  __shared__ int32_t warp_sums[kRouteWarps];
+  constexpr int NW = NT / 32;
+  extern __shared__ int32_t hist[];  // [NW][E]
+  __shared__ int32_t warp_sums[NW];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Launched in plain stream order; the kernels after it wait for it to
   // complete before they read what it writes.
   pdl_trigger();
   const int R = T * K;
-  const int seg = (R + kRouteWarps - 1) / kRouteWarps;
+  const int seg = (R + NW - 1) / NW;
   const int beg = min(R, warp * seg), end = min(R, beg + seg);
 
-  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
-  for (int i = tid; i < P; i += kRouteThreads) permuted_to_token[i] = -1;
-  for (int i = tid; i < MT; i += kRouteThreads) {
+  for (int i = tid; i < NW * E; i += NT) hist[i] = 0;
+  for (int i = tid; i < P; i += NT) permuted_to_token[i] = -1;
+  for (int i = tid; i < MT; i += NT) {
     tile_expert[i] = -1;
     tile_row_limit[i] = -1;
   }
@@ -69,7 +74,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // Per expert: scan over warps (warp-relative starts) and the padded count.
   int padded = 0, count = 0;
   if (tid < E) {
-    for (int w = 0; w < kRouteWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const int c = hist[w * E + tid];
       hist[w * E + tid] = count;
       count += c;
@@ -86,21 +91,21 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int s = warp_sums[lane];
+    int s = lane < NW ? warp_sums[lane] : 0;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, s, d);
       if (lane >= d) s += v;
     }
-    warp_sums[lane] = s;  // inclusive over warps
+    if (lane < NW) warp_sums[lane] = s;  // inclusive over warps
   }
   __syncthreads();
   const int offset = incl - padded + (warp > 0 ? warp_sums[warp - 1] : 0);
-  const int total = warp_sums[kRouteWarps - 1];
+  const int total = warp_sums[NW - 1];
   if (tid < E) {
     expert_counts[tid] = count;
     expert_offsets[tid] = offset;
-    for (int w = 0; w < kRouteWarps; ++w) hist[w * E + tid] += offset;
+    for (int w = 0; w < NW; ++w) hist[w * E + tid] += offset;
     // Tiles of this expert: [offset/tile_m, (offset+padded)/tile_m).
     const int t0 = offset / tile_m, nt = padded / tile_m;
     for (int i = 0; i < nt; ++i) {
@@ -187,13 +192,20 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_scan_kernel(
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Segments are read and written in batches of 8 so that the loads of a
+  // batch are in flight together.
+  constexpr int kBatch = 8;
   int count = 0, padded = 0;
   if (tid < E) {
-    for (int g = 0; g < G; ++g) {
-      int32_t* slot = e2p + (size_t)g * seg + tid;
-      const int c = *slot;
-      *slot = count;  // exclusive prefix over the segments
-      count += c;
+    for (int g0 = 0; g0 < G; g0 += kBatch) {
+      int c[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) c[u] = g0 + u < G ? e2p[(size_t)(g0 + u) * seg + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (g0 + u < G) e2p[(size_t)(g0 + u) * seg + tid] = count;  // exclusive prefix
+        count += c[u];
+      }
     }
     padded = (count + tile_m - 1) / tile_m * tile_m;
   }
@@ -220,7 +232,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_scan_kernel(
   if (tid < E) {
     expert_counts[tid] = count;
     expert_offsets[tid] = offset;
-    for (int g = 0; g < G; ++g) e2p[(size_t)g * seg + tid] += offset;
+    for (int g0 = 0; g0 < G; g0 += kBatch) {
+      int c[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) c[u] = g0 + u < G ? e2p[(size_t)(g0 + u) * seg + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (g0 + u < G) e2p[(size_t)(g0 + u) * seg + tid] = c[u] + offset;
+    }
     const int t0 = offset / tile_m, nt = padded / tile_m;
     for (int i = 0; i < nt; ++i) {
       tile_expert[t0 + i] = tid;
@@ -323,12 +342,18 @@ cudaError_t launch_route_permute(const int32_t* topk_ids, int T, int K, int E, i
     return launch_kernel(route_scatter_kernel, dim3(G), dim3(kRouteThreads), smem, stream, true,
                          topk_ids, T * K, K, E, seg, e2p, p2t);
   }
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(route_permute_kernel),
+  if (T * K <= 2048 && E <= 256) {
+    route_permute_kernel<256><<<1, 256, sizeof(int32_t) * 8 * (size_t)E, stream>>>(
+        topk_ids, T, K, E, tile_m, P, MT, counts, offsets, e2p, p2t, tile_expert, tile_row_limit,
+        totals, status);
+    return cudaGetLastError();
+  }
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(route_permute_kernel<kRouteThreads>),
                                       (int)route_smem_bytes(1024));
   if (err != cudaSuccess) return err;
-  route_permute_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, T, K, E, tile_m, P, MT,
-                                                            counts, offsets, e2p, p2t, tile_expert,
-                                                            tile_row_limit, totals, status);
+  route_permute_kernel<kRouteThreads><<<1, kRouteThreads, smem, stream>>>(
+      topk_ids, T, K, E, tile_m, P, MT, counts, offsets, e2p, p2t, tile_expert, tile_row_limit,
+      totals, status);
   return cudaGetLastError();
 }
 
