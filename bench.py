@@ -261,7 +261,8 @@ def run_ours(args, w) -> None:
             ev[2].record(stream)
         B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out)
 
-    launches_per_step = 5
+    # route/permute (1 or 3 kernels), quantize, GEMM1, GEMM2, finalize
+    launches_per_step = B.route_kernels(T, K, E) + 4
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -356,7 +357,8 @@ def run_ours(args, w) -> None:
         "vs_baseline": None, "dtype": "e2m1xue4m3 (fp32 accumulate)", "data": "synthetic",
         "config": {**_config(w), "l2": f"{len(copies)} rotating prepared weight copies "
                                         f"({len(copies) * layer_bytes / 1e9:.2f} GB > L2)",
-                   "launch": "CUDA graph per step (5 kernels)" if graphs else "eager (5 kernels per step)"},
+                   "launch": (f"CUDA graph per step ({launches_per_step} kernels)" if graphs
+                              else f"eager ({launches_per_step} kernels per step)")},
         "roofline": ({"bound": "hbm", "kernel": "grouped_gemm_kernel<1> (GEMM1 + SwiGLU + requant)",
                       "achieved": gemm1_gbs, "peak": peak, "unit": "GB/s", "frac": gemm1_gbs / peak,
                       "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,

@@ -138,6 +138,11 @@ int moe_prepare_weights(const void* w13, const void* w13_sf, const void* w2,
 int moe_route_sizes(int T, int K, int E, int tile_m, int* max_padded_rows,
                     int* max_tiles);
 
+/* Kernels moe_route_permute enqueues for this shape: 1 (one CTA, few
+ * routes) or 3 (count / scan / scatter over segments of about 2048 routes,
+ * from T*K >= 4096). Returns the count, or a negative status for a bad shape. */
+int moe_route_kernels(int T, int K, int E);
+
 int moe_route_permute(const int32_t* topk_ids, int T, int K, int E,
                       int tile_m, int32_t* expert_counts,
                       int32_t* expert_offsets, int32_t* expanded_to_permuted,

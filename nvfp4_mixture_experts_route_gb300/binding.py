@@ -62,6 +62,7 @@ _I = C.c_int
 _SIGNATURES = {
     "moe_last_error": ([], C.c_char_p),
     "moe_abi_version": ([], _I),
+    "moe_route_kernels": ([_I, _I, _I], _I),
     "moe_prepared_sizes": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_prepare_weights": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_route_sizes": ([_I, _I, _I, _I, C.POINTER(_I), C.POINTER(_I)], _I),
@@ -175,6 +176,14 @@ def prepare_weights(w13, w13_sf, w2, w2_sf, stream=None) -> dict:
         _ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, H, I,
         _ptr(out["w13"]), _ptr(out["w13_sf"]), _ptr(out["w2"]), _ptr(out["w2_sf"]), _stream(stream)))
     return out
+
+
+def route_kernels(T: int, K: int, E: int) -> int:
+    """Kernels route_permute launches for this shape (1 or 3)."""
+    n = load().moe_route_kernels(T, K, E)
+    if n < 0:
+        _check(n)
+    return n
 
 
 def route_sizes(T: int, K: int, E: int, tile_m: int) -> tuple[int, int]:

@@ -13,6 +13,7 @@ cudaError_t launch_route_permute(const int32_t*, int, int, int, int, int, int, i
                                  int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
                                  cudaStream_t);
 size_t route_smem_bytes(int E);
+int route_kernel_count(int T, int K, int E);
 cudaError_t launch_quantize_permute(const void*, const void*, const void*, const float*,
                                     const int32_t*, const int32_t*, const int32_t*, int, int, int,
                                     int, int, int, uint8_t*, uint8_t*, cudaStream_t);
@@ -199,6 +200,13 @@ int moe_route_sizes(int T, int K, int E, int tile_m, int* max_padded_rows, int* 
   if (max_padded_rows) *max_padded_rows = d.P;
   if (max_tiles) *max_tiles = d.MT;
   return MOE_OK;
+}
+
+int moe_route_kernels(int T, int K, int E) {
+  RouteDims d;
+  int rc = route_dims(T, K, E, 32, &d);
+  if (rc) return rc;
+  return moe::route_kernel_count(T, K, E);
 }
 
 int moe_route_permute(const int32_t* topk_ids, int T, int K, int E, int tile_m,

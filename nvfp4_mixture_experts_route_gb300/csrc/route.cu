@@ -323,6 +323,11 @@ static bool multi_segments(int R, int E, int* G, int* seg) {
 
 size_t route_smem_bytes(int E) { return sizeof(int32_t) * kRouteWarps * (size_t)E; }
 
+int route_kernel_count(int T, int K, int E) {
+  int G = 0, seg = 0;
+  return multi_segments(T * K, E, &G, &seg) ? 3 : 1;
+}
+
 cudaError_t launch_route_permute(const int32_t* topk_ids, int T, int K, int E, int tile_m, int P,
                                  int MT, int32_t* counts, int32_t* offsets, int32_t* e2p,
                                  int32_t* p2t, int32_t* tile_expert, int32_t* tile_row_limit,

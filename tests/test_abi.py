@@ -77,3 +77,14 @@ def test_null_pointers_refused_before_any_launch(lib):
     # undersized workspace
     rc = lib.moe_experts_gemm2(C.byref(w), C.byref(r), 4, 256, 128, 8, 2, 32, 16, 1024, 16, None, None)
     assert rc == -3
+
+
+def test_route_kernel_count():
+    """One CTA for few routes, count / scan / scatter from 2 full segments
+    of 2048 routes whose last segment holds E slots."""
+    assert B.route_kernels(8, 8, 128) == 1
+    assert B.route_kernels(511, 8, 64) == 1      # 4088 routes: one segment
+    assert B.route_kernels(512, 8, 64) == 3      # 4096 routes: two segments
+    assert B.route_kernels(8192, 8, 128) == 3
+    assert B.route_kernels(0, 8, 128) == 1
+    assert B.route_kernels(2047, 2, 1024) == 1   # two segments, but the last holds < E slots
