@@ -87,4 +87,4 @@ def test_route_kernel_count():
     assert B.route_kernels(512, 8, 64) == 3      # 4096 routes: two segments
     assert B.route_kernels(8192, 8, 128) == 3
     assert B.route_kernels(0, 8, 128) == 1
-    assert B.route_kernels(2047, 2, 1024) == 1   # two segments, but the last holds < E slots
+    assert B.route_kernels(2047, 2, 1024) == 1   # 4094 routes: one segment
