@@ -385,6 +385,164 @@ def run_ours(args, w) -> None:
     print(json.dumps(line), flush=True)
 
 
+DENSE_METRIC = "pooler projection tokens/s at 1 GB300 and % of HBM (few tokens) / bf16 tensor (many) roofline"
+
+
+def run_dense(args, d) -> None:
+    """The pooler / unpooler projection alone (moe_dense_bf16), weights
+    rotated over copies that together exceed L2."""
+    import numpy as np
+    import torch
+
+    from nvfp4_mixture_experts_route_gb300 import binding as B
+    from nvfp4_mixture_experts_route_gb300 import inputs
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+    data = inputs.make_dense(d, seed=rank)
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    x = bf(data["x"])
+    w0 = bf(data["w"])
+    w_bytes = w0.numel() * 2
+    n_copies = max(args.copies, int(np.ceil(3 * 129e6 / w_bytes)))
+    ws_ = [w0] + [w0.clone() for _ in range(n_copies - 1)]
+    y = torch.empty((d.T, d.Dout), dtype=torch.bfloat16, device=dev)
+    need = B.dense_bf16_workspace_size(d.T, d.Din, d.Dout)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches = 2 if need else 1
+
+    def step(i):
+        B.dense_bf16(x, ws_[i % len(ws_)], out=y, ws=ws, status=status)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    graphs = []
+    if args.graph:
+        for c in range(len(ws_)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(c)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            if graphs:
+                graphs[i % len(graphs)].replay()
+            else:
+                step(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = _max_over_ranks(world, start.elapsed_time(end))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} in the timed region")
+
+    # e2e: pinned host x in, y out, copies timed
+    x_h = torch.from_numpy(data["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_h = torch.empty((d.T, d.Dout), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+
+    def e2e_step(i):
+        x_d.copy_(x_h, non_blocking=True)
+        B.dense_bf16(x_d, ws_[i % len(ws_)], out=y, ws=ws, status=status)
+        y_h.copy_(y, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
+    if rank != 0:
+        return
+    step_ms = total_ms / args.steps
+    tokens_total = d.T * args.steps * world
+    pk = _peaks()
+    alg_bytes = w_bytes + d.T * (d.Din + d.Dout) * 2
+    flops = 2.0 * d.T * d.Din * d.Dout
+    tensor_bound = d.T >= 256
+    kern = "dense_bf16_kernel" + (" + dense_reduce_kernel" if need else "")
+    if tensor_bound:
+        ach = flops / (step_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": kern, "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16"], "peak_kind": f"{pk['kind']} burst bf16", "traffic": None,
+                "algorithmic_flops": flops, "launch_ms": step_ms}
+    else:
+        ach = alg_bytes / (step_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": ach / pk["hbm"], "peak_kind": f"{pk['kind']} copy bandwidth", "traffic": None,
+                "algorithmic_bytes": alg_bytes, "launch_ms": step_ms}
+    line = {
+        "metric": DENSE_METRIC, "value": tokens_total / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": d.name, "T": d.T, "Din": d.Din, "Dout": d.Dout, "parallelism": "replicas",
+                   "l2": f"{len(ws_)} rotating weight copies ({len(ws_) * w_bytes / 1e9:.2f} GB > L2)",
+                   "launch": (f"CUDA graph per step ({launches} kernels)" if graphs
+                              else f"eager ({launches} kernels per step)")},
+        "roofline": roof,
+        "clocks": clocks.summary(),
+        "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2, "d2h_bytes_per_step": y_h.numel() * 2},
+        "gpu_launches": launches * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import dense as odense
+
+        tok = min(d.T, 256)
+        t0 = time.perf_counter()
+        odense.dense_bf16(data["x"][:tok], data["w"])
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{tok} of {d.T} tokens of {d.name}, fp64 numpy BLAS, {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def run_dense_reference(args, d) -> None:
+    """The dense oracle (fp64 numpy BLAS) on min(T, 64) tokens per step."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from nvfp4_mixture_experts_route_gb300 import inputs
+    from oracle import dense as odense
+
+    data = inputs.make_dense(d)
+    tok = min(d.T, 64)
+    for _ in range(args.warmup):
+        odense.dense_bf16(data["x"][:tok], data["w"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        odense.dense_bf16(data["x"][:tok], data["w"])
+    dt = time.perf_counter() - t0
+    value = tok * args.steps / dt
+    sample = f"{tok} of {d.T} tokens of {d.name} per step, fp64 numpy BLAS on the host's default threads"
+    print(json.dumps({
+        "impl": "reference", "metric": DENSE_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": d.name, "T": d.T, "Din": d.Din, "Dout": d.Dout, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,6 +559,12 @@ def main() -> None:
     args = ap.parse_args()
     from nvfp4_mixture_experts_route_gb300 import inputs
 
+    if args.workload in inputs.DENSE_WORKLOADS:
+        if args.impl == "reference":
+            run_dense_reference(args, inputs.DENSE_WORKLOADS[args.workload])
+        else:
+            run_dense(args, inputs.DENSE_WORKLOADS[args.workload])
+        return
     w = inputs.WORKLOADS[args.workload]
     if args.tile_m:
         import dataclasses

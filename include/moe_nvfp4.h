@@ -334,6 +334,22 @@ int moe_experts_norm_quantize(const void* x, const void* gamma, float eps,
                               int H, int I, int E, int K, int tile_m, void* ws,
                               size_t ws_bytes, int32_t* status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Pooler / unpooler (the model page: the MoE block's `pooler`
+ * ReplicatedLinear(hidden_size, moe_hidden_size, bias=False,
+ * quant_config=None) before the experts, `unpooler` back after them):
+ *   y[t, o] = bf16( sum_i x[t, i] * w[o, i] )   (fp32 accumulation)
+ * x bf16 [T, Din] row-major, w bf16 [Dout, Din] row-major (the Linear
+ * weight), y bf16 [T, Dout]. Din % 64 == 0, Dout % 128 == 0, every pointer
+ * 16-byte aligned. For few tokens K is split into slices whose fp32 partials
+ * go to ws and are summed in a fixed order (deterministic); ws may be NULL
+ * when moe_dense_bf16_workspace_size reports 0. T == 0 is valid.
+ * ---------------------------------------------------------------------- */
+int moe_dense_bf16_workspace_size(int T, int Din, int Dout, size_t* ws_bytes);
+
+int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void* y,
+                   void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -97,6 +97,8 @@ _SIGNATURES = {
         [C.POINTER(C.c_void_p), _I, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P], _I),
     "moe_musespark1x_routing": ([_P, _P, _P, _I, _I, _I, C.c_float, C.c_float, _P, _P, _P], _I),
     "moe_rmsnorm_nvfp4_quant": ([_P, _P, C.c_float, _P, _I, _I, _P, _P, _P], _I),
+    "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
+    "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
     "moe_experts_norm_quantize": (
         [_P, _P, C.c_float, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P], _I),
 }
@@ -389,3 +391,25 @@ def experts_norm_quantize(route: Route, ws, *, x, gamma, eps: float, a1_gscale, 
     _check(load().moe_experts_norm_quantize(_ptr(x), _ptr(gamma), float(eps), _ptr(a1_gscale), C.byref(rs), T,
                                             H, I, E, K, route.tile_m, _ptr(ws), ws.numel(), _ptr(status),
                                             _stream(stream)))
+
+
+def dense_bf16_workspace_size(T: int, Din: int, Dout: int) -> int:
+    n = C.c_size_t()
+    _check(load().moe_dense_bf16_workspace_size(T, Din, Dout, C.byref(n)))
+    return n.value
+
+
+def dense_bf16(x, w, *, out=None, ws=None, status=None, stream=None):
+    """Pooler / unpooler projection: bf16 y [T, Dout] = x [T, Din] . w[Dout, Din]^T."""
+    import torch
+
+    T, Din = x.shape
+    Dout = w.shape[0]
+    y = out if out is not None else torch.empty((T, Dout), dtype=torch.bfloat16, device=x.device)
+    need = dense_bf16_workspace_size(T, Din, Dout)
+    if need and ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check(load().moe_dense_bf16(_ptr(x), _ptr(w), T, Din, Dout, _ptr(y), _ptr(ws), ws.numel() if ws is not None else 0,
+                                 _ptr(status), _stream(stream)))
+    return y
+

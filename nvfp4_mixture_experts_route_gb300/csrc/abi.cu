@@ -37,6 +37,9 @@ int launch_gemm1(const void*, const void*, const float*, const float*, const flo
 int launch_gemm2(const void*, const void*, const float*, const int32_t*, const int32_t*,
                  const int32_t*, const uint8_t*, const uint8_t*, void*, int, int, int, int, int,
                  int, int32_t*, cudaStream_t, bool, const char**);
+int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
+                      const char**);
+int dense_slices_here(int, int, int);
 }  // namespace moe
 
 namespace {
@@ -461,3 +464,35 @@ int moe_experts_norm_quantize(const void* x, const void* gamma, float eps, const
 }
 
 }  // extern "C"
+
+static int dense_shape(int T, int Din, int Dout) {
+  if (T < 0 || Din < 64 || Dout < 128 || Din % 64 || Dout % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "dense shape: need Din %% 64 == 0, Dout %% 128 == 0 (T=%d Din=%d Dout=%d)",
+                T, Din, Dout);
+  return MOE_OK;
+}
+
+extern "C" int moe_dense_bf16_workspace_size(int T, int Din, int Dout, size_t* ws_bytes) {
+  int rc = dense_shape(T, Din, Dout);
+  if (rc) return rc;
+  if (!ws_bytes) return fail(MOE_ERR_INVALID_ARG, "ws_bytes is null");
+  const int s = T > 0 ? moe::dense_slices_here(T, Din, Dout) : 1;
+  *ws_bytes = s > 1 ? (size_t)s * T * Dout * sizeof(float) : 0;
+  return MOE_OK;
+}
+
+extern "C" int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void* y,
+                              void* ws, size_t ws_bytes, int32_t* status, void* stream) {
+  size_t need = 0;
+  int rc = moe_dense_bf16_workspace_size(T, Din, Dout, &need);
+  if (rc) return rc;
+  if (T == 0) return MOE_OK;
+  if (!x || !w || !y) return fail(MOE_ERR_INVALID_ARG, "dense x, w or y is null");
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16))
+    return fail(MOE_ERR_INVALID_ARG, "dense x, w and y must be 16-byte aligned");
+  if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16)))
+    return fail(MOE_ERR_WORKSPACE, "dense workspace: need %zu bytes, 16-byte aligned", need);
+  const char* why = "";
+  rc = moe::launch_dense_bf16(x, w, T, Din, Dout, y, ws, status, as_stream(stream), &why);
+  return rc ? fail(rc, "%s", why) : MOE_OK;
+}

@@ -75,6 +75,34 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DenseWorkload:
+    """The MoE pooler / unpooler projection alone: x bf16 [T, Din] times the
+    Linear weight bf16 [Dout, Din]. The pages print neither hidden_size nor
+    moe_hidden_size; both are taken as the expert block's H = 5120."""
+
+    name: str
+    T: int
+    Din: int
+    Dout: int
+
+
+DENSE_WORKLOADS = {
+    d.name: d
+    for d in (
+        DenseWorkload("pooler_b8", T=8, Din=5120, Dout=5120),
+        DenseWorkload("pooler_t8192", T=8192, Din=5120, Dout=5120),
+    )
+}
+
+
+def make_dense(d: DenseWorkload, seed: int = 0) -> dict[str, np.ndarray]:
+    """x ~ N(0, 1) and w ~ N(0, 1/Din) as bf16 bit patterns."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, d.T, d.Din, d.Dout]))
+    return {"x": _to_bf16_bits(rng.standard_normal((d.T, d.Din))),
+            "w": _to_bf16_bits(rng.standard_normal((d.Dout, d.Din)) / np.sqrt(d.Din))}
+
+
 def _rngs(seed: int) -> dict[str, np.random.Generator]:
     kids = np.random.SeedSequence(seed).spawn(len(CHILDREN))
     return {name: np.random.default_rng(k) for name, k in zip(CHILDREN, kids)}
