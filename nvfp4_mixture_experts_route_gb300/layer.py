@@ -72,3 +72,36 @@ class NvFp4MoE:
         B.post_expert_finalize(b["rows"], b["route"].expanded_to_permuted, topk_weights, self.gamma, self.eps,
                                self.weight_before_norm, out=o)
         return o, b
+
+    # -- CUDA-graph serving path -------------------------------------------
+    def graph_buffers(self, T: int, K: int) -> dict:
+        """Static input and output tensors of the graphed step for (T, K):
+        ``x`` bf16 [T, H], ``topk_ids`` int32 [T, K], ``topk_weights`` fp32
+        [T, K] (fill them, e.g. straight from pinned host memory), and
+        ``out`` bf16 [T, H] (read it after ``replay``)."""
+        key = ("graph", T, K)
+        if key not in self._buffers:
+            dev = self.device
+            self._buffers[key] = {
+                "x": torch.zeros((T, self.H), dtype=torch.bfloat16, device=dev),
+                "topk_ids": torch.full((T, K), -1, dtype=torch.int32, device=dev),
+                "topk_weights": torch.zeros((T, K), dtype=torch.float32, device=dev),
+                "out": torch.empty((T, self.H), dtype=torch.bfloat16, device=dev),
+                "graph": None,
+            }
+        return self._buffers[key]
+
+    def replay(self, T: int, K: int) -> torch.Tensor:
+        """Run the step on ``graph_buffers(T, K)`` as one CUDA graph replay
+        (captured on first use: routing, expert body and finalize, with the
+        weights current at capture time). Returns the static ``out``."""
+        g = self.graph_buffers(T, K)
+        if g["graph"] is None:
+            self.forward(g["x"], g["topk_ids"], g["topk_weights"], out=g["out"])  # warm-up, outside capture
+            torch.cuda.current_stream(self.device).synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                self.forward(g["x"], g["topk_ids"], g["topk_weights"], out=g["out"])
+            g["graph"] = graph
+        g["graph"].replay()
+        return g["out"]

@@ -300,3 +300,27 @@ def test_prefill_t8192_sampled(full, record_property):
     err = rel_l2(got["out"][pick], ref["out"])
     record_property("out_rel_l2", err)
     assert err < OUT_BAR
+
+
+def test_graphed_serving_path_matches_eager():
+    """NvFp4MoE.replay (the step captured once as a CUDA graph on static
+    buffers) gives the eager forward's output bit for bit, for two batches
+    written into the same static inputs."""
+    from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
+
+    w = inputs.WORKLOADS["tiny_t4"]
+    raw = inputs.make_layer(w)
+    moe = NvFp4MoE(raw, 1.0, 1.0, raw["gamma"], tile_m=w.tile_m)
+    gb = moe.graph_buffers(w.T, w.K)
+    for seed in (0, 1):
+        batch = inputs.make_batch(w, seed=seed)
+        x = bf16_dev(batch["x"])
+        ids = torch.from_numpy(batch["topk_ids"]).to("cuda")
+        tw = torch.from_numpy(batch["topk_weights"]).to("cuda")
+        eager = moe.forward(x, ids, tw)[0].clone()
+        gb["x"].copy_(x)
+        gb["topk_ids"].copy_(ids)
+        gb["topk_weights"].copy_(tw)
+        got = moe.replay(w.T, w.K)
+        torch.cuda.synchronize()
+        assert torch.equal(got, eager)
