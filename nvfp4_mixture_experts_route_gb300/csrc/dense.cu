@@ -8,10 +8,10 @@
 // features (weight rows), N = a tile of tokens (32, 64, 128 or 256 by T);
 // a unit is (token tile, 128-feature tile, K slice). Few tokens give few
 // (token, feature) tiles, so K is split into slices until there are about
-// four units per SM; each slice then writes an fp32 partial [slice][T][Dout]
+// four units per CTA; each slice then writes an fp32 partial [slice][T][Dout]
 // and dense_reduce_kernel sums the slices in order and rounds once.
 //
-// Persistent, warp-specialised kernel, one CTA per SM, 6 warps: warp 0 lane 0
+// Persistent, warp-specialised kernel, one or two CTAs per SM, 6 warps: warp 0 lane 0
 // is the TMA producer (per stage of K = 64 elements: a 128 x 128 B weight box
 // and an N x 128 B token box, both 128-byte swizzled, on one mbarrier), warp 1
 // lane 0 issues 4 MMAs of K = 16 per stage and commits the stage back, warps
@@ -34,9 +34,12 @@ struct DenseParams {
   int T, Din, Dout, slices;
 };
 
+// Token tiles of up to 64 run two CTAs per SM (two TMA producers and MMA
+// issuers streaming weights), larger ones one.
+__host__ __device__ constexpr int dense_ctas(int n) { return n <= 64 ? 2 : 1; }
 __host__ __device__ constexpr uint32_t dense_stage_bytes(int n) { return kDWBytes + (uint32_t)n * 128; }
 __host__ __device__ constexpr int dense_stages(int n) {
-  const int st = (232448 - 1024) / (int)dense_stage_bytes(n);
+  const int st = ((dense_ctas(n) == 1 ? 232448 : 115456) - 1024) / (int)dense_stage_bytes(n);
   return st > kDMaxStages ? kDMaxStages : st;
 }
 __host__ __device__ constexpr size_t dense_smem_bytes(int n) {
@@ -61,7 +64,7 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
 }
 
 template <int N>
-__global__ void __launch_bounds__(kDThreads, 1)
+__global__ void __launch_bounds__(kDThreads, dense_ctas(N))
     dense_bf16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const DenseParams p) {
   extern __shared__ uint8_t dsmem[];
@@ -261,7 +264,7 @@ int dense_slices(int T, int Din, int Dout, int nsm) {
   const int base = ((T + n - 1) / n) * (Dout / 128);
   const int KC = Din / 64;
   int s = 1;
-  while (base * s < 4 * nsm && KC / (s * 2) >= 4) s *= 2;
+  while (base * s < 4 * dense_ctas(n) * nsm && KC / (s * 2) >= 4) s *= 2;
   const int spc = (KC + s - 1) / s;
   return (KC + spc - 1) / spc;
 }
@@ -275,8 +278,8 @@ static cudaError_t launch_dense_n(const CUtensorMap& tw, const CUtensorMap& tx, 
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)dense_smem_bytes(N));
   if (err != cudaSuccess) return err;
   const long long units = (long long)((p.T + N - 1) / N) * (p.Dout / 128) * p.slices;
-  const int nsm = dense_sm_count();
-  const int grid = (int)(units < nsm ? units : nsm);
+  const int slots = dense_ctas(N) * dense_sm_count();
+  const int grid = (int)(units < slots ? units : slots);
   return launch_kernel(kern, dim3(grid), dim3(kDThreads), dense_smem_bytes(N), stream, true, tw, tx, p);
 }
 
