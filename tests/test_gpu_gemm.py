@@ -324,3 +324,31 @@ def test_graphed_serving_path_matches_eager():
         got = moe.replay(w.T, w.K)
         torch.cuda.synchronize()
         assert torch.equal(got, eager)
+
+
+@pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf", "prefill_t8192_zipf"])
+def test_timed_launch_path_matches_split_path(full, name):
+    """The path bench.py times (route_permute, the fused moe_nvfp4_experts
+    whose GEMMs are programmatic dependents that prefetch weights, the
+    finalize; eager and as a graph replay) gives exactly the split entry
+    points' output at full size; those are held to the oracle above."""
+    from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
+
+    raw, prep = full
+    w = inputs.WORKLOADS[name]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    split = run_gpu(prep, batch, w.tile_m, a1, a2, export=False)
+    assert split["status"] == 0
+    moe = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=w.tile_m)
+    x = bf16_dev(batch["x"])
+    ids = torch.from_numpy(batch["topk_ids"]).to(DEV)
+    tw = torch.from_numpy(batch["topk_weights"]).to(DEV)
+    eager = bf16_host_f64(moe.forward(x, ids, tw)[0])
+    assert np.array_equal(eager, split["out"])
+    gb = moe.graph_buffers(w.T, w.K)
+    gb["x"].copy_(x)
+    gb["topk_ids"].copy_(ids)
+    gb["topk_weights"].copy_(tw)
+    graphed = bf16_host_f64(moe.replay(w.T, w.K))
+    assert np.array_equal(graphed, split["out"])
