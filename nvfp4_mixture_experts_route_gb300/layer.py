@@ -82,14 +82,30 @@ class NvFp4MoE:
         key = ("graph", T, K)
         if key not in self._buffers:
             dev = self.device
+            # x, topk_ids and topk_weights share one allocation (``inputs``,
+            # bytes) so that a caller can fill all three with one copy, e.g.
+            # from a pinned host buffer laid out by ``input_layout``.
+            offs, nbytes = self.input_layout(T, K)
+            flat = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
             self._buffers[key] = {
-                "x": torch.zeros((T, self.H), dtype=torch.bfloat16, device=dev),
-                "topk_ids": torch.full((T, K), -1, dtype=torch.int32, device=dev),
-                "topk_weights": torch.zeros((T, K), dtype=torch.float32, device=dev),
+                "inputs": flat,
+                "x": flat[offs["x"]:offs["x"] + T * self.H * 2].view(torch.bfloat16).view(T, self.H),
+                "topk_ids": flat[offs["topk_ids"]:offs["topk_ids"] + T * K * 4].view(torch.int32).view(T, K),
+                "topk_weights": flat[offs["topk_weights"]:offs["topk_weights"] + T * K * 4]
+                .view(torch.float32).view(T, K),
                 "out": torch.empty((T, self.H), dtype=torch.bfloat16, device=dev),
                 "graph": None,
             }
+            self._buffers[key]["topk_ids"].fill_(-1)
         return self._buffers[key]
+
+    def input_layout(self, T: int, K: int) -> tuple[dict, int]:
+        """Byte offsets of x, topk_ids and topk_weights inside ``inputs`` (each
+        16-byte aligned) and its size."""
+        up = lambda n: (n + 15) // 16 * 16  # noqa: E731
+        o_ids = up(T * self.H * 2)
+        o_w = o_ids + up(T * K * 4)
+        return {"x": 0, "topk_ids": o_ids, "topk_weights": o_w}, o_w + up(T * K * 4)
 
     def replay(self, T: int, K: int) -> torch.Tensor:
         """Run the step on ``graph_buffers(T, K)`` as one CUDA graph replay
