@@ -156,6 +156,24 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
   }
 }
 
+// Packed fp32x2 arithmetic (one instruction for two lanes of the pair):
+// d = a * b + c and d = a * b, each element rounded as its scalar form.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<unsigned long long*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 // The same finalize with the token's K rows staged in shared memory by bulk
 // copies, one mbarrier per route: one thread issues them all up front, and
 // the CTA normalises route k as soon as its row has landed while the later
@@ -198,14 +216,15 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
     }
   }
   // gain g = 1 + gamma (fp32) while the rows arrive
-  float g[VPT][8], acc[VPT][8];
+  // Pairs of hidden-dimension elements in packed fp32x2 arithmetic.
+  float2 g[VPT][4], acc[VPT][4];
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = threadIdx.x + i * kFinThreads;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      g[i][q] = 1.f;
-      acc[i][q] = 0.f;
+    for (int q = 0; q < 4; ++q) {
+      g[i][q] = make_float2(1.f, 1.f);
+      acc[i][q] = make_float2(0.f, 0.f);
     }
     if (v < nvec) {
       const uint4 u = *reinterpret_cast<const uint4*>(gamma + 8 * v);
@@ -213,8 +232,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float2 f = __bfloat1622float2(h[q]);
-        g[i][2 * q] = 1.f + f.x;
-        g[i][2 * q + 1] = 1.f + f.y;
+        g[i][q] = make_float2(1.f + f.x, 1.f + f.y);  // gain centre added in fp32
       }
     }
   }
@@ -242,8 +260,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
         return;
       }
     }
-    float f[VPT][8];  // route k's row, converted once
-    float ss = 0.f;
+    float2 f[VPT][4];  // route k's row, converted once
+    float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int v = threadIdx.x + i * kFinThreads;
@@ -252,16 +270,12 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float2 x = __bfloat1622float2(h[q]);
-        f[i][2 * q] = x.x;
-        f[i][2 * q + 1] = x.y;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float a = weight_before_norm ? f[i][q] * g[i][q] : f[i][q];
-        ss = fmaf(a, a, ss);
+        f[i][q] = __bfloat1622float2(h[q]);
+        const float2 a = weight_before_norm ? fmul2(f[i][q], g[i][q]) : f[i][q];
+        ss2 = ffma2(a, a, ss2);
       }
     }
+    float ss = ss2.x + ss2.y;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
     if (lane == 0) red[k & 1][warp] = ss;  // two buffers: one barrier per route
@@ -270,10 +284,11 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
 #pragma unroll
     for (int w = 0; w < kFinWarps; ++w) total += red[k & 1][w];  // fixed order
     const float ck = topk_w[(size_t)t * K + k] / sqrtf(total * inv_h + eps);
+    const float2 ck2 = make_float2(ck, ck);
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[i][q] = fmaf(f[i][q], ck, acc[i][q]);
+      for (int q = 0; q < 4; ++q) acc[i][q] = ffma2(f[i][q], ck2, acc[i][q]);
   }
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
@@ -282,8 +297,10 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
       uint4 o;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        h[q] = __floats2bfloat162_rn(acc[i][2 * q] * g[i][2 * q], acc[i][2 * q + 1] * g[i][2 * q + 1]);
+      for (int q = 0; q < 4; ++q) {
+        const float2 r = fmul2(acc[i][q], g[i][q]);
+        h[q] = __floats2bfloat162_rn(r.x, r.y);
+      }
       *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * v) = o;
     }
   }
