@@ -350,6 +350,17 @@ int moe_dense_bf16_workspace_size(int T, int Din, int Dout, size_t* ws_bytes);
 int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void* y,
                    void* ws, size_t ws_bytes, int32_t* status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Self-test of the failure path: runs the library's bounded mbarrier wait on
+ * a barrier that nothing completes, with limit_ns (1 us .. 1 s). On return
+ * (after a stream sync) *status holds MOE_ERR_TIMEOUT and result[0..1] == {1, 1}:
+ * the waiting thread gave up at the limit, a second waiter (whose own limit
+ * is 1 s) through the CTA's abort flag, after result[2] microseconds.
+ * result is int32 [3]. No trap, no hang; the context stays usable.
+ * ---------------------------------------------------------------------- */
+int moe_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, int32_t* result,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

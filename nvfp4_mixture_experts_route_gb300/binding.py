@@ -99,6 +99,7 @@ _SIGNATURES = {
     "moe_rmsnorm_nvfp4_quant": ([_P, _P, C.c_float, _P, _I, _I, _P, _P, _P], _I),
     "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
+    "moe_selftest_wait_timeout": ([C.c_uint64, _P, _P, _P], _I),
     "moe_experts_norm_quantize": (
         [_P, _P, C.c_float, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P], _I),
 }
@@ -412,4 +413,10 @@ def dense_bf16(x, w, *, out=None, ws=None, status=None, stream=None):
     _check(load().moe_dense_bf16(_ptr(x), _ptr(w), T, Din, Dout, _ptr(y), _ptr(ws), ws.numel() if ws is not None else 0,
                                  _ptr(status), _stream(stream)))
     return y
+
+
+def selftest_wait_timeout(limit_ns: int, status, result, stream=None) -> None:
+    """Run the bounded-wait failure path (see the header); status int32 [1]
+    and result int32 [3] on the device."""
+    _check(load().moe_selftest_wait_timeout(int(limit_ns), _ptr(status), _ptr(result), _stream(stream)))
 

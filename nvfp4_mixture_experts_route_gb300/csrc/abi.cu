@@ -40,6 +40,7 @@ int launch_gemm2(const void*, const void*, const float*, const int32_t*, const i
 int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
                       const char**);
 int dense_slices_here(int, int, int);
+int launch_selftest_wait(uint64_t, int32_t*, int32_t*, cudaStream_t);
 }  // namespace moe
 
 namespace {
@@ -496,3 +497,13 @@ extern "C" int moe_dense_bf16(const void* x, const void* w, int T, int Din, int 
   rc = moe::launch_dense_bf16(x, w, T, Din, Dout, y, ws, status, as_stream(stream), &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
 }
+
+extern "C" int moe_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, int32_t* result,
+                                         void* stream) {
+  if (!status || !result) return fail(MOE_ERR_INVALID_ARG, "status and result are required");
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns must be within [1 us, 1 s]");
+  const int rc = moe::launch_selftest_wait(limit_ns, status, result, as_stream(stream));
+  return rc ? fail(rc, "self-test launch failed") : MOE_OK;
+}
+

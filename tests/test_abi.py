@@ -88,3 +88,9 @@ def test_route_kernel_count():
     assert B.route_kernels(8192, 8, 128) == 3
     assert B.route_kernels(0, 8, 128) == 1
     assert B.route_kernels(2047, 2, 1024) == 1   # 4094 routes: one segment
+
+
+def test_selftest_arguments_refused_before_launch(lib):
+    assert lib.moe_selftest_wait_timeout(2_000_000, None, None, None) == -1
+    assert lib.moe_selftest_wait_timeout(10, 16, 16, None) == -1          # below 1 us
+    assert lib.moe_selftest_wait_timeout(5_000_000_000, 16, 16, None) == -1  # above 1 s

@@ -287,3 +287,21 @@ def test_finalize_readings_are_distinguished():
     a = olayer.finalize(r, e2p, w, gamma, 1e-6, False)["out"]
     b = olayer.finalize(r, e2p, w, gamma, 1e-6, True)["out"]
     assert rel_l2(a, b) > 0.1
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """The failure path of every pipelined kernel: a wait on an mbarrier that
+    nothing completes gives up at a forced 2 ms limit with MOE_ERR_TIMEOUT in
+    the status word, a second waiter leaves through the abort flag well
+    before its own 1 s limit, and the context then runs kernels normally."""
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    result = torch.zeros(3, dtype=torch.int32, device=DEV)
+    B.selftest_wait_timeout(2_000_000, status, result)
+    torch.cuda.synchronize()
+    r = result.cpu().tolist()
+    assert int(status.item()) == -5
+    assert r[0] == 1 and r[1] == 1
+    assert r[2] < 500_000  # microseconds: the abort flag, not the 1 s limit
+    ids = np.array([[0, 3], [3, 1]], np.int32)
+    got = _route_np(_route_gpu(ids, 8, 32))
+    _assert_route_equal(got, orouting.route_metadata(ids, 8, 32))
