@@ -110,6 +110,9 @@ class ClockSampler:
 
 
 def _dist():
+    """(world, rank, local rank) from the launcher's environment; for N > 1
+    a process group over NCCL (one rank per GPU), or gloo where no GPU is
+    visible (the CPU tests of this path)."""
     import torch
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -118,8 +121,11 @@ def _dist():
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -136,7 +142,8 @@ def _max_over_ranks(world, value: float) -> float:
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
