@@ -3,15 +3,17 @@
 
 One step = the whole hot path over one batch: routing metadata, NVFP4 input
 quantization into permuted order, GEMM1 with the fused SwiGLU + requant
-epilogue, GEMM2, and the post-expert finalize -- five kernel launches through
-the C ABI, inputs resident in HBM. The default workload is the b = 8 decode
+epilogue, GEMM2, and the post-expert finalize -- four to six kernel launches
+through the C ABI (for decode-sized route tiles both GEMMs are one persistent
+launch), inputs resident in HBM. The default workload is the b = 8 decode
 batch (T = 8, H = 5120, I = 2048, E = 128, top-8, uniform routing).
 
 Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
 the launching stream, bracketed by a barrier and a device synchronize; the
 layer's prepared weights rotate over several copies whose total exceeds L2,
-so no step reads the previous step's weights from L2. The GEMM1 launches are
-bracketed by their own events for the roofline. `e2e` repeats the
+so no step reads the previous step's weights from L2. For the roofline, the
+same steps run once more with the dominant kernel -- the one-launch GEMMs at
+decode, GEMM1 at prefill -- bracketed by its own events. `e2e` repeats the
 measurement through the public layer call with host (pinned) inputs and
 outputs, the copies inside the timed region.
 
@@ -42,6 +44,30 @@ FALLBACK_HBM_GBS = 6800.0
 
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the roofline kernel, from one ncu capture of it on this workload's batch,
+# and the SHA-256 of the kernel sources it was taken on (gemm.cu,
+# common.cuh, layout.cuh in that order): once those change, traffic is null.
+NCU_TRAFFIC = {
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_455_936 + 6_357_248,
+                  "sources": "82131a26b41654f7e1e0a01bddad30e1a4d169b8e129f2eba8b481c77684c326"},
+}
+
+
+def _traffic(workload: str, kernel: str):
+    """Captured DRAM bytes per launch of `kernel`, or None when there is no
+    capture for it or its sources have changed since."""
+    import hashlib
+
+    t = NCU_TRAFFIC.get(workload)
+    if t is None or not kernel.startswith(t["kernel"]):
+        return None
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "layout.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_mixture_experts_route_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return t["bytes"] if h.hexdigest() == t["sources"] else None
 
 
 def _peaks() -> dict:
@@ -248,7 +274,9 @@ def run_ours(args, w) -> None:
     route, ws, rows, out, status = bufs["route"], bufs["ws"], bufs["rows"], bufs["out"], bufs["status"]
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
+    fused = B.experts_kernels(tile) == 2
+
+    def step(i, ev=None, split=True):
         wts = copies[i % len(copies)]
         B.route_permute(ids, E, tile, route=route, status=status)
         if ev is None:
@@ -262,21 +290,28 @@ def run_ours(args, w) -> None:
             B.experts_quantize(route, ws, x=x, a1_gscale=moe.a1_gscale, T=T, H=H, I=I, E=E, K=K,
                                status=status)
             ev[0].record(stream)
-            B.experts_gemm1(wts, route, ws, a2_gscale=moe.a2_gscale, T=T, H=H, I=I, E=E, K=K, status=status)
-            ev[1].record(stream)
-            B.experts_gemm2(wts, route, ws, rows, T=T, H=H, I=I, E=E, K=K, status=status)
+            if split:
+                B.experts_gemm1(wts, route, ws, a2_gscale=moe.a2_gscale, T=T, H=H, I=I, E=E, K=K,
+                                status=status)
+                ev[1].record(stream)
+                B.experts_gemm2(wts, route, ws, rows, T=T, H=H, I=I, E=E, K=K, status=status)
+            else:
+                B.experts_gemms(wts, route, ws, rows, a2_gscale=moe.a2_gscale, T=T, H=H, I=I, E=E, K=K,
+                                status=status)
+                ev[1].record(stream)
             ev[2].record(stream)
         B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out)
 
-    # route/permute (1 or 3 kernels), quantize, GEMM1, GEMM2, finalize
-    launches_per_step = B.route_kernels(T, K, E) + 4
+    # route/permute (1 or 3 kernels), quantize, the expert GEMMs (one fused
+    # launch or two), finalize
+    launches_per_step = B.route_kernels(T, K, E) + B.experts_kernels(tile) + 1
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} during warm-up")
 
-    # One CUDA graph per weight copy holds the five launches of a step (the ABI
+    # One CUDA graph per weight copy holds the launches of a step (the ABI
     # calls allocate nothing and never synchronise, so they capture as is).
     graphs = []
     if args.graph:
@@ -313,6 +348,14 @@ def run_ours(args, w) -> None:
     torch.cuda.synchronize()
     gemm1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     gemm2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    fused_ms = None
+    if fused:
+        # the one-launch GEMMs the timed step runs (the launch's time includes
+        # the 4-byte-per-route-tile counter memset of the standalone entry point)
+        for i in range(args.steps):
+            step(i, evs[i], split=False)
+        torch.cuda.synchronize()
+        fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
 
     # e2e: the public serving call (NvFp4MoE.replay: the step as one CUDA
     # graph on the layer's static buffers) fed from pinned host memory, with
@@ -361,6 +404,7 @@ def run_ours(args, w) -> None:
     pk = _peaks()
     peak, peak_kind = pk["hbm"], pk["kind"]
     gemm1_gbs = n_touch * w13_bytes / (gemm1_ms * 1e-3) / 1e9
+    fused_gbs = n_touch * (w13_bytes + w2_bytes) / (fused_ms * 1e-3) / 1e9 if fused else None
     live_routes = int(np.sum(batch["topk_ids"] >= 0))
     gemm1_tflops = 2.0 * live_routes * (2 * I) * H / (gemm1_ms * 1e-3) / 1e12
     tensor_bound = live_routes >= 8 * w.E * 8  # many routes per expert: the MMA, not HBM, bounds
@@ -375,7 +419,14 @@ def run_ours(args, w) -> None:
                                         f"({len(copies) * layer_bytes / 1e9:.2f} GB > L2)",
                    "launch": (f"CUDA graph per step ({launches_per_step} kernels)" if graphs
                               else f"eager ({launches_per_step} kernels per step)")},
-        "roofline": ({"bound": "hbm", "kernel": "grouped_gemm_kernel<1> (GEMM1 + SwiGLU + requant)",
+        "roofline": ({"bound": "hbm",
+                      "kernel": f"grouped_gemm_kernel<3, {tile}> (GEMM1 + SwiGLU + requant + GEMM2, one launch)",
+                      "achieved": fused_gbs, "peak": peak, "unit": "GB/s", "frac": fused_gbs / peak,
+                      "peak_kind": f"{peak_kind} copy bandwidth",
+                      "traffic": _traffic(w.name, f"grouped_gemm_kernel<3, {tile}>"),
+                      "algorithmic_bytes": n_touch * (w13_bytes + w2_bytes), "launch_ms": fused_ms}
+                     if fused and not tensor_bound else
+                     {"bound": "hbm", "kernel": "grouped_gemm_kernel<1> (GEMM1 + SwiGLU + requant)",
                       "achieved": gemm1_gbs, "peak": peak, "unit": "GB/s", "frac": gemm1_gbs / peak,
                       "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
                       "algorithmic_bytes": n_touch * w13_bytes, "launch_ms": gemm1_ms}
@@ -389,7 +440,7 @@ def run_ours(args, w) -> None:
                           "achieved_gbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9,
                           "frac_of_measured": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9 / peak,
                           "frac_of_8tbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 8e12,
-                          "gemm2_ms": gemm2_ms},
+                          "gemm1_ms": gemm1_ms, "gemm2_ms": gemm2_ms, "fused_gemms_ms": fused_ms},
         "clocks": clocks.summary(),
         "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": in_h.numel(),

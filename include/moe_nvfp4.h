@@ -176,13 +176,22 @@ typedef struct moe_route {
                                           the rows of its routes */
 } moe_route;
 
-/* Workspace bytes moe_nvfp4_experts needs (the permuted NVFP4 activations
- * and the quantized intermediate; contents opaque). */
+/* Kernels moe_nvfp4_experts enqueues for this route-tile size: 2 (the
+ * quantizer and one persistent launch of both GEMMs, tile_m <= 64) or 3
+ * (the quantizer, GEMM1, GEMM2). Returns the count, or a negative status
+ * for an unsupported tile_m. */
+int moe_experts_kernels(int tile_m);
+
+/* Workspace bytes moe_nvfp4_experts needs (the permuted NVFP4 activations,
+ * the quantized intermediate and one completion counter per route tile;
+ * contents opaque). */
 int moe_experts_workspace_size(int T, int K, int E, int H, int I, int tile_m,
                                size_t* ws_bytes);
 
 /* The whole expert body: a1 quantization into permuted order, GEMM1 with
- * the SwiGLU + NVFP4 requant epilogue, GEMM2. Give either x (bf16 [T, H]) or
+ * the SwiGLU + NVFP4 requant epilogue, GEMM2 (for tile_m <= 64 both GEMMs
+ * in one persistent launch, where a GEMM2 tile starts once every GEMM1 tile
+ * of its route tile has written its intermediate). Give either x (bf16 [T, H]) or
  * a pre-quantized a (uint8 [T, H/2]) with a_sf (e4m3 [T, H/16], row-major,
  * as scaled_fp4_quant(..., is_sf_swizzled_layout=False) returns it) and
  * pass NULL for the other. a1_gscale, a2_gscale: device fp32 [1].
@@ -213,6 +222,18 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H,
                       int I, int E, int K, int tile_m, void* gemm2_rows,
                       void* ws, size_t ws_bytes, int32_t* status,
                       void* stream);
+
+/* GEMM1 and GEMM2 as the one persistent launch moe_nvfp4_experts uses for
+ * tile_m <= 64 (any supported tile_m is accepted): after
+ * moe_experts_quantize it equals moe_experts_gemm1 followed by
+ * moe_experts_gemm2, bit for bit. It first clears the workspace's per-tile
+ * completion counters (one memset of 4 bytes per route tile), so it may be
+ * called again on the same quantized workspace. Arguments as for
+ * moe_experts_gemm1 and moe_experts_gemm2. */
+int moe_experts_gemms(const moe_weights* w, const float* a2_gscale,
+                      const moe_route* r, int T, int H, int I, int E, int K,
+                      int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream);
 
 /* Copy a quantized operand out of / into the workspace, in permuted row
  * order with row-major scales: which = 0 for the activations a (codes

@@ -63,6 +63,7 @@ _SIGNATURES = {
     "moe_last_error": ([], C.c_char_p),
     "moe_abi_version": ([], _I),
     "moe_route_kernels": ([_I, _I, _I], _I),
+    "moe_experts_kernels": ([_I], _I),
     "moe_prepared_sizes": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_prepare_weights": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_route_sizes": ([_I, _I, _I, _I, C.POINTER(_I), C.POINTER(_I)], _I),
@@ -79,6 +80,10 @@ _SIGNATURES = {
     ),
     "moe_experts_gemm1": (
         [C.POINTER(MoeWeights), _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P],
+        _I,
+    ),
+    "moe_experts_gemms": (
+        [C.POINTER(MoeWeights), _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, C.c_size_t, _P, _P],
         _I,
     ),
     "moe_experts_gemm2": (
@@ -189,6 +194,14 @@ def route_kernels(T: int, K: int, E: int) -> int:
     return n
 
 
+def experts_kernels(tile_m: int) -> int:
+    """Kernels nvfp4_experts launches for this route-tile size (2 or 3)."""
+    n = load().moe_experts_kernels(tile_m)
+    if n < 0:
+        _check(n)
+    return n
+
+
 def route_sizes(T: int, K: int, E: int, tile_m: int) -> tuple[int, int]:
     P, MT = C.c_int(), C.c_int()
     _check(load().moe_route_sizes(T, K, E, tile_m, C.byref(P), C.byref(MT)))
@@ -290,6 +303,14 @@ def experts_gemm2(w: MoeWeights, route: Route, ws, gemm2_rows, *, T, H, I, E, K,
     rs = route.struct()
     _check(load().moe_experts_gemm2(C.byref(w), C.byref(rs), T, H, I, E, K, route.tile_m, _ptr(gemm2_rows),
                                     _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+
+
+def experts_gemms(w: MoeWeights, route: Route, ws, gemm2_rows, *, a2_gscale, T, H, I, E, K, status=None,
+                  stream=None):
+    """GEMM1 and GEMM2 in one persistent launch (equal to experts_gemm1 then experts_gemm2)."""
+    rs = route.struct()
+    _check(load().moe_experts_gemms(C.byref(w), _ptr(a2_gscale), C.byref(rs), T, H, I, E, K, route.tile_m,
+                                    _ptr(gemm2_rows), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
 
 
 def experts_export(which: int, ws, *, T, H, I, E, K, tile_m, stream=None):

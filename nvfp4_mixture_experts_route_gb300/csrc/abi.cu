@@ -16,7 +16,7 @@ size_t route_smem_bytes(int E);
 int route_kernel_count(int T, int K, int E);
 cudaError_t launch_quantize_permute(const void*, const void*, const void*, const float*,
                                     const int32_t*, const int32_t*, const int32_t*, int, int, int,
-                                    int, int, int, uint8_t*, uint8_t*, cudaStream_t);
+                                    int, int, int, uint8_t*, uint8_t*, int32_t*, cudaStream_t);
 cudaError_t launch_act_scales_io(int, uint8_t*, uint8_t*, int, int, int, cudaStream_t);
 cudaError_t launch_prepare_weights(const void*, const void*, const void*, const void*, int, int,
                                    int, void*, void*, void*, void*, cudaStream_t);
@@ -37,6 +37,10 @@ int launch_gemm1(const void*, const void*, const float*, const float*, const flo
 int launch_gemm2(const void*, const void*, const float*, const int32_t*, const int32_t*,
                  const int32_t*, const uint8_t*, const uint8_t*, void*, int, int, int, int, int,
                  int, int32_t*, cudaStream_t, bool, const char**);
+int launch_gemms_fused(const void*, const void*, const float*, const float*, const float*, const void*,
+                       const void*, const float*, const int32_t*, const int32_t*, const int32_t*,
+                       const uint8_t*, const uint8_t*, uint8_t*, uint8_t*, void*, int32_t*, int, int, int,
+                       int, int, int, int32_t*, cudaStream_t, bool, const char**);
 int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
                       const char**);
 int dense_slices_here(int, int, int);
@@ -89,7 +93,7 @@ int route_dims(int T, int K, int E, int tile_m, RouteDims* d) {
 // Workspace of the expert body: permuted NVFP4 activations and the quantized
 // intermediate (codes row-major, scales as per-tile atoms; see quant.cu).
 struct WsLayout {
-  size_t a_codes = 0, a_sf = 0, h_codes = 0, h_sf = 0, total = 0;
+  size_t a_codes = 0, a_sf = 0, h_codes = 0, h_sf = 0, done = 0, total = 0;
   int P = 0, MT = 0;
 };
 
@@ -111,6 +115,8 @@ int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
   off = round_up(off + (size_t)d.P * (I / 2), 1024);
   w->h_sf = off;
   off = round_up(off + (size_t)d.MT * (I / 64) * S * moe::kAtomBytes, 1024);
+  w->done = off;  // per route tile: GEMM1 completions the fused GEMM2 units wait for
+  off = round_up(off + (size_t)(d.MT > 0 ? d.MT : 1) * sizeof(int32_t), 1024);
   w->total = off;
   return MOE_OK;
 }
@@ -213,6 +219,12 @@ int moe_route_kernels(int T, int K, int E) {
   return moe::route_kernel_count(T, K, E);
 }
 
+int moe_experts_kernels(int tile_m) {
+  if (tile_m != 32 && tile_m != 64 && tile_m != 128 && tile_m != 256)
+    return fail(MOE_ERR_UNSUPPORTED, "tile_m must be 32, 64, 128 or 256");
+  return tile_m <= 64 ? 2 : 3;
+}
+
 int moe_route_permute(const int32_t* topk_ids, int T, int K, int E, int tile_m,
                       int32_t* expert_counts, int32_t* expert_offsets,
                       int32_t* expanded_to_permuted, int32_t* permuted_to_token,
@@ -261,7 +273,8 @@ int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const f
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   cudaError_t err = moe::launch_quantize_permute(
       x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, r->expanded_to_permuted, r->tile_row_limit,
-      r->totals, T, K, H, tile_m, L.P, L.MT, base + L.a_codes, base + L.a_sf, as_stream(stream));
+      r->totals, T, K, H, tile_m, L.P, L.MT, base + L.a_codes, base + L.a_sf,
+      reinterpret_cast<int32_t*>(base + L.done), as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
 }
 
@@ -318,6 +331,43 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, in
   return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, false);
 }
 
+// Both GEMMs as one persistent grid. pdl as for the split GEMMs;
+// zero_counters: clear the per-tile completion counters first (one memset;
+// the quantizer already leaves them zero inside moe_nvfp4_experts).
+static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
+                         int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
+                         int32_t* status, void* stream, bool pdl, bool zero_counters) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L)) || (rc = check_route(r)) || (rc = check_weights(w, true)) ||
+      (rc = check_weights(w, false)))
+    return rc;
+  if (!a2_gscale) return fail(MOE_ERR_INVALID_ARG, "a2_gscale is null");
+  if (L.P == 0) return MOE_OK;
+  if (!gemm2_rows || !aligned(gemm2_rows, 16))
+    return fail(MOE_ERR_INVALID_ARG, "gemm2_rows must be non-null and 16-byte aligned");
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  if (zero_counters) {
+    const cudaError_t err = cudaMemsetAsync(base + L.done, 0, (size_t)L.MT * sizeof(int32_t), as_stream(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "moe_experts_gemms");
+  }
+  const char* why = "";
+  rc = moe::launch_gemms_fused(w->w13, w->w13_sf, w->g1_alphas, w->g1_scale_c, a2_gscale, w->w2, w->w2_sf,
+                               w->g2_alphas, r->tile_expert, r->tile_row_limit, r->totals,
+                               base + L.a_codes, base + L.a_sf, base + L.h_codes, base + L.h_sf, gemm2_rows,
+                               reinterpret_cast<int32_t*>(base + L.done), E, H, I, tile_m, L.P, L.MT, status,
+                               as_stream(stream), pdl, &why);
+  return rc ? fail(rc, "%s", why) : MOE_OK;
+}
+
+int moe_experts_gemms(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
+                      int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream) {
+  return experts_fused(w, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream,
+                       false, true);
+}
+
 int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const void* a_sf,
                       const float* a1_gscale, const float* a2_gscale, const moe_route* r, int T,
                       int H, int I, int E, int K, int tile_m, void* gemm2_rows, void* ws,
@@ -327,12 +377,21 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const 
   rc = moe_experts_quantize(x, a, a_sf, a1_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status,
                             stream);
   if (rc) return rc;
-  // The two GEMMs follow the quantizer and each other as programmatic
-  // dependents: each starts streaming its first weight stages while the
-  // kernel before it drains.
-  rc = experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream, true);
-  if (rc) return rc;
-  return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true);
+  // Decode-sized route tiles (tile_m <= 64): both GEMMs run as one
+  // persistent grid, a programmatic dependent of the quantizer that starts
+  // streaming its first weight stages while the quantizer drains; a route
+  // tile's GEMM2 units start once its GEMM1 units have stored the
+  // intermediate (the quantizer zeroed their counters), so GEMM2 has no ramp
+  // of its own. Prefill tiles issue-bound on the tensor pipe gain nothing
+  // from that and keep two launches, each a programmatic dependent of the
+  // kernel before it.
+  if (moe_experts_kernels(tile_m) == 3) {
+    rc = experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream, true);
+    if (rc) return rc;
+    return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true);
+  }
+  return experts_fused(w, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream,
+                       true, false);
 }
 
 int moe_experts_export(int which, const void* ws, size_t ws_bytes, int T, int H, int I, int E,

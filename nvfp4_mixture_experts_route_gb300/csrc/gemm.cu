@@ -59,20 +59,28 @@ constexpr uint32_t kSfStageBytes = 4 * kAtomBytes;     // 4 K=64 steps
 constexpr int kMaxStages = 8;
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
 
-struct GemmParams {
+// One GEMM's operands: GEMM1 (w13 against the permuted activations, writes
+// the intermediate) or GEMM2 (w2 against the intermediate, writes rows).
+struct GemmSide {
   const uint8_t* w_sf;  // prepared scale atoms [E][rows_w/128][K/64][512]
   const uint8_t* b_sf;  // workspace scale atoms [tiles][K/64][S][512]
+  const float* s0;      // g1_alphas (GEMM1) or g2_alphas (GEMM2)
+  const float* s1;      // g1_scale_c (GEMM1)
+  int rows_w, K, out_cols;
+};
+
+struct GemmParams {
+  GemmSide g[2];  // [0] GEMM1, [1] GEMM2
   const int32_t* tile_expert;
   const int32_t* tile_row_limit;
   const int32_t* totals;
-  const float* s0;         // g1_alphas (GEMM1) or g2_alphas (GEMM2)
-  const float* s1;         // g1_scale_c (GEMM1)
   const float* a2_gscale;  // GEMM1
   uint8_t* hq;             // GEMM1: intermediate codes [P][I/2]
   uint8_t* hq_sf;          // GEMM1: intermediate scale atoms [tiles][I/64][S][512]
   __nv_bfloat16* rows;     // GEMM2: [P][H]
+  int32_t* done;           // both GEMMs in one grid: per route tile, zeroed by the quantizer
   int32_t* status;
-  int E, rows_w, K, tile_m, out_cols;
+  int tile_m;
   // Set when the launch follows this library's previous step kernel with
   // programmatic dependent launch: the producer then loads the weights of its
   // first stages before waiting for that kernel (the weights and the routing
@@ -229,13 +237,24 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
   __syncwarp();
 }
 
-// One instantiation per (GEMM, route-tile size): the tile's launch shape,
-// pipeline depth and scale-atom count are compile-time, so the MMA issuer's
-// per-stage loops unroll and its descriptors are base + constant.
-template <int KIND, int TILE>
+// One instantiation per (mode, route-tile size). MODE 1 runs GEMM1 units, 2
+// GEMM2 units, 3 both in one persistent grid: every CTA walks its GEMM1
+// units, then its GEMM2 units, and the producer of a GEMM2 unit waits until
+// the GEMM1 units of its route tile have stored their intermediate (a
+// per-tile counter that every epilogue warp of those units raises after its
+// stores), so a route tile's GEMM2 starts while later tiles' GEMM1 units
+// still run and neither GEMM has a ramp or a tail of its own. Units are
+// dealt round-robin, each CTA in order, and a waited-for GEMM1 unit is
+// always earlier in its CTA's order than the GEMM2 unit waiting, so every
+// wait ends once the grid's CTAs are resident (the grid never exceeds what
+// fits at once). The tile's launch shape, pipeline depth and scale-atom
+// count are compile-time, so the MMA issuer's per-stage loops unroll and its
+// descriptors are base + constant.
+template <int MODE, int TILE>
 __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(TILE).ctas)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                        const GemmParams p) {
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -251,16 +270,31 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
     if (tid == 0) pdl_trigger();
   }
   const int ntiles = __ldcg(p.totals);
-  const int tiles_w = p.rows_w / kWTile;
-  const int n_units = ntiles * tiles_w;
+  // weight tiles per route tile of each GEMM, and the units: GEMM1's, then GEMM2's
+  const int tw1 = MODE != 2 ? p.g[0].rows_w / kWTile : 0;
+  const int tw2 = MODE != 1 ? p.g[1].rows_w / kWTile : 0;
+  const int n1 = ntiles * tw1;
+  const int n_units = n1 + ntiles * tw2;
   if ((int)blockIdx.x >= n_units) {
     // Even an idle CTA must not let this grid complete before its
     // predecessor: the kernels after it rely on that ordering.
     if (p.prefetch) pdl_wait();
     return;
   }
+  // unit u -> (GEMM 0 or 1, route tile, weight tile)
+  auto unit_of = [&](int u, int& gi, int& tau, int& mt) {
+    if (u < n1) {
+      gi = 0;
+      tau = u / tw1;
+      mt = u % tw1;
+    } else {
+      gi = 1;
+      tau = (u - n1) / tw2;
+      mt = (u - n1) % tw2;
+    }
+  };
 
-  constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, KIND);
+  constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, MODE == 2 ? 2 : 1);
   constexpr int NB = acc_bufs_for(TILE), CH = chunks_for(TILE), EPW = epi_warps_for(TILE);
   constexpr bool kRouteM = tile_cfg(TILE).route_m;
   // Per stage: CH chunks of K = 256, i.e. up to 4 * CH MMA steps of K = 64.
@@ -273,10 +307,13 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
   const uint32_t sSFA = sB + ST * b_stage;
   const uint32_t sSFB = sSFA + ST * sfa_stage;
   const uint32_t sEpi = sSFB + ST * sfb_stage;
-  const int KC = p.K / 64;
   constexpr int steps_per_stage = 4 * CH;
-  const int nks = (KC + steps_per_stage - 1) / steps_per_stage;
+  const int KC1 = MODE != 2 ? p.g[0].K / 64 : 0, KC2 = MODE != 1 ? p.g[1].K / 64 : 0;
+  const int nks1 = (KC1 + steps_per_stage - 1) / steps_per_stage;
+  const int nks2 = (KC2 + steps_per_stage - 1) / steps_per_stage;
   constexpr uint32_t ncols = tmem_cols_for(tile_m, ST, NB);
+  // completions a route tile's GEMM1 units report when their intermediate is stored
+  const int done_target = tw1 * EPW;
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -290,8 +327,14 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
     mbar_init(smem_u32(&drain_bar), 1);
     abort_flag = 0;
     fence_barrier_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    if (MODE != 2) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+    }
+    if (MODE != 1) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_slot), ncols);
@@ -313,12 +356,15 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
       // ST of them) is held back until the previous kernel has completed.
       bool waited = !p.prefetch;
       int held = 0;
-      int held_s[kMaxStages], held_ks[kMaxStages], held_tau[kMaxStages], held_kk[kMaxStages];
-      auto load_route_half = [&](int s, int ks, int tau, int kk) {
+      int held_s[kMaxStages], held_ks[kMaxStages], held_tau[kMaxStages], held_kk[kMaxStages],
+          held_gi[kMaxStages];
+      auto load_route_half = [&](int s, int ks, int tau, int kk, int gi) {
         const uint32_t fb = smem_u32(&full_bar[s]);
-        const uint8_t* bsf = p.b_sf + (size_t)tau * KC * S * kAtomBytes;
+        const int KC = gi == 0 ? KC1 : KC2;
+        const CUtensorMap* tmB = gi == 0 ? &tmB1 : &tmB2;
+        const uint8_t* bsf = p.g[gi].b_sf + (size_t)tau * KC * S * kAtomBytes;
         for (int c = 0; 4 * c < kk; ++c)
-          tma_load_2d(sB + s * b_stage + c * b_bytes, &tmB, fb, (ks * CH + c) * kStageRowBytes,
+          tma_load_2d(sB + s * b_stage + c * b_bytes, tmB, fb, (ks * CH + c) * kStageRowBytes,
                       tau * tile_m);
         bulk_load(sSFB + s * sfb_stage, bsf + (size_t)steps_per_stage * ks * S * kAtomBytes,
                   (uint32_t)kk * S * kAtomBytes, fb);
@@ -326,15 +372,46 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
       auto release_held = [&]() {
         pdl_wait();
         pdl_trigger();
-        for (int h = 0; h < held; ++h) load_route_half(held_s[h], held_ks[h], held_tau[h], held_kk[h]);
+        for (int h = 0; h < held; ++h)
+          load_route_half(held_s[h], held_ks[h], held_tau[h], held_kk[h], held_gi[h]);
         held = 0;
         waited = true;
       };
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const int mt = u % tiles_w, tau = u / tiles_w;
+        int gi, tau, mt;
+        unit_of(u, gi, tau, mt);
+        const GemmSide& gs = p.g[gi];
+        const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2, tw = gi == 0 ? tw1 : tw2;
+        const CUtensorMap* tmA = gi == 0 ? &tmA1 : &tmA2;
         const int e = __ldcg(p.tile_expert + tau);
-        const int a_row = e * p.rows_w + mt * kWTile;
-        const uint8_t* wsf = p.w_sf + ((size_t)e * tiles_w + mt) * KC * kAtomBytes;
+        const int a_row = e * gs.rows_w + mt * kWTile;
+        const uint8_t* wsf = gs.w_sf + ((size_t)e * tw + mt) * KC * kAtomBytes;
+        if (MODE == 3 && gi == 1) {
+          // This route tile's intermediate must be complete: its GEMM1 units
+          // (earlier in every CTA's order) report through p.done.
+          if (!waited) release_held();
+          const uint64_t t0 = global_timer_ns();
+          for (uint32_t n = 0;; ++n) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.done + tau) : "memory");
+            if (v >= done_target) break;
+            if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+              stop = true;
+              break;
+            }
+            if (n >= 8) __nanosleep(64);
+            if ((n & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) {
+              record_status(p.status, MOE_ERR_TIMEOUT);
+              abort_flag = 1;
+              stop = true;
+              break;
+            }
+          }
+          if (stop) break;
+          // the intermediate was stored through the generic proxy; the loads
+          // below read it through the async proxy
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         for (int ks = 0; ks < nks; ++ks, ++it) {
           const int s = it % ST, round = it / ST;
           if (round > 0) {
@@ -349,17 +426,18 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
           const uint32_t fb = smem_u32(&full_bar[s]);
           mbar_arrive_expect_tx(fb, nc * (kABytes + b_bytes) + (uint32_t)kk * kAtomBytes * (1 + S));
           for (int c = 0; c < (int)nc; ++c)
-            tma_load_2d(sA + s * a_stage + c * kABytes, &tmA, fb, (ks * CH + c) * kStageRowBytes,
+            tma_load_2d(sA + s * a_stage + c * kABytes, tmA, fb, (ks * CH + c) * kStageRowBytes,
                         a_row);
           bulk_load(sSFA + s * sfa_stage, wsf + (size_t)steps_per_stage * ks * kAtomBytes,
                     (uint32_t)kk * kAtomBytes, fb);
           if (waited) {
-            load_route_half(s, ks, tau, kk);
+            load_route_half(s, ks, tau, kk, gi);
           } else {
             held_s[held] = s;
             held_ks[held] = ks;
             held_tau[held] = tau;
             held_kk[held] = kk;
+            held_gi[held] = gi;
             ++held;
           }
         }
@@ -385,6 +463,8 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
       uint32_t phase = 0;  // ring position: stage s, its current full phase
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++uc) {
+        const int gi = u < n1 ? 0 : 1;
+        const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2;
         const int b = uc % NB, use = uc / NB;
         if (use > 0 &&
             !mbar_wait(smem_u32(&acce_bar[b]), (use - 1) & 1, &abort_flag, p.status))
@@ -453,7 +533,10 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
-      const int mt = u % tiles_w, tau = u / tiles_w;
+      int gi, tau, mt;
+      unit_of(u, gi, tau, mt);
+      const bool g1 = MODE == 1 || (MODE == 3 && gi == 0);  // this unit is a GEMM1 unit
+      const GemmSide& gs = p.g[gi];
       const int e = p.tile_expert[tau];
       const int row0 = tau * tile_m;
       const uint32_t taddr = tmem + (uint32_t)(b * tile_m) + ((uint32_t)(32 * q) << 16);
@@ -471,11 +554,11 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&acce_bar[b]));
-        if constexpr (KIND == 1) {
+        if (g1) {
           // columns 32cc..32cc+31: gate and up of intermediate columns
           // 16 (4 mt + cc) + 0..15 (the prepared w13 granules)
-          const float s0 = p.s0[e], s1 = p.s1[e], a2g = *p.a2_gscale;
-          const int I = p.out_cols;
+          const float s0 = gs.s0[e], s1 = gs.s1[e], a2g = *p.a2_gscale;
+          const int I = gs.out_cols;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int cc = half + 2 * k;
@@ -493,7 +576,7 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
             p.hq_sf[act_sf_offset(r, 4 * mt + cc, tile_m, I / 64, S)] = static_cast<uint8_t>(sfc);
           }
         } else {
-          const float g2 = p.s0[e];
+          const float g2 = gs.s0[e];
           if (r < p.tile_row_limit[tau]) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -505,44 +588,54 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
                                                                 __uint_as_float(acc[k][2 * i + 1]) * g2);
                 w[i] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              uint4* dst = reinterpret_cast<uint4*>(p.rows + (size_t)r * p.out_cols + mt * kWTile + 32 * cc);
+              uint4* dst = reinterpret_cast<uint4*>(p.rows + (size_t)r * gs.out_cols + mt * kWTile + 32 * cc);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
             }
           }
         }
-        continue;  // the buffer went back above
-      } else if (KIND == 1) {
-        const float sc = lane < 16 ? p.s0[e] : p.s1[e];
-        const float a2g = *p.a2_gscale;
-        const int I = p.out_cols;
-        const int cols = epi_cols_for(tile_m);
-        for (int c0 = half * cols; c0 < tile_m; c0 += kSplit * cols) {
-          if (cols == 32)
-            gemm1_epilogue_chunk<32>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
-                                     p.hq, p.hq_sf);
-          else
-            gemm1_epilogue_chunk<16>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
-                                     p.hq, p.hq_sf);
-        }
       } else {
-        const float g2 = p.s0[e];
-        const int limit = p.tile_row_limit[tau];
-        const int colx = mt * kWTile + 32 * q + lane;
-        for (int c0 = half * 32; c0 < tile_m; c0 += kSplit * 32) {
-          float v[32];
-          tmem_ld32(taddr + c0, v);
+        if (g1) {
+          const float sc = lane < 16 ? gs.s0[e] : gs.s1[e];
+          const float a2g = *p.a2_gscale;
+          const int I = gs.out_cols;
+          const int cols = epi_cols_for(tile_m);
+          for (int c0 = half * cols; c0 < tile_m; c0 += kSplit * cols) {
+            if (cols == 32)
+              gemm1_epilogue_chunk<32>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
+                                       p.hq, p.hq_sf);
+            else
+              gemm1_epilogue_chunk<16>(taddr + c0, stage, lane, sc, a2g, row0 + c0, I, mt, q, tile_m, S,
+                                       p.hq, p.hq_sf);
+          }
+        } else {
+          const float g2 = gs.s0[e];
+          const int limit = p.tile_row_limit[tau];
+          const int colx = mt * kWTile + 32 * q + lane;
+          for (int c0 = half * 32; c0 < tile_m; c0 += kSplit * 32) {
+            float v[32];
+            tmem_ld32(taddr + c0, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int r = row0 + c0 + i;
-            if (r < limit) p.rows[(size_t)r * p.out_cols + colx] = __float2bfloat16_rn(v[i] * g2);
+            for (int i = 0; i < 32; ++i) {
+              const int rr = row0 + c0 + i;
+              if (rr < limit) p.rows[(size_t)rr * gs.out_cols + colx] = __float2bfloat16_rn(v[i] * g2);
+            }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&acce_bar[b]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce_bar[b]));
+      if (MODE == 3 && g1) {
+        // This warp's share of the tile's intermediate is stored: publish it
+        // to the GEMM2 units of the tile, whose TMA loads (async proxy) read
+        // it (release at GPU scope).
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.done + tau, 1);
+      }
     }
   }
 
@@ -572,102 +665,183 @@ static int sm_count() {
   return n;
 }
 
-template <int KIND, int TILE>
-static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
-                              int max_tiles, cudaStream_t stream, bool pdl) {
-  p.prefetch = pdl ? 1 : 0;
-  constexpr size_t smem = gemm_smem_bytes(TILE, KIND);
-  auto kern = grouped_gemm_kernel<KIND, TILE>;
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
+// CTAs of a kernel that fit on one SM at once, from its compiled resources
+// and the device's per-SM limits: shared memory (each CTA also takes the
+// runtime's per-block reserve), registers (allocated per warp in units of
+// 256) and threads. The runtime's occupancy query answers 1 for these
+// tensor-memory kernels although the SM holds as many as these limits allow
+// (tensor memory itself is budgeted at compile time).
+static cudaError_t resident_ctas(const void* kern, int threads, size_t dyn_smem, int* fit) {
+  cudaFuncAttributes fa{};
+  cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+  int dev = 0, smem_sm = 0, reserve = 0, regs_sm = 0, threads_sm = 0, blocks_sm = 0;
+  if (err == cudaSuccess) err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+  if (err == cudaSuccess)
+    err = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&blocks_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev);
   if (err != cudaSuccess) return err;
-  // ctas_per_sm CTAs per SM; CTAs past the live unit count exit at once.
-  const long long units = (long long)max_tiles * (p.rows_w / kWTile);
-  const long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
-  const int grid = (int)(units < slots ? units : slots);
-  return launch_kernel(kern, dim3(grid), dim3(64 + 32 * epi_warps_for(TILE)), smem, stream, pdl, ta,
-                       tb, p);
+  const long long cta_smem = (long long)dyn_smem + (long long)fa.sharedSizeBytes + reserve;
+  const long long warps = (threads + 31) / 32;
+  const long long cta_regs = warps * (((long long)fa.numRegs * 32 + 255) / 256 * 256);
+  long long n = blocks_sm;
+  if (cta_smem > 0 && smem_sm / cta_smem < n) n = smem_sm / cta_smem;
+  if (cta_regs > 0 && regs_sm / cta_regs < n) n = regs_sm / cta_regs;
+  if (threads_sm / threads < n) n = threads_sm / threads;
+  *fit = (int)n;
+  return cudaSuccess;
 }
 
-template <int KIND>
-static cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, GemmParams& p,
-                               int max_tiles, cudaStream_t stream, bool pdl) {
+template <int MODE, int TILE>
+static cudaError_t launch_one(const CUtensorMap* maps, GemmParams& p, int max_tiles, cudaStream_t stream,
+                              bool pdl) {
+  p.prefetch = pdl ? 1 : 0;
+  constexpr size_t smem = gemm_smem_bytes(TILE, MODE == 2 ? 2 : 1);
+  auto kern = grouped_gemm_kernel<MODE, TILE>;
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
+  if (err != cudaSuccess) return err;
+  // ctas_per_sm CTAs per SM (all resident at once); CTAs past the live unit
+  // count exit at once.
+  const long long units =
+      (long long)max_tiles * ((MODE != 2 ? p.g[0].rows_w : 0) + (MODE != 1 ? p.g[1].rows_w : 0)) / kWTile;
+  long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
+  if (MODE == 3) {
+    // The fused grid's waits end only if all of its CTAs are resident at once.
+    int fit = 0;
+    err = resident_ctas(reinterpret_cast<const void*>(kern), 64 + 32 * epi_warps_for(TILE), smem, &fit);
+    if (err != cudaSuccess) return err;
+    if ((long long)fit * sm_count() < slots) slots = (long long)fit * sm_count();
+    if (slots < 1) return cudaErrorInvalidConfiguration;
+  }
+  const int grid = (int)(units < slots ? units : slots);
+  return launch_kernel(kern, dim3(grid), dim3(64 + 32 * epi_warps_for(TILE)), smem, stream, pdl, maps[0],
+                       maps[1], maps[2], maps[3], p);
+}
+
+template <int MODE>
+static cudaError_t launch_mode(const CUtensorMap* maps, GemmParams& p, int max_tiles, cudaStream_t stream,
+                               bool pdl) {
   switch (p.tile_m) {
     case 32:
-      return launch_one<KIND, 32>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<MODE, 32>(maps, p, max_tiles, stream, pdl);
     case 64:
-      return launch_one<KIND, 64>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<MODE, 64>(maps, p, max_tiles, stream, pdl);
     case 128:
-      return launch_one<KIND, 128>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<MODE, 128>(maps, p, max_tiles, stream, pdl);
     default:
-      return launch_one<KIND, 256>(ta, tb, p, max_tiles, stream, pdl);
+      return launch_one<MODE, 256>(maps, p, max_tiles, stream, pdl);
   }
 }
 
-// GEMM1: weights p_w13 [E*2I, H/2], route rows a [P, H/2]; writes hq.
+// GEMM1's side: weights p_w13 [E*2I, H/2], route rows a [P, H/2]; writes hq.
+static bool gemm1_side(GemmParams& p, CUtensorMap* ta, CUtensorMap* tb, const void* p_w13,
+                       const void* p_w13_sf, const float* g1_alphas, const float* g1_scale_c,
+                       const uint8_t* a_codes, const uint8_t* a_sf, int E, int H, int I, int tile_m, int P) {
+  if (encode_rows_map(ta, p_w13, H / 2, (uint64_t)E * 2 * I, kWTile) != CUDA_SUCCESS ||
+      encode_rows_map(tb, a_codes, H / 2, (uint64_t)P, (uint32_t)tile_m) != CUDA_SUCCESS)
+    return false;
+  p.g[0] = GemmSide{reinterpret_cast<const uint8_t*>(p_w13_sf), a_sf, g1_alphas, g1_scale_c, 2 * I, H, I};
+  return true;
+}
+
+// GEMM2's side: weights p_w2 [E*H, I/2], route rows hq [P, I/2]; writes bf16 rows.
+static bool gemm2_side(GemmParams& p, CUtensorMap* ta, CUtensorMap* tb, const void* p_w2,
+                       const void* p_w2_sf, const float* g2_alphas, const uint8_t* h_codes,
+                       const uint8_t* h_sf, int E, int H, int I, int tile_m, int P) {
+  if (encode_rows_map(ta, p_w2, I / 2, (uint64_t)E * H, kWTile) != CUDA_SUCCESS ||
+      encode_rows_map(tb, h_codes, I / 2, (uint64_t)P, (uint32_t)tile_m) != CUDA_SUCCESS)
+    return false;
+  p.g[1] = GemmSide{reinterpret_cast<const uint8_t*>(p_w2_sf), h_sf, g2_alphas, nullptr, H, I, H};
+  return true;
+}
+
 int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas,
                  const float* g1_scale_c, const float* a2_gscale, const int32_t* tile_expert,
                  const int32_t* tile_row_limit, const int32_t* totals, const uint8_t* a_codes,
                  const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, int E, int H, int I,
                  int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream, bool pdl,
                  const char** why) {
-  CUtensorMap ta, tb;
-  if (encode_rows_map(&ta, p_w13, H / 2, (uint64_t)E * 2 * I, kWTile) != CUDA_SUCCESS ||
-      encode_rows_map(&tb, a_codes, H / 2, (uint64_t)P, (uint32_t)tile_m) != CUDA_SUCCESS) {
+  CUtensorMap maps[4];
+  GemmParams p{};
+  if (!gemm1_side(p, &maps[0], &maps[1], p_w13, p_w13_sf, g1_alphas, g1_scale_c, a_codes, a_sf, E, H, I,
+                  tile_m, P)) {
     *why = "cuTensorMapEncodeTiled failed for GEMM1";
     return MOE_ERR_CUDA;
   }
-  GemmParams p{};
-  p.w_sf = reinterpret_cast<const uint8_t*>(p_w13_sf);
-  p.b_sf = a_sf;
+  maps[2] = maps[0];
+  maps[3] = maps[1];
   p.tile_expert = tile_expert;
   p.tile_row_limit = tile_row_limit;
   p.totals = totals;
-  p.s0 = g1_alphas;
-  p.s1 = g1_scale_c;
   p.a2_gscale = a2_gscale;
   p.hq = h_codes;
   p.hq_sf = h_sf;
   p.status = status;
-  p.E = E;
-  p.rows_w = 2 * I;
-  p.K = H;
   p.tile_m = tile_m;
-  p.out_cols = I;
-  if (launch_kind<1>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
+  if (launch_mode<1>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM1 launch failed";
     return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
 
-// GEMM2: weights p_w2 [E*H, I/2], route rows hq [P, I/2]; writes bf16 rows.
 int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
                  const int32_t* tile_expert, const int32_t* tile_row_limit, const int32_t* totals,
                  const uint8_t* h_codes, const uint8_t* h_sf, void* rows, int E, int H, int I,
                  int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream, bool pdl,
                  const char** why) {
-  CUtensorMap ta, tb;
-  if (encode_rows_map(&ta, p_w2, I / 2, (uint64_t)E * H, kWTile) != CUDA_SUCCESS ||
-      encode_rows_map(&tb, h_codes, I / 2, (uint64_t)P, (uint32_t)tile_m) != CUDA_SUCCESS) {
+  CUtensorMap maps[4];
+  GemmParams p{};
+  if (!gemm2_side(p, &maps[2], &maps[3], p_w2, p_w2_sf, g2_alphas, h_codes, h_sf, E, H, I, tile_m, P)) {
     *why = "cuTensorMapEncodeTiled failed for GEMM2";
     return MOE_ERR_CUDA;
   }
-  GemmParams p{};
-  p.w_sf = reinterpret_cast<const uint8_t*>(p_w2_sf);
-  p.b_sf = h_sf;
+  maps[0] = maps[2];
+  maps[1] = maps[3];
   p.tile_expert = tile_expert;
   p.tile_row_limit = tile_row_limit;
   p.totals = totals;
-  p.s0 = g2_alphas;
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
   p.status = status;
-  p.E = E;
-  p.rows_w = H;
-  p.K = I;
   p.tile_m = tile_m;
-  p.out_cols = H;
-  if (launch_kind<2>(ta, tb, p, max_tiles, stream, pdl) != cudaSuccess) {
+  if (launch_mode<2>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {
     *why = "GEMM2 launch failed";
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+// Both GEMMs in one persistent grid (GEMM2 units of a route tile start once
+// its GEMM1 units have stored the intermediate; done[] must be zero).
+int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_alphas,
+                       const float* g1_scale_c, const float* a2_gscale, const void* p_w2,
+                       const void* p_w2_sf, const float* g2_alphas, const int32_t* tile_expert,
+                       const int32_t* tile_row_limit, const int32_t* totals, const uint8_t* a_codes,
+                       const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, void* rows, int32_t* done,
+                       int E, int H, int I, int tile_m, int P, int max_tiles, int32_t* status,
+                       cudaStream_t stream, bool pdl, const char** why) {
+  CUtensorMap maps[4];
+  GemmParams p{};
+  if (!gemm1_side(p, &maps[0], &maps[1], p_w13, p_w13_sf, g1_alphas, g1_scale_c, a_codes, a_sf, E, H, I,
+                  tile_m, P) ||
+      !gemm2_side(p, &maps[2], &maps[3], p_w2, p_w2_sf, g2_alphas, h_codes, h_sf, E, H, I, tile_m, P)) {
+    *why = "cuTensorMapEncodeTiled failed for the expert GEMMs";
+    return MOE_ERR_CUDA;
+  }
+  p.tile_expert = tile_expert;
+  p.tile_row_limit = tile_row_limit;
+  p.totals = totals;
+  p.a2_gscale = a2_gscale;
+  p.hq = h_codes;
+  p.hq_sf = h_sf;
+  p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
+  p.done = done;
+  p.status = status;
+  p.tile_m = tile_m;
+  if (launch_mode<3>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {
+    *why = "expert GEMM launch failed";
     return MOE_ERR_CUDA;
   }
   return MOE_OK;

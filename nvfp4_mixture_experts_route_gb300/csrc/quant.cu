@@ -53,9 +53,11 @@ __global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
     const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
     const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales) {
+    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int MT) {
   pdl_wait();
   pdl_trigger();
+  // the per-tile GEMM1 completion counters of the expert GEMMs that follow
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < MT; i += gridDim.x * blockDim.x) done[i] = 0;
   const int ng = H / 64;  // four-block groups per row
   const int nb = H / 16;
   const float g = (x != nullptr) ? *gscale : 0.f;
@@ -148,7 +150,7 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                                     const float* a1_gscale, const int32_t* e2p,
                                     const int32_t* tile_row_limit, const int32_t* totals, int T,
                                     int K, int H, int tile_m, int P, int MT, uint8_t* codes,
-                                    uint8_t* scales, cudaStream_t stream) {
+                                    uint8_t* scales, int32_t* done, cudaStream_t stream) {
   (void)P;
   // enough warps for one padding item each (one global read then one store
   // per lane), and threads for the token items
@@ -157,7 +159,7 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
   return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
                        reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, e2p, tile_row_limit, totals,
-                       T, K, H, tile_m, codes, scales);
+                       T, K, H, tile_m, codes, scales, done, MT);
 }
 
 cudaError_t launch_act_scales_io(int to_linear, uint8_t* atoms, uint8_t* linear, int K,

@@ -38,8 +38,10 @@ def test_workspace_size_formula(lib):
     def up(v):
         return (v + 1023) // 1024 * 1024
 
-    # codes row-major; scales as one 512-byte atom per K=64 step per 128 rows of a tile
-    want = up(P * H // 2) + up(MT * (H // 64) * 512) + up(P * I // 2) + up(MT * (I // 64) * 512)
+    # codes row-major; scales as one 512-byte atom per K=64 step per 128 rows of a tile;
+    # then one int32 completion counter per route tile
+    want = (up(P * H // 2) + up(MT * (H // 64) * 512) + up(P * I // 2) + up(MT * (I // 64) * 512)
+            + up(MT * 4))
     assert B.experts_workspace_size(T, K, E, H, I, tm) == want
 
 
@@ -77,6 +79,13 @@ def test_null_pointers_refused_before_any_launch(lib):
     # undersized workspace
     rc = lib.moe_experts_gemm2(C.byref(w), C.byref(r), 4, 256, 128, 8, 2, 32, 16, 1024, 16, None, None)
     assert rc == -3
+
+
+def test_experts_kernel_count():
+    assert B.experts_kernels(32) == 2 and B.experts_kernels(64) == 2
+    assert B.experts_kernels(128) == 3 and B.experts_kernels(256) == 3
+    with pytest.raises(B.MoeError):
+        B.experts_kernels(48)
 
 
 def test_route_kernel_count():

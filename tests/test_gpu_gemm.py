@@ -113,6 +113,53 @@ def small_cases():
     return out
 
 
+def _fused_rows(prep, batch, tile, a1, a2, calls=2):
+    """quantize, then moe_experts_gemms `calls` times on the same workspace."""
+    E, H, I = prep.E, prep.H, prep.I
+    ids = _dev(batch["topk_ids"].astype(np.int32))
+    T, K = ids.shape
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r = B.route_permute(ids, E, tile, status=status)
+    ws = B.alloc_workspace(T, K, E, H, I, tile, DEV)
+    g1 = torch.tensor([a1], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([a2], dtype=torch.float32, device=DEV)
+    B.experts_quantize(r, ws, x=bf16_dev(batch["x"]), a1_gscale=g1, T=T, H=H, I=I, E=E, K=K, status=status)
+    P, _ = B.route_sizes(T, K, E, tile)
+    outs = []
+    for _ in range(calls):
+        rows = torch.zeros((max(P, 1), H), dtype=torch.bfloat16, device=DEV)
+        B.experts_gemms(prep.w, r, ws, rows, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K, status=status)
+        outs.append(rows)
+    torch.cuda.synchronize()
+    return int(status.item()), [bf16_host_f64(o) for o in outs]
+
+
+FUSED_EXTRA = [
+    (1, 256, 128, 8, 1, "uniform", 32, 4.0, 1e-3),      # one route tile: GEMM2 units wait on GEMM1 units
+    (3, 512, 384, 2, 2, "uniform", 64, 4.0, 1e-3),      # one expert, few units, ragged K
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL) + len(FUSED_EXTRA)))
+def test_fused_gemms_match_split_gemms(small_cases, idx):
+    """The one-launch GEMM1+GEMM2 (per-route-tile completion counters) gives
+    the split launches' GEMM2 rows bit for bit, at every tile size, and again
+    when called a second time on the same workspace."""
+    if idx < len(SMALL):
+        w, raw, batch, tile, a1, a2 = small_cases[idx]
+    else:
+        T, H, I, E, K, routing, tile, a1, a2 = FUSED_EXTRA[idx - len(SMALL)]
+        w = _workload(T, H, I, E, K, routing, tile)
+        raw, batch = inputs.make_layer(w), inputs.make_batch(w)
+    prep = Prepared(raw)
+    split = run_gpu(prep, batch, tile, a1, a2, export=False)
+    assert split["status"] == 0
+    status, fused = _fused_rows(prep, batch, tile, a1, a2)
+    assert status == 0
+    for rows in fused:
+        assert np.array_equal(rows, split["rows"])
+
+
 @pytest.mark.parametrize("idx", range(len(SMALL)))
 def test_gemm2_on_identical_operands(small_cases, idx, record_property):
     w, raw, batch, tile, a1, a2 = small_cases[idx]
@@ -328,10 +375,13 @@ def test_graphed_serving_path_matches_eager():
 
 @pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf", "prefill_t8192_zipf"])
 def test_timed_launch_path_matches_split_path(full, name):
-    """The path bench.py times (route_permute, the fused moe_nvfp4_experts
-    whose GEMMs are programmatic dependents that prefetch weights, the
-    finalize; eager and as a graph replay) gives exactly the split entry
-    points' output at full size; those are held to the oracle above."""
+    """The path bench.py times (route_permute, moe_nvfp4_experts -- the
+    quantizer, then for decode tiles one persistent launch of both GEMMs,
+    for prefill tiles two GEMM launches, each a programmatic dependent that
+    prefetches weights -- the finalize; eager and as a graph replay) gives
+    exactly the split entry points' output at full size; those are held to
+    the oracle above. moe_experts_gemms at that size gives the split GEMM2
+    rows too."""
     from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
 
     raw, prep = full
@@ -352,3 +402,5 @@ def test_timed_launch_path_matches_split_path(full, name):
     gb["topk_weights"].copy_(tw)
     graphed = bf16_host_f64(moe.replay(w.T, w.K))
     assert np.array_equal(graphed, split["out"])
+    status, fused = _fused_rows(prep, batch, w.tile_m, a1, a2, calls=1)
+    assert status == 0 and np.array_equal(fused[0], split["rows"])
