@@ -362,9 +362,13 @@ int moe_experts_norm_quantize(const void* x, const void* gamma, float eps,
  *   y[t, o] = bf16( sum_i x[t, i] * w[o, i] )   (fp32 accumulation)
  * x bf16 [T, Din] row-major, w bf16 [Dout, Din] row-major (the Linear
  * weight), y bf16 [T, Dout]. Din % 64 == 0, Dout % 128 == 0, every pointer
- * 16-byte aligned. For few tokens K is split into slices whose fp32 partials
- * go to ws and are summed in a fixed order (deterministic); ws may be NULL
- * when moe_dense_bf16_workspace_size reports 0. T == 0 is valid.
+ * 16-byte aligned. For few tokens the (output tile, K) work is split evenly
+ * over the CTAs; tiles split between CTAs leave fp32 partials and arrival
+ * counters in ws, and the last arrival sums the partials in a fixed order
+ * (deterministic) inside the same kernel. The call clears the counters
+ * (one memset of at most a few KB) before the kernel, so ws needs no
+ * initialisation; its contents are opaque. ws may be NULL when
+ * moe_dense_bf16_workspace_size reports 0. T == 0 is valid.
  * ---------------------------------------------------------------------- */
 int moe_dense_bf16_workspace_size(int T, int Din, int Dout, size_t* ws_bytes);
 

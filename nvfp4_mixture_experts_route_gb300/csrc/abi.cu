@@ -43,7 +43,7 @@ int launch_gemms_fused(const void*, const void*, const float*, const float*, con
                        int, int, int, int32_t*, cudaStream_t, bool, const char**);
 int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
                       const char**);
-int dense_slices_here(int, int, int);
+size_t dense_workspace_here(int, int, int);
 int launch_selftest_wait(uint64_t, int32_t*, int32_t*, cudaStream_t);
 }  // namespace moe
 
@@ -536,8 +536,7 @@ extern "C" int moe_dense_bf16_workspace_size(int T, int Din, int Dout, size_t* w
   int rc = dense_shape(T, Din, Dout);
   if (rc) return rc;
   if (!ws_bytes) return fail(MOE_ERR_INVALID_ARG, "ws_bytes is null");
-  const int s = T > 0 ? moe::dense_slices_here(T, Din, Dout) : 1;
-  *ws_bytes = s > 1 ? (size_t)s * T * Dout * sizeof(float) : 0;
+  *ws_bytes = moe::dense_workspace_here(T, Din, Dout);
   return MOE_OK;
 }
 

@@ -22,7 +22,9 @@ def _ulp_bf16(v):
 
 @pytest.mark.parametrize("T,Din,Dout", [
     (1, 64, 128),        # one stage, one tile
-    (8, 5120, 5120),     # decode-sized: K split into slices, fp32 partials summed in order
+    (8, 5120, 5120),     # decode-sized: stream-K split, partial tiles summed in CTA order
+    (64, 2048, 1280),    # 10 tiles on every CTA: each range spans tile boundaries
+    (8, 64, 5120),       # one K step per tile: every CTA owns whole tiles
     (37, 320, 384),      # ragged tokens, odd stage count
     (300, 1024, 256),    # 256-token tiles with a ragged tail
 ])
@@ -65,7 +67,7 @@ def test_dense_bf16_deterministic_and_empty():
 
 
 def test_dense_bf16_prefill_sampled():
-    """T = 8192 tokens through 5120 x 5120 (256-token tiles, no slices),
+    """T = 8192 tokens through 5120 x 5120 (256-token tiles, whole tiles per CTA),
     checked on 64 sampled tokens."""
     rng = np.random.default_rng(7)
     T, D = 8192, 5120
