@@ -52,6 +52,8 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 NCU_TRAFFIC = {
     "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_455_936 + 6_357_248,
                   "sources": "82131a26b41654f7e1e0a01bddad30e1a4d169b8e129f2eba8b481c77684c326"},
+    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_721_983_000 + 85_326_080,
+                           "sources": "82131a26b41654f7e1e0a01bddad30e1a4d169b8e129f2eba8b481c77684c326"},
 }
 
 
@@ -426,16 +428,17 @@ def run_ours(args, w) -> None:
                       "traffic": _traffic(w.name, f"grouped_gemm_kernel<3, {tile}>"),
                       "algorithmic_bytes": n_touch * (w13_bytes + w2_bytes), "launch_ms": fused_ms}
                      if fused and not tensor_bound else
-                     {"bound": "hbm", "kernel": "grouped_gemm_kernel<1> (GEMM1 + SwiGLU + requant)",
+                     {"bound": "hbm", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
                       "achieved": gemm1_gbs, "peak": peak, "unit": "GB/s", "frac": gemm1_gbs / peak,
                       "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
                       "algorithmic_bytes": n_touch * w13_bytes, "launch_ms": gemm1_ms}
                      if not tensor_bound else
-                     {"bound": "tensor", "kernel": "grouped_gemm_kernel<1> (GEMM1 + SwiGLU + requant)",
+                     {"bound": "tensor", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
                       "achieved": gemm1_tflops, "peak": pk["bf16_sust"] * FP4_PER_BF16, "unit": "TFLOP/s",
                       "frac": gemm1_tflops / (pk["bf16_sust"] * FP4_PER_BF16),
                       "peak_kind": f"{peak_kind} sustained bf16 x {FP4_PER_BF16:g} (nominal fp4/bf16 ratio)",
-                      "traffic": None, "algorithmic_flops": 2.0 * live_routes * 2 * I * H, "launch_ms": gemm1_ms}),
+                      "traffic": _traffic(w.name, f"grouped_gemm_kernel<1, {tile}>"),
+                      "algorithmic_flops": 2.0 * live_routes * 2 * I * H, "launch_ms": gemm1_ms}),
         "step_roofline": {"bytes": n_touch * (w13_bytes + w2_bytes), "touched_experts": int(n_touch),
                           "achieved_gbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9,
                           "frac_of_measured": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9 / peak,
