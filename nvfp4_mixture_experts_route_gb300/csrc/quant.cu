@@ -38,17 +38,19 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
   }
 }
 
-// Token work item (token t, 16-element block b): the block is quantized once
-// and its 8 code bytes are written to the row of each of the token's routes,
-// found through expanded_to_permuted; the first thread of each quad writes
-// the quad's 4 scale bytes (contiguous in the scale atom). Padding work item (a warp, tile tau, group c):
-// lane i zeroes the 4 scale bytes of rows 32j + i (j < tile_m / 32) of the
-// tile that lie past its row limit; with a zero block scale the codes, always
-// finite e2m1 values, contribute exactly 0 to every product, so padding-row
-// codes are never written. The padding items come first (warp-granular: each
-// warp takes a whole item), then the token items. Reads x once; writes each
-// route row once.
-__global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
+// Token work item (a warp, token t, chunk j): lane l quantizes block
+// b = 32 j + l of the token once and writes its 8 code bytes to the row of
+// each of the token's routes; the first lane of each quad writes the quad's
+// 4 scale bytes (blocks 4m..4m+3, contiguous in the scale atom). Lanes k and
+// k + 32 of the item first look up route k's permuted row (expanded_to_
+// permuted) and the offset of that row's scale bytes for block 0, so the
+// per-block work is a shuffle and the stores. Padding work item (a warp,
+// tile tau, group c): lane i zeroes the 4 scale bytes of rows 32j + i
+// (j < tile_m / 32) of the tile that lie past its row limit; with a zero
+// block scale the codes, always finite e2m1 values, contribute exactly 0 to
+// every product, so padding-row codes are never written. The padding items
+// come first, then the token items. Reads x once; writes each route row once.
+__global__ void __launch_bounds__(256) quantize_permute_kernel(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
     const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
@@ -62,34 +64,45 @@ __global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
   const int nb = H / 16;
   const float g = (x != nullptr) ? *gscale : 0.f;
   const int S = sf_atoms_per_tile(tile_m);
+  const int lane = threadIdx.x & 31;
+  const int warp0 = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * (blockDim.x / 32);
   // Padding: one warp per (tile, group).
   {
-    const int lane = threadIdx.x & 31;
-    const long long n_pad = (long long)totals[0] * ng;
-    const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
-    for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_pad;
-         w += nwarps) {
-      const int tau = (int)(w / ng), c = (int)(w % ng);
+    const int n_pad = totals[0] * ng;
+    for (int w = warp0; w < n_pad; w += nwarps) {
+      const int tau = w / ng, c = w - (w / ng) * ng;
       const int limit = tile_row_limit[tau];
       for (int j = 0; j < tile_m; j += 32) {
         const int p = tau * tile_m + j + lane;
         if (p >= limit)
-          *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, H / 64, S)) = 0u;
+          *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, 4 * c, tile_m, ng, S)) = 0u;
       }
     }
   }
-  // Tokens: one thread per (token, 16-element block); the four threads of a
-  // quad hold the four blocks whose scale bytes are contiguous in the atom
-  // (nb is a multiple of 8, so quads never straddle a token or the end).
-  const int lane = threadIdx.x & 31;
-  const unsigned quad = 0xFu << (lane & ~3);
-  const long long n_tok = (long long)T * nb;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n_tok;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(idx / nb), b = (int)(idx % nb);
-    uint2 q;
-    uint32_t sfc;
-    if (x != nullptr) {
+  // Tokens: one warp per (token, chunk of 32 blocks). nb is a multiple of 8,
+  // so a quad's four lanes are all in range or all out of it.
+  const int nchunks = (nb + 31) / 32;
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  const size_t group_step = (size_t)S * kAtomBytes;  // scale bytes between consecutive 4-block groups
+  for (int w = warp0; w < T * nchunks; w += nwarps) {
+    const int t = w / nchunks, j = w - t * nchunks;
+    // routes k = lane and lane + 32: permuted row and its block-0 scale offset
+    int p_lo = -1, p_hi = -1;
+    size_t s_lo = 0, s_hi = 0;
+    if (lane < K) {
+      p_lo = e2p[(size_t)t * K + lane];
+      if (p_lo >= 0) s_lo = act_sf_offset(p_lo, 0, tile_m, ng, S);
+    }
+    if (lane + 32 < K) {
+      p_hi = e2p[(size_t)t * K + lane + 32];
+      if (p_hi >= 0) s_hi = act_sf_offset(p_hi, 0, tile_m, ng, S);
+    }
+    const int b = 32 * j + lane;
+    const bool on = b < nb;  // every lane stays for the warp-wide shuffles
+    uint2 q = make_uint2(0u, 0u);
+    uint32_t sfc = 0;
+    if (on && x != nullptr) {
       const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 16 * b);
       const uint4 u0 = src[0], u1 = src[1];
       const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
@@ -105,20 +118,23 @@ __global__ void __launch_bounds__(256, 6) quantize_permute_kernel(
         v[8 + 2 * i + 1] = f1.y;
       }
       quantize_block16(v, g, q.x, q.y, sfc);
-    } else {
+    } else if (on) {
       q = *reinterpret_cast<const uint2*>(a_in + (size_t)t * (H / 2) + 8 * b);
       sfc = a_sf_in[(size_t)t * nb + b];
     }
     // the quad's four scale bytes, block 4 * (b / 4) in the low byte
     const int base = lane & ~3;
-    const uint32_t sf4 = __shfl_sync(quad, sfc, base) | (__shfl_sync(quad, sfc, base + 1) << 8) |
-                         (__shfl_sync(quad, sfc, base + 2) << 16) | (__shfl_sync(quad, sfc, base + 3) << 24);
+    const uint32_t sf4 = __shfl_sync(kFull, sfc, base) | (__shfl_sync(kFull, sfc, base + 1) << 8) |
+                         (__shfl_sync(kFull, sfc, base + 2) << 16) | (__shfl_sync(kFull, sfc, base + 3) << 24);
+    const size_t sf_b = (size_t)(b >> 2) * group_step;
     for (int k = 0; k < K; ++k) {
-      const int p = e2p[(size_t)t * K + k];
-      if (p < 0) continue;
-      *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = q;
-      if ((b & 3) == 0)
-        *reinterpret_cast<uint32_t*>(scales + act_sf_offset(p, b, tile_m, H / 64, S)) = sf4;
+      const int p = __shfl_sync(kFull, k < 32 ? p_lo : p_hi, k & 31);
+      if (p < 0) continue;  // the same p in every lane
+      const size_t so = __shfl_sync(kFull, k < 32 ? s_lo : s_hi, k & 31);
+      if (on) {
+        *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = q;
+        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(scales + so + sf_b) = sf4;
+      }
     }
   }
 }
@@ -153,8 +169,9 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                                     uint8_t* scales, int32_t* done, cudaStream_t stream) {
   (void)P;
   // enough warps for one padding item each (one global read then one store
-  // per lane), and threads for the token items
-  const long long pad_threads = (long long)MT * (H / 64) * 32, tok_threads = (long long)T * (H / 16);
+  // per lane), and one warp per token item
+  const long long pad_threads = (long long)MT * (H / 64) * 32,
+                  tok_threads = (long long)T * ((H / 16 + 31) / 32) * 32;
   const int grid = grid_for(pad_threads > tok_threads ? pad_threads : tok_threads, 256);
   return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
