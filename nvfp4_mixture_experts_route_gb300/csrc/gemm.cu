@@ -283,11 +283,15 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
   }
   // unit u -> (GEMM 0 or 1, route tile, weight tile)
   auto unit_of = [&](int u, int& gi, int& tau, int& mt) {
-    if (u < n1) {
-      gi = 0;
-      tau = u / tw1;
-      mt = u % tw1;
-    } else {
+    if constexpr (MODE != 2) {
+      if (MODE == 1 || u < n1) {
+        gi = 0;
+        tau = u / tw1;
+        mt = u % tw1;
+        return;
+      }
+    }
+    if constexpr (MODE != 1) {
       gi = 1;
       tau = (u - n1) / tw2;
       mt = (u - n1) % tw2;
