@@ -50,10 +50,10 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # and the SHA-256 of the kernel sources it was taken on (gemm.cu,
 # common.cuh, layout.cuh in that order): once those change, traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_382_208 + 6_073_344,
-                  "sources": "7e98f267e2985559ee5d1d1cc25617ae86056adc9d68238bcba8d5c29b2b8a14"},
-    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_723_200_512 + 84_609_024,
-                           "sources": "7e98f267e2985559ee5d1d1cc25617ae86056adc9d68238bcba8d5c29b2b8a14"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_375_552 + 6_129_152,
+                  "sources": "3a5e8dc9d9cea7ba51060e7fcdf5ed62e76471378e69e74afe15e5d36e85f383"},
+    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_725_851_616 + 86_599_072,
+                           "sources": "3a5e8dc9d9cea7ba51060e7fcdf5ed62e76471378e69e74afe15e5d36e85f383"},
 }
 
 

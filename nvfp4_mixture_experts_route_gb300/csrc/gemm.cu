@@ -14,7 +14,7 @@
 // work unit is one (route tile tau, weight tile mt) pair over the whole K.
 //
 // Persistent, warp-specialised kernel, one to three CTAs per SM (tile_cfg
-// below), 2 + 4 or 2 + 8 warps:
+// below), 2 + 4 or 2 + 8 warps (+ 1 for GEMM1 over 128-row tiles):
 //   - warp 0 / lane 0: TMA producer. Walks this CTA's units in order and, per
 //     pipeline stage (K = 256 elements = 128 bytes per row per chunk), loads
 //     the 128 x 128 B weight box and the tile_m x 128 B route box (both
@@ -26,6 +26,10 @@
 //     the stage's MMAs of K = 64 into the unit's accumulator buffer, and
 //     commits the stage back to the producer; after a unit's last stage it
 //     commits the accumulator to the epilogue.
+//   - GEMM1 over 128-row tiles (prefill, where the MMA thread's issue rate
+//     bounds the kernel): a last warp's lane 0 makes the scale copies of each
+//     landed stage instead and commits them to the stage's sfready barrier,
+//     on which the MMA thread then waits.
 //   - warps 2..: epilogue. Warp w reads TMEM lane quadrant w % 4 (32 weight
 //     rows) of the finished accumulator (with 8 warps, two per quadrant split
 //     the route columns), then hands the buffer back. With two accumulator
@@ -237,6 +241,14 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
   __syncwarp();
 }
 
+// GEMM1 over 128-row tiles (issue-bound at prefill) gives the scale-factor
+// copies their own warp, so the MMA thread issues only MMAs and commits.
+// (GEMM2's shorter units measured slower that way.)
+__host__ __device__ constexpr bool scale_warp_for(int mode, int tile_m) { return mode == 1 && tile_m == 128; }
+__host__ __device__ constexpr int gemm_threads(int mode, int tile_m) {
+  return 64 + 32 * tile_cfg(tile_m).epi_warps + (scale_warp_for(mode, tile_m) ? 32 : 0);
+}
+
 // One instantiation per (mode, route-tile size). MODE 1 runs GEMM1 units, 2
 // GEMM2 units, 3 both in one persistent grid: every CTA walks its GEMM1
 // units, then its GEMM2 units, and the producer of a GEMM2 unit waits until
@@ -251,7 +263,7 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
 // count are compile-time, so the MMA issuer's per-stage loops unroll and its
 // descriptors are base + constant.
 template <int MODE, int TILE>
-__global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(TILE).ctas)
+__global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                         const GemmParams p) {
@@ -261,6 +273,8 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
   __shared__ __align__(8) uint64_t accf_bar[2];
   __shared__ __align__(8) uint64_t acce_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t sfready_bar[kMaxStages];  // a stage's scales are in tensor memory
+  __shared__ __align__(8) uint64_t sfdrain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -301,6 +315,7 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
   constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, MODE == 2 ? 2 : 1);
   constexpr int NB = acc_bufs_for(TILE), CH = chunks_for(TILE), EPW = epi_warps_for(TILE);
   constexpr bool kRouteM = tile_cfg(TILE).route_m;
+  constexpr bool kSW = scale_warp_for(MODE, TILE);
   // Per stage: CH chunks of K = 256, i.e. up to 4 * CH MMA steps of K = 64.
   constexpr uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;  // one chunk of the route box
   constexpr uint32_t a_stage = CH * kABytes, b_stage = CH * b_bytes;
@@ -329,6 +344,8 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
       mbar_init(smem_u32(&acce_bar[b]), EPW);
     }
     mbar_init(smem_u32(&drain_bar), 1);
+    for (int s = 0; s < ST; ++s) mbar_init(smem_u32(&sfready_bar[s]), 1);
+    mbar_init(smem_u32(&sfdrain_bar), 1);
     abort_flag = 0;
     fence_barrier_init();
     if (MODE != 2) {
@@ -476,7 +493,8 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
         tc_fence_after();
         const uint32_t dacc = tmem + (uint32_t)(b * tile_m);
         for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait(smem_u32(&full_bar[s]), phase, &abort_flag, p.status)) {
+          if (!mbar_wait(smem_u32(&full_bar[s]), phase, &abort_flag, p.status) ||
+              (kSW && !mbar_wait(smem_u32(&sfready_bar[s]), phase, &abort_flag, p.status))) {
             stop = true;
             break;
           }
@@ -490,7 +508,7 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
           const uint64_t sbd = sfb_desc0 + ((s * sfb_stage) >> 4);
 #pragma unroll
           for (int j = 0; j < steps_per_stage; ++j) {
-            if (j < kk) {
+            if (j < kk && !kSW) {
               tc_copy_scale_atom(fa + 4 * j, sad + j * (kAtomBytes >> 4));
 #pragma unroll
               for (int sub = 0; sub < S; ++sub)
@@ -520,6 +538,53 @@ __global__ void __launch_bounds__(64 + 32 * tile_cfg(TILE).epi_warps, tile_cfg(T
         if (stop) break;
         tc_commit(smem_u32(&accf_bar[b]));
       }
+    }
+    __syncwarp();
+  } else if (kSW && warp == 2 + EPW) {
+    // --------------------------- scale-factor copies -------------------------
+    // Waits for each stage to land, copies its scale atoms into the stage's
+    // tensor-memory columns and commits to the stage's sfready barrier, on
+    // which the MMA thread waits. A stage's columns are rewritten only after
+    // its next full phase, i.e. after the producer refilled it, which it does
+    // only once the MMAs that read the columns have completed.
+    if (lane == 0) {
+      const uint64_t sfa_desc0 = smem_desc(sSFA, 0, 128, 0);
+      const uint64_t sfb_desc0 = smem_desc(sSFB, 0, 128, 0);
+      int s = 0;
+      uint32_t phase = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const int gi = u < n1 ? 0 : 1;
+        const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2;
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait(smem_u32(&full_bar[s]), phase, &abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
+          const uint32_t fa = t_sfa + s * 16 * CH, fbc = t_sfb + s * 16 * CH * S;
+          const uint64_t sad = sfa_desc0 + ((s * sfa_stage) >> 4);
+          const uint64_t sbd = sfb_desc0 + ((s * sfb_stage) >> 4);
+#pragma unroll
+          for (int j = 0; j < steps_per_stage; ++j) {
+            if (j < kk) {
+              tc_copy_scale_atom(fa + 4 * j, sad + j * (kAtomBytes >> 4));
+#pragma unroll
+              for (int sub = 0; sub < S; ++sub)
+                tc_copy_scale_atom(fbc + 4 * (j * S + sub), sbd + (j * S + sub) * (kAtomBytes >> 4));
+            }
+          }
+          tc_commit(smem_u32(&sfready_bar[s]));
+          if (++s == ST) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy this thread issued has landed before tensor memory is freed
+      tc_commit(smem_u32(&sfdrain_bar));
+      mbar_wait_cleanup(smem_u32(&sfdrain_bar), 0);
     }
     __syncwarp();
   } else {
@@ -714,13 +779,13 @@ static cudaError_t launch_one(const CUtensorMap* maps, GemmParams& p, int max_ti
   if (MODE == 3) {
     // The fused grid's waits end only if all of its CTAs are resident at once.
     int fit = 0;
-    err = resident_ctas(reinterpret_cast<const void*>(kern), 64 + 32 * epi_warps_for(TILE), smem, &fit);
+    err = resident_ctas(reinterpret_cast<const void*>(kern), gemm_threads(MODE, TILE), smem, &fit);
     if (err != cudaSuccess) return err;
     if ((long long)fit * sm_count() < slots) slots = (long long)fit * sm_count();
     if (slots < 1) return cudaErrorInvalidConfiguration;
   }
   const int grid = (int)(units < slots ? units : slots);
-  return launch_kernel(kern, dim3(grid), dim3(64 + 32 * epi_warps_for(TILE)), smem, stream, pdl, maps[0],
+  return launch_kernel(kern, dim3(grid), dim3(gemm_threads(MODE, TILE)), smem, stream, pdl, maps[0],
                        maps[1], maps[2], maps[3], p);
 }
 
