@@ -386,6 +386,14 @@ int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void*
 int moe_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, int32_t* result,
                               void* stream);
 
+/* The same for the completion-counter wait of the one-launch expert GEMMs
+ * (a GEMM2 unit polling the count of its route tile's finished GEMM1
+ * units): both waiters poll *counter for a value of at least 1. counter is
+ * a caller-owned device int32 that stays 0 (4-byte aligned); status, result
+ * and the outcome are as for moe_selftest_wait_timeout. */
+int moe_selftest_counter_timeout(uint64_t limit_ns, const int32_t* counter,
+                                 int32_t* status, int32_t* result, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

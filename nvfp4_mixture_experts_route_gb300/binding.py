@@ -105,6 +105,7 @@ _SIGNATURES = {
     "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
     "moe_selftest_wait_timeout": ([C.c_uint64, _P, _P, _P], _I),
+    "moe_selftest_counter_timeout": ([C.c_uint64, _P, _P, _P, _P], _I),
     "moe_experts_norm_quantize": (
         [_P, _P, C.c_float, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P], _I),
 }
@@ -440,4 +441,11 @@ def selftest_wait_timeout(limit_ns: int, status, result, stream=None) -> None:
     """Run the bounded-wait failure path (see the header); status int32 [1]
     and result int32 [3] on the device."""
     _check(load().moe_selftest_wait_timeout(int(limit_ns), _ptr(status), _ptr(result), _stream(stream)))
+
+
+def selftest_counter_timeout(limit_ns: int, counter, status, result, stream=None) -> None:
+    """The completion-counter wait's failure path on a counter that stays 0
+    (see moe_selftest_counter_timeout)."""
+    _check(load().moe_selftest_counter_timeout(int(limit_ns), _ptr(counter), _ptr(status), _ptr(result),
+                                               _stream(stream)))
 

@@ -45,6 +45,7 @@ int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int
                       const char**);
 size_t dense_workspace_here(int, int, int);
 int launch_selftest_wait(uint64_t, int32_t*, int32_t*, cudaStream_t);
+int launch_selftest_counter(uint64_t, const int32_t*, int32_t*, int32_t*, cudaStream_t);
 }  // namespace moe
 
 namespace {
@@ -565,3 +566,12 @@ extern "C" int moe_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, int
   return rc ? fail(rc, "self-test launch failed") : MOE_OK;
 }
 
+extern "C" int moe_selftest_counter_timeout(uint64_t limit_ns, const int32_t* counter, int32_t* status,
+                                            int32_t* result, void* stream) {
+  if (!counter || !status || !result) return fail(MOE_ERR_INVALID_ARG, "counter, status and result are required");
+  if (!aligned(counter, 4)) return fail(MOE_ERR_INVALID_ARG, "counter must be 4-byte aligned");
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns must be within [1 us, 1 s]");
+  const int rc = moe::launch_selftest_counter(limit_ns, counter, status, result, as_stream(stream));
+  return rc ? fail(rc, "self-test launch failed") : MOE_OK;
+}

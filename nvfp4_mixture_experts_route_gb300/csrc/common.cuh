@@ -149,6 +149,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait until the int32 *counter (global memory, raised by other CTAs
+// after a GPU-scope release) is at least target: acquire loads at GPU scope,
+// a short sleep between polls after the first eight. Gives up through the
+// CTA's abort flag, or after limit_ns recording MOE_ERR_TIMEOUT and raising
+// the flag; returns whether the count was reached.
+__device__ __forceinline__ bool wait_counter_at_least(const int32_t* counter, int32_t target,
+                                                      volatile int* abort, int32_t* status,
+                                                      uint64_t limit_ns = kWaitLimitNs) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 0;; ++n) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+    if (*abort) return false;
+    if (n >= 8) __nanosleep(64);
+    if ((n & 15u) == 15u && global_timer_ns() - t0 > limit_ns) {
+      record_status(status, MOE_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Bounded wait used only on the clean-up path (no status update).
 __device__ __forceinline__ void mbar_wait_cleanup(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();

@@ -411,24 +411,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           // This route tile's intermediate must be complete: its GEMM1 units
           // (earlier in every CTA's order) report through p.done.
           if (!waited) release_held();
-          const uint64_t t0 = global_timer_ns();
-          for (uint32_t n = 0;; ++n) {
-            int v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.done + tau) : "memory");
-            if (v >= done_target) break;
-            if (*reinterpret_cast<volatile int*>(&abort_flag)) {
-              stop = true;
-              break;
-            }
-            if (n >= 8) __nanosleep(64);
-            if ((n & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) {
-              record_status(p.status, MOE_ERR_TIMEOUT);
-              abort_flag = 1;
-              stop = true;
-              break;
-            }
+          if (!wait_counter_at_least(p.done + tau, done_target, &abort_flag, p.status)) {
+            stop = true;
+            break;
           }
-          if (stop) break;
           // the intermediate was stored through the generic proxy; the loads
           // below read it through the async proxy
           asm volatile("fence.proxy.async.global;" ::: "memory");

@@ -31,6 +31,30 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* status, int32_t
   }
 }
 
+// The same for the completion-counter wait (wait_counter_at_least) the
+// one-launch expert GEMMs use between GEMM1 and GEMM2 units: both waiters
+// poll a counter the caller keeps at 0 for a target of 1.
+__global__ void selftest_counter_kernel(uint64_t limit_ns, const int32_t* counter, int32_t* status,
+                                        int32_t* result) {
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    const uint64_t limit = warp == 0 ? limit_ns : kWaitLimitNs;
+    const uint64_t t0 = global_timer_ns();
+    const bool ok = wait_counter_at_least(counter, 1, &abort_flag, warp == 0 ? status : nullptr, limit);
+    result[warp] = ok ? 0 : 1;
+    if (warp == 1) result[2] = (int32_t)((global_timer_ns() - t0) / 1000u);
+  }
+}
+
+int launch_selftest_counter(uint64_t limit_ns, const int32_t* counter, int32_t* status, int32_t* result,
+                            cudaStream_t stream) {
+  selftest_counter_kernel<<<1, 64, 0, stream>>>(limit_ns, counter, status, result);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int launch_selftest_wait(uint64_t limit_ns, int32_t* status, int32_t* result, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 64, 0, stream>>>(limit_ns, status, result);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

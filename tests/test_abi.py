@@ -103,3 +103,6 @@ def test_selftest_arguments_refused_before_launch(lib):
     assert lib.moe_selftest_wait_timeout(2_000_000, None, None, None) == -1
     assert lib.moe_selftest_wait_timeout(10, 16, 16, None) == -1          # below 1 us
     assert lib.moe_selftest_wait_timeout(5_000_000_000, 16, 16, None) == -1  # above 1 s
+    assert lib.moe_selftest_counter_timeout(2_000_000, None, 16, 16, None) == -1
+    assert lib.moe_selftest_counter_timeout(2_000_000, 18, 16, 16, None) == -1  # misaligned counter
+    assert lib.moe_selftest_counter_timeout(10, 16, 16, 16, None) == -1       # below 1 us

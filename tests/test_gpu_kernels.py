@@ -305,3 +305,24 @@ def test_bounded_wait_times_out_and_context_survives():
     ids = np.array([[0, 3], [3, 1]], np.int32)
     got = _route_np(_route_gpu(ids, 8, 32))
     _assert_route_equal(got, orouting.route_metadata(ids, 8, 32))
+
+
+def test_counter_wait_times_out_and_context_survives():
+    """The one-launch expert GEMMs' wait of a GEMM2 unit for its route
+    tile's GEMM1 units (a GPU-scope acquire poll of a completion counter):
+    on a counter that stays 0 it gives up at a forced 2 ms limit with
+    MOE_ERR_TIMEOUT, a second waiter leaves through the abort flag, the
+    counter is left untouched and the context then runs kernels normally."""
+    counter = torch.zeros(1, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    result = torch.zeros(3, dtype=torch.int32, device=DEV)
+    B.selftest_counter_timeout(2_000_000, counter, status, result)
+    torch.cuda.synchronize()
+    r = result.cpu().tolist()
+    assert int(status.item()) == -5
+    assert r[0] == 1 and r[1] == 1
+    assert r[2] < 500_000  # microseconds: the abort flag, not the 1 s limit
+    assert int(counter.item()) == 0
+    ids = np.array([[0, 3], [3, 1]], np.int32)
+    got = _route_np(_route_gpu(ids, 8, 32))
+    _assert_route_equal(got, orouting.route_metadata(ids, 8, 32))
