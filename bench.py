@@ -50,10 +50,10 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # and the SHA-256 of the kernel sources it was taken on (gemm.cu,
 # common.cuh, layout.cuh in that order): once those change, traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_423_168 + 6_081_792,
-                  "sources": "ecfbd688218cec7c3ad08b076b239c4de8fbd3823f703aaee64ae60e8412e73d"},
-    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_725_207_808 + 89_055_744,
-                           "sources": "ecfbd688218cec7c3ad08b076b239c4de8fbd3823f703aaee64ae60e8412e73d"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_346_880 + 6_121_728,
+                  "sources": "c1b521c3bc9b98c8d9d044fa06a01c23c327d1eb599f047e2f2e0ac8b6770727"},
+    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_725_889_152 + 86_745_856,
+                           "sources": "c1b521c3bc9b98c8d9d044fa06a01c23c327d1eb599f047e2f2e0ac8b6770727"},
 }
 
 

@@ -90,6 +90,9 @@ struct GemmParams {
   // first stages before waiting for that kernel (the weights and the routing
   // metadata are complete by then; only the route operand is not).
   int prefetch;
+  // GEMM2: rows and their pitch are 32-byte aligned, so the epilogue stores
+  // whole 32-byte sectors (st.global.v8)
+  int rows32;
 };
 
 // Launch shape per route-tile size: CTAs per SM, accumulator buffers, K=256
@@ -643,10 +646,20 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
                                                                 __uint_as_float(acc[k][2 * i + 1]) * g2);
                 w[i] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              uint4* dst = reinterpret_cast<uint4*>(p.rows + (size_t)r * gs.out_cols + mt * kWTile + 32 * cc);
+              __nv_bfloat16* dp = p.rows + (size_t)r * gs.out_cols + mt * kWTile + 32 * cc;
+              if (p.rows32) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                for (int i = 0; i < 2; ++i)
+                  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dp + 16 * i),
+                               "r"(w[8 * i]), "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]),
+                               "r"(w[8 * i + 4]), "r"(w[8 * i + 5]), "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
+                               : "memory");
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(dp);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+              }
             }
           }
         }
@@ -859,6 +872,7 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
   p.tile_row_limit = tile_row_limit;
   p.totals = totals;
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
+  p.rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
   p.status = status;
   p.tile_m = tile_m;
   if (launch_mode<2>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {
@@ -892,6 +906,7 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
   p.hq = h_codes;
   p.hq_sf = h_sf;
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
+  p.rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
   p.done = done;
   p.status = status;
   p.tile_m = tile_m;

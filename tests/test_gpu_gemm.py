@@ -160,6 +160,35 @@ def test_fused_gemms_match_split_gemms(small_cases, idx):
         assert np.array_equal(rows, split["rows"])
 
 
+def test_gemm2_rows_only_16_byte_aligned():
+    """GEMM2's 128-row-tile epilogue writes whole 32-byte sectors when the rows
+    buffer allows it and 16-byte pieces when it is only 16-byte aligned (the
+    header's requirement): both give the same rows."""
+    T, H, I, E, K = 70, 512, 256, 4, 4
+    w = _workload(T, H, I, E, K, "zipf", 128)
+    raw, batch = inputs.make_layer(w), inputs.make_batch(w)
+    prep = Prepared(raw)
+    ids = _dev(batch["topk_ids"].astype(np.int32))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r = B.route_permute(ids, E, 128, status=status)
+    ws = B.alloc_workspace(T, K, E, H, I, 128, DEV)
+    g1 = torch.tensor([4.0], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([1e-3], dtype=torch.float32, device=DEV)
+    B.experts_quantize(r, ws, x=bf16_dev(batch["x"]), a1_gscale=g1, T=T, H=H, I=I, E=E, K=K, status=status)
+    B.experts_gemm1(prep.w, r, ws, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K, status=status)
+    P, _ = B.route_sizes(T, K, E, 128)
+    aligned = torch.zeros((P, H), dtype=torch.bfloat16, device=DEV)
+    flat = torch.zeros(P * H + 64, dtype=torch.bfloat16, device=DEV)
+    base = flat.data_ptr() % 32 // 2  # elements to the next 32-byte boundary
+    off = flat[base + 8 : base + 8 + P * H].view(P, H)  # 16 bytes past it
+    assert off.data_ptr() % 32 == 16
+    B.experts_gemm2(prep.w, r, ws, aligned, T=T, H=H, I=I, E=E, K=K, status=status)
+    B.experts_gemm2(prep.w, r, ws, off, T=T, H=H, I=I, E=E, K=K, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(aligned, off)
+
+
 @pytest.mark.parametrize("idx", range(len(SMALL)))
 def test_gemm2_on_identical_operands(small_cases, idx, record_property):
     w, raw, batch, tile, a1, a2 = small_cases[idx]
