@@ -600,14 +600,16 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       const uint32_t taddr = tmem + (uint32_t)(b * tile_m) + ((uint32_t)(32 * q) << 16);
       if constexpr (kRouteM) {
         // lane = route row r; accumulator column c = weight row mt * 128 + c.
-        // This warp takes column groups cc = half and half + 2 (32 columns
-        // each): both are read out of TMEM, the buffer goes back to the MMA
-        // issuer, and only then are they converted and stored.
+        // This warp takes the adjacent column groups cc = 2 half and
+        // 2 half + 1 (32 columns each), so that a lane's results for the unit
+        // are contiguous in its row: both groups are read out of TMEM, the
+        // buffer goes back to the MMA issuer, and only then are they converted
+        // and stored.
         static_assert(EPW == 8, "the route-rows-on-M epilogue takes two warps per quadrant");
         const int r = row0 + 32 * q + lane;
         uint32_t acc[2][32];
-        tmem_ld32_async(taddr + 32 * half, acc[0]);
-        tmem_ld32_async(taddr + 32 * (half + 2), acc[1]);
+        tmem_ld32_async(taddr + 64 * half, acc[0]);
+        tmem_ld32_async(taddr + 64 * half + 32, acc[1]);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -617,9 +619,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           // 16 (4 mt + cc) + 0..15 (the prepared w13 granules)
           const float s0 = gs.s0[e], s1 = gs.s1[e], a2g = *p.a2_gscale;
           const int I = gs.out_cols;
+          uint32_t cw[4], sf2 = 0;  // the two groups' 16 code bytes and 2 scale bytes
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const int cc = half + 2 * k;
             float h[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -630,15 +632,22 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
             uint2 codes;
             uint32_t sfc;
             quant16(h, a2g, codes, sfc);
-            *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 8 * cc) = codes;
-            p.hq_sf[act_sf_offset(r, 4 * mt + cc, tile_m, I / 64, S)] = static_cast<uint8_t>(sfc);
+            cw[2 * k] = codes.x;
+            cw[2 * k + 1] = codes.y;
+            sf2 |= sfc << (8 * k);
           }
+          // blocks 4 mt + 2 half and + 1: 16 contiguous code bytes, and two
+          // adjacent scale bytes of the row's atom
+          *reinterpret_cast<uint4*>(p.hq + (size_t)r * (I / 2) + 32 * mt + 16 * half) =
+              make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint16_t*>(p.hq_sf + act_sf_offset(r, 4 * mt + 2 * half, tile_m, I / 64, S)) =
+              static_cast<uint16_t>(sf2);
         } else {
           const float g2 = gs.s0[e];
           if (r < p.tile_row_limit[tau]) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const int cc = half + 2 * k;
+              const int cc = 2 * half + k;
               uint32_t w[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
