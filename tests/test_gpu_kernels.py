@@ -155,6 +155,7 @@ def _quant_case(T, H, E, K, tile, g, seed=0, scale=1.0):
     (8, 5120, 128, 8, 32, 618.8201293945312, 1.0),
     (37, 1024, 16, 4, 64, 3.0, 100.0),        # ragged, several tiles, saturation
     (300, 512, 8, 8, 256, 2.0, 1.0),          # two scale atoms per tile
+    (256, 5120, 16, 8, 128, 3.0, 1.0),        # full row width: ten 32-block chunks per token
     (16, 256, 4, 2, 128, 1e-3, 1e-5),         # scales in the e4m3 subnormals / zero
 ])
 def test_quantize_permute_bit_exact(T, H, E, K, tile, g, scale):
@@ -170,8 +171,9 @@ def test_quantize_permute_bit_exact(T, H, E, K, tile, g, scale):
     assert not scales[pad].any()  # padding rows: zero scales (their codes are not written)
 
 
-def test_quantize_prequantized_input_is_a_gather():
-    T, H, E, K, tile = 12, 512, 8, 4, 32
+@pytest.mark.parametrize("T", [12, 260])
+def test_quantize_prequantized_input_is_a_gather(T):
+    H, E, K, tile = 512, 8, 4, 32
     rng = np.random.default_rng(1)
     a = rng.integers(0, 256, (T, H // 2), dtype=np.uint8)
     a_sf = rng.integers(0, 0x7F, (T, H // 16), dtype=np.uint8)
