@@ -8,7 +8,7 @@ from oracle import codecs, layer as olayer, layout as olayout, quant as oquant, 
 from nvfp4_mixture_experts_route_gb300 import binding as B
 from nvfp4_mixture_experts_route_gb300 import inputs
 
-from _util import bf16_dev, bf16_host_f64, canon_codes, canon_packed, rel_l2
+from _util import bf16_dev, bf16_host_f64, canon_packed, rel_l2
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"

@@ -1,6 +1,5 @@
 """Pins of the oracle's expert block and post-expert finalize (no GPU)."""
 import numpy as np
-import pytest
 import torch
 
 from oracle import codecs, layer, layout, routing
