@@ -359,29 +359,31 @@ def run_ours(args, w) -> None:
         torch.cuda.synchronize()
         fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
 
-    # e2e: the public serving call (NvFp4MoE.replay: the step as one CUDA
-    # graph on the layer's static buffers) fed from pinned host memory, with
-    # the host->device copies of the step's inputs and the device->host copy
-    # of its output inside the timed region. One weight copy: a step streams
-    # the touched experts' weights (far larger than L2) from HBM anyway.
-    # --no-graph times the eager public call (NvFp4MoE.forward) instead.
-    # One pinned host buffer in the layer's input layout: x, topk_ids and
-    # topk_weights travel in one host->device copy per step.
+    # e2e: the public serving call NvFp4MoE.replay_host: one CUDA graph per
+    # step that copies the step's inputs from the layer's pinned host buffer
+    # to the device (x, topk_ids and topk_weights in one copy, laid out by
+    # input_layout), runs routing, expert body and finalize, and copies the
+    # output back into pinned host memory; the copies are inside the timed
+    # region. One weight copy: a step streams the touched experts' weights
+    # (far larger than L2) from HBM anyway. --no-graph times the eager public
+    # call (NvFp4MoE.forward) with the same two copies around it.
     offs, nbytes = moe.input_layout(T, K)
-    in_h = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    moe.weights = copies[0]
+    hb = moe.host_buffers(T, K)
+    in_h, out_h = hb["host_inputs"], hb["host_out"]
     in_h[offs["x"]:offs["x"] + T * H * 2].copy_(torch.from_numpy(batch["x"].view(np.uint8).reshape(-1)))
     in_h[offs["topk_ids"]:offs["topk_ids"] + T * K * 4].copy_(
         torch.from_numpy(batch["topk_ids"].view(np.uint8).reshape(-1)))
     in_h[offs["topk_weights"]:offs["topk_weights"] + T * K * 4].copy_(
         torch.from_numpy(batch["topk_weights"].view(np.uint8).reshape(-1)))
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    moe.weights = copies[0]
     gb = moe.graph_buffers(T, K)
 
     def e2e_step(i):
-        gb["inputs"].copy_(in_h, non_blocking=True)
-        o = moe.replay(T, K) if args.graph else moe.forward(gb["x"], gb["topk_ids"], gb["topk_weights"])[0]
-        out_h.copy_(o, non_blocking=True)
+        if args.graph:
+            moe.replay_host(T, K)
+        else:
+            gb["inputs"].copy_(in_h, non_blocking=True)
+            out_h.copy_(moe.forward(gb["x"], gb["topk_ids"], gb["topk_weights"])[0], non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i)

@@ -99,6 +99,45 @@ class NvFp4MoE:
             self._buffers[key]["topk_ids"].fill_(-1)
         return self._buffers[key]
 
+    def host_buffers(self, T: int, K: int) -> dict:
+        """Pinned host staging of the step for (T, K): ``host_inputs`` (bytes
+        laid out by ``input_layout``: x, topk_ids, topk_weights) and
+        ``host_out`` bf16 [T, H]. ``replay_host`` copies the one in and the
+        other out inside its graph."""
+        key = ("host", T, K)
+        if key not in self._buffers:
+            _, nbytes = self.input_layout(T, K)
+            self._buffers[key] = {
+                "host_inputs": torch.zeros(nbytes, dtype=torch.uint8).pin_memory(),
+                "host_out": torch.empty((T, self.H), dtype=torch.bfloat16).pin_memory(),
+                "graph": None,
+            }
+        return self._buffers[key]
+
+    def replay_host(self, T: int, K: int) -> torch.Tensor:
+        """One CUDA graph replay that copies ``host_buffers(T, K)["host_inputs"]``
+        to the device, runs the step (routing, expert body, finalize) and
+        copies the output into ``host_out``, all on the current stream: a
+        serving step with one launch. Returns ``host_out``; read it after the
+        stream is synchronised."""
+        h = self.host_buffers(T, K)
+        g = self.graph_buffers(T, K)
+
+        def step():
+            g["inputs"].copy_(h["host_inputs"], non_blocking=True)
+            self.forward(g["x"], g["topk_ids"], g["topk_weights"], out=g["out"])
+            h["host_out"].copy_(g["out"], non_blocking=True)
+
+        if h["graph"] is None:
+            step()  # warm-up, outside capture
+            torch.cuda.current_stream(self.device).synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            h["graph"] = graph
+        h["graph"].replay()
+        return h["host_out"]
+
     def input_layout(self, T: int, K: int) -> tuple[dict, int]:
         """Byte offsets of x, topk_ids and topk_weights inside ``inputs`` (each
         16-byte aligned) and its size."""

@@ -409,8 +409,9 @@ def test_timed_launch_path_matches_split_path(full, name):
     for prefill tiles two GEMM launches, each a programmatic dependent that
     prefetches weights -- the finalize; eager and as a graph replay) gives
     exactly the split entry points' output at full size; those are held to
-    the oracle above. moe_experts_gemms at that size gives the split GEMM2
-    rows too."""
+    the oracle above; so does the host-staged serving call (its copies inside
+    the graph). moe_experts_gemms at that size gives the split GEMM2 rows
+    too."""
     from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
 
     raw, prep = full
@@ -431,5 +432,11 @@ def test_timed_launch_path_matches_split_path(full, name):
     gb["topk_weights"].copy_(tw)
     graphed = bf16_host_f64(moe.replay(w.T, w.K))
     assert np.array_equal(graphed, split["out"])
+    # the serving call with its host copies inside the graph
+    hb = moe.host_buffers(w.T, w.K)
+    hb["host_inputs"].copy_(gb["inputs"].cpu())
+    host = moe.replay_host(w.T, w.K)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host_f64(host), split["out"])
     status, fused = _fused_rows(prep, batch, w.tile_m, a1, a2, calls=1)
     assert status == 0 and np.array_equal(fused[0], split["rows"])
