@@ -1,12 +1,14 @@
 """The C-ABI library loads, exports every declared entry point, and checks
 its arguments on the host (no GPU calls)."""
 import ctypes as C
+import os
 
 import pytest
 
 from nvfp4_mixture_experts_route_gb300 import binding as B
 from nvfp4_mixture_experts_route_gb300 import build
 
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
@@ -106,3 +108,18 @@ def test_selftest_arguments_refused_before_launch(lib):
     assert lib.moe_selftest_counter_timeout(2_000_000, None, 16, 16, None) == -1
     assert lib.moe_selftest_counter_timeout(2_000_000, 18, 16, 16, None) == -1  # misaligned counter
     assert lib.moe_selftest_counter_timeout(10, 16, 16, 16, None) == -1       # below 1 us
+
+
+def test_header_compiles_as_c_and_cpp():
+    """include/moe_nvfp4.h is a plain C header: no C++ types leak into the
+    boundary, and it also compiles as C++."""
+    import shutil
+    import subprocess
+
+    hdr = os.path.join(ROOT, "include", "moe_nvfp4.h")
+    for cc, std, lang in (("gcc", "-std=c99", "c"), ("g++", "-std=c++17", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not installed")
+        r = subprocess.run([cc, "-fsyntax-only", std, "-Wall", "-Wextra", "-Werror", "-x", lang, hdr],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
