@@ -240,40 +240,70 @@ def _config(w) -> dict:
             "tile_m": w.tile_m, "parallelism": "replicas"}
 
 
-def run_ours(args, w) -> None:
+def measure_fp4_peak(B, torch, stream) -> dict:
+    """Dense NVFP4 tensor-core rate of this GPU, measured live with the
+    library's own probe (moe_fp4_mma_rate: back-to-back tcgen05 kind::mxf4nvf4
+    MMAs of 128 x 256 x 64 on shared-memory operands, one CTA per SM, 16 MMAs
+    per commit), the best of three launches of about 0.2 s: the burst rate a
+    kernel timed on its own between events can reach."""
+    status = torch.zeros(1, dtype=torch.int32, device=stream.device)
+    B.fp4_mma_rate(256, 0, 16, 1, 64, status=status, stream=stream)
+    best = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        flops = B.fp4_mma_rate(256, 0, 16, 1, 2000, status=status, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    if int(status.item()) != 0:
+        raise RuntimeError("fp4 rate probe: device status " + B.STATUS_NAMES.get(int(status.item()), "?"))
+    return {"tflops": best, "how": "moe_fp4_mma_rate(n=256, sf_copies=0, mmas_per_commit=16, 1 CTA/SM), "
+                                   "best of 3 launches of ~0.2 s, measured in this run"}
+
+
+class Layer:
+    """One prepared layer on this GPU plus rotating copies of its prepared
+    weights (together larger than L2), shared by every workload of a run."""
+
+    def __init__(self, args, w, dev):
+        from nvfp4_mixture_experts_route_gb300 import binding as B
+        from nvfp4_mixture_experts_route_gb300 import inputs
+        from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
+
+        self.raw = inputs.make_layer(w)
+        self.a1, self.a2 = inputs.global_scales(w)
+        self.moe = NvFp4MoE(self.raw, self.a1, self.a2, self.raw["gamma"], tile_m=w.tile_m, device=dev)
+        self.copies = [self.moe.weights]
+        self.keep = [self.moe.prepared]
+        self.layer_bytes = sum(t.numel() for t in self.moe.prepared.values())
+        for _ in range(max(1, args.copies) - 1):
+            p = {k: v.clone() for k, v in self.moe.prepared.items()}
+            self.keep.append(p)
+            self.copies.append(B.weights_struct(p, self.moe.g1_alphas, self.moe.g1_scale_c, self.moe.g2_alphas))
+
+
+def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
+    """Time one workload's step (graph-replayed, K steps between events) and
+    its dominant kernel, and the end-to-end serving call; returns the fields
+    of its bench line."""
     import numpy as np
     import torch
 
     from nvfp4_mixture_experts_route_gb300 import binding as B
     from nvfp4_mixture_experts_route_gb300 import inputs
-    from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
 
-    world, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    B.load()
-
-    raw = inputs.make_layer(w)
     batch = inputs.make_batch(w, seed=rank)
-    a1, a2 = inputs.global_scales(w)
     T, K, E, H, I, tile = w.T, w.K, w.E, w.H, w.I, w.tile_m
-
-    # Prepared weight copies, rotated so that every step streams from HBM.
-    moe = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=tile, device=dev)
-    copies = [moe.weights]
-    keep = [moe.prepared]
-    layer_bytes = sum(t.numel() for t in moe.prepared.values())
-    n_copies = max(1, args.copies)
-    for _ in range(n_copies - 1):
-        p = {k: v.clone() for k, v in moe.prepared.items()}
-        keep.append(p)
-        copies.append(B.weights_struct(p, moe.g1_alphas, moe.g1_scale_c, moe.g2_alphas))
+    moe, copies = layer.moe, layer.copies
+    moe.tile_m = tile
 
     x = torch.from_numpy(batch["x"].view(np.int16)).view(torch.bfloat16).to(dev)
     ids = torch.from_numpy(batch["topk_ids"]).to(dev)
     tw = torch.from_numpy(batch["topk_weights"]).to(dev)
     bufs = moe.buffers(T, K)
     route, ws, rows, out, status = bufs["route"], bufs["ws"], bufs["rows"], bufs["out"], bufs["status"]
+    status.zero_()
     stream = torch.cuda.current_stream(dev)
 
     fused = B.experts_kernels(tile) == 2
@@ -302,7 +332,8 @@ def run_ours(args, w) -> None:
                                 status=status)
                 ev[1].record(stream)
             ev[2].record(stream)
-        B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out)
+        B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out,
+                               status=status)
 
     # route/permute (1 or 3 kernels), quantize, the expert GEMMs (one fused
     # launch or two), finalize
@@ -329,7 +360,7 @@ def run_ours(args, w) -> None:
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(dev.index or 0) as clocks:
         start.record(stream)
         for i in range(args.steps):
             if graphs:
@@ -341,6 +372,7 @@ def run_ours(args, w) -> None:
     total_ms = _max_over_ranks(world, start.elapsed_time(end))
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} in the timed region")
+    del graphs
 
     # The same steps launched one by one, GEMM launches between events on the
     # launching stream: the per-kernel durations of the roofline.
@@ -399,8 +431,6 @@ def run_ours(args, w) -> None:
     e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
     moe.weights = copies[0]
 
-    if rank != 0:
-        return
     touched = np.unique(batch["topk_ids"][batch["topk_ids"] >= 0])
     n_touch = len(touched)
     w13_bytes = 2 * I * (H // 2) + 2 * I * (H // 16)
@@ -410,41 +440,46 @@ def run_ours(args, w) -> None:
     gemm1_gbs = n_touch * w13_bytes / (gemm1_ms * 1e-3) / 1e9
     fused_gbs = n_touch * (w13_bytes + w2_bytes) / (fused_ms * 1e-3) / 1e9 if fused else None
     live_routes = int(np.sum(batch["topk_ids"] >= 0))
-    gemm1_tflops = 2.0 * live_routes * (2 * I) * H / (gemm1_ms * 1e-3) / 1e12
+    gemm1_flops = 2.0 * live_routes * (2 * I) * H
+    gemm2_flops = 2.0 * live_routes * H * I
     tensor_bound = live_routes >= 8 * w.E * 8  # many routes per expert: the MMA, not HBM, bounds
     tokens_total = T * args.steps * world
-    value = tokens_total / (total_ms * 1e-3)
     step_ms = total_ms / args.steps
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e2m1xue4m3 (fp32 accumulate)", "data": "synthetic",
+    weight_bytes = n_touch * (w13_bytes + w2_bytes)
+    if fused and not tensor_bound:
+        roof = {"bound": "hbm",
+                "kernel": f"grouped_gemm_kernel<3, {tile}> (GEMM1 + SwiGLU + requant + GEMM2, one launch)",
+                "achieved": fused_gbs, "peak": peak, "unit": "GB/s", "frac": fused_gbs / peak,
+                "peak_kind": f"{peak_kind} copy bandwidth",
+                "traffic": _traffic(w.name, f"grouped_gemm_kernel<3, {tile}>"),
+                "algorithmic_bytes": weight_bytes, "launch_ms": fused_ms}
+    elif not tensor_bound:
+        roof = {"bound": "hbm", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
+                "achieved": gemm1_gbs, "peak": peak, "unit": "GB/s", "frac": gemm1_gbs / peak,
+                "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                "algorithmic_bytes": n_touch * w13_bytes, "launch_ms": gemm1_ms}
+    else:
+        ach = gemm1_flops / (gemm1_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
+                "achieved": ach, "peak": fp4_peak["tflops"], "unit": "TFLOP/s", "frac": ach / fp4_peak["tflops"],
+                "peak_kind": "measured dense NVFP4 (burst): " + fp4_peak["how"],
+                "frac_of_bf16x6": ach / (pk["bf16"] * FP4_PER_BF16),
+                "traffic": _traffic(w.name, f"grouped_gemm_kernel<1, {tile}>"),
+                "algorithmic_flops": gemm1_flops, "launch_ms": gemm1_ms,
+                "gemm2": {"achieved": gemm2_flops / (gemm2_ms * 1e-3) / 1e12,
+                          "frac": gemm2_flops / (gemm2_ms * 1e-3) / 1e12 / fp4_peak["tflops"],
+                          "launch_ms": gemm2_ms}}
+    res = {
+        "value": tokens_total / (total_ms * 1e-3), "ms_per_step": step_ms,
         "config": {**_config(w), "l2": f"{len(copies)} rotating prepared weight copies "
-                                        f"({len(copies) * layer_bytes / 1e9:.2f} GB > L2)",
-                   "launch": (f"CUDA graph per step ({launches_per_step} kernels)" if graphs
+                                        f"({len(copies) * layer.layer_bytes / 1e9:.2f} GB > L2)",
+                   "launch": (f"CUDA graph per step ({launches_per_step} kernels)" if args.graph
                               else f"eager ({launches_per_step} kernels per step)")},
-        "roofline": ({"bound": "hbm",
-                      "kernel": f"grouped_gemm_kernel<3, {tile}> (GEMM1 + SwiGLU + requant + GEMM2, one launch)",
-                      "achieved": fused_gbs, "peak": peak, "unit": "GB/s", "frac": fused_gbs / peak,
-                      "peak_kind": f"{peak_kind} copy bandwidth",
-                      "traffic": _traffic(w.name, f"grouped_gemm_kernel<3, {tile}>"),
-                      "algorithmic_bytes": n_touch * (w13_bytes + w2_bytes), "launch_ms": fused_ms}
-                     if fused and not tensor_bound else
-                     {"bound": "hbm", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
-                      "achieved": gemm1_gbs, "peak": peak, "unit": "GB/s", "frac": gemm1_gbs / peak,
-                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
-                      "algorithmic_bytes": n_touch * w13_bytes, "launch_ms": gemm1_ms}
-                     if not tensor_bound else
-                     {"bound": "tensor", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
-                      "achieved": gemm1_tflops, "peak": pk["bf16_sust"] * FP4_PER_BF16, "unit": "TFLOP/s",
-                      "frac": gemm1_tflops / (pk["bf16_sust"] * FP4_PER_BF16),
-                      "peak_kind": f"{peak_kind} sustained bf16 x {FP4_PER_BF16:g} (nominal fp4/bf16 ratio)",
-                      "traffic": _traffic(w.name, f"grouped_gemm_kernel<1, {tile}>"),
-                      "algorithmic_flops": 2.0 * live_routes * 2 * I * H, "launch_ms": gemm1_ms}),
-        "step_roofline": {"bytes": n_touch * (w13_bytes + w2_bytes), "touched_experts": int(n_touch),
-                          "achieved_gbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9,
-                          "frac_of_measured": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 1e9 / peak,
-                          "frac_of_8tbs": n_touch * (w13_bytes + w2_bytes) / (step_ms * 1e-3) / 8e12,
+        "roofline": roof,
+        "step_roofline": {"bytes": weight_bytes, "touched_experts": int(n_touch),
+                          "achieved_gbs": weight_bytes / (step_ms * 1e-3) / 1e9,
+                          "frac_of_measured": weight_bytes / (step_ms * 1e-3) / 1e9 / peak,
+                          "frac_of_8tbs": weight_bytes / (step_ms * 1e-3) / 8e12,
                           "gemm1_ms": gemm1_ms, "gemm2_ms": gemm2_ms, "fused_gemms_ms": fused_ms},
         "clocks": clocks.summary(),
         "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -452,8 +487,60 @@ def run_ours(args, w) -> None:
                 "d2h_bytes_per_step": out_h.numel() * 2},
         "gpu_launches": launches_per_step * args.steps,
     }
+    if tensor_bound:
+        # the step's HBM bytes as the method moves them: the layer's weights
+        # and scales, the bf16 GEMM2 rows written and read back, the
+        # intermediate written and read, x and out, the quantized activations
+        P, _ = B.route_sizes(T, K, E, tile)
+        hbm = (E * (w13_bytes + w2_bytes) + 2 * live_routes * H * 2 + 2 * live_routes * (I // 2 + I // 16)
+               + 2 * T * H * 2 + 2 * live_routes * (H // 2 + H // 16))
+        res["step_roofline"].update(
+            {"bytes": hbm, "achieved_gbs": hbm / (step_ms * 1e-3) / 1e9,
+             "frac_of_measured": hbm / (step_ms * 1e-3) / 1e9 / peak, "frac_of_8tbs": hbm / (step_ms * 1e-3) / 8e12,
+             "step_tflops": (gemm1_flops + gemm2_flops) / (step_ms * 1e-3) / 1e12,
+             "step_frac_of_fp4": (gemm1_flops + gemm2_flops) / (step_ms * 1e-3) / 1e12 / fp4_peak["tflops"]})
+    del batch
+    return res
+
+
+def run_ours(args, w) -> None:
+    import torch
+
+    from nvfp4_mixture_experts_route_gb300 import binding as B
+    from nvfp4_mixture_experts_route_gb300 import inputs
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+    stream = torch.cuda.current_stream(dev)
+    fp4_peak = measure_fp4_peak(B, torch, stream)
+
+    layer = Layer(args, w, dev)
+    head = measure_workload(args, w, layer, world, rank, dev, fp4_peak)
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1xue4m3 (fp32 accumulate)", "data": "synthetic",
+        **{k: head[k] for k in ("config", "roofline", "step_roofline", "clocks", "e2e", "gpu_launches")},
+        "fp4_peak": fp4_peak,
+    }
+    # The other configurations of the same layer (the b = 64 Zipf decode
+    # batch and the 8192-token prefill), each timed the same way on the same
+    # prepared weights; each reports its own timed region's launches.
+    extra = [n for n in args.also.split(",") if n] if args.also is not None else []
+    if extra:
+        line["workloads"] = {}
+        for name in extra:
+            wx = inputs.WORKLOADS[name]
+            if wx.layer_key != w.layer_key:
+                continue
+            line["workloads"][name] = measure_workload(args, wx, layer, world, rank, dev, fp4_peak)
+    if rank != 0:
+        return
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(w, raw, batch, a1, a2, tokens=args.cpu_tokens)
+        line["cpu_baseline"] = cpu_oracle_sample(w, layer.raw, inputs.make_batch(w, seed=rank), layer.a1, layer.a2,
+                                                 tokens=args.cpu_tokens)
     print(json.dumps(line), flush=True)
 
 
@@ -626,6 +713,10 @@ def main() -> None:
     ap.add_argument("--cpu-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile-m", type=int, default=0, help="route tile rows (default: the workload's)")
+    ap.add_argument("--also", default=None,
+                    help="comma-separated further workloads of the same layer, timed in the same run and "
+                         "reported under 'workloads' (default with decode_b8: decode_b64_zipf,prefill_t8192_zipf; "
+                         "'' for none)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps one by one instead of replaying CUDA graphs")
     args = ap.parse_args()
@@ -642,6 +733,8 @@ def main() -> None:
         import dataclasses
 
         w = dataclasses.replace(w, tile_m=args.tile_m)
+    if args.also is None and args.workload == "decode_b8" and not args.tile_m:
+        args.also = "decode_b64_zipf,prefill_t8192_zipf"
     if args.impl == "reference":
         run_reference(args, w)
     else:

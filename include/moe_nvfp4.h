@@ -263,13 +263,17 @@ int moe_experts_import(int which, const void* codes, const void* scales,
  * moe_noalloc_scratch_bytes() bytes (32 MiB) that the library defines in
  * device memory; every GPU that loads the library holds that array until
  * the process exits. Shapes whose workspace (moe_experts_workspace_size)
- * is larger are refused with MOE_ERR_WORKSPACE before anything is enqueued;
- * at H = 5120, I = 2048, E = 128, top-8, tile_m = 32 that admits up to 64
- * tokens.
+ * is larger are refused with MOE_ERR_WORKSPACE before anything is enqueued.
+ * The workspace size depends only on the shape, not on the routing: compare
+ * moe_experts_workspace_size with moe_noalloc_scratch_bytes(). At H = 5120,
+ * I = 2048, E = 128, top-8 and tile_m = 32 that admits up to 287 tokens
+ * (tile_m = 128: 8 tokens; the padded-row bound grows with the tile).
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture. Every other argument, the outputs
+ * first call before any stream capture. The address is looked up again
+ * when the device's context has changed since (after a cudaDeviceReset),
+ * so make the first call after a reset outside a capture too. Every other argument, the outputs
  * and the status word behave as in moe_nvfp4_experts, and the caller still
  * owns x / a / a_sf, the routing metadata and gemm2_rows. All calls share
  * the one array: two calls whose work overlaps on the GPU (different
@@ -295,30 +299,34 @@ size_t moe_noalloc_scratch_bytes(void);
  *   weight_before_norm != 0:  u = g*r,  N = u * rsqrt(mean(u^2) + eps)
  *   weight_before_norm == 0:  N = g * r * rsqrt(mean(r^2) + eps)
  * all in fp32 over the full hidden size H, summed over k in order 0..K-1.
- * rows: bf16 [*, H] (GEMM2 rows); expanded_to_permuted int32 [T, K];
- * topk_weights fp32 [T, K]; gamma bf16 [H]; out bf16 [T, H] (caller-owned,
- * may not alias rows). H % 8 == 0, H <= 16384; T == 0 is valid.
+ * rows: bf16 [num_rows, H] (GEMM2 rows); expanded_to_permuted int32
+ * [T, K]; topk_weights fp32 [T, K]; gamma bf16 [H]; out bf16 [T, H]
+ * (caller-owned, may not alias rows). H % 8 == 0, H <= 16384, num_rows >= 0;
+ * T == 0 is valid. An expanded_to_permuted entry outside [-1, num_rows)
+ * records MOE_ERR_INVALID_ROUTE in *status (optional device word) and that
+ * route is skipped as if it were -1: no row outside the buffer is read.
  * ---------------------------------------------------------------------- */
-int moe_post_expert_finalize(const void* rows,
+int moe_post_expert_finalize(const void* rows, int num_rows,
                              const int32_t* expanded_to_permuted,
                              const float* topk_weights, const void* gamma,
                              float eps, int weight_before_norm, int T, int K,
-                             int H, void* out, void* stream);
+                             int H, void* out, int32_t* status, void* stream);
 
 /* Expert-TP tail (the expert_tp page: with expert tensor parallelism every
  * rank computes K-partial GEMM2 rows over its intermediate slice, and they
  * are summed -- "FP32 sum, one BF16 rounding" -- before the per-route norm;
  * the muse_moe_runner page's TP finalize fuses that sum into the norm).
  * rows_parts is a HOST array of nparts (1..16) device pointers to bf16
- * [*, H] row buffers indexed alike; each route's row is
+ * [num_rows, H] row buffers indexed alike; each route's row is
  * bf16(sum_r float(part_r[p])) and then finalized exactly as
- * moe_post_expert_finalize does. With nparts = 1 it equals
- * moe_post_expert_finalize. */
+ * moe_post_expert_finalize does (the same row bound and status word). With
+ * nparts = 1 it equals moe_post_expert_finalize. */
 int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts,
+                                int num_rows,
                                 const int32_t* expanded_to_permuted,
                                 const float* topk_weights, const void* gamma,
                                 float eps, int weight_before_norm, int T, int K,
-                                int H, void* out, void* stream);
+                                int H, void* out, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * Steps that feed the block (the model page, MuseSpark1xMoE).
@@ -376,6 +384,29 @@ int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void*
                    void* ws, size_t ws_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Dense NVFP4 tensor-core rate of this GPU, for the roofline of the
+ * compute-bound (prefill) expert GEMMs. The pages print no throughput; this
+ * measures the instruction the expert GEMMs issue
+ * (tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X, M = 128,
+ * K = 64, e2m1 operands with ue4m3 scales per 16 elements, fp32 accumulate in
+ * tensor memory) on operands held in shared memory: every CTA (ctas_per_sm per
+ * SM, on every SM) issues `stages` stages of mmas_per_commit MMAs of N = n,
+ * each stage ending in one tcgen05.commit, three stages in flight. With
+ * sf_copies = 0 the scale factors are copied into tensor memory once; with
+ * 1, 2 or 3 every stage's are copied (tcgen05.cp, one per 128 rows of each
+ * operand per K = 64 step, as the expert GEMMs do) by the MMA thread itself
+ * (1), by a second warp that hands each stage over through an mbarrier (2),
+ * or by two more warps, one per operand (3). Supported: n = 128
+ * (ctas_per_sm 1 or 2) or 256 (ctas_per_sm 1); mmas_per_commit 4, or 16 with
+ * sf_copies = 0; stages 1 .. 2^24. *flops (host) receives the launch's FLOPs,
+ * 2 * 128 * n * 64 * mmas_per_commit * stages * CTAs; time the launch with
+ * events on `stream`. A wait that gives up records MOE_ERR_TIMEOUT in *status
+ * (optional device word). Operands and outputs are scratch inside the kernel.
+ * ---------------------------------------------------------------------- */
+int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm,
+                     int stages, double* flops, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Self-test of the failure path: runs the library's bounded mbarrier wait on
  * a barrier that nothing completes, with limit_ns (1 us .. 1 s). On return
  * (after a stream sync) *status holds MOE_ERR_TIMEOUT and result[0..1] == {1, 1}:
@@ -393,6 +424,13 @@ int moe_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, int32_t* resul
  * and the outcome are as for moe_selftest_wait_timeout. */
 int moe_selftest_counter_timeout(uint64_t limit_ns, const int32_t* counter,
                                  int32_t* status, int32_t* result, void* stream);
+
+/* Holds SMs the way another stream's kernel would, for testing that the
+ * library's kernels finish while other work occupies part of the GPU: ctas
+ * CTAs of one warp, each with smem_bytes (<= 227 KB) of dynamic shared memory
+ * so that nothing else fits beside it on its SM, each exiting after ns
+ * nanoseconds (at most 2 s) of spinning on the global timer. */
+int moe_selftest_occupy(int ctas, int smem_bytes, uint64_t ns, void* stream);
 
 #ifdef __cplusplus
 }

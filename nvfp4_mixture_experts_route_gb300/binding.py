@@ -92,19 +92,21 @@ _SIGNATURES = {
     ),
     "moe_experts_export": ([_I, _P, C.c_size_t, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_experts_import": ([_I, _P, _P, _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P], _I),
-    "moe_post_expert_finalize": ([_P, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P], _I),
+    "moe_post_expert_finalize": ([_P, _I, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_nvfp4_experts_noalloc": (
         [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _P],
         _I,
     ),
     "moe_noalloc_scratch_bytes": ([], C.c_size_t),
     "moe_post_expert_finalize_tp": (
-        [C.POINTER(C.c_void_p), _I, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P], _I),
+        [C.POINTER(C.c_void_p), _I, _I, _P, _P, _P, C.c_float, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_musespark1x_routing": ([_P, _P, _P, _I, _I, _I, C.c_float, C.c_float, _P, _P, _P], _I),
     "moe_rmsnorm_nvfp4_quant": ([_P, _P, C.c_float, _P, _I, _I, _P, _P, _P], _I),
     "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
+    "moe_fp4_mma_rate": ([_I, _I, _I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
     "moe_selftest_wait_timeout": ([C.c_uint64, _P, _P, _P], _I),
+    "moe_selftest_occupy": ([_I, _I, C.c_uint64, _P], _I),
     "moe_selftest_counter_timeout": ([C.c_uint64, _P, _P, _P, _P], _I),
     "moe_experts_norm_quantize": (
         [_P, _P, C.c_float, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P], _I),
@@ -352,7 +354,9 @@ def nvfp4_experts_noalloc(w: MoeWeights, route: Route, *, x=None, a=None, a_sf=N
 
 
 def post_expert_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps: float,
-                         weight_before_norm: bool = True, out=None, stream=None):
+                         weight_before_norm: bool = True, out=None, status=None, stream=None):
+    """rows: bf16 [num_rows, H]; entries of expanded_to_permuted outside
+    [-1, num_rows) are skipped and recorded in status (MOE_ERR_INVALID_ROUTE)."""
     import torch
 
     T, K = expanded_to_permuted.shape
@@ -360,13 +364,13 @@ def post_expert_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps: f
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=gamma.device)
     _check(load().moe_post_expert_finalize(
-        _ptr(rows), _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
-        1 if weight_before_norm else 0, T, K, H, _ptr(out), _stream(stream)))
+        _ptr(rows), rows.shape[0], _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
+        1 if weight_before_norm else 0, T, K, H, _ptr(out), _ptr(status), _stream(stream)))
     return out
 
 
 def post_expert_finalize_tp(row_parts, expanded_to_permuted, topk_weights, gamma, eps: float,
-                            weight_before_norm: bool = True, out=None, stream=None):
+                            weight_before_norm: bool = True, out=None, status=None, stream=None):
     """Finalize from tp K-partial row buffers (summed in fp32, one bf16
     rounding, before the norm)."""
     import torch
@@ -376,9 +380,10 @@ def post_expert_finalize_tp(row_parts, expanded_to_permuted, topk_weights, gamma
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=gamma.device)
     arr = (C.c_void_p * len(row_parts))(*[r.data_ptr() for r in row_parts])
+    num_rows = min(r.shape[0] for r in row_parts)
     _check(load().moe_post_expert_finalize_tp(
-        arr, len(row_parts), _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
-        1 if weight_before_norm else 0, T, K, H, _ptr(out), _stream(stream)))
+        arr, len(row_parts), num_rows, _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
+        1 if weight_before_norm else 0, T, K, H, _ptr(out), _ptr(status), _stream(stream)))
     return out
 
 
@@ -437,6 +442,16 @@ def dense_bf16(x, w, *, out=None, ws=None, status=None, stream=None):
     return y
 
 
+def fp4_mma_rate(n: int, sf_copies: int, mmas_per_commit: int, ctas_per_sm: int, stages: int, status=None,
+                 stream=None) -> float:
+    """Launch the dense NVFP4 tensor-core rate probe (see the header);
+    returns the launch's FLOPs. Time it with events on the same stream."""
+    f = C.c_double()
+    _check(load().moe_fp4_mma_rate(n, int(sf_copies), mmas_per_commit, ctas_per_sm, stages, C.byref(f),
+                                   _ptr(status), _stream(stream)))
+    return f.value
+
+
 def selftest_wait_timeout(limit_ns: int, status, result, stream=None) -> None:
     """Run the bounded-wait failure path (see the header); status int32 [1]
     and result int32 [3] on the device."""
@@ -449,3 +464,8 @@ def selftest_counter_timeout(limit_ns: int, counter, status, result, stream=None
     _check(load().moe_selftest_counter_timeout(int(limit_ns), _ptr(counter), _ptr(status), _ptr(result),
                                                _stream(stream)))
 
+
+
+def selftest_occupy(ctas: int, smem_bytes: int, ns: int, stream=None) -> None:
+    """Hold SMs for ns nanoseconds from another stream (see the header)."""
+    _check(load().moe_selftest_occupy(int(ctas), int(smem_bytes), int(ns), _stream(stream)))

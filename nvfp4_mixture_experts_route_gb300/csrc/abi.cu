@@ -20,10 +20,10 @@ cudaError_t launch_quantize_permute(const void*, const void*, const void*, const
 cudaError_t launch_act_scales_io(int, uint8_t*, uint8_t*, int, int, int, cudaStream_t);
 cudaError_t launch_prepare_weights(const void*, const void*, const void*, const void*, int, int,
                                    int, void*, void*, void*, void*, cudaStream_t);
-cudaError_t launch_finalize(const void*, const int32_t*, const float*, const void*, float, int,
-                            int, int, int, void*, cudaStream_t);
-cudaError_t launch_finalize_parts(const void* const*, int, const int32_t*, const float*, const void*,
-                                  float, int, int, int, int, void*, cudaStream_t);
+cudaError_t launch_finalize(const void*, int, const int32_t*, const float*, const void*, float, int,
+                            int, int, int, void*, int32_t*, cudaStream_t);
+cudaError_t launch_finalize_parts(const void* const*, int, int, const int32_t*, const float*, const void*,
+                                  float, int, int, int, int, void*, int32_t*, cudaStream_t);
 cudaError_t launch_musespark1x_routing(const float*, const float*, const uint8_t*, int, int, int, float,
                                        float, int32_t*, float*, cudaStream_t);
 cudaError_t launch_rmsnorm_nvfp4(const void*, const void*, float, const float*, int, int, void*, void*,
@@ -46,6 +46,7 @@ int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int
 size_t dense_workspace_here(int, int, int);
 int launch_selftest_wait(uint64_t, int32_t*, int32_t*, cudaStream_t);
 int launch_selftest_counter(uint64_t, const int32_t*, int32_t*, int32_t*, cudaStream_t);
+int launch_selftest_occupy(int, int, uint64_t, cudaStream_t);
 }  // namespace moe
 
 namespace {
@@ -116,8 +117,10 @@ int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
   off = round_up(off + (size_t)d.P * (I / 2), 1024);
   w->h_sf = off;
   off = round_up(off + (size_t)d.MT * (I / 64) * S * moe::kAtomBytes, 1024);
-  w->done = off;  // per route tile: GEMM1 completions the fused GEMM2 units wait for
-  off = round_up(off + (size_t)(d.MT > 0 ? d.MT : 1) * sizeof(int32_t), 1024);
+  // per route tile: GEMM1 completions the fused GEMM2 units wait for, then
+  // the fused GEMMs' unit ticket
+  w->done = off;
+  off = round_up(off + (size_t)(d.MT + 1) * sizeof(int32_t), 1024);
   w->total = off;
   return MOE_OK;
 }
@@ -173,7 +176,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-int moe_abi_version(void) { return 2; }
+int moe_abi_version(void) { return 3; }
 
 int moe_prepared_sizes(int E, int H, int I, size_t out_bytes[4]) {
   if (!out_bytes) return fail(MOE_ERR_INVALID_ARG, "out_bytes is null");
@@ -274,7 +277,7 @@ int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const f
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   cudaError_t err = moe::launch_quantize_permute(
       x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, r->expanded_to_permuted, r->tile_row_limit,
-      r->totals, T, K, H, tile_m, L.P, L.MT, base + L.a_codes, base + L.a_sf,
+      r->totals, T, K, H, tile_m, L.P, L.MT + 1, base + L.a_codes, base + L.a_sf,
       reinterpret_cast<int32_t*>(base + L.done), as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
 }
@@ -333,8 +336,9 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, in
 }
 
 // Both GEMMs as one persistent grid. pdl as for the split GEMMs;
-// zero_counters: clear the per-tile completion counters first (one memset;
-// the quantizer already leaves them zero inside moe_nvfp4_experts).
+// zero_counters: clear the per-tile completion counters and the unit ticket
+// first (one memset; the quantizer already leaves them zero inside
+// moe_nvfp4_experts).
 static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
                          int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
                          int32_t* status, void* stream, bool pdl, bool zero_counters) {
@@ -350,7 +354,8 @@ static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe
     return fail(MOE_ERR_INVALID_ARG, "gemm2_rows must be non-null and 16-byte aligned");
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   if (zero_counters) {
-    const cudaError_t err = cudaMemsetAsync(base + L.done, 0, (size_t)L.MT * sizeof(int32_t), as_stream(stream));
+    const cudaError_t err =
+        cudaMemsetAsync(base + L.done, 0, (size_t)(L.MT + 1) * sizeof(int32_t), as_stream(stream));
     if (err != cudaSuccess) return cuda_fail(err, "moe_experts_gemms");
   }
   const char* why = "";
@@ -439,29 +444,29 @@ int moe_experts_import(int which, const void* codes, const void* scales, int T, 
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_import");
 }
 
-int moe_post_expert_finalize(const void* rows, const int32_t* expanded_to_permuted,
+int moe_post_expert_finalize(const void* rows, int num_rows, const int32_t* expanded_to_permuted,
                              const float* topk_weights, const void* gamma, float eps,
                              int weight_before_norm, int T, int K, int H, void* out,
-                             void* stream) {
-  if (T < 0 || K < 1 || H < 8 || H % 8 || H > 16384)
-    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d", T, K, H);
+                             int32_t* status, void* stream) {
+  if (T < 0 || K < 1 || H < 8 || H % 8 || H > 16384 || num_rows < 0)
+    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d rows=%d", T, K, H, num_rows);
   if (T == 0) return MOE_OK;
-  if (!rows || !expanded_to_permuted || !topk_weights || !gamma || !out)
+  if ((num_rows > 0 && !rows) || !expanded_to_permuted || !topk_weights || !gamma || !out)
     return fail(MOE_ERR_INVALID_ARG, "finalize pointer is null");
   if (!aligned(rows, 16) || !aligned(gamma, 16) || !aligned(out, 16))
     return fail(MOE_ERR_INVALID_ARG, "rows / gamma / out must be 16-byte aligned");
   if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
-  cudaError_t err = moe::launch_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps,
-                                         weight_before_norm, T, K, H, out, as_stream(stream));
+  cudaError_t err = moe::launch_finalize(rows, num_rows, expanded_to_permuted, topk_weights, gamma, eps,
+                                         weight_before_norm, T, K, H, out, status, as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize");
 }
 
-int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts,
+int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts, int num_rows,
                                 const int32_t* expanded_to_permuted, const float* topk_weights,
                                 const void* gamma, float eps, int weight_before_norm, int T, int K,
-                                int H, void* out, void* stream) {
-  if (T < 0 || K < 1 || H < 8 || H % 8 || H > 16384)
-    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d", T, K, H);
+                                int H, void* out, int32_t* status, void* stream) {
+  if (T < 0 || K < 1 || H < 8 || H % 8 || H > 16384 || num_rows < 0)
+    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d rows=%d", T, K, H, num_rows);
   if (nparts < 1 || nparts > 16) return fail(MOE_ERR_UNSUPPORTED, "nparts %d not in [1, 16]", nparts);
   if (T == 0) return MOE_OK;
   if (!rows_parts || !expanded_to_permuted || !topk_weights || !gamma || !out)
@@ -472,8 +477,9 @@ int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts,
   if (!aligned(gamma, 16) || !aligned(out, 16))
     return fail(MOE_ERR_INVALID_ARG, "gamma / out must be 16-byte aligned");
   if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
-  cudaError_t err = moe::launch_finalize_parts(rows_parts, nparts, expanded_to_permuted, topk_weights, gamma,
-                                               eps, weight_before_norm, T, K, H, out, as_stream(stream));
+  cudaError_t err = moe::launch_finalize_parts(rows_parts, nparts, num_rows, expanded_to_permuted, topk_weights,
+                                               gamma, eps, weight_before_norm, T, K, H, out, status,
+                                               as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize_tp");
 }
 
@@ -574,4 +580,12 @@ extern "C" int moe_selftest_counter_timeout(uint64_t limit_ns, const int32_t* co
     return fail(MOE_ERR_INVALID_ARG, "limit_ns must be within [1 us, 1 s]");
   const int rc = moe::launch_selftest_counter(limit_ns, counter, status, result, as_stream(stream));
   return rc ? fail(rc, "self-test launch failed") : MOE_OK;
+}
+
+extern "C" int moe_selftest_occupy(int ctas, int smem_bytes, uint64_t ns, void* stream) {
+  if (ctas < 1 || ctas > 65535 || smem_bytes < 0 || smem_bytes > 227 * 1024)
+    return fail(MOE_ERR_INVALID_ARG, "occupy: ctas in [1, 65535], smem_bytes in [0, 227 KB]");
+  if (ns > 2000000000ull) return fail(MOE_ERR_INVALID_ARG, "occupy: ns must be at most 2 s");
+  const int rc = moe::launch_selftest_occupy(ctas, smem_bytes, ns, as_stream(stream));
+  return rc ? fail(rc, "occupy launch failed") : MOE_OK;
 }

@@ -26,6 +26,18 @@ struct RowParts {
   int n;
 };
 
+// A route's row index as read from expanded_to_permuted: -1 (not routed) and
+// [0, num_rows) are valid; anything else records MOE_ERR_INVALID_ROUTE and
+// is treated as -1, so that no row outside the buffer is ever read (each
+// thread of the CTA takes the same decision; only thread 0 records it).
+__device__ __forceinline__ int checked_row(int p, int num_rows, int32_t* status) {
+  if (p < -1 || p >= num_rows) {
+    if (threadIdx.x == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
+    return -1;
+  }
+  return p;
+}
+
 __device__ __forceinline__ uint4 load_row_vec(const RowParts& parts, size_t off) {
   if (parts.n == 1) return *reinterpret_cast<const uint4*>(parts.p[0] + off);
   float acc[8];
@@ -54,7 +66,7 @@ template <int VPT, int CH>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const RowParts rows, const int32_t* __restrict__ e2p,
     const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
-    int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out) {
+    int weight_before_norm, int K, int H, int num_rows, __nv_bfloat16* __restrict__ out, int32_t* status) {
   __shared__ float red[kFinWarps][CH];
   pdl_wait();
   pdl_trigger();
@@ -89,7 +101,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     uint4 raw[CH][VPT];
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
-      pr[c] = c < kc ? e2p[(size_t)t * K + k0 + c] : -1;
+      pr[c] = c < kc ? checked_row(e2p[(size_t)t * K + k0 + c], num_rows, status) : -1;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = threadIdx.x + i * kFinThreads;
@@ -191,7 +203,7 @@ template <int VPT>
 __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
     const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ e2p,
     const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
-    int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out) {
+    int weight_before_norm, int K, int H, int num_rows, __nv_bfloat16* __restrict__ out, int32_t* status) {
   extern __shared__ __align__(16) uint8_t staged[];  // K rows of H bf16
   __shared__ __align__(8) uint64_t bar[kFinMaxK];
   __shared__ float red[2][kFinWarps];
@@ -206,7 +218,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
     for (int k = 0; k < K; ++k) mbar_init(smem_u32(&bar[k]), 1);
     fence_barrier_init();
     for (int k = 0; k < K; ++k) {
-      const int p = e2p[(size_t)t * K + k];
+      const int p = checked_row(e2p[(size_t)t * K + k], num_rows, status);
       rowp[k] = p;
       if (p >= 0) {
         mbar_arrive_expect_tx(smem_u32(&bar[k]), row_bytes);
@@ -306,10 +318,10 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
   }
 }
 
-cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const int32_t* e2p,
+cudaError_t launch_finalize_parts(const void* const* parts, int nparts, int num_rows, const int32_t* e2p,
                                   const float* w, const void* gamma, float eps,
                                   int weight_before_norm, int T, int K, int H, void* out,
-                                  cudaStream_t stream) {
+                                  int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   if (nparts < 1 || nparts > kMaxParts) return cudaErrorInvalidValue;
   RowParts rp{};
@@ -328,7 +340,7 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
                             kFinStagedMaxBytes);                                                  \
     if (err == cudaSuccess)                                                                     \
       err = launch_kernel(finalize_staged_kernel<n>, dim3(T), dim3(kFinThreads), staged, stream,  \
-                          true, rows, e2p, w, gp, eps, weight_before_norm, K, H, op);            \
+                          true, rows, e2p, w, gp, eps, weight_before_norm, K, H, num_rows, op, status);            \
     return err;
     switch (vpt) {
       MOE_FIN_STAGED(1)
@@ -345,7 +357,7 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
   case n:                                                                                   \
     err = launch_kernel(finalize_kernel<n, (n <= 2 ? kFinChunk : n <= 4 ? 4 : 2)>, dim3(T),            \
                         dim3(kFinThreads), 0, stream, true, rp, e2p, w, gp, eps,                 \
-                        weight_before_norm, K, H, op);                                           \
+                        weight_before_norm, K, H, num_rows, op, status);                         \
     break;
   switch (vpt) {
     MOE_FIN_CASE(1)
@@ -366,10 +378,11 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, const in
 }  // namespace moe
 
 namespace moe {
-cudaError_t launch_finalize(const void* rows, const int32_t* e2p, const float* w, const void* gamma,
-                            float eps, int weight_before_norm, int T, int K, int H, void* out,
-                            cudaStream_t stream) {
+cudaError_t launch_finalize(const void* rows, int num_rows, const int32_t* e2p, const float* w,
+                            const void* gamma, float eps, int weight_before_norm, int T, int K, int H,
+                            void* out, int32_t* status, cudaStream_t stream) {
   const void* parts[1] = {rows};
-  return launch_finalize_parts(parts, 1, e2p, w, gamma, eps, weight_before_norm, T, K, H, out, stream);
+  return launch_finalize_parts(parts, 1, num_rows, e2p, w, gamma, eps, weight_before_norm, T, K, H, out, status,
+                               stream);
 }
 }  // namespace moe

@@ -83,6 +83,7 @@ struct GemmParams {
   uint8_t* hq_sf;          // GEMM1: intermediate scale atoms [tiles][I/64][S][512]
   __nv_bfloat16* rows;     // GEMM2: [P][H]
   int32_t* done;           // both GEMMs in one grid: per route tile, zeroed by the quantizer
+  int32_t* ticket;         // both GEMMs in one grid: the next unit to hand out, zeroed with done
   int32_t* status;
   int tile_m;
   // Set when the launch follows this library's previous step kernel with
@@ -278,6 +279,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t sfready_bar[kMaxStages];  // a stage's scales are in tensor memory
   __shared__ __align__(8) uint64_t sfdrain_bar;
+  // Both GEMMs in one grid: the units this CTA drew, in order, from the
+  // producer to the MMA issuer and the epilogue warps.
+  constexpr int kUnitQ = 8;
+  __shared__ int unit_q[kUnitQ];
+  __shared__ __align__(8) uint64_t uq_full[kUnitQ];
+  __shared__ __align__(8) uint64_t uq_empty[kUnitQ];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -349,6 +356,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     mbar_init(smem_u32(&drain_bar), 1);
     for (int s = 0; s < ST; ++s) mbar_init(smem_u32(&sfready_bar[s]), 1);
     mbar_init(smem_u32(&sfdrain_bar), 1);
+    for (int q = 0; q < kUnitQ; ++q) {
+      mbar_init(smem_u32(&uq_full[q]), 1);
+      mbar_init(smem_u32(&uq_empty[q]), 1 + EPW);  // the MMA issuer and every epilogue warp
+    }
     abort_flag = 0;
     fence_barrier_init();
     if (MODE != 2) {
@@ -401,7 +412,57 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         held = 0;
         waited = true;
       };
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      if constexpr (MODE == 3) {
+        // Units are drawn from a ticket (below), known only after the previous
+        // kernel has completed: with p.prefetch, first prefetch into L2 the
+        // weights and weight scales of the first stages of unit blockIdx.x
+        // (the first gridDim.x tickets are exactly units [0, gridDim.x), so
+        // whichever CTA draws a unit finds its first stages in L2).
+        if (p.prefetch) {
+          int gi, tau, mt;
+          unit_of(blockIdx.x, gi, tau, mt);
+          const GemmSide& gs = p.g[gi];
+          const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2, tw = gi == 0 ? tw1 : tw2;
+          const int e = __ldcg(p.tile_expert + tau);
+          const int a_row = e * gs.rows_w + mt * kWTile;
+          const uint8_t* wsf = gs.w_sf + ((size_t)e * tw + mt) * KC * kAtomBytes;
+          for (int ks = 0; ks < nks && ks < ST; ++ks) {
+            const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
+            for (int c = 0; 4 * c < kk; ++c)
+              tma_prefetch_l2_2d(gi == 0 ? &tmA1 : &tmA2, (ks * CH + c) * kStageRowBytes, a_row);
+            bulk_prefetch_l2(wsf + (size_t)steps_per_stage * ks * kAtomBytes, (uint32_t)kk * kAtomBytes);
+          }
+          pdl_wait();
+          pdl_trigger();
+        }
+        waited = true;
+      }
+      // MODE 3: the ticket this CTA holds next (drawn one unit ahead, so that
+      // the atomic's latency overlaps the current unit's loads)
+      int next = MODE == 3 ? atomicAdd(p.ticket, 1) : 0;
+      for (int n = 0; !stop; ++n) {
+        int u;
+        if constexpr (MODE == 3) {
+          // A unit is handed out only to a running CTA, in unit order (all
+          // GEMM1 units before any GEMM2 unit): every GEMM1 unit a GEMM2 unit
+          // waits for is already held by a running CTA that reaches it
+          // without waiting on anything, so the waits end whatever else
+          // holds the GPU's SMs.
+          u = next < n_units ? next : -1;
+          const int q = n % kUnitQ;
+          if (n >= kUnitQ &&
+              !mbar_wait(smem_u32(&uq_empty[q]), ((n / kUnitQ) - 1) & 1, &abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
+          unit_q[q] = u;
+          mbar_arrive(smem_u32(&uq_full[q]));
+          if (u < 0) break;
+          next = atomicAdd(p.ticket, 1);
+        } else {
+          u = blockIdx.x + n * gridDim.x;
+          if (u >= n_units) break;
+        }
         int gi, tau, mt;
         unit_of(u, gi, tau, mt);
         const GemmSide& gs = p.g[gi];
@@ -412,7 +473,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         const uint8_t* wsf = gs.w_sf + ((size_t)e * tw + mt) * KC * kAtomBytes;
         if (MODE == 3 && gi == 1) {
           // This route tile's intermediate must be complete: its GEMM1 units
-          // (earlier in every CTA's order) report through p.done.
+          // (drawn earlier, by running CTAs) report through p.done.
           if (!waited) release_held();
           if (!wait_counter_at_least(p.done + tau, done_target, &abort_flag, p.status)) {
             stop = true;
@@ -472,7 +533,18 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       int s = 0, uc = 0;
       uint32_t phase = 0;  // ring position: stage s, its current full phase
       bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++uc) {
+      for (int n = 0; !stop; ++n, ++uc) {
+        int u;
+        if constexpr (MODE == 3) {
+          const int q = n % kUnitQ;
+          if (!mbar_wait(smem_u32(&uq_full[q]), (n / kUnitQ) & 1, &abort_flag, p.status)) break;
+          u = *reinterpret_cast<volatile int*>(&unit_q[q]);
+          mbar_arrive(smem_u32(&uq_empty[q]));
+          if (u < 0) break;
+        } else {
+          u = blockIdx.x + n * gridDim.x;
+          if (u >= n_units) break;
+        }
         const int gi = u < n1 ? 0 : 1;
         const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2;
         const int b = uc % NB, use = uc / NB;
@@ -585,7 +657,21 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
                    (warp - 2) * epi_cols_for(tile_m) * kEpiStride;
     int uc = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+    for (int n = 0;; ++n, ++uc) {
+      int u;
+      if constexpr (MODE == 3) {
+        const int q = n % kUnitQ;
+        u = -2;
+        if (lane == 0 && mbar_wait(smem_u32(&uq_full[q]), (n / kUnitQ) & 1, &abort_flag, p.status)) {
+          u = *reinterpret_cast<volatile int*>(&unit_q[q]);
+          mbar_arrive(smem_u32(&uq_empty[q]));
+        }
+        u = __shfl_sync(0xFFFFFFFFu, u, 0);
+        if (u < 0) break;
+      } else {
+        u = blockIdx.x + n * gridDim.x;
+        if (u >= n_units) break;
+      }
       const int b = uc % NB, use = uc / NB;
       const bool ok = mbar_wait(smem_u32(&accf_bar[b]), use & 1, &abort_flag, p.status);
       __syncwarp();
@@ -892,7 +978,8 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
 }
 
 // Both GEMMs in one persistent grid (GEMM2 units of a route tile start once
-// its GEMM1 units have stored the intermediate; done[] must be zero).
+// its GEMM1 units have stored the intermediate; done[0 .. max_tiles] -- the
+// per-tile counters and the unit ticket after them -- must be zero).
 int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_alphas,
                        const float* g1_scale_c, const float* a2_gscale, const void* p_w2,
                        const void* p_w2_sf, const float* g2_alphas, const int32_t* tile_expert,
@@ -917,6 +1004,7 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
   p.rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
   p.done = done;
+  p.ticket = done + max_tiles;
   p.status = status;
   p.tile_m = tile_m;
   if (launch_mode<3>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {

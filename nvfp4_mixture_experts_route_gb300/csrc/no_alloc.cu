@@ -12,10 +12,11 @@ int report_error(int code, const char* fmt, ...);
 
 namespace {
 
-// Largest workspace the no-allocation entry point can serve. It covers the
-// decode batches (b = 8 needs 11 MB, b = 64 with Zipf routing 24 MB at
-// H = 5120, I = 2048, E = 128, top-8, tile_m = 32). Every GPU that loads the
-// library holds this array until the process exits.
+// Largest workspace the no-allocation entry point can serve. The workspace
+// size depends only on the shape (moe_experts_workspace_size), never on the
+// routing: at H = 5120, I = 2048, E = 128, top-8 and tile_m = 32 a batch of 8
+// tokens needs 11 MB, 64 tokens 24 MB, and up to 287 tokens fit. Every GPU
+// that loads the library holds this array until the process exits.
 constexpr size_t kScratchBytes = size_t(32) << 20;
 // The array is 256-byte aligned; up to 768 bytes are skipped to give the
 // workspace the 1024-byte alignment moe_nvfp4_experts asks for.
@@ -25,11 +26,34 @@ __device__ __align__(256) unsigned char g_scratch[kScratchBytes + kAlignSlack];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+struct Cached {
+  CUcontext ctx;  // the context the address belongs to
+  void* addr;
+};
+Cached g_addr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device, looked up once per
-// device. In host code `g_scratch` names a host-side shadow, not the device
-// array, so it must never be passed to a kernel directly.
+// The calling thread's current context, through the driver entry point the
+// runtime hands out (the library does not link libcuda); null if unknown.
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = []() -> PFN_cuCtxGetCurrent_v4000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  }();
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of g_scratch on the current device, looked up on the first
+// call and again whenever the device's context has changed since (a
+// cudaDeviceReset tears the module down with its context; the array then
+// lives at a new address). In host code `g_scratch` names a host-side
+// shadow, not the device array, so it must never be passed to a kernel
+// directly.
 int scratch_address(void** out) {
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
@@ -37,14 +61,16 @@ int scratch_address(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return moe::report_error(MOE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
+  const CUcontext ctx = current_context();
+  if (g_addr[dev].addr == nullptr || ctx == nullptr || ctx != g_addr[dev].ctx) {
     void* p = nullptr;
     err = cudaGetSymbolAddress(&p, g_scratch);
     if (err != cudaSuccess || p == nullptr)
       return moe::report_error(MOE_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(err));
-    g_addr[dev] = p;
+    // the lookup makes the device's primary context current if it was not
+    g_addr[dev] = Cached{current_context(), p};
   }
-  *out = g_addr[dev];
+  *out = g_addr[dev].addr;
   return MOE_OK;
 }
 

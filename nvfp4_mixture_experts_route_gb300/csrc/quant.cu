@@ -55,11 +55,12 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
     const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
     const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int MT) {
+    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done) {
   pdl_wait();
   pdl_trigger();
-  // the per-tile GEMM1 completion counters of the expert GEMMs that follow
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < MT; i += gridDim.x * blockDim.x) done[i] = 0;
+  // the per-tile GEMM1 completion counters and the unit ticket of the
+  // one-launch expert GEMMs that follow
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_done; i += gridDim.x * blockDim.x) done[i] = 0;
   const int ng = H / 64;  // four-block groups per row
   const int nb = H / 16;
   const float g = (x != nullptr) ? *gscale : 0.f;
@@ -165,9 +166,10 @@ static int grid_for(long long work, int threads) {
 cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_sf,
                                     const float* a1_gscale, const int32_t* e2p,
                                     const int32_t* tile_row_limit, const int32_t* totals, int T,
-                                    int K, int H, int tile_m, int P, int MT, uint8_t* codes,
+                                    int K, int H, int tile_m, int P, int n_done, uint8_t* codes,
                                     uint8_t* scales, int32_t* done, cudaStream_t stream) {
   (void)P;
+  const int MT = n_done - 1;  // route tiles (the counters) and the ticket after them
   // enough warps for one padding item each (one global read then one store
   // per lane), and one warp per token item
   const long long pad_threads = (long long)MT * (H / 64) * 32,
@@ -176,7 +178,7 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
   return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
                        reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, e2p, tile_row_limit, totals,
-                       T, K, H, tile_m, codes, scales, done, MT);
+                       T, K, H, tile_m, codes, scales, done, n_done);
 }
 
 cudaError_t launch_act_scales_io(int to_linear, uint8_t* atoms, uint8_t* linear, int K,

@@ -49,6 +49,26 @@ __global__ void selftest_counter_kernel(uint64_t limit_ns, const int32_t* counte
   }
 }
 
+// Holds SMs for a while, as another stream's kernel would: every CTA keeps
+// `smem` bytes of dynamic shared memory (so that nothing else fits beside
+// it on its SM) and thread 0 spins on the global timer until ns have passed
+// (at most 2 s), then the CTA exits.
+__global__ void selftest_occupy_kernel(uint64_t ns) {
+  extern __shared__ uint8_t held[];
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) __nanosleep(1000);
+    held[0] = 0;
+  }
+}
+
+int launch_selftest_occupy(int ctas, int smem, uint64_t ns, cudaStream_t stream) {
+  if (ensure_smem_limit(reinterpret_cast<const void*>(selftest_occupy_kernel), 227 * 1024) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  selftest_occupy_kernel<<<ctas, 32, smem, stream>>>(ns);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int launch_selftest_counter(uint64_t limit_ns, const int32_t* counter, int32_t* status, int32_t* result,
                             cudaStream_t stream) {
   selftest_counter_kernel<<<1, 64, 0, stream>>>(limit_ns, counter, status, result);

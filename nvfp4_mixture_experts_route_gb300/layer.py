@@ -70,7 +70,7 @@ class NvFp4MoE:
                         T=T, H=self.H, I=self.I, E=self.E, K=K, gemm2_rows=b["rows"], ws=b["ws"], status=st)
         o = b["out"] if out is None else out
         B.post_expert_finalize(b["rows"], b["route"].expanded_to_permuted, topk_weights, self.gamma, self.eps,
-                               self.weight_before_norm, out=o)
+                               self.weight_before_norm, out=o, status=st)
         return o, b
 
     # -- CUDA-graph serving path -------------------------------------------

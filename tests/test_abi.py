@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_sizes(lib):
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
     assert B.prepared_sizes(128, 5120, 2048) == [
         128 * 4096 * 2560, 128 * 4096 * 320, 128 * 5120 * 1024, 128 * 5120 * 128]
     assert B.route_sizes(8, 8, 128, 32) == (2048, 64)
@@ -64,9 +64,11 @@ def test_host_refusals(lib, call, code):
 def test_null_pointers_refused_before_any_launch(lib):
     rc = lib.moe_route_permute(None, 4, 2, 8, 32, None, None, None, None, None, None, None, None, None)
     assert rc == -1 and b"null" in lib.moe_last_error()
-    rc = lib.moe_post_expert_finalize(None, None, None, None, 1e-6, 1, 4, 2, 256, None, None)
+    rc = lib.moe_post_expert_finalize(None, 8, None, None, None, 1e-6, 1, 4, 2, 256, None, None, None)
     assert rc == -1
-    rc = lib.moe_post_expert_finalize(None, None, None, None, 1e-6, 1, 4, 2, 250, None, None)
+    rc = lib.moe_post_expert_finalize(None, 8, None, None, None, 1e-6, 1, 4, 2, 250, None, None, None)
+    assert rc == -1 and b"shape" in lib.moe_last_error()
+    rc = lib.moe_post_expert_finalize(None, -1, None, None, None, 1e-6, 1, 4, 2, 256, None, None, None)
     assert rc == -1 and b"shape" in lib.moe_last_error()
     w = B.MoeWeights()
     r = B.MoeRoute()

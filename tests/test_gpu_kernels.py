@@ -276,6 +276,41 @@ def test_finalize_parity(T, K, H, gamma_sd, scale, wbn):
     assert (np.abs(got - want["out_bf16"]) <= bound).all()
 
 
+@pytest.mark.parametrize("K,H", [(8, 5120), (3, 1024), (4, 16384)])
+def test_finalize_skips_out_of_range_rows(K, H):
+    """Entries of expanded_to_permuted past the rows buffer (num_rows and
+    beyond) or below -1 are never read: the route adds nothing, as a -1 route
+    does (the muse_moe_runner page, _finalize_native: unrouted routes read as
+    zero rows), and the status word holds MOE_ERR_INVALID_ROUTE. The staged
+    (K * H * 2 bytes in shared memory) and the register kernels are both
+    covered."""
+    rng = np.random.default_rng(K * H)
+    T = 6
+    P = T * K
+    rows_bits = inputs._to_bf16_bits(rng.standard_normal((P, H)))
+    gamma = inputs._to_bf16_bits(rng.standard_normal(H) * 0.1)
+    e2p = rng.permutation(P).reshape(T, K).astype(np.int32)
+    bad = e2p.copy()
+    bad[0, 0] = P          # one past the buffer
+    bad[2, K - 1] = 1 << 30
+    bad[4, 0] = -7
+    w = rng.random((T, K)).astype(np.float32)
+    want = olayer.finalize(codecs.bf16_bits_to_f64(rows_bits), np.where((bad >= 0) & (bad < P), bad, -1), w, gamma,
+                           1e-6, True)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = B.post_expert_finalize(bf16_dev(rows_bits), torch.from_numpy(bad).to(DEV), torch.from_numpy(w).to(DEV),
+                                 bf16_dev(gamma), 1e-6, True, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    assert rel_l2(bf16_host_f64(out), want["out"]) < 2e-3
+    # the same rows with the valid map: status stays 0
+    status.zero_()
+    B.post_expert_finalize(bf16_dev(rows_bits), torch.from_numpy(e2p).to(DEV), torch.from_numpy(w).to(DEV),
+                           bf16_dev(gamma), 1e-6, True, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
 def test_finalize_readings_are_distinguished():
     """With gamma ~ N(0, 1) the two norm readings differ by far more than
     the bar, so the parity test above pins which one the kernel computes."""

@@ -1,0 +1,45 @@
+"""The dense NVFP4 tensor-core rate probe (moe_fp4_mma_rate) runs every
+supported variant to completion with a clean status word, and refuses the
+variants that do not fit tensor memory on the host."""
+import pytest
+import torch
+
+from nvfp4_mixture_experts_route_gb300 import binding as B
+
+VARIANTS = [
+    # (n, sf_copies, mmas_per_commit, ctas_per_sm)
+    (128, 0, 4, 1), (128, 0, 4, 2), (128, 1, 4, 2), (128, 0, 16, 2), (128, 2, 4, 2), (128, 3, 4, 2),
+    (256, 0, 4, 1), (256, 1, 4, 1), (256, 0, 16, 1), (256, 2, 4, 1), (256, 3, 4, 1),
+]
+
+
+def test_unfitting_variants_refused_on_host():
+    import ctypes as C
+
+    lib = B.load()
+    f = C.c_double()
+    for n, sf, mpc, ctas, want in ((256, 0, 4, 2, -2), (128, 1, 16, 1, -2), (128, 3, 16, 1, -2), (64, 0, 4, 1, -1),
+                                   (128, 0, 4, 3, -1), (128, 4, 4, 1, -1)):
+        assert lib.moe_fp4_mma_rate(n, sf, mpc, ctas, 8, C.byref(f), None, None) == want
+        assert b"fp4 rate" in lib.moe_last_error()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_rate_probe_runs(variant, record_property):
+    n, sf, mpc, ctas = variant
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.fp4_mma_rate(n, sf, mpc, ctas, 64, status=status)  # warm-up
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    flops = B.fp4_mma_rate(n, sf, mpc, ctas, 2048 // mpc * 4, status=status)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert flops == 2.0 * 128 * n * 64 * mpc * (2048 // mpc * 4) * sms * ctas
+    tflops = flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    record_property("tflops", tflops)
+    # a rate above the part's nominal dense FP4 figure would mean the MMAs
+    # did not run
+    assert 0 < tflops < 20000

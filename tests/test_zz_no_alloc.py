@@ -15,8 +15,6 @@ from nvfp4_mixture_experts_route_gb300 import inputs
 
 from _util import bf16_dev, rel_l2
 
-GEMM2_BAR = 2e-3  # the bar every GEMM2-rows comparison in these tests uses
-
 
 def test_oversized_workspace_refused_before_any_work():
     """A shape whose workspace exceeds the fixed array is refused on the host
@@ -58,8 +56,10 @@ def test_noalloc_matches_allocating_entry_point_on_two_calls():
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     e2p = route.expanded_to_permuted.cpu().numpy().reshape(-1)
-    live = e2p[e2p >= 0]
-    ref = want.float().cpu().numpy()[live]
+    live = torch.from_numpy(e2p[e2p >= 0]).to(dev)
+    # The same deterministic kernels on the same operands, only the workspace
+    # placed elsewhere: the live rows must be equal bit for bit (rel-L2 is
+    # reported only to describe a mismatch).
+    ref = want[live]
     for got in (got1, got2):
-        err = rel_l2(got.float().cpu().numpy()[live], ref)
-        assert err < GEMM2_BAR, err
+        assert torch.equal(got[live], ref), rel_l2(got[live].float().cpu().numpy(), ref.float().cpu().numpy())
