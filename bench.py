@@ -332,8 +332,11 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
                                 status=status)
                 ev[1].record(stream)
             ev[2].record(stream)
+            ev[3].record(stream)
         B.post_expert_finalize(rows, route.expanded_to_permuted, tw, moe.gamma, moe.eps, True, out=out,
                                status=status)
+        if ev is not None:
+            ev[4].record(stream)
 
     # route/permute (1 or 3 kernels), quantize, the expert GEMMs (one fused
     # launch or two), finalize
@@ -376,12 +379,13 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
 
     # The same steps launched one by one, GEMM launches between events on the
     # launching stream: the per-kernel durations of the roofline.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     for i in range(args.steps):
         step(i, evs[i])
     torch.cuda.synchronize()
     gemm1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     gemm2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    finalize_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     fused_ms = None
     if fused:
         # the one-launch GEMMs the timed step runs (the launch's time includes
@@ -480,7 +484,8 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
                           "achieved_gbs": weight_bytes / (step_ms * 1e-3) / 1e9,
                           "frac_of_measured": weight_bytes / (step_ms * 1e-3) / 1e9 / peak,
                           "frac_of_8tbs": weight_bytes / (step_ms * 1e-3) / 8e12,
-                          "gemm1_ms": gemm1_ms, "gemm2_ms": gemm2_ms, "fused_gemms_ms": fused_ms},
+                          "gemm1_ms": gemm1_ms, "gemm2_ms": gemm2_ms, "fused_gemms_ms": fused_ms,
+                          "finalize_ms": finalize_ms},
         "clocks": clocks.summary(),
         "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": in_h.numel(),

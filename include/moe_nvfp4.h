@@ -198,7 +198,8 @@ int moe_experts_workspace_size(int T, int K, int E, int H, int I, int tile_m,
  * gemm2_rows: bf16 [max_padded_rows, H]; only rows < totals[1] that carry a
  * route are written (the flashinfer_ops page trims to gemm2_rows; padding
  * rows are never read by the finalize). Requires H % 128 == 0,
- * I % 128 == 0, tile_m in {32, 64, 128, 256}; every device pointer 16-byte
+ * I % 64 == 0 (every expert-TP slice the prepared layout admits), tile_m in
+ * {32, 64, 128, 256}; every device pointer 16-byte
  * aligned; ws at least moe_experts_workspace_size bytes, 1024-byte
  * aligned. */
 int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a,
@@ -207,6 +208,25 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a,
                       int H, int I, int E, int K, int tile_m,
                       void* gemm2_rows, void* ws, size_t ws_bytes,
                       int32_t* status, void* stream);
+
+/* moe_nvfp4_experts with the first half of the post-expert norm fused into
+ * GEMM2's epilogue: besides the bf16 rows it writes, for every route row,
+ * the sums of squares of its stored values over each 32 columns,
+ *   row_sumsq[p][c] = sum_{j < 32} (g[32c + j] * rows[p][32c + j])^2
+ * with g = 1 + float(gamma) when weight_before_norm != 0 (the weight applied
+ * before the norm) and g = 1 otherwise. row_sumsq: fp32
+ * [max_padded_rows, H/32], 8-byte aligned; only the rows GEMM2 writes get
+ * values. gamma: bf16 [H], 16-byte aligned (may be NULL with
+ * weight_before_norm = 0). moe_post_expert_finalize_sumsq then finalizes
+ * from it without a reduction pass over the rows. Everything else as
+ * moe_nvfp4_experts. */
+int moe_nvfp4_experts_sumsq(const moe_weights* w, const void* x, const void* a,
+                            const void* a_sf, const float* a1_gscale,
+                            const float* a2_gscale, const moe_route* r, int T,
+                            int H, int I, int E, int K, int tile_m,
+                            void* gemm2_rows, const void* gamma,
+                            int weight_before_norm, float* row_sumsq, void* ws,
+                            size_t ws_bytes, int32_t* status, void* stream);
 
 /* The same body in its three launches, for timing one step alone. Called
  * in this order on one stream they equal moe_nvfp4_experts. */
@@ -234,6 +254,20 @@ int moe_experts_gemms(const moe_weights* w, const float* a2_gscale,
                       const moe_route* r, int T, int H, int I, int E, int K,
                       int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
                       int32_t* status, void* stream);
+
+/* moe_experts_gemm2 and moe_experts_gemms with the sums of squares of
+ * moe_nvfp4_experts_sumsq fused into GEMM2's epilogue (arguments as there). */
+int moe_experts_gemm2_sumsq(const moe_weights* w, const moe_route* r, int T,
+                            int H, int I, int E, int K, int tile_m,
+                            void* gemm2_rows, const void* gamma,
+                            int weight_before_norm, float* row_sumsq, void* ws,
+                            size_t ws_bytes, int32_t* status, void* stream);
+int moe_experts_gemms_sumsq(const moe_weights* w, const float* a2_gscale,
+                            const moe_route* r, int T, int H, int I, int E,
+                            int K, int tile_m, void* gemm2_rows,
+                            const void* gamma, int weight_before_norm,
+                            float* row_sumsq, void* ws, size_t ws_bytes,
+                            int32_t* status, void* stream);
 
 /* Copy a quantized operand out of / into the workspace, in permuted row
  * order with row-major scales: which = 0 for the activations a (codes
@@ -311,6 +345,21 @@ int moe_post_expert_finalize(const void* rows, int num_rows,
                              const float* topk_weights, const void* gamma,
                              float eps, int weight_before_norm, int T, int K,
                              int H, void* out, int32_t* status, void* stream);
+
+/* The finalize from moe_nvfp4_experts_sumsq's output: each route's norm
+ * coefficient w[t,k] / sqrt(sum_c row_sumsq[p][c] / H + eps) (the H/32
+ * partials summed in a fixed order) and then
+ *   out[t] = bf16( g * sum_k coef_k * rows[p(t,k)] ),  g = 1 + float(gamma),
+ * equal to moe_post_expert_finalize in the reading row_sumsq was made with,
+ * up to the order of the fp32 sums. rows bf16 [num_rows, H], row_sumsq fp32
+ * [num_rows, H/32]; H % 32 == 0, H <= 16384, K <= 64; the row bound and
+ * status word as for moe_post_expert_finalize. */
+int moe_post_expert_finalize_sumsq(const void* rows, const float* row_sumsq,
+                                   int num_rows,
+                                   const int32_t* expanded_to_permuted,
+                                   const float* topk_weights, const void* gamma,
+                                   float eps, int T, int K, int H, void* out,
+                                   int32_t* status, void* stream);
 
 /* Expert-TP tail (the expert_tp page: with expert tensor parallelism every
  * rank computes K-partial GEMM2 rows over its intermediate slice, and they
@@ -391,20 +440,25 @@ int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void*
  * K = 64, e2m1 operands with ue4m3 scales per 16 elements, fp32 accumulate in
  * tensor memory) on operands held in shared memory: every CTA (ctas_per_sm per
  * SM, on every SM) issues `stages` stages of mmas_per_commit MMAs of N = n,
- * each stage ending in one tcgen05.commit, three stages in flight. With
- * sf_copies = 0 the scale factors are copied into tensor memory once; with
- * 1, 2 or 3 every stage's are copied (tcgen05.cp, one per 128 rows of each
- * operand per K = 64 step, as the expert GEMMs do) by the MMA thread itself
- * (1), by a second warp that hands each stage over through an mbarrier (2),
- * or by two more warps, one per operand (3). Supported: n = 128
- * (ctas_per_sm 1 or 2) or 256 (ctas_per_sm 1); mmas_per_commit 4, or 16 with
- * sf_copies = 0; stages 1 .. 2^24. *flops (host) receives the launch's FLOPs,
+ * each stage ending in one tcgen05.commit, `ring` (3 or 5) stages in flight.
+ * sf_copies selects how the scale factors reach tensor memory: 0 once before
+ * the loop; 1 every stage as the expert GEMMs copy them (tcgen05.cp
+ * 32x128b.warpx4, one per 128 rows of each operand per K = 64 step) by the
+ * MMA thread itself; 2 by a second warp that hands each stage over through an
+ * mbarrier; 3 by two more warps, one per operand; 4 every stage by the MMA
+ * thread with 128x256b copies (two K = 64 steps per copy) for both operands;
+ * 5 the same for A only. Modes 4 and 5 time the copies, not a scale layout:
+ * every scale byte is 1.0 here. Supported: n = 128 (ctas_per_sm 1 or 2) or
+ * 256 (ctas_per_sm 1); mmas_per_commit 4, or 16 with sf_copies = 0; ring 5
+ * only with ctas_per_sm = 1 and sf_copies != 0; stages 1 .. 2^24. *flops
+ * (host) receives the launch's FLOPs,
  * 2 * 128 * n * 64 * mmas_per_commit * stages * CTAs; time the launch with
  * events on `stream`. A wait that gives up records MOE_ERR_TIMEOUT in *status
  * (optional device word). Operands and outputs are scratch inside the kernel.
  * ---------------------------------------------------------------------- */
 int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm,
-                     int stages, double* flops, int32_t* status, void* stream);
+                     int ring, int stages, double* flops, int32_t* status,
+                     void* stream);
 
 /* ------------------------------------------------------------------------
  * Self-test of the failure path: runs the library's bounded mbarrier wait on

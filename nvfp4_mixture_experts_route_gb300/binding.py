@@ -74,6 +74,18 @@ _SIGNATURES = {
          C.c_size_t, _P, _P],
         _I,
     ),
+    "moe_nvfp4_experts_sumsq": (
+        [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _I, _P,
+         _P, C.c_size_t, _P, _P],
+        _I,
+    ),
+    "moe_experts_gemm2_sumsq": (
+        [C.POINTER(MoeWeights), C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, C.c_size_t, _P,
+         _P], _I),
+    "moe_experts_gemms_sumsq": (
+        [C.POINTER(MoeWeights), _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, C.c_size_t,
+         _P, _P], _I),
+    "moe_post_expert_finalize_sumsq": ([_P, _P, _I, _P, _P, _P, C.c_float, _I, _I, _I, _P, _P, _P], _I),
     "moe_experts_quantize": (
         [_P, _P, _P, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P],
         _I,
@@ -104,7 +116,7 @@ _SIGNATURES = {
     "moe_rmsnorm_nvfp4_quant": ([_P, _P, C.c_float, _P, _I, _I, _P, _P, _P], _I),
     "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
-    "moe_fp4_mma_rate": ([_I, _I, _I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
+    "moe_fp4_mma_rate": ([_I, _I, _I, _I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
     "moe_selftest_wait_timeout": ([C.c_uint64, _P, _P, _P], _I),
     "moe_selftest_occupy": ([_I, _I, C.c_uint64, _P], _I),
     "moe_selftest_counter_timeout": ([C.c_uint64, _P, _P, _P, _P], _I),
@@ -289,6 +301,30 @@ def nvfp4_experts(w: MoeWeights, route: Route, *, x=None, a=None, a_sf=None, a1_
     return gemm2_rows, ws
 
 
+def nvfp4_experts_sumsq(w: MoeWeights, route: Route, *, x=None, a=None, a_sf=None, a1_gscale, a2_gscale,
+                        T, H, I, E, K, gamma, weight_before_norm: bool = True, gemm2_rows=None, row_sumsq=None,
+                        ws=None, status=None, stream=None):
+    """The expert body with the post-expert norm's sums of squares fused into
+    GEMM2 (see moe_nvfp4_experts_sumsq); returns (rows, row_sumsq, ws)."""
+    import torch
+
+    tile_m = route.tile_m
+    P, _ = route_sizes(T, K, E, tile_m)
+    dev = route.totals.device
+    if gemm2_rows is None:
+        gemm2_rows = torch.empty((max(P, 1), H), dtype=torch.bfloat16, device=dev)
+    if row_sumsq is None:
+        row_sumsq = torch.empty((max(P, 1), H // 32), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(T, K, E, H, I, tile_m, dev)
+    rs = route.struct()
+    _check(load().moe_nvfp4_experts_sumsq(
+        C.byref(w), _ptr(x), _ptr(a), _ptr(a_sf), _ptr(a1_gscale), _ptr(a2_gscale), C.byref(rs),
+        T, H, I, E, K, tile_m, _ptr(gemm2_rows), _ptr(gamma), 1 if weight_before_norm else 0, _ptr(row_sumsq),
+        _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return gemm2_rows, row_sumsq, ws
+
+
 def experts_quantize(route: Route, ws, *, x=None, a=None, a_sf=None, a1_gscale=None, T, H, I, E, K,
                      status=None, stream=None):
     rs = route.struct()
@@ -314,6 +350,22 @@ def experts_gemms(w: MoeWeights, route: Route, ws, gemm2_rows, *, a2_gscale, T, 
     rs = route.struct()
     _check(load().moe_experts_gemms(C.byref(w), _ptr(a2_gscale), C.byref(rs), T, H, I, E, K, route.tile_m,
                                     _ptr(gemm2_rows), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+
+
+def experts_gemm2_sumsq(w: MoeWeights, route: Route, ws, gemm2_rows, row_sumsq, *, gamma,
+                        weight_before_norm: bool = True, T, H, I, E, K, status=None, stream=None):
+    rs = route.struct()
+    _check(load().moe_experts_gemm2_sumsq(C.byref(w), C.byref(rs), T, H, I, E, K, route.tile_m, _ptr(gemm2_rows),
+                                          _ptr(gamma), 1 if weight_before_norm else 0, _ptr(row_sumsq), _ptr(ws),
+                                          ws.numel(), _ptr(status), _stream(stream)))
+
+
+def experts_gemms_sumsq(w: MoeWeights, route: Route, ws, gemm2_rows, row_sumsq, *, a2_gscale, gamma,
+                        weight_before_norm: bool = True, T, H, I, E, K, status=None, stream=None):
+    rs = route.struct()
+    _check(load().moe_experts_gemms_sumsq(C.byref(w), _ptr(a2_gscale), C.byref(rs), T, H, I, E, K, route.tile_m,
+                                          _ptr(gemm2_rows), _ptr(gamma), 1 if weight_before_norm else 0,
+                                          _ptr(row_sumsq), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
 
 
 def experts_export(which: int, ws, *, T, H, I, E, K, tile_m, stream=None):
@@ -366,6 +418,21 @@ def post_expert_finalize(rows, expanded_to_permuted, topk_weights, gamma, eps: f
     _check(load().moe_post_expert_finalize(
         _ptr(rows), rows.shape[0], _ptr(expanded_to_permuted), _ptr(topk_weights), _ptr(gamma), float(eps),
         1 if weight_before_norm else 0, T, K, H, _ptr(out), _ptr(status), _stream(stream)))
+    return out
+
+
+def post_expert_finalize_sumsq(rows, row_sumsq, expanded_to_permuted, topk_weights, gamma, eps: float, out=None,
+                               status=None, stream=None):
+    """Finalize from GEMM2's fused sums of squares (see the header)."""
+    import torch
+
+    T, K = expanded_to_permuted.shape
+    H = gamma.numel()
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=gamma.device)
+    _check(load().moe_post_expert_finalize_sumsq(
+        _ptr(rows), _ptr(row_sumsq), min(rows.shape[0], row_sumsq.shape[0]), _ptr(expanded_to_permuted),
+        _ptr(topk_weights), _ptr(gamma), float(eps), T, K, H, _ptr(out), _ptr(status), _stream(stream)))
     return out
 
 
@@ -443,11 +510,11 @@ def dense_bf16(x, w, *, out=None, ws=None, status=None, stream=None):
 
 
 def fp4_mma_rate(n: int, sf_copies: int, mmas_per_commit: int, ctas_per_sm: int, stages: int, status=None,
-                 stream=None) -> float:
+                 stream=None, ring: int = 3) -> float:
     """Launch the dense NVFP4 tensor-core rate probe (see the header);
     returns the launch's FLOPs. Time it with events on the same stream."""
     f = C.c_double()
-    _check(load().moe_fp4_mma_rate(n, int(sf_copies), mmas_per_commit, ctas_per_sm, stages, C.byref(f),
+    _check(load().moe_fp4_mma_rate(n, int(sf_copies), mmas_per_commit, ctas_per_sm, ring, stages, C.byref(f),
                                    _ptr(status), _stream(stream)))
     return f.value
 

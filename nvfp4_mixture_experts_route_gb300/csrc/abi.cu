@@ -35,12 +35,14 @@ int launch_gemm1(const void*, const void*, const float*, const float*, const flo
                  uint8_t*, uint8_t*, int, int, int, int, int, int, int32_t*, cudaStream_t, bool,
                  const char**);
 int launch_gemm2(const void*, const void*, const float*, const int32_t*, const int32_t*,
-                 const int32_t*, const uint8_t*, const uint8_t*, void*, int, int, int, int, int,
-                 int, int32_t*, cudaStream_t, bool, const char**);
+                 const int32_t*, const uint8_t*, const uint8_t*, void*, float*, const void*, int, int, int,
+                 int, int, int, int, int32_t*, cudaStream_t, bool, const char**);
 int launch_gemms_fused(const void*, const void*, const float*, const float*, const float*, const void*,
                        const void*, const float*, const int32_t*, const int32_t*, const int32_t*,
-                       const uint8_t*, const uint8_t*, uint8_t*, uint8_t*, void*, int32_t*, int, int, int,
-                       int, int, int, int32_t*, cudaStream_t, bool, const char**);
+                       const uint8_t*, const uint8_t*, uint8_t*, uint8_t*, void*, float*, const void*, int,
+                       int32_t*, int, int, int, int, int, int, int32_t*, cudaStream_t, bool, const char**);
+cudaError_t launch_finalize_sumsq(const void*, const float*, int, const int32_t*, const float*, const void*,
+                                  float, int, int, int, void*, int32_t*, cudaStream_t);
 int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
                       const char**);
 size_t dense_workspace_here(int, int, int);
@@ -103,8 +105,8 @@ int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
   RouteDims d;
   int rc = route_dims(T, K, E, tile_m, &d);
   if (rc) return rc;
-  if (H < 128 || I < 128 || H % 128 || I % 128)
-    return fail(MOE_ERR_UNSUPPORTED, "hidden %d and intermediate %d must be multiples of 128", H, I);
+  if (H < 128 || I < 64 || H % 128 || I % 64)
+    return fail(MOE_ERR_UNSUPPORTED, "hidden %d and intermediate %d must be multiples of 128 and 64", H, I);
   w->P = d.P;
   w->MT = d.MT;
   const size_t S = (size_t)moe::sf_atoms_per_tile(tile_m);
@@ -310,9 +312,17 @@ int moe_experts_gemm1(const moe_weights* w, const float* a2_gscale, const moe_ro
   return experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream, false);
 }
 
+// The post-expert norm's sums of squares, fused into GEMM2's epilogue when
+// row_ss is set (gamma and the norm reading then given too).
+struct SumSq {
+  float* row_ss = nullptr;
+  const void* gamma = nullptr;
+  int wbn = 0;
+};
+
 static int experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E,
                          int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
-                         int32_t* status, void* stream, bool pdl) {
+                         int32_t* status, void* stream, bool pdl, SumSq ss = SumSq()) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -324,8 +334,8 @@ static int experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H,
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   const char* why = "";
   rc = moe::launch_gemm2(w->w2, w->w2_sf, w->g2_alphas, r->tile_expert, r->tile_row_limit,
-                         r->totals, base + L.h_codes, base + L.h_sf, gemm2_rows, E, H, I, tile_m,
-                         L.P, L.MT, status, as_stream(stream), pdl, &why);
+                         r->totals, base + L.h_codes, base + L.h_sf, gemm2_rows, ss.row_ss, ss.gamma, ss.wbn, E,
+                         H, I, tile_m, L.P, L.MT, status, as_stream(stream), pdl, &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
 }
 
@@ -341,7 +351,7 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, in
 // moe_nvfp4_experts).
 static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
                          int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
-                         int32_t* status, void* stream, bool pdl, bool zero_counters) {
+                         int32_t* status, void* stream, bool pdl, bool zero_counters, SumSq ss = SumSq()) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -362,8 +372,8 @@ static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe
   rc = moe::launch_gemms_fused(w->w13, w->w13_sf, w->g1_alphas, w->g1_scale_c, a2_gscale, w->w2, w->w2_sf,
                                w->g2_alphas, r->tile_expert, r->tile_row_limit, r->totals,
                                base + L.a_codes, base + L.a_sf, base + L.h_codes, base + L.h_sf, gemm2_rows,
-                               reinterpret_cast<int32_t*>(base + L.done), E, H, I, tile_m, L.P, L.MT, status,
-                               as_stream(stream), pdl, &why);
+                               ss.row_ss, ss.gamma, ss.wbn, reinterpret_cast<int32_t*>(base + L.done), E, H, I,
+                               tile_m, L.P, L.MT, status, as_stream(stream), pdl, &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
 }
 
@@ -374,10 +384,10 @@ int moe_experts_gemms(const moe_weights* w, const float* a2_gscale, const moe_ro
                        false, true);
 }
 
-int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const void* a_sf,
-                      const float* a1_gscale, const float* a2_gscale, const moe_route* r, int T,
-                      int H, int I, int E, int K, int tile_m, void* gemm2_rows, void* ws,
-                      size_t ws_bytes, int32_t* status, void* stream) {
+static int experts_body(const moe_weights* w, const void* x, const void* a, const void* a_sf,
+                        const float* a1_gscale, const float* a2_gscale, const moe_route* r, int T, int H,
+                        int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
+                        int32_t* status, void* stream, SumSq ss) {
   int rc = check_weights(w, true);
   if (rc || (rc = check_weights(w, false))) return rc;
   rc = moe_experts_quantize(x, a, a_sf, a1_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status,
@@ -394,10 +404,61 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const 
   if (moe_experts_kernels(tile_m) == 3) {
     rc = experts_gemm1(w, a2_gscale, r, T, H, I, E, K, tile_m, ws, ws_bytes, status, stream, true);
     if (rc) return rc;
-    return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true);
+    return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true, ss);
   }
   return experts_fused(w, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream,
-                       true, false);
+                       true, false, ss);
+}
+
+// The sums-of-squares arguments of the *_sumsq entry points, checked.
+static int sumsq_args(const void* gamma, int weight_before_norm, float* row_sumsq, SumSq* ss) {
+  if (!row_sumsq || !aligned(row_sumsq, 8)) return fail(MOE_ERR_INVALID_ARG, "row_sumsq must be 8-byte aligned");
+  if (weight_before_norm && (!gamma || !aligned(gamma, 16)))
+    return fail(MOE_ERR_INVALID_ARG, "gamma must be given, 16-byte aligned, with weight_before_norm");
+  ss->row_ss = row_sumsq;
+  ss->gamma = gamma;
+  ss->wbn = weight_before_norm ? 1 : 0;
+  return MOE_OK;
+}
+
+int moe_experts_gemm2_sumsq(const moe_weights* w, const moe_route* r, int T, int H, int I, int E, int K,
+                            int tile_m, void* gemm2_rows, const void* gamma, int weight_before_norm,
+                            float* row_sumsq, void* ws, size_t ws_bytes, int32_t* status, void* stream) {
+  SumSq ss;
+  const int rc = sumsq_args(gamma, weight_before_norm, row_sumsq, &ss);
+  if (rc) return rc;
+  return experts_gemm2(w, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, false, ss);
+}
+
+int moe_experts_gemms_sumsq(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
+                            int I, int E, int K, int tile_m, void* gemm2_rows, const void* gamma,
+                            int weight_before_norm, float* row_sumsq, void* ws, size_t ws_bytes,
+                            int32_t* status, void* stream) {
+  SumSq ss;
+  const int rc = sumsq_args(gamma, weight_before_norm, row_sumsq, &ss);
+  if (rc) return rc;
+  return experts_fused(w, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, false,
+                       true, ss);
+}
+
+int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const void* a_sf,
+                      const float* a1_gscale, const float* a2_gscale, const moe_route* r, int T,
+                      int H, int I, int E, int K, int tile_m, void* gemm2_rows, void* ws,
+                      size_t ws_bytes, int32_t* status, void* stream) {
+  return experts_body(w, x, a, a_sf, a1_gscale, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes,
+                      status, stream, SumSq());
+}
+
+int moe_nvfp4_experts_sumsq(const moe_weights* w, const void* x, const void* a, const void* a_sf,
+                            const float* a1_gscale, const float* a2_gscale, const moe_route* r, int T, int H,
+                            int I, int E, int K, int tile_m, void* gemm2_rows, const void* gamma,
+                            int weight_before_norm, float* row_sumsq, void* ws, size_t ws_bytes,
+                            int32_t* status, void* stream) {
+  SumSq ss;
+  const int rc = sumsq_args(gamma, weight_before_norm, row_sumsq, &ss);
+  if (rc) return rc;
+  return experts_body(w, x, a, a_sf, a1_gscale, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes,
+                      status, stream, ss);
 }
 
 int moe_experts_export(int which, const void* ws, size_t ws_bytes, int T, int H, int I, int E,
@@ -459,6 +520,23 @@ int moe_post_expert_finalize(const void* rows, int num_rows, const int32_t* expa
   cudaError_t err = moe::launch_finalize(rows, num_rows, expanded_to_permuted, topk_weights, gamma, eps,
                                          weight_before_norm, T, K, H, out, status, as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize");
+}
+
+int moe_post_expert_finalize_sumsq(const void* rows, const float* row_sumsq, int num_rows,
+                                   const int32_t* expanded_to_permuted, const float* topk_weights,
+                                   const void* gamma, float eps, int T, int K, int H, void* out,
+                                   int32_t* status, void* stream) {
+  if (T < 0 || K < 1 || K > 64 || H < 32 || H % 32 || H > 16384 || num_rows < 0)
+    return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d rows=%d", T, K, H, num_rows);
+  if (T == 0) return MOE_OK;
+  if ((num_rows > 0 && (!rows || !row_sumsq)) || !expanded_to_permuted || !topk_weights || !gamma || !out)
+    return fail(MOE_ERR_INVALID_ARG, "finalize pointer is null");
+  if (!aligned(rows, 16) || !aligned(gamma, 16) || !aligned(out, 16) || !aligned(row_sumsq, 4))
+    return fail(MOE_ERR_INVALID_ARG, "rows / gamma / out must be 16-byte aligned");
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  cudaError_t err = moe::launch_finalize_sumsq(rows, row_sumsq, num_rows, expanded_to_permuted, topk_weights,
+                                               gamma, eps, T, K, H, out, status, as_stream(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_post_expert_finalize_sumsq");
 }
 
 int moe_post_expert_finalize_tp(const void* const* rows_parts, int nparts, int num_rows,

@@ -386,3 +386,95 @@ cudaError_t launch_finalize(const void* rows, int num_rows, const int32_t* e2p, 
                                stream);
 }
 }  // namespace moe
+
+namespace moe {
+
+// The finalize when GEMM2's epilogue already produced each route row's sums
+// of squares (row_ss [num_rows][H / 32], fp32 partials over 32 columns, gain
+// weighted for the weight-before-norm reading): every route's coefficient
+// w[t, k] / sqrt(mean + eps) is known before any row is read, so the rows
+// stream through once with no reduction between a row's load and its use.
+// One CTA per token: warp k first sums route k's H / 32 partials (a fixed
+// order: lane-strided sums, then a butterfly), then every thread takes
+// 8-element vectors of the hidden dimension, issues the loads of all of its
+// routes' vectors at once (up to eight in flight), and accumulates
+// coef_k * r_k in fp32; out = bf16(g * sum), g = 1 + gamma, in both readings.
+constexpr int kFinSsThreads = 256;
+
+__global__ void __launch_bounds__(kFinSsThreads) finalize_sumsq_kernel(
+    const __nv_bfloat16* __restrict__ rows, const float* __restrict__ row_ss, int num_rows,
+    const int32_t* __restrict__ e2p, const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma,
+    float eps, int K, int H, __nv_bfloat16* __restrict__ out, int32_t* status) {
+  __shared__ float coef[kFinMaxK];
+  __shared__ int32_t rowp[kFinMaxK];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = H / 32;
+  for (int k = warp; k < K; k += kFinSsThreads / 32) {
+    int p = e2p[(size_t)t * K + k];
+    if (p < -1 || p >= num_rows) {
+      if (lane == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
+      p = -1;
+    }
+    float ss = 0.f;
+    if (p >= 0)
+      for (int g = lane; g < G; g += 32) ss += row_ss[(size_t)p * G + g];
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, d);
+    if (lane == 0) {
+      rowp[k] = p;
+      coef[k] = p >= 0 ? topk_w[(size_t)t * K + k] / sqrtf(ss / (float)H + eps) : 0.f;
+    }
+  }
+  __syncthreads();
+  const int nvec = H / 8;
+  for (int v = threadIdx.x; v < nvec; v += kFinSsThreads) {
+    float2 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      uint4 raw[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = k0 + c;
+        const int p = k < K ? rowp[k] : -1;
+        raw[c] = p >= 0 ? __ldcs(reinterpret_cast<const uint4*>(rows + (size_t)p * H) + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = k0 + c;
+        if (k >= K) break;
+        const float2 ck = make_float2(coef[k], coef[k]);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[c]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = ffma2(__bfloat1622float2(h[q]), ck, acc[q]);
+      }
+    }
+    const uint4 gu = *reinterpret_cast<const uint4*>(gamma + 8 * v);
+    const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gu);
+    uint4 o;
+    __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 gf = __bfloat1622float2(gh[q]);
+      const float2 r = fmul2(acc[q], make_float2(1.f + gf.x, 1.f + gf.y));  // gain centre added in fp32
+      oh[q] = __floats2bfloat162_rn(r.x, r.y);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * v) = o;
+  }
+}
+
+cudaError_t launch_finalize_sumsq(const void* rows, const float* row_ss, int num_rows, const int32_t* e2p,
+                                  const float* w, const void* gamma, float eps, int T, int K, int H, void* out,
+                                  int32_t* status, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  if (K > kFinMaxK) return cudaErrorInvalidValue;
+  return launch_kernel(finalize_sumsq_kernel, dim3(T), dim3(kFinSsThreads), 0, stream, true,
+                       reinterpret_cast<const __nv_bfloat16*>(rows), row_ss, num_rows, e2p, w,
+                       reinterpret_cast<const __nv_bfloat16*>(gamma), eps, K, H,
+                       reinterpret_cast<__nv_bfloat16*>(out), status);
+}
+
+}  // namespace moe

@@ -94,7 +94,47 @@ struct GemmParams {
   // GEMM2: rows and their pitch are 32-byte aligned, so the epilogue stores
   // whole 32-byte sectors (st.global.v8)
   int rows32;
+  // GEMM2, optional: the post-expert norm's sums of squares of the stored
+  // bf16 rows, one fp32 partial per 32 columns (row_ss[P][H / 32]); weighted
+  // by the norm's gain g = 1 + gamma when ss_wbn is set (the weight applied
+  // before the norm), else plain.
+  float* row_ss;
+  const __nv_bfloat16* ss_gamma;
+  int ss_wbn;
 };
+
+// Sum over a warp's 32 lanes of each of 32 values: afterwards lane l holds
+// the total of x[l] (a butterfly that halves the array at every level; 31
+// shuffles, a fixed order of additions).
+__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    const bool upper = (lane & d) != 0;
+#pragma unroll
+    for (int i = 0; i < d; ++i) {
+      const float send = upper ? x[i] : x[i + d];
+      const float keep = upper ? x[i + d] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, d);
+    }
+  }
+  return x[0];
+}
+
+// The norm's gain for 32 consecutive columns (uniform across the warp).
+__device__ __forceinline__ void gain32(const __nv_bfloat16* gamma, int col0, float (&g)[32]) {
+  const uint4* src = reinterpret_cast<const uint4*>(gamma + col0);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 u = __ldg(src + j);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      g[8 * j + 2 * q] = 1.f + f.x;
+      g[8 * j + 2 * q + 1] = 1.f + f.y;
+    }
+  }
+}
 
 // Launch shape per route-tile size: CTAs per SM, accumulator buffers, K=256
 // chunks per pipeline stage, epilogue warps and GEMM1 epilogue staging
@@ -731,6 +771,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         } else {
           const float g2 = gs.s0[e];
           if (r < p.tile_row_limit[tau]) {
+            float ss2[2] = {0.f, 0.f};  // this row's sums of squares of the two 32-column groups
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const int cc = 2 * half + k;
@@ -740,6 +781,20 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(acc[k][2 * i]) * g2,
                                                                 __uint_as_float(acc[k][2 * i + 1]) * g2);
                 w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              if (p.row_ss != nullptr) {
+                // of the stored (bf16) values, gain-weighted for the
+                // weight-before-norm reading
+                float gn[32];
+                if (p.ss_wbn) gain32(p.ss_gamma, mt * kWTile + 32 * cc, gn);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+                  const float a = p.ss_wbn ? f.x * gn[2 * i] : f.x;
+                  const float c = p.ss_wbn ? f.y * gn[2 * i + 1] : f.y;
+                  ss2[k] = fmaf(a, a, ss2[k]);
+                  ss2[k] = fmaf(c, c, ss2[k]);
+                }
               }
               __nv_bfloat16* dp = p.rows + (size_t)r * gs.out_cols + mt * kWTile + 32 * cc;
               if (p.rows32) {
@@ -756,6 +811,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
                   dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
               }
             }
+            if (p.row_ss != nullptr)
+              *reinterpret_cast<float2*>(p.row_ss + (size_t)r * (gs.out_cols / 32) + 4 * mt + 2 * half) =
+                  make_float2(ss2[0], ss2[1]);
           }
         }
       } else {
@@ -776,13 +834,25 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           const float g2 = gs.s0[e];
           const int limit = p.tile_row_limit[tau];
           const int colx = mt * kWTile + 32 * q + lane;
+          // this lane's column's gain (weight-before-norm sums of squares)
+          const float gn = p.row_ss != nullptr && p.ss_wbn ? 1.f + __bfloat162float(p.ss_gamma[colx]) : 1.f;
           for (int c0 = half * 32; c0 < tile_m; c0 += kSplit * 32) {
             float v[32];
             tmem_ld32(taddr + c0, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int rr = row0 + c0 + i;
-              if (rr < limit) p.rows[(size_t)rr * gs.out_cols + colx] = __float2bfloat16_rn(v[i] * g2);
+              const __nv_bfloat16 hv = __float2bfloat16_rn(v[i] * g2);
+              if (rr < limit) p.rows[(size_t)rr * gs.out_cols + colx] = hv;
+              const float y = __bfloat162float(hv) * gn;
+              v[i] = y * y;
+            }
+            if (p.row_ss != nullptr) {
+              // lane i: route row row0 + c0 + i, its 32 columns of this
+              // quadrant summed over the warp's lanes
+              const float tot = transpose_reduce32(v, lane);
+              const int rr = row0 + c0 + lane;
+              if (rr < limit) p.row_ss[(size_t)rr * (gs.out_cols / 32) + 4 * mt + q] = tot;
             }
           }
         }
@@ -952,9 +1022,9 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
 
 int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
                  const int32_t* tile_expert, const int32_t* tile_row_limit, const int32_t* totals,
-                 const uint8_t* h_codes, const uint8_t* h_sf, void* rows, int E, int H, int I,
-                 int tile_m, int P, int max_tiles, int32_t* status, cudaStream_t stream, bool pdl,
-                 const char** why) {
+                 const uint8_t* h_codes, const uint8_t* h_sf, void* rows, float* row_ss,
+                 const void* ss_gamma, int ss_wbn, int E, int H, int I, int tile_m, int P, int max_tiles,
+                 int32_t* status, cudaStream_t stream, bool pdl, const char** why) {
   CUtensorMap maps[4];
   GemmParams p{};
   if (!gemm2_side(p, &maps[2], &maps[3], p_w2, p_w2_sf, g2_alphas, h_codes, h_sf, E, H, I, tile_m, P)) {
@@ -968,6 +1038,9 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
   p.totals = totals;
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
   p.rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
+  p.row_ss = row_ss;
+  p.ss_gamma = reinterpret_cast<const __nv_bfloat16*>(ss_gamma);
+  p.ss_wbn = ss_wbn;
   p.status = status;
   p.tile_m = tile_m;
   if (launch_mode<2>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {
@@ -984,9 +1057,9 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
                        const float* g1_scale_c, const float* a2_gscale, const void* p_w2,
                        const void* p_w2_sf, const float* g2_alphas, const int32_t* tile_expert,
                        const int32_t* tile_row_limit, const int32_t* totals, const uint8_t* a_codes,
-                       const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, void* rows, int32_t* done,
-                       int E, int H, int I, int tile_m, int P, int max_tiles, int32_t* status,
-                       cudaStream_t stream, bool pdl, const char** why) {
+                       const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, void* rows, float* row_ss,
+                       const void* ss_gamma, int ss_wbn, int32_t* done, int E, int H, int I, int tile_m, int P,
+                       int max_tiles, int32_t* status, cudaStream_t stream, bool pdl, const char** why) {
   CUtensorMap maps[4];
   GemmParams p{};
   if (!gemm1_side(p, &maps[0], &maps[1], p_w13, p_w13_sf, g1_alphas, g1_scale_c, a_codes, a_sf, E, H, I,
@@ -1003,6 +1076,9 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
   p.hq_sf = h_sf;
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
   p.rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
+  p.row_ss = row_ss;
+  p.ss_gamma = reinterpret_cast<const __nv_bfloat16*>(ss_gamma);
+  p.ss_wbn = ss_wbn;
   p.done = done;
   p.ticket = done + max_tiles;
   p.status = status;

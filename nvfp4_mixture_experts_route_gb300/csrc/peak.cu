@@ -20,18 +20,23 @@
 
 namespace moe {
 
-constexpr int kRateRing = 3;  // stages in flight (as the prefill GEMMs' ring)
-
 // Tensor-memory columns: the accumulator (N) plus scale columns -- per stage
 // of MPC MMAs, 4 columns for A's atom and 4 per 128 rows of B -- for every
 // ring stage when copied per stage, or for one K = 256 stage loaded once.
-__host__ __device__ constexpr int rate_sf_cols(int n, int sfcp, int mpc) {
-  return (sfcp ? kRateRing * mpc : 4) * 4 * (1 + n / 128);
+__host__ __device__ constexpr int rate_sf_cols(int n, int sfcp, int mpc, int ring) {
+  return (sfcp ? ring * mpc : 4) * 4 * (1 + n / 128);
 }
-__host__ __device__ constexpr uint32_t rate_tmem_cols(int n, int sfcp, int mpc) {
+__host__ __device__ constexpr uint32_t rate_tmem_cols(int n, int sfcp, int mpc, int ring) {
   uint32_t c = 32;
-  while ((int)c < n + rate_sf_cols(n, sfcp, mpc)) c <<= 1;
+  while ((int)c < n + rate_sf_cols(n, sfcp, mpc, ring)) c <<= 1;
   return c;
+}
+
+// One tcgen05.cp of a 128-row x 32-byte shared-memory matrix into 128 lanes
+// x 8 columns (no replication): the cost of a wider copy, timed against the
+// 512-byte 32x128b.warpx4 atoms.
+__device__ __forceinline__ void tc_copy_128x256b(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 // Shared memory: one 128-byte-swizzled K = 256 chunk of A (128 rows) and of
 // B (N rows), and four K = 64 steps of scale atoms for each.
@@ -42,22 +47,25 @@ __host__ __device__ constexpr uint32_t rate_smem_bytes(int n) {
 // SFCP: 0 scales copied once; 1 copied every stage by the MMA thread; 2 by
 // a second warp's lane 0, which commits each stage's copies to a barrier the
 // MMA thread waits on (the expert GEMM1's scale-copy warp); 3 by two more
-// warps, one for A's atoms and one for B's.
+// warps, one for A's atoms and one for B's; 4 every stage by the MMA thread
+// with 128x256b copies (two K = 64 steps each) for both operands; 5 the same
+// for A only. Modes 4 and 5 time the copies only: the scale values are all
+// the same, so the columns' layout does not matter to the MMAs here.
 __host__ __device__ constexpr int rate_threads(int sfcp) { return sfcp == 2 ? 64 : sfcp == 3 ? 96 : 32; }
 
-template <int N, int SFCP, int MPC>
+template <int N, int SFCP, int MPC, int RING>
 __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int stages, int32_t* status) {
   extern __shared__ uint8_t dsmem[];
-  __shared__ __align__(8) uint64_t bar[kRateRing];
-  __shared__ __align__(8) uint64_t sfa_ready[kRateRing];
-  __shared__ __align__(8) uint64_t sfb_ready[kRateRing];
+  __shared__ __align__(8) uint64_t bar[RING];
+  __shared__ __align__(8) uint64_t sfa_ready[RING];
+  __shared__ __align__(8) uint64_t sfb_ready[RING];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t cp_drain[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   constexpr int S = N / 128;  // scale atoms of B per K = 64 step
   constexpr int SL = SFCP ? MPC : 4;  // K = 64 steps whose scales a column slot holds
-  constexpr uint32_t ncols = rate_tmem_cols(N, SFCP, MPC);
+  constexpr uint32_t ncols = rate_tmem_cols(N, SFCP, MPC, RING);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t sA = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sB = sA + 128 * 128;
@@ -75,7 +83,7 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
       *reinterpret_cast<uint32_t*>(base + i) = 0x38383838u;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (lane == 0) {
-      for (int r = 0; r < kRateRing; ++r) {
+      for (int r = 0; r < RING; ++r) {
         mbar_init(smem_u32(&bar[r]), 1);
         mbar_init(smem_u32(&sfa_ready[r]), 1);
         mbar_init(smem_u32(&sfb_ready[r]), 1);
@@ -113,6 +121,19 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
         tc_copy_scale_atom(sfb_col(r, j) + 4 * sub, sfb_desc + (uint64_t)(((j & 3) * S + sub) * (kAtomBytes >> 4)));
     };
     auto copy_scales = [&](int r, int j) {
+      if (SFCP >= 4) {
+        // 128 rows x 32 bytes from the scale region (4 KB inside the
+        // operand buffer) into the 8 columns of steps j and j + 1
+        if ((j & 1) == 0) {
+          tc_copy_128x256b(sfa_col(r, j), smem_desc(sSFA, 128, 256, 0));
+          if (SFCP == 4) {
+#pragma unroll
+            for (int sub = 0; sub < S; ++sub) tc_copy_128x256b(sfb_col(r, j) + 8 * sub, smem_desc(sSFA, 128, 256, 0));
+          }
+        }
+        if (SFCP == 5) copy_b(r, j);
+        return;
+      }
       copy_a(r, j);
       copy_b(r, j);
     };
@@ -121,8 +142,8 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
       // s - ring (same slot) have completed
       bool do_a = SFCP == 2 || warp == 1, do_b = SFCP == 2 || warp == 2;
       for (int s = 0; s < stages; ++s) {
-        const int r = s % kRateRing;
-        if (s >= kRateRing && !mbar_wait(smem_u32(&bar[r]), ((s / kRateRing) - 1) & 1, &abort_flag, status))
+        const int r = s % RING;
+        if (s >= RING && !mbar_wait(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status))
           break;
         tc_fence_after();
 #pragma unroll
@@ -140,14 +161,14 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
       for (int j = 0; j < 4; ++j) copy_scales(0, j);  // once; ordered before the MMAs that read them
     }
     for (int s = 0; s < stages; ++s) {
-      const int r = s % kRateRing;
-      if (SFCP <= 1 && s >= kRateRing &&
-          !mbar_wait(smem_u32(&bar[r]), ((s / kRateRing) - 1) & 1, &abort_flag, status))
+      const int r = s % RING;
+      const bool copy_warps = SFCP == 2 || SFCP == 3;
+      if (!copy_warps && s >= RING && !mbar_wait(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status))
         break;
-      if (SFCP >= 2 && !mbar_wait(smem_u32(&sfa_ready[r]), (s / kRateRing) & 1, &abort_flag, status)) break;
-      if (SFCP == 3 && !mbar_wait(smem_u32(&sfb_ready[r]), (s / kRateRing) & 1, &abort_flag, status)) break;
+      if (copy_warps && !mbar_wait(smem_u32(&sfa_ready[r]), (s / RING) & 1, &abort_flag, status)) break;
+      if (SFCP == 3 && !mbar_wait(smem_u32(&sfb_ready[r]), (s / RING) & 1, &abort_flag, status)) break;
       tc_fence_after();
-      if (SFCP == 1) {
+      if (SFCP == 1 || SFCP >= 4) {
 #pragma unroll
         for (int j = 0; j < MPC; ++j) copy_scales(r, j);
       }
@@ -170,9 +191,9 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
-template <int N, int SFCP, int MPC>
+template <int N, int SFCP, int MPC, int RING = 3>
 static cudaError_t launch_rate(int grid, int smem, int stages, int32_t* status, cudaStream_t stream) {
-  auto kern = fp4_mma_rate_kernel<N, SFCP, MPC>;
+  auto kern = fp4_mma_rate_kernel<N, SFCP, MPC, RING>;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, rate_threads(SFCP), smem, stream>>>(stages, status);
@@ -180,13 +201,15 @@ static cudaError_t launch_rate(int grid, int smem, int stages, int32_t* status, 
 }
 
 // Host check of a variant: MOE_OK, or an error code with the reason.
-int fp4_mma_rate_check(int n, int sf_copies, int mpc, int ctas_per_sm, int stages, const char** why) {
-  if (!((n == 128 || n == 256) && sf_copies >= 0 && sf_copies <= 3 && (mpc == 4 || mpc == 16) &&
-        (ctas_per_sm == 1 || ctas_per_sm == 2) && stages >= 1 && stages <= (1 << 24))) {
-    *why = "fp4 rate: n in {128, 256}, sf_copies in 0..3, mmas_per_commit in {4, 16}, ctas_per_sm in {1, 2}";
+int fp4_mma_rate_check(int n, int sf_copies, int mpc, int ctas_per_sm, int ring, int stages, const char** why) {
+  if (!((n == 128 || n == 256) && sf_copies >= 0 && sf_copies <= 5 && (mpc == 4 || mpc == 16) &&
+        (ctas_per_sm == 1 || ctas_per_sm == 2) && (ring == 3 || ring == 5) && stages >= 1 &&
+        stages <= (1 << 24))) {
+    *why = "fp4 rate: n in {128, 256}, sf_copies in 0..5, mmas_per_commit in {4, 16}, ctas_per_sm in {1, 2}, "
+           "ring in {3, 5}";
     return MOE_ERR_INVALID_ARG;
   }
-  if ((n == 256 && ctas_per_sm == 2) || (sf_copies && mpc == 16)) {
+  if ((n == 256 && ctas_per_sm == 2) || (sf_copies && mpc == 16) || (ring == 5 && (ctas_per_sm == 2 || !sf_copies))) {
     *why = "fp4 rate: that variant does not fit tensor memory";
     return MOE_ERR_UNSUPPORTED;
   }
@@ -198,9 +221,9 @@ int fp4_mma_rate_check(int n, int sf_copies, int mpc, int ctas_per_sm, int stage
 // mpc: MMAs per commit (4: a K = 256 stage; 16: a K = 1024 stage, only
 // without per-stage copies); ctas_per_sm: 1 or 2 (2 only for n = 128, whose
 // tensor memory then fits two CTAs).
-int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int stages, int sms,
+int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring, int stages, int sms,
                         int32_t* status, cudaStream_t stream, double* flops, const char** why) {
-  const int rc = fp4_mma_rate_check(n, sf_copies, mpc, ctas_per_sm, stages, why);
+  const int rc = fp4_mma_rate_check(n, sf_copies, mpc, ctas_per_sm, ring, stages, why);
   if (rc) return rc;
   // Shared memory requested per CTA so that exactly ctas_per_sm fit an SM:
   // their tensor memory (at most 512 / ctas_per_sm columns each) then never
@@ -209,17 +232,36 @@ int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int stag
   const int grid = sms * ctas_per_sm;
   *flops = 2.0 * 128.0 * n * 64.0 * (double)mpc * (double)stages * (double)grid;
   cudaError_t err;
-  switch ((n == 256 ? 100 : 0) + 10 * sf_copies + (mpc == 16 ? 1 : 0)) {
-    case 0: err = launch_rate<128, 0, 4>(grid, smem, stages, status, stream); break;
-    case 1: err = launch_rate<128, 0, 16>(grid, smem, stages, status, stream); break;
-    case 10: err = launch_rate<128, 1, 4>(grid, smem, stages, status, stream); break;
-    case 20: err = launch_rate<128, 2, 4>(grid, smem, stages, status, stream); break;
-    case 30: err = launch_rate<128, 3, 4>(grid, smem, stages, status, stream); break;
-    case 100: err = launch_rate<256, 0, 4>(grid, smem, stages, status, stream); break;
-    case 101: err = launch_rate<256, 0, 16>(grid, smem, stages, status, stream); break;
-    case 110: err = launch_rate<256, 1, 4>(grid, smem, stages, status, stream); break;
-    case 120: err = launch_rate<256, 2, 4>(grid, smem, stages, status, stream); break;
-    default: err = launch_rate<256, 3, 4>(grid, smem, stages, status, stream); break;
+  const int key = (n == 256 ? 1000 : 0) + (ring == 5 ? 100 : 0) + 10 * sf_copies + (mpc == 16 ? 1 : 0);
+  switch (key) {
+#define MOE_RATE(k, nn, cp, mpcv, rg) \
+  case k: err = launch_rate<nn, cp, mpcv, rg>(grid, smem, stages, status, stream); break;
+    MOE_RATE(0, 128, 0, 4, 3)
+    MOE_RATE(1, 128, 0, 16, 3)
+    MOE_RATE(10, 128, 1, 4, 3)
+    MOE_RATE(20, 128, 2, 4, 3)
+    MOE_RATE(30, 128, 3, 4, 3)
+    MOE_RATE(40, 128, 4, 4, 3)
+    MOE_RATE(50, 128, 5, 4, 3)
+    MOE_RATE(110, 128, 1, 4, 5)
+    MOE_RATE(120, 128, 2, 4, 5)
+    MOE_RATE(130, 128, 3, 4, 5)
+    MOE_RATE(1000, 256, 0, 4, 3)
+    MOE_RATE(1001, 256, 0, 16, 3)
+    MOE_RATE(1010, 256, 1, 4, 3)
+    MOE_RATE(1020, 256, 2, 4, 3)
+    MOE_RATE(1030, 256, 3, 4, 3)
+    MOE_RATE(1040, 256, 4, 4, 3)
+    MOE_RATE(1050, 256, 5, 4, 3)
+    MOE_RATE(1110, 256, 1, 4, 5)
+    MOE_RATE(1120, 256, 2, 4, 5)
+    MOE_RATE(1130, 256, 3, 4, 5)
+    MOE_RATE(1140, 256, 4, 4, 5)
+    MOE_RATE(1150, 256, 5, 4, 5)
+#undef MOE_RATE
+    default:
+      *why = "fp4 rate: variant not built";
+      return MOE_ERR_UNSUPPORTED;
   }
   if (err != cudaSuccess) {
     *why = cudaGetErrorString(err);
@@ -228,8 +270,9 @@ int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int stag
   return MOE_OK;
 }
 
-static_assert(rate_tmem_cols(128, 1, 4) <= 256 && rate_tmem_cols(128, 0, 16) <= 256 &&
-                  rate_tmem_cols(256, 1, 4) <= 512 && rate_tmem_cols(256, 0, 16) <= 512,
+static_assert(rate_tmem_cols(128, 1, 4, 3) <= 256 && rate_tmem_cols(128, 0, 16, 3) <= 256 &&
+                  rate_tmem_cols(256, 1, 4, 5) <= 512 && rate_tmem_cols(256, 0, 16, 3) <= 512 &&
+                  rate_tmem_cols(128, 1, 4, 5) <= 512,
               "a rate-probe variant overflows its tensor-memory share");
 static_assert(rate_smem_bytes(256) <= 96 * 1024, "rate-probe operands overflow shared memory");
 
@@ -239,18 +282,18 @@ namespace moe {
 int report_error(int code, const char* fmt, ...);
 }
 
-extern "C" int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm, int stages,
-                                double* flops, int32_t* status, void* stream) {
+extern "C" int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm, int ring,
+                                int stages, double* flops, int32_t* status, void* stream) {
   if (!flops) return moe::report_error(MOE_ERR_INVALID_ARG, "flops is null");
   const char* why = "";
-  int rc = moe::fp4_mma_rate_check(n, sf_copies, mmas_per_commit, ctas_per_sm, stages, &why);
+  int rc = moe::fp4_mma_rate_check(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, stages, &why);
   if (rc) return moe::report_error(rc, "%s", why);
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess || sms < 1)
     return moe::report_error(MOE_ERR_CUDA, "fp4 rate: no device (%s)", cudaGetErrorString(err));
-  rc = moe::launch_fp4_mma_rate(n, sf_copies, mmas_per_commit, ctas_per_sm, stages, sms, status,
+  rc = moe::launch_fp4_mma_rate(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, stages, sms, status,
                                           reinterpret_cast<cudaStream_t>(stream), flops, &why);
   return rc ? moe::report_error(rc, "%s", why) : MOE_OK;
 }

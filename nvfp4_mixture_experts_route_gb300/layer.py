@@ -16,10 +16,15 @@ from . import binding as B
 
 class NvFp4MoE:
     def __init__(self, raw: dict, a1_gscale: float, a2_gscale: float, gamma_bits, eps: float = 1e-6,
-                 tile_m: int = 32, weight_before_norm: bool = True, device="cuda"):
+                 tile_m: int = 32, weight_before_norm: bool = True, device="cuda", fused_norm: bool = False):
         """``raw``: numpy or torch uint8 w13 [E,2I,H/2], w13_sf [E,2I,H/16],
         w2 [E,H,I/2], w2_sf [E,H,I/16]; fp32 g1_alphas, g1_scale_c, g2_alphas
-        [E]. ``gamma_bits``: bf16 bit patterns [H] (uint16) or a bf16 tensor."""
+        [E]. ``gamma_bits``: bf16 bit patterns [H] (uint16) or a bf16 tensor.
+        ``fused_norm``: GEMM2's epilogue also writes the rows' sums of squares
+        and the finalize streams the rows once (moe_nvfp4_experts_sumsq and
+        moe_post_expert_finalize_sumsq); otherwise (the default, faster on
+        GB300 at every measured batch size) the plain pair moe_nvfp4_experts
+        and moe_post_expert_finalize."""
         dev = torch.device(device)
         t = {k: torch.as_tensor(raw[k]).to(dev) for k in ("w13", "w13_sf", "w2", "w2_sf")}
         self.E, twoI, half_h = t["w13"].shape
@@ -40,6 +45,7 @@ class NvFp4MoE:
         self.eps = float(eps)
         self.tile_m = tile_m
         self.weight_before_norm = weight_before_norm
+        self.fused_norm = fused_norm
         self.device = dev
         self.weights = B.weights_struct(self.prepared, self.g1_alphas, self.g1_scale_c, self.g2_alphas)
         self._buffers: dict = {}
@@ -53,6 +59,7 @@ class NvFp4MoE:
                 "route": B.alloc_route(T, K, self.E, self.tile_m, self.device),
                 "ws": B.alloc_workspace(T, K, self.E, self.H, self.I, self.tile_m, self.device),
                 "rows": torch.empty((max(P, 1), self.H), dtype=torch.bfloat16, device=self.device),
+                "row_sumsq": torch.empty((max(P, 1), self.H // 32), dtype=torch.float32, device=self.device),
                 "out": torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device),
                 "status": torch.zeros(1, dtype=torch.int32, device=self.device),
             }
@@ -66,9 +73,17 @@ class NvFp4MoE:
         b = self.buffers(T, K)
         st = b["status"] if status is None else status
         B.route_permute(topk_ids, self.E, self.tile_m, route=b["route"], status=st)
+        o = b["out"] if out is None else out
+        if self.fused_norm:
+            B.nvfp4_experts_sumsq(self.weights, b["route"], x=x, a1_gscale=self.a1_gscale,
+                                  a2_gscale=self.a2_gscale, T=T, H=self.H, I=self.I, E=self.E, K=K,
+                                  gamma=self.gamma, weight_before_norm=self.weight_before_norm,
+                                  gemm2_rows=b["rows"], row_sumsq=b["row_sumsq"], ws=b["ws"], status=st)
+            B.post_expert_finalize_sumsq(b["rows"], b["row_sumsq"], b["route"].expanded_to_permuted, topk_weights,
+                                         self.gamma, self.eps, out=o, status=st)
+            return o, b
         B.nvfp4_experts(self.weights, b["route"], x=x, a1_gscale=self.a1_gscale, a2_gscale=self.a2_gscale,
                         T=T, H=self.H, I=self.I, E=self.E, K=K, gemm2_rows=b["rows"], ws=b["ws"], status=st)
-        o = b["out"] if out is None else out
         B.post_expert_finalize(b["rows"], b["route"].expanded_to_permuted, topk_weights, self.gamma, self.eps,
                                self.weight_before_norm, out=o, status=st)
         return o, b

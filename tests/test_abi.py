@@ -41,9 +41,9 @@ def test_workspace_size_formula(lib):
         return (v + 1023) // 1024 * 1024
 
     # codes row-major; scales as one 512-byte atom per K=64 step per 128 rows of a tile;
-    # then one int32 completion counter per route tile
+    # then one int32 completion counter per route tile and the unit ticket
     want = (up(P * H // 2) + up(MT * (H // 64) * 512) + up(P * I // 2) + up(MT * (I // 64) * 512)
-            + up(MT * 4))
+            + up((MT + 1) * 4))
     assert B.experts_workspace_size(T, K, E, H, I, tm) == want
 
 
@@ -52,7 +52,8 @@ def test_workspace_size_formula(lib):
     (lambda: B.prepared_sizes(8, 256, 96), "MOE_ERR_UNSUPPORTED"),
     (lambda: B.route_sizes(4, 2, 8, 48), "MOE_ERR_UNSUPPORTED"),
     (lambda: B.route_sizes(4, 2, 0, 32), "MOE_ERR_INVALID_ARG"),
-    (lambda: B.experts_workspace_size(4, 2, 8, 256, 64, 32), "MOE_ERR_UNSUPPORTED"),
+    (lambda: B.experts_workspace_size(4, 2, 8, 256, 96, 32), "MOE_ERR_UNSUPPORTED"),
+    (lambda: B.experts_workspace_size(4, 2, 8, 192, 128, 32), "MOE_ERR_UNSUPPORTED"),
 ])
 def test_host_refusals(lib, call, code):
     with pytest.raises(B.MoeError) as ei:

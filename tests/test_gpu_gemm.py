@@ -101,6 +101,11 @@ SMALL = [
     (29, 640, 384, 4, 3, "zipf", 64, 4.0, 1e-3),           # ragged K (2.5 and 1.5 stages)
     (70, 512, 256, 4, 4, "zipf", 128, 4.0, 1e-3),          # tile 128
     (150, 256, 256, 4, 4, "uniform", 256, 4.0, 1e-3),      # tile 256: two scale atoms per tile
+    # I % 128 == 64 (expert-TP slices the prepared layout admits): a GEMM2 K
+    # stage of one or three K = 64 steps reads past the row end (zero fill)
+    (19, 256, 192, 4, 2, "uniform", 32, 4.0, 1e-3),
+    (40, 256, 320, 4, 3, "zipf", 128, 4.0, 1e-3),
+    (9, 512, 64, 4, 2, "uniform", 64, 4.0, 1e-3),
 ]
 
 
@@ -272,6 +277,61 @@ def test_gemm1_intermediate_and_end_to_end(small_cases, idx, record_property):
     for k, v in (("sf_match", sf_match), ("code_match", code_match), ("rows_rel_l2", err_rows), ("out_rel_l2", err)):
         record_property(k, float(v))
     assert err < OUT_BAR, f"out rel-L2 {err:.3g}; gpu {finite_summary(got['out'])}"
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+@pytest.mark.parametrize("wbn", [True, False])
+def test_fused_sums_of_squares_and_streaming_finalize(small_cases, idx, wbn, record_property):
+    """moe_nvfp4_experts_sumsq: the rows equal moe_nvfp4_experts's bit for bit;
+    every written row's 32-column sums of squares equal, to fp32 rounding,
+    the fp64 sums of the stored bf16 values (gain-weighted in the weight-
+    before-norm reading); the split GEMM2 / one-launch entry points write the
+    same partials; moe_post_expert_finalize_sumsq equals the oracle's
+    finalize of those rows (gamma ~ N(0, 1) so that the two readings differ)."""
+    w, raw, batch, tile, a1, a2 = small_cases[idx]
+    raw = dict(raw)
+    raw["gamma"] = inputs._to_bf16_bits(np.random.default_rng(3).standard_normal(w.H))
+    prep = Prepared(raw)
+    T, K, E, H, I = w.T, w.K, w.E, w.H, w.I
+    ids = _dev(batch["topk_ids"].astype(np.int32))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r = B.route_permute(ids, E, tile, status=status)
+    g1 = torch.tensor([a1], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([a2], dtype=torch.float32, device=DEV)
+    x = bf16_dev(batch["x"])
+    plain, _ = B.nvfp4_experts(prep.w, r, x=x, a1_gscale=g1, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K, status=status)
+    rows, ss, ws = B.nvfp4_experts_sumsq(prep.w, r, x=x, a1_gscale=g1, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K,
+                                         gamma=prep.gamma, weight_before_norm=wbn, status=status)
+    # the split entry points' partials
+    rows2 = torch.zeros_like(rows)
+    ss2 = torch.zeros_like(ss)
+    B.experts_gemm2_sumsq(prep.w, r, ws, rows2, ss2, gamma=prep.gamma, weight_before_norm=wbn, T=T, H=H, I=I, E=E,
+                          K=K, status=status)
+    ss3 = torch.zeros_like(ss)
+    B.experts_gemms_sumsq(prep.w, r, ws, torch.zeros_like(rows), ss3, a2_gscale=g2, gamma=prep.gamma,
+                          weight_before_norm=wbn, T=T, H=H, I=I, E=E, K=K, status=status)
+    tw = _dev(batch["topk_weights"])
+    out = B.post_expert_finalize_sumsq(rows, ss, r.expanded_to_permuted, tw, prep.gamma, 1e-6, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    e2p = r.expanded_to_permuted.cpu().numpy()
+    live = e2p.reshape(-1)
+    live = live[live >= 0]
+    assert torch.equal(rows[live], plain[live])
+    got_rows = bf16_host_f64(rows)[live]
+    gain = 1.0 + codecs.bf16_bits_to_f64(raw["gamma"]) if wbn else np.ones(H)
+    want_ss = ((got_rows * gain[None, :]) ** 2).reshape(len(live), H // 32, 32).sum(axis=-1)
+    got_ss = ss.cpu().numpy().astype(np.float64)[live]
+    assert np.allclose(got_ss, want_ss, rtol=1e-5, atol=0), np.max(np.abs(got_ss / want_ss - 1))
+    assert np.array_equal(ss2.cpu().numpy()[live], ss.cpu().numpy()[live])
+    assert np.array_equal(ss3.cpu().numpy()[live], ss.cpu().numpy()[live])
+    want = olayer.finalize(bf16_host_f64(rows), e2p, batch["topk_weights"], raw["gamma"], 1e-6, wbn)
+    got = bf16_host_f64(out)
+    err = rel_l2(got, want["out"])
+    record_property("finalize_rel_l2", err)
+    assert err < 2e-3
+    rms = np.sqrt(np.mean(want["out"] ** 2))
+    assert (np.abs(got - want["out_bf16"]) <= np.abs(want["out_bf16"]) * 2.0**-7 + 1e-4 * rms).all()
 
 
 def test_weight_before_norm_reading_end_to_end(small_cases):
@@ -576,3 +636,30 @@ def test_timed_launch_path_matches_split_path(full, name):
     assert np.array_equal(bf16_host_f64(host), split["out"])
     status, fused = _fused_rows(prep, batch, w.tile_m, a1, a2, calls=1)
     assert status == 0 and np.array_equal(fused[0], split["rows"])
+    # The layer with the norm's sums of squares fused into GEMM2 and the
+    # finalize streaming the rows once: the same rows bit for bit; the output
+    # equal up to the order of the fp32 sums; its graph replays equal its
+    # eager call.
+    del moe
+    torch.cuda.empty_cache()
+    fn = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=w.tile_m, fused_norm=True)
+    got, bufs = fn.forward(x, ids, tw)
+    got = bf16_host_f64(got)
+    torch.cuda.synchronize()
+    assert int(bufs["status"].item()) == 0
+    P, _ = B.route_sizes(w.T, w.K, w.E, w.tile_m)
+    live = split["e2p"].reshape(-1)
+    live = live[live >= 0]
+    assert np.array_equal(bf16_host_f64(bufs["rows"])[live], split["rows"][live])
+    assert rel_l2(got, split["out"]) < 1e-3
+    assert (np.abs(got - split["out"]) <= np.abs(split["out"]) * 2.0**-7 + 1e-3 * np.sqrt(np.mean(split["out"] ** 2))).all()
+    gb = fn.graph_buffers(w.T, w.K)
+    gb["x"].copy_(x)
+    gb["topk_ids"].copy_(ids)
+    gb["topk_weights"].copy_(tw)
+    assert np.array_equal(bf16_host_f64(fn.replay(w.T, w.K)), got)
+    hb = fn.host_buffers(w.T, w.K)
+    hb["host_inputs"].copy_(gb["inputs"].cpu())
+    host = fn.replay_host(w.T, w.K)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host_f64(host), got)

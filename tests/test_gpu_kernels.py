@@ -303,6 +303,17 @@ def test_finalize_skips_out_of_range_rows(K, H):
     torch.cuda.synchronize()
     assert int(status.item()) == -6
     assert rel_l2(bf16_host_f64(out), want["out"]) < 2e-3
+    # the streaming finalize from sums of squares skips the same entries
+    rows64 = codecs.bf16_bits_to_f64(rows_bits)
+    g = 1.0 + codecs.bf16_bits_to_f64(gamma)
+    ss = ((rows64 * g[None, :]) ** 2).reshape(P, H // 32, 32).sum(axis=-1).astype(np.float32)
+    status.zero_()
+    out2 = B.post_expert_finalize_sumsq(bf16_dev(rows_bits), torch.from_numpy(ss).to(DEV),
+                                        torch.from_numpy(bad).to(DEV), torch.from_numpy(w).to(DEV), bf16_dev(gamma),
+                                        1e-6, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    assert rel_l2(bf16_host_f64(out2), want["out"]) < 2e-3
     # the same rows with the valid map: status stays 0
     status.zero_()
     B.post_expert_finalize(bf16_dev(rows_bits), torch.from_numpy(e2p).to(DEV), torch.from_numpy(w).to(DEV),

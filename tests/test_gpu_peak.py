@@ -7,9 +7,11 @@ import torch
 from nvfp4_mixture_experts_route_gb300 import binding as B
 
 VARIANTS = [
-    # (n, sf_copies, mmas_per_commit, ctas_per_sm)
-    (128, 0, 4, 1), (128, 0, 4, 2), (128, 1, 4, 2), (128, 0, 16, 2), (128, 2, 4, 2), (128, 3, 4, 2),
-    (256, 0, 4, 1), (256, 1, 4, 1), (256, 0, 16, 1), (256, 2, 4, 1), (256, 3, 4, 1),
+    # (n, sf_copies, mmas_per_commit, ctas_per_sm, ring)
+    (128, 0, 4, 1, 3), (128, 0, 4, 2, 3), (128, 1, 4, 2, 3), (128, 0, 16, 2, 3), (128, 2, 4, 2, 3),
+    (128, 3, 4, 2, 3), (128, 4, 4, 2, 3), (128, 5, 4, 2, 3), (128, 2, 4, 1, 5), (128, 3, 4, 1, 5),
+    (256, 0, 4, 1, 3), (256, 1, 4, 1, 3), (256, 0, 16, 1, 3), (256, 2, 4, 1, 3), (256, 3, 4, 1, 3),
+    (256, 1, 4, 1, 5), (256, 2, 4, 1, 5), (256, 3, 4, 1, 5), (256, 4, 4, 1, 5), (256, 5, 4, 1, 5),
 ]
 
 
@@ -18,21 +20,22 @@ def test_unfitting_variants_refused_on_host():
 
     lib = B.load()
     f = C.c_double()
-    for n, sf, mpc, ctas, want in ((256, 0, 4, 2, -2), (128, 1, 16, 1, -2), (128, 3, 16, 1, -2), (64, 0, 4, 1, -1),
-                                   (128, 0, 4, 3, -1), (128, 4, 4, 1, -1)):
-        assert lib.moe_fp4_mma_rate(n, sf, mpc, ctas, 8, C.byref(f), None, None) == want
+    for n, sf, mpc, ctas, ring, want in ((256, 0, 4, 2, 3, -2), (128, 1, 16, 1, 3, -2), (128, 3, 16, 1, 3, -2),
+                                         (128, 1, 4, 2, 5, -2), (64, 0, 4, 1, 3, -1), (128, 0, 4, 3, 3, -1),
+                                         (128, 6, 4, 1, 3, -1), (128, 1, 4, 1, 4, -1)):
+        assert lib.moe_fp4_mma_rate(n, sf, mpc, ctas, ring, 8, C.byref(f), None, None) == want
         assert b"fp4 rate" in lib.moe_last_error()
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_rate_probe_runs(variant, record_property):
-    n, sf, mpc, ctas = variant
+    n, sf, mpc, ctas, ring = variant
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.fp4_mma_rate(n, sf, mpc, ctas, 64, status=status)  # warm-up
+    B.fp4_mma_rate(n, sf, mpc, ctas, 64, status=status, ring=ring)  # warm-up
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    flops = B.fp4_mma_rate(n, sf, mpc, ctas, 2048 // mpc * 4, status=status)
+    flops = B.fp4_mma_rate(n, sf, mpc, ctas, 2048 // mpc * 4, status=status, ring=ring)
     e1.record()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
