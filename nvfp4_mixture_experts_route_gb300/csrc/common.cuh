@@ -372,6 +372,27 @@ __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
   return r & 0xFFu;
 }
 
+// NVFP4 of one 16-element block with global scale g; same arithmetic as the
+// input quantization (s = amax*g/6, sf = e4m3(s), q = e2m1(v * g/sf)).
+__device__ __forceinline__ void quant16(const float (&v)[16], float g, uint2& codes,
+                                        uint32_t& sf_code) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  sf_code = f32_to_e4m3((amax * g) / 6.0f);
+  const float sfv = e4m3_to_f32(sf_code);
+  uint32_t lo = 0, hi = 0;
+  if (sfv > 0.f) {
+    const float inv = g / sfv;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) lo |= f32x2_to_e2m1x2(v[i] * inv, v[i + 1] * inv) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+      hi |= f32x2_to_e2m1x2(v[8 + i] * inv, v[9 + i] * inv) << (4 * i);
+  }
+  codes = make_uint2(lo, hi);
+}
+
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------

@@ -61,6 +61,12 @@ constexpr int kWTile = 128;                    // weight rows per unit (MMA M)
 constexpr uint32_t kABytes = kWTile * kStageRowBytes;  // 16 KiB
 constexpr uint32_t kSfStageBytes = 4 * kAtomBytes;     // 4 K=64 steps
 constexpr int kMaxStages = 8;
+// Stages of its first unit's weights a CTA of the one-launch GEMMs prefetches
+// into L2 while the previous kernel (the quantizer) finishes.
+#ifndef MOE_HEAD_PREFETCH_STAGES
+#define MOE_HEAD_PREFETCH_STAGES 2
+#endif
+constexpr int kHeadPrefetchStages = MOE_HEAD_PREFETCH_STAGES;
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
 
 // One GEMM's operands: GEMM1 (w13 against the permuted activations, writes
@@ -229,27 +235,6 @@ static_assert(tile_fits(32, 1) && tile_fits(64, 1) && tile_fits(128, 1) && tile_
                   tile_fits(32, 2) && tile_fits(64, 2) && tile_fits(128, 2) && tile_fits(256, 2),
               "a route-tile shape overflows its pipeline, tensor memory or shared memory budget");
 
-
-// NVFP4 of one 16-element block with global scale g; same arithmetic as the
-// input quantization (s = amax*g/6, sf = e4m3(s), q = e2m1(v * g/sf)).
-__device__ __forceinline__ void quant16(const float (&v)[16], float g, uint2& codes,
-                                        uint32_t& sf_code) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  sf_code = f32_to_e4m3((amax * g) / 6.0f);
-  const float sfv = e4m3_to_f32(sf_code);
-  uint32_t lo = 0, hi = 0;
-  if (sfv > 0.f) {
-    const float inv = g / sfv;
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) lo |= f32x2_to_e2m1x2(v[i] * inv, v[i + 1] * inv) << (4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; i += 2)
-      hi |= f32x2_to_e2m1x2(v[8 + i] * inv, v[9 + i] * inv) << (4 * i);
-  }
-  codes = make_uint2(lo, hi);
-}
 
 // GEMM1 epilogue for COLS route columns of one accumulator: lanes write
 // scale * acc (gate rows 0-15, up rows 16-31 of this quadrant) to the warp's
@@ -466,7 +451,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           const int e = __ldcg(p.tile_expert + tau);
           const int a_row = e * gs.rows_w + mt * kWTile;
           const uint8_t* wsf = gs.w_sf + ((size_t)e * tw + mt) * KC * kAtomBytes;
-          for (int ks = 0; ks < nks && ks < ST; ++ks) {
+          for (int ks = 0; ks < nks && ks < kHeadPrefetchStages; ++ks) {
             const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
             for (int c = 0; 4 * c < kk; ++c)
               tma_prefetch_l2_2d(gi == 0 ? &tmA1 : &tmA2, (ks * CH + c) * kStageRowBytes, a_row);

@@ -106,6 +106,10 @@ SMALL = [
     (19, 256, 192, 4, 2, "uniform", 32, 4.0, 1e-3),
     (40, 256, 320, 4, 3, "zipf", 128, 4.0, 1e-3),
     (9, 512, 64, 4, 2, "uniform", 64, 4.0, 1e-3),
+    # 128-row tiles with a last K stage of two steps: GEMM2 (K = 384) here,
+    # GEMM1 (K = 640) below
+    (150, 768, 384, 4, 4, "zipf", 128, 4.0, 1e-3),
+    (90, 640, 384, 3, 3, "uniform", 128, 4.0, 1e-3),
 ]
 
 
