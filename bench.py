@@ -50,10 +50,10 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # and the SHA-256 of the kernel sources it was taken on (gemm.cu,
 # common.cuh, layout.cuh in that order): once those change, traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 948_401_408 + 6_216_192,
-                  "sources": "1dc9685ab1b35347cd862da71e7b1f459cb113961f5f1407b43718d692c4f3b4"},
-    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_721_626_976 + 84_110_080,
-                           "sources": "1dc9685ab1b35347cd862da71e7b1f459cb113961f5f1407b43718d692c4f3b4"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 955_106_048 + 6_885_120,
+                  "sources": "e3931971c24efbeb40762cde27f9abac12385a04362c031e0c71c7976e93c625"},
+    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_722_510_848 + 84_121_344,
+                           "sources": "e3931971c24efbeb40762cde27f9abac12385a04362c031e0c71c7976e93c625"},
 }
 
 

@@ -318,6 +318,98 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
   }
 }
 
+// The finalize for few tokens (decode batches), where its latency counts:
+// one CTA per token and one thread per 8-element vector of the hidden
+// dimension (H / 8 threads, H up to 5120), each loading its vector of all K
+// (<= 8) route rows at once (the rows were just written, mostly still in
+// L2). Every thread's share of each route's sum of squares goes to shared
+// memory, one warp per route sums them in a fixed order, and after a
+// single block barrier every thread adds coef_k * r_k from its registers and
+// applies the gain: out = bf16(g * sum_k coef_k r_k). One reduction round
+// for all routes, where the staged kernel waits on one per route.
+constexpr int kFinFewMaxK = 8;
+constexpr int kFinFewMaxThreads = 640;
+constexpr int kFinFewMaxTokens = 128;
+
+__global__ void __launch_bounds__(kFinFewMaxThreads, 1) finalize_few_kernel(
+    const __nv_bfloat16* __restrict__ rows, int num_rows, const int32_t* __restrict__ e2p,
+    const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
+    int weight_before_norm, int K, int H, __nv_bfloat16* __restrict__ out, int32_t* status) {
+  __shared__ __align__(16) float part[kFinFewMaxThreads][kFinFewMaxK];
+  __shared__ float coef[kFinFewMaxK];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int v = threadIdx.x, lane = v & 31, warp = v >> 5, nwarps = blockDim.x >> 5;
+  const bool on = v < H / 8;
+  uint4 raw[kFinFewMaxK];
+#pragma unroll
+  for (int k = 0; k < kFinFewMaxK; ++k) {
+    const int p = k < K ? checked_row(e2p[(size_t)t * K + k], num_rows, status) : -1;
+    raw[k] = (on && p >= 0) ? *(reinterpret_cast<const uint4*>(rows + (size_t)p * H) + v) : make_uint4(0, 0, 0, 0);
+  }
+  float2 g[4];
+  {
+    const uint4 gu = on ? __ldg(reinterpret_cast<const uint4*>(gamma + 8 * v)) : make_uint4(0, 0, 0, 0);
+    const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gu);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(gh[q]);
+      g[q] = make_float2(1.f + f.x, 1.f + f.y);  // gain centre added in fp32
+    }
+  }
+  {
+    float ss[kFinFewMaxK];
+#pragma unroll
+    for (int k = 0; k < kFinFewMaxK; ++k) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        const float2 a = weight_before_norm ? fmul2(f, g[q]) : f;
+        s2 = ffma2(a, a, s2);
+      }
+      ss[k] = s2.x + s2.y;
+    }
+    float4* dst = reinterpret_cast<float4*>(&part[v][0]);
+    dst[0] = make_float4(ss[0], ss[1], ss[2], ss[3]);
+    dst[1] = make_float4(ss[4], ss[5], ss[6], ss[7]);
+  }
+  __syncthreads();
+  for (int k = warp; k < K; k += nwarps) {
+    // route k: the threads' shares in a fixed order
+    float ss = 0.f;
+    for (int i = lane; i < (int)blockDim.x; i += 32) ss += part[i][k];
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, d);
+    const int p = e2p[(size_t)t * K + k];
+    if (lane == 0)
+      coef[k] = (p >= 0 && p < num_rows) ? topk_w[(size_t)t * K + k] / sqrtf(ss / (float)H + eps) : 0.f;
+  }
+  __syncthreads();
+  if (!on) return;
+  float2 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kFinFewMaxK; ++k) {
+    const float c = k < K ? coef[k] : 0.f;
+    const float2 ck = make_float2(c, c);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = ffma2(__bfloat1622float2(h[q]), ck, acc[q]);
+  }
+  uint4 o;
+  __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 r = fmul2(acc[q], g[q]);
+    oh[q] = __floats2bfloat162_rn(r.x, r.y);
+  }
+  *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * v) = o;
+}
+
 cudaError_t launch_finalize_parts(const void* const* parts, int nparts, int num_rows, const int32_t* e2p,
                                   const float* w, const void* gamma, float eps,
                                   int weight_before_norm, int T, int K, int H, void* out,
@@ -332,6 +424,11 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, int num_
   auto op = reinterpret_cast<__nv_bfloat16*>(out);
   cudaError_t err = cudaSuccess;
   const size_t staged = (size_t)K * H * 2;
+  // few tokens: the latency of one reduction round matters more than bandwidth
+  if (nparts == 1 && T <= kFinFewMaxTokens && K <= kFinFewMaxK && H <= 8 * kFinFewMaxThreads)
+    return launch_kernel(finalize_few_kernel, dim3(T), dim3((H / 8 + 31) / 32 * 32), 0, stream, true,
+                         reinterpret_cast<const __nv_bfloat16*>(parts[0]), num_rows, e2p, w, gp, eps,
+                         weight_before_norm, K, H, op, status);
   if (nparts == 1 && K <= kFinMaxK && staged <= (size_t)kFinStagedMaxBytes && vpt <= 5) {
     auto rows = reinterpret_cast<const __nv_bfloat16*>(parts[0]);
 #define MOE_FIN_STAGED(n)                                                                       \

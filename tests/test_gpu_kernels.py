@@ -255,6 +255,12 @@ def test_tp_slice_layout_identity_on_gpu():
     (33, 8, 4096, 0.1, 1e-3),
     (5, 3, 16384, 1.0, 1.0),
     (3, 1, 8, 0.5, 1.0),
+    # the two-CTA register kernel (K <= 8, H % 16 == 0, H <= 8192): many
+    # waves, the widest row, a row of three vectors per CTA; and K > 8
+    (600, 8, 5120, 1.0, 1.0),
+    (5, 8, 8192, 0.5, 1.0),
+    (9, 4, 48, 1.0, 1.0),
+    (7, 12, 1024, 1.0, 1.0),
 ])
 @pytest.mark.parametrize("wbn", [True, False])
 def test_finalize_parity(T, K, H, gamma_sd, scale, wbn):
