@@ -310,13 +310,14 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
 
     def step(i, ev=None, split=True):
         wts = copies[i % len(copies)]
-        B.route_permute(ids, E, tile, route=route, status=status)
         if ev is None:
-            # The expert body as one call: its GEMMs start as programmatic
-            # dependents of the kernel before them.
-            B.nvfp4_experts(wts, route, x=x, a1_gscale=moe.a1_gscale, a2_gscale=moe.a2_gscale, T=T, H=H,
-                            I=I, E=E, K=K, gemm2_rows=rows, ws=ws, status=status)
+            # Routing and the expert body as one call (for few routes the
+            # routing runs inside the input quantizer); the GEMMs start as
+            # programmatic dependents of the kernel before them.
+            B.nvfp4_experts_routed(wts, ids, route, x=x, a1_gscale=moe.a1_gscale, a2_gscale=moe.a2_gscale,
+                                   H=H, I=I, E=E, gemm2_rows=rows, ws=ws, status=status)
         else:
+            B.route_permute(ids, E, tile, route=route, status=status)
             # The same kernels through the split entry points (plain launches),
             # with events between them for the per-kernel durations.
             B.experts_quantize(route, ws, x=x, a1_gscale=moe.a1_gscale, T=T, H=H, I=I, E=E, K=K,
@@ -338,9 +339,10 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         if ev is not None:
             ev[4].record(stream)
 
-    # route/permute (1 or 3 kernels), quantize, the expert GEMMs (one fused
-    # launch or two), finalize
-    launches_per_step = B.route_kernels(T, K, E) + B.experts_kernels(tile) + 1
+    # routing + expert body (routing fused into the quantizer for few routes,
+    # else 1 or 3 routing kernels, the quantizer and one or two GEMM
+    # launches), then the finalize
+    launches_per_step = B.routed_experts_kernels(T, K, E, tile) + 1
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()

@@ -209,6 +209,31 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a,
                       void* gemm2_rows, void* ws, size_t ws_bytes,
                       int32_t* status, void* stream);
 
+/* Routing and the whole expert body in one call: the result of
+ * moe_route_permute (same buffers, same contents, readable after the call,
+ * e.g. by the finalize) followed by moe_nvfp4_experts on that route. With few
+ * routes (T*K <= 2048, E <= 256) and tile_m <= 64 the routing runs inside the
+ * input quantizer: every CTA of that kernel computes the routing in its own
+ * shared memory and the first also writes it out, so the step has no kernel
+ * boundary between routing and quantization (2 kernels in all, see
+ * moe_routed_experts_kernels). Otherwise it enqueues the routing kernels and
+ * then moe_nvfp4_experts. Arguments as for those two entry points; an invalid
+ * expert id is reported in status as moe_route_permute reports it. */
+int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids,
+                             const void* x, const void* a, const void* a_sf,
+                             const float* a1_gscale, const float* a2_gscale,
+                             int T, int H, int I, int E, int K, int tile_m,
+                             int32_t* expert_counts, int32_t* expert_offsets,
+                             int32_t* expanded_to_permuted,
+                             int32_t* permuted_to_token, int32_t* tile_expert,
+                             int32_t* tile_row_limit, int32_t* totals,
+                             void* gemm2_rows, void* ws, size_t ws_bytes,
+                             int32_t* status, void* stream);
+
+/* Kernels moe_nvfp4_experts_routed enqueues for these sizes (a negative
+ * status for invalid ones). */
+int moe_routed_experts_kernels(int T, int K, int E, int tile_m);
+
 /* moe_nvfp4_experts with the first half of the post-expert norm fused into
  * GEMM2's epilogue: besides the bf16 rows it writes, for every route row,
  * the sums of squares of its stored values over each 32 columns,

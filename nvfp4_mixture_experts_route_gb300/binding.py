@@ -74,6 +74,12 @@ _SIGNATURES = {
          C.c_size_t, _P, _P],
         _I,
     ),
+    "moe_nvfp4_experts_routed": (
+        [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+         _P, C.c_size_t, _P, _P],
+        _I,
+    ),
+    "moe_routed_experts_kernels": ([_I, _I, _I, _I], _I),
     "moe_nvfp4_experts_sumsq": (
         [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _I, _P,
          _P, C.c_size_t, _P, _P],
@@ -217,6 +223,15 @@ def experts_kernels(tile_m: int) -> int:
     return n
 
 
+def routed_experts_kernels(T: int, K: int, E: int, tile_m: int) -> int:
+    """Kernels nvfp4_experts_routed launches for these sizes (2 when the
+    routing runs inside the input quantizer)."""
+    n = load().moe_routed_experts_kernels(T, K, E, tile_m)
+    if n < 0:
+        _check(n)
+    return n
+
+
 def route_sizes(T: int, K: int, E: int, tile_m: int) -> tuple[int, int]:
     P, MT = C.c_int(), C.c_int()
     _check(load().moe_route_sizes(T, K, E, tile_m, C.byref(P), C.byref(MT)))
@@ -281,6 +296,28 @@ def alloc_workspace(T, K, E, H, I, tile_m, device):
     raw = torch.empty(n + 1024, dtype=torch.uint8, device=device)
     off = (-raw.data_ptr()) % 1024
     return raw[off: off + n]
+
+
+def nvfp4_experts_routed(w: MoeWeights, topk_ids, route: Route, *, x=None, a=None, a_sf=None, a1_gscale,
+                         a2_gscale, H, I, E, gemm2_rows=None, ws=None, status=None, stream=None):
+    """moe_nvfp4_experts_routed: routing into `route` (allocated with
+    alloc_route) and the expert body, in one call."""
+    import torch
+
+    T, K = topk_ids.shape
+    tile_m = route.tile_m
+    P, _ = route_sizes(T, K, E, tile_m)
+    dev = route.totals.device
+    if gemm2_rows is None:
+        gemm2_rows = torch.empty((max(P, 1), H), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = alloc_workspace(T, K, E, H, I, tile_m, dev)
+    _check(load().moe_nvfp4_experts_routed(
+        C.byref(w), _ptr(topk_ids), _ptr(x), _ptr(a), _ptr(a_sf), _ptr(a1_gscale), _ptr(a2_gscale), T, H, I, E,
+        K, tile_m, _ptr(route.expert_counts), _ptr(route.expert_offsets), _ptr(route.expanded_to_permuted),
+        _ptr(route.permuted_to_token), _ptr(route.tile_expert), _ptr(route.tile_row_limit), _ptr(route.totals),
+        _ptr(gemm2_rows), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return gemm2_rows, ws
 
 
 def nvfp4_experts(w: MoeWeights, route: Route, *, x=None, a=None, a_sf=None, a1_gscale, a2_gscale,

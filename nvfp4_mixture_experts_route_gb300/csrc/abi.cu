@@ -18,6 +18,10 @@ cudaError_t launch_quantize_permute(const void*, const void*, const void*, const
                                     const int32_t*, const int32_t*, const int32_t*, int, int, int,
                                     int, int, int, uint8_t*, uint8_t*, int32_t*, cudaStream_t);
 cudaError_t launch_act_scales_io(int, uint8_t*, uint8_t*, int, int, int, cudaStream_t);
+bool route_quantize_fits(int T, int K, int E);
+cudaError_t launch_route_quantize(const int32_t*, int, int, int, int, int, int, int32_t*, int32_t*, int32_t*,
+                                  int32_t*, int32_t*, int32_t*, int32_t*, const void*, const void*, const void*,
+                                  const float*, int, uint8_t*, uint8_t*, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_prepare_weights(const void*, const void*, const void*, const void*, int, int,
                                    int, void*, void*, void*, void*, cudaStream_t);
 cudaError_t launch_finalize(const void*, int, const int32_t*, const float*, const void*, float, int,
@@ -447,6 +451,64 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a, const 
                       size_t ws_bytes, int32_t* status, void* stream) {
   return experts_body(w, x, a, a_sf, a1_gscale, a2_gscale, r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes,
                       status, stream, SumSq());
+}
+
+// Routing and the expert body in one call: with few routes and decode-sized
+// route tiles the routing runs inside the input quantizer (one kernel, then
+// the one-launch GEMMs as its programmatic dependent); otherwise the routing
+// kernels, then moe_nvfp4_experts.
+static bool routed_fused(int T, int K, int E, int tile_m) {
+  return T > 0 && moe::route_quantize_fits(T, K, E) && moe_experts_kernels(tile_m) == 2;
+}
+
+int moe_routed_experts_kernels(int T, int K, int E, int tile_m) {
+  RouteDims d;
+  int rc = route_dims(T, K, E, tile_m, &d);
+  if (rc) return rc;
+  if (routed_fused(T, K, E, tile_m)) return 2;
+  return moe::route_kernel_count(T, K, E) + (d.P > 0 ? moe_experts_kernels(tile_m) : 0);
+}
+
+int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
+                             const void* a_sf, const float* a1_gscale, const float* a2_gscale, int T, int H,
+                             int I, int E, int K, int tile_m, int32_t* expert_counts, int32_t* expert_offsets,
+                             int32_t* expanded_to_permuted, int32_t* permuted_to_token, int32_t* tile_expert,
+                             int32_t* tile_row_limit, int32_t* totals, void* gemm2_rows, void* ws,
+                             size_t ws_bytes, int32_t* status, void* stream) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc || (rc = check_weights(w, true)) || (rc = check_weights(w, false))) return rc;
+  const moe_route r{permuted_to_token, tile_expert, tile_row_limit, totals, expanded_to_permuted};
+  if (!routed_fused(T, K, E, tile_m)) {
+    rc = moe_route_permute(topk_ids, T, K, E, tile_m, expert_counts, expert_offsets, expanded_to_permuted,
+                           permuted_to_token, tile_expert, tile_row_limit, totals, status, stream);
+    if (rc) return rc;
+    return moe_nvfp4_experts(w, x, a, a_sf, a1_gscale, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws,
+                             ws_bytes, status, stream);
+  }
+  if (!expert_counts || !expert_offsets || !topk_ids || !expanded_to_permuted || !permuted_to_token ||
+      !tile_expert || !tile_row_limit || !totals)
+    return fail(MOE_ERR_INVALID_ARG, "routing buffer is null");
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  if (x) {
+    if (!a1_gscale) return fail(MOE_ERR_INVALID_ARG, "a1_gscale is null");
+    if (!aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  } else {
+    if (!a || !a_sf) return fail(MOE_ERR_INVALID_ARG, "give x, or a and a_sf");
+    if (!aligned(a, 16) || !aligned(a_sf, 4))
+      return fail(MOE_ERR_INVALID_ARG, "a must be 16-byte and a_sf 4-byte aligned");
+  }
+  if (!a2_gscale) return fail(MOE_ERR_INVALID_ARG, "a2_gscale is null");
+  if (!gemm2_rows || !aligned(gemm2_rows, 16))
+    return fail(MOE_ERR_INVALID_ARG, "gemm2_rows must be non-null and 16-byte aligned");
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  cudaError_t err = moe::launch_route_quantize(
+      topk_ids, T, K, E, tile_m, L.P, L.MT, expert_counts, expert_offsets, expanded_to_permuted, permuted_to_token,
+      tile_expert, tile_row_limit, totals, x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, H, base + L.a_codes,
+      base + L.a_sf, reinterpret_cast<int32_t*>(base + L.done), status, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_nvfp4_experts_routed");
+  return experts_fused(w, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true,
+                       false);
 }
 
 int moe_nvfp4_experts_sumsq(const moe_weights* w, const void* x, const void* a, const void* a_sf,

@@ -107,6 +107,9 @@ struct GemmParams {
   float* row_ss;
   const __nv_bfloat16* ss_gamma;
   int ss_wbn;
+  // both GEMMs in one grid: the experts and the route tiles the buffers hold
+  // (bounds for the head prefetch, which reads the routing as a hint)
+  int num_experts, max_tiles;
 };
 
 // Sum over a warp's 32 lanes of each of 32 values: afterwards lane l holds
@@ -291,6 +294,34 @@ __host__ __device__ constexpr int gemm_threads(int mode, int tile_m) {
 // fits at once). The tile's launch shape, pipeline depth and scale-atom
 // count are compile-time, so the MMA issuer's per-stage loops unroll and its
 // descriptors are base + constant.
+// Both GEMMs in one grid: L2 prefetch of the first kHeadPrefetchStages
+// stages of weights and weight scales of unit blockIdx.x, from a routing
+// read before the previous kernel has completed (a hint: the route-tile
+// count and the expert are bounded before any address is formed; a stale
+// value only wastes the prefetch). Kept out of line so that its registers
+// do not weigh on the kernel's steady-state loops.
+template <int SPST>
+__device__ __noinline__ void prefetch_head_hint(const CUtensorMap& tmA1, const CUtensorMap& tmA2, const GemmParams& p,
+                                                int tw1, int tw2) {
+  const int nt = min(max(__ldcg(p.totals), 0), p.max_tiles);
+  const int u = blockIdx.x, n1h = nt * tw1;
+  const int gi = u < n1h ? 0 : 1;
+  const int tau = gi == 0 ? u / tw1 : (u - n1h) / tw2, mt = gi == 0 ? u % tw1 : (u - n1h) % tw2;
+  const int e = tau < nt ? __ldcg(p.tile_expert + tau) : -1;
+  if (e < 0 || e >= p.num_experts) return;
+  const GemmSide& gs = p.g[gi];
+  const int KC = gs.K / 64, tw = gi == 0 ? tw1 : tw2;
+  const int nks = (KC + SPST - 1) / SPST;
+  const int a_row = e * gs.rows_w + mt * kWTile;
+  const uint8_t* wsf = gs.w_sf + ((size_t)e * tw + mt) * KC * kAtomBytes;
+  for (int ks = 0; ks < nks && ks < kHeadPrefetchStages; ++ks) {
+    const int kk = min(SPST, KC - SPST * ks);
+    for (int c = 0; 4 * c < kk; ++c)
+      tma_prefetch_l2_2d(gi == 0 ? &tmA1 : &tmA2, (ks * (SPST / 4) + c) * kStageRowBytes, a_row);
+    bulk_prefetch_l2(wsf + (size_t)SPST * ks * kAtomBytes, (uint32_t)kk * kAtomBytes);
+  }
+}
+
 template <int MODE, int TILE>
 __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
@@ -314,39 +345,30 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (!p.prefetch) {
-    pdl_wait();
-    if (tid == 0) pdl_trigger();
-  }
-  const int ntiles = __ldcg(p.totals);
   // weight tiles per route tile of each GEMM, and the units: GEMM1's, then GEMM2's
   const int tw1 = MODE != 2 ? p.g[0].rows_w / kWTile : 0;
   const int tw2 = MODE != 1 ? p.g[1].rows_w / kWTile : 0;
-  const int n1 = ntiles * tw1;
-  const int n_units = n1 + ntiles * tw2;
-  if ((int)blockIdx.x >= n_units) {
+  // Both GEMMs in one grid, launched before the previous kernel (the
+  // quantizer, or the fused routing + quantizer) has completed: the route
+  // tiles are read after the wait, which comes after the setup below.
+  const bool late = MODE == 3 && p.prefetch;
+  if (late && tid == 0) {
+    // Prefetch into L2 the weights and weight scales of the first stages of
+    // unit blockIdx.x (the first gridDim.x tickets are exactly units
+    // [0, gridDim.x), so whichever CTA draws a unit finds its first stages in
+    // L2). The routing read here is only a hint, bounded before use.
+    prefetch_head_hint<4 * chunks_for(TILE)>(tmA1, tmA2, p, tw1, tw2);
+  } else if (!p.prefetch) {
+    pdl_wait();
+    if (tid == 0) pdl_trigger();
+  }
+  const int ntiles_early = late ? 0 : __ldcg(p.totals);
+  if (!late && (int)blockIdx.x >= ntiles_early * (tw1 + tw2)) {
     // Even an idle CTA must not let this grid complete before its
     // predecessor: the kernels after it rely on that ordering.
     if (p.prefetch) pdl_wait();
     return;
   }
-  // unit u -> (GEMM 0 or 1, route tile, weight tile)
-  auto unit_of = [&](int u, int& gi, int& tau, int& mt) {
-    if constexpr (MODE != 2) {
-      if (MODE == 1 || u < n1) {
-        gi = 0;
-        tau = u / tw1;
-        mt = u % tw1;
-        return;
-      }
-    }
-    if constexpr (MODE != 1) {
-      gi = 1;
-      tau = (u - n1) / tw2;
-      mt = (u - n1) % tw2;
-    }
-  };
-
   constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, MODE == 2 ? 2 : 1);
   constexpr int NB = acc_bufs_for(TILE), CH = chunks_for(TILE), EPW = epi_warps_for(TILE);
   constexpr bool kRouteM = tile_cfg(TILE).route_m;
@@ -404,6 +426,32 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  if (late) {
+    // Units come from the ticket, so a CTA with none to do simply draws a
+    // ticket past the end and runs through to the teardown.
+    pdl_wait();
+    if (tid == 0) pdl_trigger();
+  }
+  const int ntiles = late ? __ldcg(p.totals) : ntiles_early;
+  const int n1 = ntiles * tw1;
+  const int n_units = n1 + ntiles * tw2;
+  // unit u -> (GEMM 0 or 1, route tile, weight tile)
+  auto unit_of = [&](int u, int& gi, int& tau, int& mt) {
+    if constexpr (MODE != 2) {
+      if (MODE == 1 || u < n1) {
+        gi = 0;
+        tau = u / tw1;
+        mt = u % tw1;
+        return;
+      }
+    }
+    if constexpr (MODE != 1) {
+      gi = 1;
+      tau = (u - n1) / tw2;
+      mt = (u - n1) % tw2;
+    }
+  };
+
   const uint32_t t_sfa = tmem + (uint32_t)(NB * tile_m);
   const uint32_t t_sfb = t_sfa + ST * 16 * CH;
 
@@ -437,31 +485,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         held = 0;
         waited = true;
       };
-      if constexpr (MODE == 3) {
-        // Units are drawn from a ticket (below), known only after the previous
-        // kernel has completed: with p.prefetch, first prefetch into L2 the
-        // weights and weight scales of the first stages of unit blockIdx.x
-        // (the first gridDim.x tickets are exactly units [0, gridDim.x), so
-        // whichever CTA draws a unit finds its first stages in L2).
-        if (p.prefetch) {
-          int gi, tau, mt;
-          unit_of(blockIdx.x, gi, tau, mt);
-          const GemmSide& gs = p.g[gi];
-          const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2, tw = gi == 0 ? tw1 : tw2;
-          const int e = __ldcg(p.tile_expert + tau);
-          const int a_row = e * gs.rows_w + mt * kWTile;
-          const uint8_t* wsf = gs.w_sf + ((size_t)e * tw + mt) * KC * kAtomBytes;
-          for (int ks = 0; ks < nks && ks < kHeadPrefetchStages; ++ks) {
-            const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
-            for (int c = 0; 4 * c < kk; ++c)
-              tma_prefetch_l2_2d(gi == 0 ? &tmA1 : &tmA2, (ks * CH + c) * kStageRowBytes, a_row);
-            bulk_prefetch_l2(wsf + (size_t)steps_per_stage * ks * kAtomBytes, (uint32_t)kk * kAtomBytes);
-          }
-          pdl_wait();
-          pdl_trigger();
-        }
-        waited = true;
-      }
+      // Units are drawn from a ticket (below), known only after the previous
+      // kernel has completed: the grid's prologue waited for it.
+      if constexpr (MODE == 3) waited = true;
       // MODE 3: the ticket this CTA holds next (drawn one unit ahead, so that
       // the atomic's latency overlaps the current unit's loads)
       int next = MODE == 3 ? atomicAdd(p.ticket, 1) : 0;
@@ -1066,6 +1092,8 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
   p.ss_wbn = ss_wbn;
   p.done = done;
   p.ticket = done + max_tiles;
+  p.num_experts = E;
+  p.max_tiles = max_tiles;
   p.status = status;
   p.tile_m = tile_m;
   if (launch_mode<3>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {

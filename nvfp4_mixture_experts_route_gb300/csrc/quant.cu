@@ -16,8 +16,13 @@
 // tile, so one bulk copy per pipeline stage brings every scale of the tile.
 #include "common.cuh"
 #include "layout.cuh"
+#include "route_small.cuh"
 
 namespace moe {
+
+// Routes up to which routing runs inside the input quantizer: every CTA
+// redoes it, so it must stay a few microseconds of one CTA's work.
+constexpr int kFusedMaxRoutes = 2048;
 
 __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, uint32_t& lo,
                                                  uint32_t& hi, uint32_t& sf_code) {
@@ -50,14 +55,15 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
 // block scale the codes, always finite e2m1 values, contribute exactly 0 to
 // every product, so padding-row codes are never written. The padding items
 // come first, then the token items. Reads x once; writes each route row once.
-__global__ void __launch_bounds__(256) quantize_permute_kernel(
+//
+// e2p and tile_row_limit may point to global or shared memory (the fused
+// routing + quantization kernel keeps its own copy of the routing there);
+// n_tiles is the number of route tiles in use.
+__device__ __forceinline__ void quantize_permute_items(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
-    const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
-    const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
-    const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
+    const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale, const int32_t* e2p,
+    const int32_t* tile_row_limit, int n_tiles, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done) {
-  pdl_wait();
-  pdl_trigger();
   // the per-tile GEMM1 completion counters and the unit ticket of the
   // one-launch expert GEMMs that follow
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_done; i += gridDim.x * blockDim.x) done[i] = 0;
@@ -70,7 +76,7 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
   const int nwarps = gridDim.x * (blockDim.x / 32);
   // Padding: one warp per (tile, group).
   {
-    const int n_pad = totals[0] * ng;
+    const int n_pad = n_tiles * ng;
     for (int w = warp0; w < n_pad; w += nwarps) {
       const int tau = w / ng, c = w - (w / ng) * ng;
       const int limit = tile_row_limit[tau];
@@ -140,6 +146,53 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
   }
 }
 
+__global__ void __launch_bounds__(256) quantize_permute_kernel(
+    const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
+    const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
+    const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
+    const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done) {
+  pdl_wait();
+  pdl_trigger();
+  quantize_permute_items(x, a_in, a_sf_in, gscale, e2p, tile_row_limit, totals[0], T, K, H, tile_m, codes, scales,
+                         done, n_done);
+}
+
+// Steps a2 and a1 in one kernel, for few routes (T*K <= kFusedMaxRoutes,
+// E <= 256): every CTA runs the single-CTA routing into its own shared
+// memory (a few microseconds of work, far less than a kernel boundary on
+// the step's critical path), CTA 0 also writes the routing metadata out,
+// and each CTA then quantizes its share of the items from its shared copy.
+// The results equal the routing kernel's followed by quantize_permute_kernel.
+// Shared memory: hist [8][E], e2p_s [T*K], limit_s [MT], totals_s [2].
+__global__ void __launch_bounds__(256) route_quantize_kernel(
+    const int32_t* __restrict__ topk_ids, int T, int K, int E, int tile_m, int P, int MT,
+    int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_offsets,
+    int32_t* __restrict__ expanded_to_permuted, int32_t* __restrict__ permuted_to_token,
+    int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row_limit, int32_t* __restrict__ totals,
+    const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in, const uint8_t* __restrict__ a_sf_in,
+    const float* __restrict__ gscale, int H, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+    int32_t* __restrict__ done, int32_t* status) {
+  extern __shared__ int32_t rq_smem[];
+  int32_t* hist = rq_smem;
+  int32_t* e2p_s = hist + 8 * E;
+  int32_t* limit_s = e2p_s + T * K;
+  int32_t* totals_s = limit_s + MT;
+  // the previous kernel in the stream may still read what CTA 0 writes
+  pdl_wait();
+  const bool writer = blockIdx.x == 0;
+  route_small<256>(topk_ids, T, K, E, tile_m, P, MT, hist, writer, expert_counts, expert_offsets,
+                   expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals, e2p_s, limit_s,
+                   totals_s, status);
+  // The GEMMs that follow read the route totals and tile table as a prefetch
+  // hint before they wait for this grid (and again, for their work, after):
+  // push CTA 0's copy out before this grid lets them launch.
+  if (writer) __threadfence();
+  pdl_trigger();
+  quantize_permute_items(x, a_in, a_sf_in, gscale, e2p_s, limit_s, totals_s[0], T, K, H, tile_m, codes, scales, done,
+                         MT + 1);
+}
+
 // Scale atoms <-> row-major scales [rows, K/16].
 __global__ void act_scales_io_kernel(int to_linear, uint8_t* __restrict__ atoms,
                                      uint8_t* __restrict__ linear, int rows, int K, int tile_m) {
@@ -179,6 +232,38 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
                        reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, e2p, tile_row_limit, totals,
                        T, K, H, tile_m, codes, scales, done, n_done);
+}
+
+size_t route_quantize_smem(int T, int K, int E, int MT) {
+  return sizeof(int32_t) * ((size_t)8 * E + (size_t)T * K + (size_t)MT + 2);
+}
+
+bool route_quantize_fits(int T, int K, int E) { return T * K <= kFusedMaxRoutes && E <= 256; }
+
+cudaError_t launch_route_quantize(const int32_t* topk_ids, int T, int K, int E, int tile_m, int P, int MT,
+                                  int32_t* counts, int32_t* offsets, int32_t* e2p, int32_t* p2t,
+                                  int32_t* tile_expert, int32_t* tile_row_limit, int32_t* totals, const void* x,
+                                  const void* a, const void* a_sf, const float* a1_gscale, int H, uint8_t* codes,
+                                  uint8_t* scales, int32_t* done, int32_t* status, cudaStream_t stream) {
+  // One CTA per SM at most: the routing is redone in every CTA, and fewer
+  // CTAs leave room beside them for the GEMM CTAs that launch early.
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+    sms = n;
+  }
+  const long long pad_threads = (long long)MT * (H / 64) * 32,
+                  tok_threads = (long long)T * ((H / 16 + 31) / 32) * 32;
+  int grid = grid_for(pad_threads > tok_threads ? pad_threads : tok_threads, 256);
+  if (grid > sms) grid = sms;
+  const size_t smem = route_quantize_smem(T, K, E, MT);
+  return launch_kernel(route_quantize_kernel, dim3(grid), dim3(256), smem, stream, true, topk_ids, T, K, E,
+                       tile_m, P, MT, counts, offsets, e2p, p2t, tile_expert, tile_row_limit, totals,
+                       reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
+                       reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, H, codes, scales, done, status);
 }
 
 cudaError_t launch_act_scales_io(int to_linear, uint8_t* atoms, uint8_t* linear, int K,

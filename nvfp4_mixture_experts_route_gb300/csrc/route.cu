@@ -15,15 +15,13 @@
 // expert. Pass 2 walks the segment again and hands out rows in order (rank
 // inside the chunk = peers below the lane).
 #include "common.cuh"
+#include "route_small.cuh"
 
 namespace moe {
 
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
-// NT threads (E <= NT): 1024 in general, 256 for few routes and experts,
-// where the per-expert scans over the warps and the block barriers are the
-// latency.
 template <int NT>
 __global__ void __launch_bounds__(NT, 1)
     route_permute_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int tile_m,
@@ -33,112 +31,13 @@ __global__ void __launch_bounds__(NT, 1)
                          int32_t* __restrict__ permuted_to_token, int32_t* __restrict__ tile_expert,
                          int32_t* __restrict__ tile_row_limit, int32_t* __restrict__ totals,
                          int32_t* status) {
-  constexpr int NW = NT / 32;
-  extern __shared__ int32_t hist[];  // [NW][E]
-  __shared__ int32_t warp_sums[NW];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ int32_t hist[];  // [NT/32][E]
   // Launched in plain stream order; the kernels after it wait for it to
   // complete before they read what it writes.
   pdl_trigger();
-  const int R = T * K;
-  const int seg = (R + NW - 1) / NW;
-  const int beg = min(R, warp * seg), end = min(R, beg + seg);
-
-  for (int i = tid; i < NW * E; i += NT) hist[i] = 0;
-  for (int i = tid; i < P; i += NT) permuted_to_token[i] = -1;
-  for (int i = tid; i < MT; i += NT) {
-    tile_expert[i] = -1;
-    tile_row_limit[i] = -1;
-  }
-  __syncthreads();
-
-  // Pass 1: warp-private histogram.
-  int32_t* my = hist + warp * E;
-  bool bad = false;
-  for (int base = beg; base < end; base += 32) {
-    const int j = base + lane;
-    int e = (j < end) ? topk_ids[j] : -1;
-    if (e < -1 || e >= E) {
-      bad = true;
-      e = -1;
-    }
-    // Lanes without a route get a key no expert uses, unique per lane.
-    const int key = (e >= 0) ? e : -2 - lane;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-    __syncwarp();
-  }
-  if (bad) record_status(status, MOE_ERR_INVALID_ROUTE);
-  __syncthreads();
-
-  // Per expert: scan over warps (warp-relative starts) and the padded count.
-  int padded = 0, count = 0;
-  if (tid < E) {
-    for (int w = 0; w < NW; ++w) {
-      const int c = hist[w * E + tid];
-      hist[w * E + tid] = count;
-      count += c;
-    }
-    padded = (count + tile_m - 1) / tile_m * tile_m;
-  }
-  // Block-wide exclusive scan of padded over the experts (E <= 1024).
-  int incl = padded;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int s = lane < NW ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, s, d);
-      if (lane >= d) s += v;
-    }
-    if (lane < NW) warp_sums[lane] = s;  // inclusive over warps
-  }
-  __syncthreads();
-  const int offset = incl - padded + (warp > 0 ? warp_sums[warp - 1] : 0);
-  const int total = warp_sums[NW - 1];
-  if (tid < E) {
-    expert_counts[tid] = count;
-    expert_offsets[tid] = offset;
-    for (int w = 0; w < NW; ++w) hist[w * E + tid] += offset;
-    // Tiles of this expert: [offset/tile_m, (offset+padded)/tile_m).
-    const int t0 = offset / tile_m, nt = padded / tile_m;
-    for (int i = 0; i < nt; ++i) {
-      tile_expert[t0 + i] = tid;
-      tile_row_limit[t0 + i] = offset + count;
-    }
-  }
-  if (tid == 0) {
-    expert_offsets[E] = total;
-    totals[0] = total / tile_m;
-    totals[1] = total;
-  }
-  __syncthreads();
-
-  // Pass 2: hand out rows in ascending j.
-  for (int base = beg; base < end; base += 32) {
-    const int j = base + lane;
-    int e = (j < end) ? topk_ids[j] : -1;
-    if (e < -1 || e >= E) e = -1;
-    const int key = (e >= 0) ? e : -2 - lane;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (e >= 0) {
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int p = my[e] + rank;
-      expanded_to_permuted[j] = p;
-      permuted_to_token[p] = j / K;
-    } else if (j < end) {
-      expanded_to_permuted[j] = -1;
-    }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-    __syncwarp();
-  }
+  route_small<NT>(topk_ids, T, K, E, tile_m, P, MT, hist, true, expert_counts, expert_offsets,
+                  expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals, nullptr, nullptr,
+                  nullptr, status);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,9 +1,9 @@
 """The routed NVFP4 expert block as one object over the C ABI.
 
 ``NvFp4MoE`` holds one layer's prepared weights and scalars on the device and
-runs the four entry points in order on the current stream: routing metadata,
-the expert body (input quantization, GEMM1 + SwiGLU + requant, GEMM2), and
-the post-expert finalize. It only allocates (once, then reuses) and passes
+runs the entry points in order on the current stream: routing metadata and
+the expert body (input quantization, GEMM1 + SwiGLU + requant, GEMM2) in one
+call, then the post-expert finalize. It only allocates (once, then reuses) and passes
 pointers; the work is the library's.
 """
 from __future__ import annotations
@@ -23,7 +23,7 @@ class NvFp4MoE:
         ``fused_norm``: GEMM2's epilogue also writes the rows' sums of squares
         and the finalize streams the rows once (moe_nvfp4_experts_sumsq and
         moe_post_expert_finalize_sumsq); otherwise (the default, faster on
-        GB300 at every measured batch size) the plain pair moe_nvfp4_experts
+        GB300 at every measured batch size) the plain pair moe_nvfp4_experts_routed
         and moe_post_expert_finalize."""
         dev = torch.device(device)
         t = {k: torch.as_tensor(raw[k]).to(dev) for k in ("w13", "w13_sf", "w2", "w2_sf")}
@@ -72,9 +72,9 @@ class NvFp4MoE:
         T, K = topk_ids.shape
         b = self.buffers(T, K)
         st = b["status"] if status is None else status
-        B.route_permute(topk_ids, self.E, self.tile_m, route=b["route"], status=st)
         o = b["out"] if out is None else out
         if self.fused_norm:
+            B.route_permute(topk_ids, self.E, self.tile_m, route=b["route"], status=st)
             B.nvfp4_experts_sumsq(self.weights, b["route"], x=x, a1_gscale=self.a1_gscale,
                                   a2_gscale=self.a2_gscale, T=T, H=self.H, I=self.I, E=self.E, K=K,
                                   gamma=self.gamma, weight_before_norm=self.weight_before_norm,
@@ -82,8 +82,11 @@ class NvFp4MoE:
             B.post_expert_finalize_sumsq(b["rows"], b["row_sumsq"], b["route"].expanded_to_permuted, topk_weights,
                                          self.gamma, self.eps, out=o, status=st)
             return o, b
-        B.nvfp4_experts(self.weights, b["route"], x=x, a1_gscale=self.a1_gscale, a2_gscale=self.a2_gscale,
-                        T=T, H=self.H, I=self.I, E=self.E, K=K, gemm2_rows=b["rows"], ws=b["ws"], status=st)
+        # routing and the expert body in one call (for few routes the routing
+        # runs inside the input quantizer)
+        B.nvfp4_experts_routed(self.weights, topk_ids, b["route"], x=x, a1_gscale=self.a1_gscale,
+                               a2_gscale=self.a2_gscale, H=self.H, I=self.I, E=self.E, gemm2_rows=b["rows"],
+                               ws=b["ws"], status=st)
         B.post_expert_finalize(b["rows"], b["route"].expanded_to_permuted, topk_weights, self.gamma, self.eps,
                                self.weight_before_norm, out=o, status=st)
         return o, b

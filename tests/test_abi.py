@@ -84,6 +84,17 @@ def test_null_pointers_refused_before_any_launch(lib):
     # undersized workspace
     rc = lib.moe_experts_gemm2(C.byref(w), C.byref(r), 4, 256, 128, 8, 2, 32, 16, 1024, 16, None, None)
     assert rc == -3
+    # the routed entry (routing inside the quantizer at these sizes): null
+    # routing buffers, then an undersized workspace
+    rc = lib.moe_nvfp4_experts_routed(C.byref(w), 16, 16, None, None, 16, 16, 4, 256, 128, 8, 2, 32, None, 16, 16,
+                                      16, 16, 16, 16, 16, 1024, 1 << 20, None, None)
+    assert rc == -1 and b"null" in lib.moe_last_error()
+    rc = lib.moe_nvfp4_experts_routed(C.byref(w), 16, 16, None, None, 16, 16, 4, 256, 128, 8, 2, 32, 16, 16, 16,
+                                      16, 16, 16, 16, 16, 1024, 16, None, None)
+    assert rc == -3
+    rc = lib.moe_nvfp4_experts_routed(C.byref(B.MoeWeights()), 16, 16, None, None, 16, 16, 4, 256, 128, 8, 2, 32,
+                                      16, 16, 16, 16, 16, 16, 16, 16, 1024, 1 << 20, None, None)
+    assert rc == -1
 
 
 def test_experts_kernel_count():
@@ -102,6 +113,22 @@ def test_route_kernel_count():
     assert B.route_kernels(8192, 8, 128) == 3
     assert B.route_kernels(0, 8, 128) == 1
     assert B.route_kernels(2047, 2, 1024) == 1   # 4094 routes: one segment
+
+
+def test_routed_experts_kernel_count():
+    """Routing runs inside the input quantizer (2 kernels in all) for at most
+    2048 routes, at most 256 experts and tile_m <= 64; otherwise the routing
+    kernels come first, then the body's kernels (none when nothing routes)."""
+    assert B.routed_experts_kernels(8, 8, 128, 32) == 2
+    assert B.routed_experts_kernels(64, 8, 128, 32) == 2
+    assert B.routed_experts_kernels(256, 8, 128, 64) == 2    # 2048 routes
+    assert B.routed_experts_kernels(257, 8, 128, 32) == 1 + 2
+    assert B.routed_experts_kernels(8, 8, 300, 32) == 1 + 2  # E > 256
+    assert B.routed_experts_kernels(8, 8, 128, 128) == 1 + 3
+    assert B.routed_experts_kernels(8192, 8, 128, 128) == 3 + 3
+    assert B.routed_experts_kernels(0, 8, 128, 32) == 1
+    with pytest.raises(B.MoeError):
+        B.routed_experts_kernels(8, 8, 128, 48)
 
 
 def test_selftest_arguments_refused_before_launch(lib):

@@ -171,6 +171,93 @@ def test_fused_gemms_match_split_gemms(small_cases, idx):
         assert np.array_equal(rows, split["rows"])
 
 
+ROUTED_EXTRA = [
+    # (T, H, I, E, K, routing, tile, a1, a2)
+    (256, 256, 128, 16, 8, "uniform", 32, 4.0, 1e-3),   # T*K = 2048: most routes routed in the quantizer
+    (257, 256, 128, 16, 8, "uniform", 32, 4.0, 1e-3),   # T*K = 2056: the routing kernels, then the body
+    (5, 256, 128, 200, 4, "zipf", 64, 4.0, 1e-3),       # E = 200: 8 warps x E histogram, few routes
+    (3, 256, 128, 300, 2, "uniform", 32, 4.0, 1e-3),    # E > 256: the routing kernels, then the body
+]
+
+_ROUTE_FIELDS = ("expert_counts", "expert_offsets", "expanded_to_permuted", "permuted_to_token", "tile_expert",
+                 "tile_row_limit", "totals")
+
+
+def _routed_vs_split(prep, ids_np, x_bits, tile, a1, a2):
+    """(status, route, rows) of route_permute + nvfp4_experts and of
+    nvfp4_experts_routed (called twice on the same buffers)."""
+    E, H, I = prep.E, prep.H, prep.I
+    ids = _dev(ids_np.astype(np.int32))
+    T, K = ids.shape
+    x = bf16_dev(x_bits)
+    g1 = torch.tensor([a1], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([a2], dtype=torch.float32, device=DEV)
+    st_a = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r_a = B.route_permute(ids, E, tile, status=st_a)
+    rows_a, _ = B.nvfp4_experts(prep.w, r_a, x=x, a1_gscale=g1, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K, status=st_a)
+    st_b = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r_b = B.alloc_route(T, K, E, tile, DEV)
+    for f in _ROUTE_FIELDS:  # what the call must overwrite
+        getattr(r_b, f).fill_(12345)
+    ws = B.alloc_workspace(T, K, E, H, I, tile, DEV)
+    outs = []
+    for _ in range(2):
+        rows_b = torch.zeros_like(rows_a)
+        B.nvfp4_experts_routed(prep.w, ids, r_b, x=x, a1_gscale=g1, a2_gscale=g2, H=H, I=I, E=E, gemm2_rows=rows_b,
+                               ws=ws, status=st_b)
+        outs.append(rows_b)
+    torch.cuda.synchronize()
+    return (int(st_a.item()), r_a, rows_a), (int(st_b.item()), r_b, outs)
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL) + len(ROUTED_EXTRA)))
+def test_routed_entry_matches_route_then_experts(small_cases, idx):
+    """moe_nvfp4_experts_routed writes moe_route_permute's metadata bit for
+    bit and moe_nvfp4_experts's GEMM2 rows (every row that carries a route)
+    on that route, whether the routing ran inside the input quantizer (few
+    routes, tile_m <= 64: 2 kernels) or as its own kernels before the body,
+    and again on a second call over the same buffers."""
+    if idx < len(SMALL):
+        w, raw, batch, tile, a1, a2 = small_cases[idx]
+    else:
+        T, H, I, E, K, routing, tile, a1, a2 = ROUTED_EXTRA[idx - len(SMALL)]
+        w = _workload(T, H, I, E, K, routing, tile)
+        raw, batch = inputs.make_layer(w), inputs.make_batch(w)
+    prep = Prepared(raw)
+    fused = w.T * w.K <= 2048 and w.E <= 256 and tile <= 64
+    want_kernels = 2 if fused else B.route_kernels(w.T, w.K, w.E) + B.experts_kernels(tile)
+    assert B.routed_experts_kernels(w.T, w.K, w.E, tile) == want_kernels
+    (st_a, r_a, rows_a), (st_b, r_b, outs) = _routed_vs_split(prep, batch["topk_ids"], batch["x"], tile, a1, a2)
+    assert st_a == 0 and st_b == 0
+    for f in _ROUTE_FIELDS:
+        assert torch.equal(getattr(r_a, f), getattr(r_b, f)), f
+    live = r_a.expanded_to_permuted.reshape(-1)
+    live = live[live >= 0]
+    for rows_b in outs:
+        assert torch.equal(rows_b[live], rows_a[live])
+
+
+def test_routed_entry_unrouted_and_bad_ids(small_cases):
+    """Routes marked -1 are skipped and an id out of range is skipped and
+    reported (MOE_ERR_INVALID_ROUTE), by the routing inside the quantizer as
+    by moe_route_permute; the rows of the other routes agree bit for bit."""
+    w, raw, batch, tile, a1, a2 = small_cases[1]
+    assert w.T * w.K <= 2048 and tile <= 64
+    ids = batch["topk_ids"].copy()
+    ids[::3, 0] = -1
+    ids[1, 1] = w.E
+    prep = Prepared(raw)
+    (st_a, r_a, rows_a), (st_b, r_b, outs) = _routed_vs_split(prep, ids, batch["x"], tile, a1, a2)
+    assert st_a == -6 and st_b == -6
+    for f in _ROUTE_FIELDS:
+        assert torch.equal(getattr(r_a, f), getattr(r_b, f)), f
+    live = r_a.expanded_to_permuted.reshape(-1)
+    live = live[live >= 0]
+    assert len(live) == w.T * w.K - len(ids[::3]) - 1
+    for rows_b in outs:
+        assert torch.equal(rows_b[live], rows_a[live])
+
+
 def test_fused_gemms_finish_while_other_work_holds_most_sms():
     """The one-launch GEMMs hand their units out by ticket to running CTAs
     only, so a GEMM2 unit never waits for a GEMM1 unit that no running CTA
@@ -400,6 +487,25 @@ def test_decode_b8_full_size(full, record_property):
     err2 = rel_l2(same["rows"][e2p], ref["routes"]["rows_bf16"])
     record_property("gemm2_rel_l2", err2)
     assert err2 < GEMM2_BAR
+
+
+@pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf"])
+def test_routed_entry_full_size(full, name):
+    """At full size (H = 5120, I = 2048, E = 128, K = 8) the routing inside
+    the input quantizer gives moe_route_permute's metadata and the split
+    path's GEMM2 rows bit for bit."""
+    raw, prep = full
+    w = inputs.WORKLOADS[name]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    assert B.routed_experts_kernels(w.T, w.K, w.E, w.tile_m) == 2
+    (st_a, r_a, rows_a), (st_b, r_b, outs) = _routed_vs_split(prep, batch["topk_ids"], batch["x"], w.tile_m, a1, a2)
+    assert st_a == 0 and st_b == 0
+    for f in _ROUTE_FIELDS:
+        assert torch.equal(getattr(r_a, f), getattr(r_b, f)), f
+    live = r_a.expanded_to_permuted.reshape(-1)
+    for rows_b in outs:
+        assert torch.equal(rows_b[live], rows_a[live])
 
 
 def test_expert_tp_identity(full, record_property):
