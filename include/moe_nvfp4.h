@@ -234,13 +234,46 @@ int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids,
  * status for invalid ones). */
 int moe_routed_experts_kernels(int T, int K, int E, int tile_m);
 
+/* The whole routed expert block in one call: routing, the expert body with
+ * the post-expert norm's sums of squares fused into GEMM2's epilogue
+ * (moe_nvfp4_experts_sumsq), and the finalize from those sums
+ * (moe_post_expert_finalize_sumsq): out bf16 [T, H]. The result equals, bit
+ * for bit, moe_route_permute, then moe_nvfp4_experts_sumsq, then
+ * moe_post_expert_finalize_sumsq on the same buffers (the routing buffers,
+ * gemm2_rows and row_sumsq [max_padded_rows, H/32] fp32 hold what those
+ * calls leave). With few routes (T*K <= 2048, E <= 256), tile_m <= 64 and
+ * K <= 8 it is 2 kernels: the routing inside the input quantizer, then one
+ * persistent launch of both GEMMs whose last units are the finalize, one per
+ * (token, column slice), each started as soon as every GEMM2 tile of its
+ * token's routes has stored its rows; otherwise the routing kernels, the
+ * expert body and the finalize kernel (moe_moe_block_kernels). topk_weights
+ * fp32 [T, K]; gamma bf16 [H] (zero-centred gain, 16-byte aligned), eps,
+ * weight_before_norm as for moe_post_expert_finalize; out 16-byte aligned;
+ * the rest as for moe_nvfp4_experts_routed. */
+int moe_nvfp4_moe_block(const moe_weights* w, const int32_t* topk_ids,
+                        const float* topk_weights, const void* x, const void* a,
+                        const void* a_sf, const float* a1_gscale,
+                        const float* a2_gscale, const void* gamma, float eps,
+                        int weight_before_norm, int T, int H, int I, int E,
+                        int K, int tile_m, int32_t* expert_counts,
+                        int32_t* expert_offsets, int32_t* expanded_to_permuted,
+                        int32_t* permuted_to_token, int32_t* tile_expert,
+                        int32_t* tile_row_limit, int32_t* totals,
+                        void* gemm2_rows, float* row_sumsq, void* out,
+                        void* ws, size_t ws_bytes, int32_t* status,
+                        void* stream);
+
+/* Kernels moe_nvfp4_moe_block enqueues for these sizes (a negative status
+ * for invalid ones). */
+int moe_moe_block_kernels(int T, int K, int E, int tile_m);
+
 /* moe_nvfp4_experts with the first half of the post-expert norm fused into
  * GEMM2's epilogue: besides the bf16 rows it writes, for every route row,
  * the sums of squares of its stored values over each 32 columns,
  *   row_sumsq[p][c] = sum_{j < 32} (g[32c + j] * rows[p][32c + j])^2
  * with g = 1 + float(gamma) when weight_before_norm != 0 (the weight applied
  * before the norm) and g = 1 otherwise. row_sumsq: fp32
- * [max_padded_rows, H/32], 8-byte aligned; only the rows GEMM2 writes get
+ * [max_padded_rows, H/32], 16-byte aligned; only the rows GEMM2 writes get
  * values. gamma: bf16 [H], 16-byte aligned (may be NULL with
  * weight_before_norm = 0). moe_post_expert_finalize_sumsq then finalizes
  * from it without a reduction pass over the rows. Everything else as
@@ -377,8 +410,8 @@ int moe_post_expert_finalize(const void* rows, int num_rows,
  *   out[t] = bf16( g * sum_k coef_k * rows[p(t,k)] ),  g = 1 + float(gamma),
  * equal to moe_post_expert_finalize in the reading row_sumsq was made with,
  * up to the order of the fp32 sums. rows bf16 [num_rows, H], row_sumsq fp32
- * [num_rows, H/32]; H % 32 == 0, H <= 16384, K <= 64; the row bound and
- * status word as for moe_post_expert_finalize. */
+ * [num_rows, H/32], both 16-byte aligned; H % 128 == 0, H <= 16384,
+ * K <= 64; the row bound and status word as for moe_post_expert_finalize. */
 int moe_post_expert_finalize_sumsq(const void* rows, const float* row_sumsq,
                                    int num_rows,
                                    const int32_t* expanded_to_permuted,

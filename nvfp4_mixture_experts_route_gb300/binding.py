@@ -80,6 +80,12 @@ _SIGNATURES = {
         _I,
     ),
     "moe_routed_experts_kernels": ([_I, _I, _I, _I], _I),
+    "moe_nvfp4_moe_block": (
+        [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, _P, _P, _P, C.c_float, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
+         _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, _P],
+        _I,
+    ),
+    "moe_moe_block_kernels": ([_I, _I, _I, _I], _I),
     "moe_nvfp4_experts_sumsq": (
         [C.POINTER(MoeWeights), _P, _P, _P, _P, _P, C.POINTER(MoeRoute), _I, _I, _I, _I, _I, _I, _P, _P, _I, _P,
          _P, C.c_size_t, _P, _P],
@@ -232,6 +238,15 @@ def routed_experts_kernels(T: int, K: int, E: int, tile_m: int) -> int:
     return n
 
 
+def moe_block_kernels(T: int, K: int, E: int, tile_m: int) -> int:
+    """Kernels moe_block launches for these sizes (2 when routing runs inside
+    the input quantizer and the finalize inside the GEMMs' launch)."""
+    n = load().moe_moe_block_kernels(T, K, E, tile_m)
+    if n < 0:
+        _check(n)
+    return n
+
+
 def route_sizes(T: int, K: int, E: int, tile_m: int) -> tuple[int, int]:
     P, MT = C.c_int(), C.c_int()
     _check(load().moe_route_sizes(T, K, E, tile_m, C.byref(P), C.byref(MT)))
@@ -318,6 +333,35 @@ def nvfp4_experts_routed(w: MoeWeights, topk_ids, route: Route, *, x=None, a=Non
         _ptr(route.permuted_to_token), _ptr(route.tile_expert), _ptr(route.tile_row_limit), _ptr(route.totals),
         _ptr(gemm2_rows), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
     return gemm2_rows, ws
+
+
+def moe_block(w: MoeWeights, topk_ids, topk_weights, route: Route, *, x=None, a=None, a_sf=None, a1_gscale,
+              a2_gscale, gamma, eps: float, weight_before_norm: bool = True, H, I, E, gemm2_rows=None,
+              row_sumsq=None, out=None, ws=None, status=None, stream=None):
+    """moe_nvfp4_moe_block: routing into `route`, the expert body with the
+    sums of squares fused into GEMM2 and the finalize, in one call. Returns
+    (out, gemm2_rows, row_sumsq, ws)."""
+    import torch
+
+    T, K = topk_ids.shape
+    tile_m = route.tile_m
+    P, _ = route_sizes(T, K, E, tile_m)
+    dev = route.totals.device
+    if gemm2_rows is None:
+        gemm2_rows = torch.empty((max(P, 1), H), dtype=torch.bfloat16, device=dev)
+    if row_sumsq is None:
+        row_sumsq = torch.empty((max(P, 1), H // 32), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = alloc_workspace(T, K, E, H, I, tile_m, dev)
+    _check(load().moe_nvfp4_moe_block(
+        C.byref(w), _ptr(topk_ids), _ptr(topk_weights), _ptr(x), _ptr(a), _ptr(a_sf), _ptr(a1_gscale),
+        _ptr(a2_gscale), _ptr(gamma), float(eps), 1 if weight_before_norm else 0, T, H, I, E, K, tile_m,
+        _ptr(route.expert_counts), _ptr(route.expert_offsets), _ptr(route.expanded_to_permuted),
+        _ptr(route.permuted_to_token), _ptr(route.tile_expert), _ptr(route.tile_row_limit), _ptr(route.totals),
+        _ptr(gemm2_rows), _ptr(row_sumsq), _ptr(out), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return out, gemm2_rows, row_sumsq, ws
 
 
 def nvfp4_experts(w: MoeWeights, route: Route, *, x=None, a=None, a_sf=None, a1_gscale, a2_gscale,

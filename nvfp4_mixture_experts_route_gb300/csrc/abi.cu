@@ -44,7 +44,8 @@ int launch_gemm2(const void*, const void*, const float*, const int32_t*, const i
 int launch_gemms_fused(const void*, const void*, const float*, const float*, const float*, const void*,
                        const void*, const float*, const int32_t*, const int32_t*, const int32_t*,
                        const uint8_t*, const uint8_t*, uint8_t*, uint8_t*, void*, float*, const void*, int,
-                       int32_t*, int, int, int, int, int, int, int32_t*, cudaStream_t, bool, const char**);
+                       int32_t*, int, int, int, int, int, int, const int32_t*, const float*, const void*, float,
+                       void*, int, int, int32_t*, cudaStream_t, bool, const char**);
 cudaError_t launch_finalize_sumsq(const void*, const float*, int, const int32_t*, const float*, const void*,
                                   float, int, int, int, void*, int32_t*, cudaStream_t);
 int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
@@ -100,6 +101,10 @@ int route_dims(int T, int K, int E, int tile_m, RouteDims* d) {
 
 // Workspace of the expert body: permuted NVFP4 activations and the quantized
 // intermediate (codes row-major, scales as per-tile atoms; see quant.cu).
+// Counters after the per-route-tile ones: the unit ticket, the GEMM2
+// completion count and the finalize ticket, 128 bytes apart.
+constexpr int kDoneExtra = 65;
+
 struct WsLayout {
   size_t a_codes = 0, a_sf = 0, h_codes = 0, h_sf = 0, done = 0, total = 0;
   int P = 0, MT = 0;
@@ -124,9 +129,10 @@ int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
   w->h_sf = off;
   off = round_up(off + (size_t)d.MT * (I / 64) * S * moe::kAtomBytes, 1024);
   // per route tile: GEMM1 completions the fused GEMM2 units wait for, then
-  // the fused GEMMs' unit ticket
+  // the fused GEMMs' unit ticket, the GEMM2 completion count (at MT + 32) and
+  // the ticket of the fused finalize units (at MT + 64)
   w->done = off;
-  off = round_up(off + (size_t)(d.MT + 1) * sizeof(int32_t), 1024);
+  off = round_up(off + (size_t)(d.MT + kDoneExtra) * sizeof(int32_t), 1024);
   w->total = off;
   return MOE_OK;
 }
@@ -283,7 +289,7 @@ int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const f
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   cudaError_t err = moe::launch_quantize_permute(
       x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, r->expanded_to_permuted, r->tile_row_limit,
-      r->totals, T, K, H, tile_m, L.P, L.MT + 1, base + L.a_codes, base + L.a_sf,
+      r->totals, T, K, H, tile_m, L.P, L.MT + kDoneExtra, base + L.a_codes, base + L.a_sf,
       reinterpret_cast<int32_t*>(base + L.done), as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
 }
@@ -324,6 +330,17 @@ struct SumSq {
   int wbn = 0;
 };
 
+// The post-expert finalize as the one-launch GEMMs' last units (with the
+// sums of squares above): out set.
+struct FusedFin {
+  const int32_t* e2p = nullptr;
+  const float* w = nullptr;
+  const void* gamma = nullptr;
+  float eps = 0.f;
+  void* out = nullptr;
+  int T = 0, K = 0;
+};
+
 static int experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E,
                          int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
                          int32_t* status, void* stream, bool pdl, SumSq ss = SumSq()) {
@@ -355,7 +372,8 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, in
 // moe_nvfp4_experts).
 static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
                          int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
-                         int32_t* status, void* stream, bool pdl, bool zero_counters, SumSq ss = SumSq()) {
+                         int32_t* status, void* stream, bool pdl, bool zero_counters, SumSq ss = SumSq(),
+                         FusedFin fin = FusedFin()) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -369,7 +387,7 @@ static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   if (zero_counters) {
     const cudaError_t err =
-        cudaMemsetAsync(base + L.done, 0, (size_t)(L.MT + 1) * sizeof(int32_t), as_stream(stream));
+        cudaMemsetAsync(base + L.done, 0, (size_t)(L.MT + kDoneExtra) * sizeof(int32_t), as_stream(stream));
     if (err != cudaSuccess) return cuda_fail(err, "moe_experts_gemms");
   }
   const char* why = "";
@@ -377,7 +395,8 @@ static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe
                                w->g2_alphas, r->tile_expert, r->tile_row_limit, r->totals,
                                base + L.a_codes, base + L.a_sf, base + L.h_codes, base + L.h_sf, gemm2_rows,
                                ss.row_ss, ss.gamma, ss.wbn, reinterpret_cast<int32_t*>(base + L.done), E, H, I,
-                               tile_m, L.P, L.MT, status, as_stream(stream), pdl, &why);
+                               tile_m, L.P, L.MT, fin.e2p, fin.w, fin.gamma, fin.eps, fin.out, fin.T, fin.K, status,
+                               as_stream(stream), pdl, &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
 }
 
@@ -416,7 +435,7 @@ static int experts_body(const moe_weights* w, const void* x, const void* a, cons
 
 // The sums-of-squares arguments of the *_sumsq entry points, checked.
 static int sumsq_args(const void* gamma, int weight_before_norm, float* row_sumsq, SumSq* ss) {
-  if (!row_sumsq || !aligned(row_sumsq, 8)) return fail(MOE_ERR_INVALID_ARG, "row_sumsq must be 8-byte aligned");
+  if (!row_sumsq || !aligned(row_sumsq, 16)) return fail(MOE_ERR_INVALID_ARG, "row_sumsq must be 16-byte aligned");
   if (weight_before_norm && (!gamma || !aligned(gamma, 16)))
     return fail(MOE_ERR_INVALID_ARG, "gamma must be given, 16-byte aligned, with weight_before_norm");
   ss->row_ss = row_sumsq;
@@ -469,12 +488,16 @@ int moe_routed_experts_kernels(int T, int K, int E, int tile_m) {
   return moe::route_kernel_count(T, K, E) + (d.P > 0 ? moe_experts_kernels(tile_m) : 0);
 }
 
-int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
-                             const void* a_sf, const float* a1_gscale, const float* a2_gscale, int T, int H,
-                             int I, int E, int K, int tile_m, int32_t* expert_counts, int32_t* expert_offsets,
-                             int32_t* expanded_to_permuted, int32_t* permuted_to_token, int32_t* tile_expert,
-                             int32_t* tile_row_limit, int32_t* totals, void* gemm2_rows, void* ws,
-                             size_t ws_bytes, int32_t* status, void* stream) {
+// The body of the routed entry points: routing inside the quantizer when
+// routed_fused, else the routing kernels then experts_body. ss / fin: the
+// sums of squares and the finalize units of the one-launch GEMMs (fin only
+// on the fused path; the caller checked their pointers).
+static int routed_body(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
+                       const void* a_sf, const float* a1_gscale, const float* a2_gscale, int T, int H, int I,
+                       int E, int K, int tile_m, int32_t* expert_counts, int32_t* expert_offsets,
+                       int32_t* expanded_to_permuted, int32_t* permuted_to_token, int32_t* tile_expert,
+                       int32_t* tile_row_limit, int32_t* totals, void* gemm2_rows, void* ws, size_t ws_bytes,
+                       int32_t* status, void* stream, SumSq ss, FusedFin fin) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc || (rc = check_weights(w, true)) || (rc = check_weights(w, false))) return rc;
@@ -483,8 +506,8 @@ int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, cons
     rc = moe_route_permute(topk_ids, T, K, E, tile_m, expert_counts, expert_offsets, expanded_to_permuted,
                            permuted_to_token, tile_expert, tile_row_limit, totals, status, stream);
     if (rc) return rc;
-    return moe_nvfp4_experts(w, x, a, a_sf, a1_gscale, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws,
-                             ws_bytes, status, stream);
+    return experts_body(w, x, a, a_sf, a1_gscale, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes,
+                        status, stream, ss);
   }
   if (!expert_counts || !expert_offsets || !topk_ids || !expanded_to_permuted || !permuted_to_token ||
       !tile_expert || !tile_row_limit || !totals)
@@ -506,9 +529,67 @@ int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, cons
       topk_ids, T, K, E, tile_m, L.P, L.MT, expert_counts, expert_offsets, expanded_to_permuted, permuted_to_token,
       tile_expert, tile_row_limit, totals, x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, H, base + L.a_codes,
       base + L.a_sf, reinterpret_cast<int32_t*>(base + L.done), status, as_stream(stream));
-  if (err != cudaSuccess) return cuda_fail(err, "moe_nvfp4_experts_routed");
+  if (err != cudaSuccess) return cuda_fail(err, "routing + input quantization");
   return experts_fused(w, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true,
-                       false);
+                       false, ss, fin);
+}
+
+int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
+                             const void* a_sf, const float* a1_gscale, const float* a2_gscale, int T, int H,
+                             int I, int E, int K, int tile_m, int32_t* expert_counts, int32_t* expert_offsets,
+                             int32_t* expanded_to_permuted, int32_t* permuted_to_token, int32_t* tile_expert,
+                             int32_t* tile_row_limit, int32_t* totals, void* gemm2_rows, void* ws,
+                             size_t ws_bytes, int32_t* status, void* stream) {
+  return routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
+                     expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
+                     gemm2_rows, ws, ws_bytes, status, stream, SumSq(), FusedFin());
+}
+
+// The whole block: the finalize runs as the one-launch GEMMs' last units
+// where routing runs inside the quantizer and K fits the finalize units.
+static bool block_fused(int T, int K, int E, int tile_m) { return routed_fused(T, K, E, tile_m) && K <= 8; }
+
+int moe_moe_block_kernels(int T, int K, int E, int tile_m) {
+  const int n = moe_routed_experts_kernels(T, K, E, tile_m);
+  if (n < 0) return n;
+  return block_fused(T, K, E, tile_m) ? n : n + (T > 0 ? 1 : 0);
+}
+
+int moe_nvfp4_moe_block(const moe_weights* w, const int32_t* topk_ids, const float* topk_weights, const void* x,
+                        const void* a, const void* a_sf, const float* a1_gscale, const float* a2_gscale,
+                        const void* gamma, float eps, int weight_before_norm, int T, int H, int I, int E, int K,
+                        int tile_m, int32_t* expert_counts, int32_t* expert_offsets, int32_t* expanded_to_permuted,
+                        int32_t* permuted_to_token, int32_t* tile_expert, int32_t* tile_row_limit,
+                        int32_t* totals, void* gemm2_rows, float* row_sumsq, void* out, void* ws, size_t ws_bytes,
+                        int32_t* status, void* stream) {
+  WsLayout L;
+  int rc = ws_layout(T, K, E, H, I, tile_m, &L);
+  if (rc) return rc;
+  if (H > 16384) return fail(MOE_ERR_UNSUPPORTED, "hidden %d above 16384", H);
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  if (T > 0 && (!topk_weights || !gamma || !out || !aligned(gamma, 16) || !aligned(out, 16)))
+    return fail(MOE_ERR_INVALID_ARG, "topk_weights, gamma and out must be given; gamma and out 16-byte aligned");
+  SumSq ss;
+  if ((rc = sumsq_args(gamma, weight_before_norm, row_sumsq, &ss))) return rc;
+  if (block_fused(T, K, E, tile_m)) {
+    FusedFin fin;
+    fin.e2p = expanded_to_permuted;
+    fin.w = topk_weights;
+    fin.gamma = gamma;
+    fin.eps = eps;
+    fin.out = out;
+    fin.T = T;
+    fin.K = K;
+    return routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
+                       expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
+                       gemm2_rows, ws, ws_bytes, status, stream, ss, fin);
+  }
+  rc = routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
+                   expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
+                   gemm2_rows, ws, ws_bytes, status, stream, ss, FusedFin());
+  if (rc) return rc;
+  return moe_post_expert_finalize_sumsq(gemm2_rows, row_sumsq, L.P, expanded_to_permuted, topk_weights, gamma, eps,
+                                        T, K, H, out, status, stream);
 }
 
 int moe_nvfp4_experts_sumsq(const moe_weights* w, const void* x, const void* a, const void* a_sf,
@@ -588,13 +669,13 @@ int moe_post_expert_finalize_sumsq(const void* rows, const float* row_sumsq, int
                                    const int32_t* expanded_to_permuted, const float* topk_weights,
                                    const void* gamma, float eps, int T, int K, int H, void* out,
                                    int32_t* status, void* stream) {
-  if (T < 0 || K < 1 || K > 64 || H < 32 || H % 32 || H > 16384 || num_rows < 0)
+  if (T < 0 || K < 1 || K > 64 || H < 128 || H % 128 || H > 16384 || num_rows < 0)
     return fail(MOE_ERR_INVALID_ARG, "bad finalize shape T=%d K=%d H=%d rows=%d", T, K, H, num_rows);
   if (T == 0) return MOE_OK;
   if ((num_rows > 0 && (!rows || !row_sumsq)) || !expanded_to_permuted || !topk_weights || !gamma || !out)
     return fail(MOE_ERR_INVALID_ARG, "finalize pointer is null");
-  if (!aligned(rows, 16) || !aligned(gamma, 16) || !aligned(out, 16) || !aligned(row_sumsq, 4))
-    return fail(MOE_ERR_INVALID_ARG, "rows / gamma / out must be 16-byte aligned");
+  if (!aligned(rows, 16) || !aligned(gamma, 16) || !aligned(out, 16) || !aligned(row_sumsq, 16))
+    return fail(MOE_ERR_INVALID_ARG, "rows / row_sumsq / gamma / out must be 16-byte aligned");
   if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
   cudaError_t err = moe::launch_finalize_sumsq(rows, row_sumsq, num_rows, expanded_to_permuted, topk_weights,
                                                gamma, eps, T, K, H, out, status, as_stream(stream));

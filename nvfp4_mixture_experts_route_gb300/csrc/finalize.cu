@@ -168,24 +168,6 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
   }
 }
 
-// Packed fp32x2 arithmetic (one instruction for two lanes of the pair):
-// d = a * b + c and d = a * b, each element rounded as its scalar form.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
-        "l"(*reinterpret_cast<unsigned long long*>(&c)));
-  return *reinterpret_cast<float2*>(&d);
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
-  return *reinterpret_cast<float2*>(&d);
-}
-
 // The same finalize with the token's K rows staged in shared memory by bulk
 // copies, one mbarrier per route: one thread issues them all up front, and
 // the CTA normalises route k as soon as its row has landed while the later
@@ -491,11 +473,14 @@ namespace moe {
 // weighted for the weight-before-norm reading): every route's coefficient
 // w[t, k] / sqrt(mean + eps) is known before any row is read, so the rows
 // stream through once with no reduction between a row's load and its use.
-// One CTA per token: warp k first sums route k's H / 32 partials (a fixed
-// order: lane-strided sums, then a butterfly), then every thread takes
-// 8-element vectors of the hidden dimension, issues the loads of all of its
-// routes' vectors at once (up to eight in flight), and accumulates
-// coef_k * r_k in fp32; out = bf16(g * sum), g = 1 + gamma, in both readings.
+// One CTA per token: route k's H / 32 partials are summed by the four lanes
+// 4 (k % 8) + j of warp k / 8, as float4s (lane j takes float4s j, j + 4,
+// ..., adding .x, .y, .z, .w in turn; then (s0 + s1) + (s2 + s3) by two xor
+// shuffles), the order the one-launch GEMMs' finalize units use too; then
+// every thread takes 8-element vectors of the hidden dimension, issues the
+// loads of all of its routes' vectors at once (up to eight in flight), and
+// accumulates coef_k * r_k in fp32; out = bf16(g * sum), g = 1 + gamma, in
+// both readings.
 constexpr int kFinSsThreads = 256;
 
 __global__ void __launch_bounds__(kFinSsThreads) finalize_sumsq_kernel(
@@ -508,19 +493,30 @@ __global__ void __launch_bounds__(kFinSsThreads) finalize_sumsq_kernel(
   pdl_trigger();
   const int t = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int G = H / 32;
-  for (int k = warp; k < K; k += kFinSsThreads / 32) {
-    int p = e2p[(size_t)t * K + k];
-    if (p < -1 || p >= num_rows) {
-      if (lane == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
-      p = -1;
+  const int G4 = H / 128;
+  {
+    const int k = 8 * warp + (lane >> 2);  // K <= 64 = 8 warps x 8 routes
+    int p = -1;
+    if (k < K) {
+      p = e2p[(size_t)t * K + k];
+      if (p < -1 || p >= num_rows) {
+        if ((lane & 3) == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
+        p = -1;
+      }
     }
+    const float4* src = reinterpret_cast<const float4*>(row_ss + (size_t)(p >= 0 ? p : 0) * (H / 32));
     float ss = 0.f;
     if (p >= 0)
-      for (int g = lane; g < G; g += 32) ss += row_ss[(size_t)p * G + g];
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, d);
-    if (lane == 0) {
+      for (int m = lane & 3; m < G4; m += 4) {
+        const float4 x = src[m];
+        ss += x.x;
+        ss += x.y;
+        ss += x.z;
+        ss += x.w;
+      }
+    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+    if (k < K && (lane & 3) == 0) {
       rowp[k] = p;
       coef[k] = p >= 0 ? topk_w[(size_t)t * K + k] / sqrtf(ss / (float)H + eps) : 0.f;
     }

@@ -110,6 +110,24 @@ struct GemmParams {
   // both GEMMs in one grid: the experts and the route tiles the buffers hold
   // (bounds for the head prefetch, which reads the routing as a hint)
   int num_experts, max_tiles;
+  // Both GEMMs in one grid, optional (fin_out set; row_ss set too): the
+  // post-expert finalize of fin_T tokens, after the GEMM units, in units of
+  // (token, 256 columns) that epilogue warps with no GEMM work left draw from
+  // fin_ticket. A unit starts once every GEMM2 unit has stored its rows and
+  // sums of squares: gemm2_done counts the epilogue warps of GEMM2 units that
+  // have (both zeroed with done).
+  int32_t* gemm2_done;
+  int32_t* fin_ticket;
+  const int32_t* fin_e2p;      // expanded_to_permuted [fin_T, fin_K]
+  const float* fin_w;          // topk_weights [fin_T, fin_K]
+  const __nv_bfloat16* fin_gamma;  // [H]: out = bf16((1 + gamma) * sum)
+  __nv_bfloat16* fin_out;      // [fin_T, H]
+  float fin_eps;
+  int fin_T, fin_K, fin_rows;  // fin_rows: rows of the GEMM2 row buffer
+  // Load the weights and their scales with an L2 evict_first policy (they
+  // stream through once), so that the rows, sums and intermediate the grid
+  // writes and reads again stay in L2.
+  int w_evict_first;
 };
 
 // Sum over a warp's 32 lanes of each of 32 values: afterwards lane l holds
@@ -294,6 +312,108 @@ __host__ __device__ constexpr int gemm_threads(int mode, int tile_m) {
 // fits at once). The tile's launch shape, pipeline depth and scale-atom
 // count are compile-time, so the MMA issuer's per-stage loops unroll and its
 // descriptors are base + constant.
+// Both GEMMs in one grid: one finalize unit, done by one epilogue warp (the
+// same arithmetic, in the same order, as the finalize from sums of squares,
+// finalize_sumsq_kernel): token t, hidden vectors (8 columns) v0 + lane.
+// fin_prepare reads what does not depend on GEMM2 (the token's rows and
+// weights, lane k holding route k's; the lane's gain vector) and may run
+// before the GEMM2 units have completed. fin_finish then loads the lane's
+// vector of every route row, and route k's H/32 partial sums of squares as
+// float4s over the four lanes 4k + j (lane j takes float4s j, j + 4, ...,
+// adding .x, .y, .z, .w in turn; then (s0 + s1) + (s2 + s3) by two xor
+// shuffles): sum_sq_k_total, coef_k = w[t, k] / sqrt(total / H + eps), and
+// out = bf16((1 + gamma) * sum_k coef_k * r_k), accumulated in fp32 in
+// route order. Rows and sums are read from L2 (ld.cg): they were written
+// during this launch.
+constexpr int kFinFusedMaxK = 8;
+
+struct FinPre {
+  int t, v, pk;
+  float wk;
+  uint4 gain;
+};
+
+__device__ __forceinline__ FinPre fin_prepare(const GemmParams& p, int t, int v0, int lane) {
+  const int K = p.fin_K, H = p.g[1].out_cols;
+  FinPre f;
+  f.t = t;
+  f.v = v0 + lane;
+  f.pk = -1;
+  f.wk = 0.f;
+  if (lane < K) {
+    f.pk = __ldcg(p.fin_e2p + (size_t)t * K + lane);
+    if (f.pk < -1 || f.pk >= p.fin_rows) {
+      record_status(p.status, MOE_ERR_INVALID_ROUTE);
+      f.pk = -1;
+    }
+    f.wk = __ldcg(p.fin_w + (size_t)t * K + lane);
+  }
+  f.gain = f.v < H / 8 ? __ldg(reinterpret_cast<const uint4*>(p.fin_gamma + 8 * f.v)) : make_uint4(0, 0, 0, 0);
+  return f;
+}
+
+__device__ __noinline__ void fin_finish(const GemmParams& p, const FinPre& f, int lane) {
+  const int K = p.fin_K, H = p.g[1].out_cols, G4 = H / 128;
+  int rp[kFinFusedMaxK];
+#pragma unroll
+  for (int k = 0; k < kFinFusedMaxK; ++k) {
+    rp[k] = __shfl_sync(0xFFFFFFFFu, f.pk, k);
+    if (k >= K) rp[k] = -1;
+  }
+  const bool on = f.v < H / 8;
+  uint4 raw[kFinFusedMaxK];
+#pragma unroll
+  for (int k = 0; k < kFinFusedMaxK; ++k)
+    raw[k] = (on && rp[k] >= 0) ? __ldcg(reinterpret_cast<const uint4*>(p.rows + (size_t)rp[k] * H) + f.v)
+                                : make_uint4(0, 0, 0, 0);
+  // route lane / 4: this lane's float4s j, j + 4, ..., five at a time
+  const int my = __shfl_sync(0xFFFFFFFFu, f.pk, lane >> 2);
+  const bool mine = (lane >> 2) < K && my >= 0;
+  const float4* src = reinterpret_cast<const float4*>(p.row_ss + (size_t)(mine ? my : 0) * (H / 32));
+  float ss = 0.f;
+  for (int m0 = lane & 3; m0 < G4; m0 += 20) {
+    float4 x[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) x[i] = (mine && m0 + 4 * i < G4) ? __ldcg(src + m0 + 4 * i) : make_float4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      if (m0 + 4 * i < G4) {
+        ss += x[i].x;
+        ss += x[i].y;
+        ss += x[i].z;
+        ss += x[i].w;
+      }
+    }
+  }
+  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+  const float wk = __shfl_sync(0xFFFFFFFFu, f.wk, lane >> 2);
+  const float coef = mine ? wk / sqrtf(ss / (float)H + p.fin_eps) : 0.f;
+  float2 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kFinFusedMaxK; ++k) {
+    const float c = __shfl_sync(0xFFFFFFFFu, coef, 4 * k);
+    if (k >= K) break;
+    const float2 ck = make_float2(c, c);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = ffma2(__bfloat1622float2(h[q]), ck, acc[q]);
+  }
+  if (!on) return;
+  const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&f.gain);
+  uint4 o;
+  __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 gf = __bfloat1622float2(gh[q]);
+    const float2 r = fmul2(acc[q], make_float2(1.f + gf.x, 1.f + gf.y));  // gain centre added in fp32
+    oh[q] = __floats2bfloat162_rn(r.x, r.y);
+  }
+  *reinterpret_cast<uint4*>(p.fin_out + (size_t)f.t * H + 8 * f.v) = o;
+}
+
 // Both GEMMs in one grid: L2 prefetch of the first kHeadPrefetchStages
 // stages of weights and weight scales of unit blockIdx.x, from a routing
 // read before the previous kernel has completed (a hint: the route-tile
@@ -343,6 +463,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __shared__ __align__(8) uint64_t uq_empty[kUnitQ];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ int fin_go;  // the finalize may start: 1, or -1 (gave up); 0 until known
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // weight tiles per route tile of each GEMM, and the units: GEMM1's, then GEMM2's
@@ -363,7 +484,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     if (tid == 0) pdl_trigger();
   }
   const int ntiles_early = late ? 0 : __ldcg(p.totals);
-  if (!late && (int)blockIdx.x >= ntiles_early * (tw1 + tw2)) {
+  if (!late && p.fin_out == nullptr && (int)blockIdx.x >= ntiles_early * (tw1 + tw2)) {
     // Even an idle CTA must not let this grid complete before its
     // predecessor: the kernels after it rely on that ordering.
     if (p.prefetch) pdl_wait();
@@ -408,6 +529,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       mbar_init(smem_u32(&uq_empty[q]), 1 + EPW);  // the MMA issuer and every epilogue warp
     }
     abort_flag = 0;
+    fin_go = 0;
     fence_barrier_init();
     if (MODE != 2) {
       tma_prefetch_desc(&tmA1);
@@ -488,6 +610,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       // Units are drawn from a ticket (below), known only after the previous
       // kernel has completed: the grid's prologue waited for it.
       if constexpr (MODE == 3) waited = true;
+      const uint64_t w_pol = p.w_evict_first ? l2_policy_evict_first() : 0;
       // MODE 3: the ticket this CTA holds next (drawn one unit ahead, so that
       // the atomic's latency overlaps the current unit's loads)
       int next = MODE == 3 ? atomicAdd(p.ticket, 1) : 0;
@@ -547,11 +670,19 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           const uint32_t nc = (uint32_t)(kk + 3) / 4;  // chunks in this stage
           const uint32_t fb = smem_u32(&full_bar[s]);
           mbar_arrive_expect_tx(fb, nc * (kABytes + b_bytes) + (uint32_t)kk * kAtomBytes * (1 + S));
-          for (int c = 0; c < (int)nc; ++c)
-            tma_load_2d(sA + s * a_stage + c * kABytes, tmA, fb, (ks * CH + c) * kStageRowBytes,
-                        a_row);
-          bulk_load(sSFA + s * sfa_stage, wsf + (size_t)steps_per_stage * ks * kAtomBytes,
-                    (uint32_t)kk * kAtomBytes, fb);
+          if (p.w_evict_first) {
+            for (int c = 0; c < (int)nc; ++c)
+              tma_load_2d_hint(sA + s * a_stage + c * kABytes, tmA, fb, (ks * CH + c) * kStageRowBytes, a_row,
+                               w_pol);
+            bulk_load_hint(sSFA + s * sfa_stage, wsf + (size_t)steps_per_stage * ks * kAtomBytes,
+                           (uint32_t)kk * kAtomBytes, fb, w_pol);
+          } else {
+            for (int c = 0; c < (int)nc; ++c)
+              tma_load_2d(sA + s * a_stage + c * kABytes, tmA, fb, (ks * CH + c) * kStageRowBytes,
+                          a_row);
+            bulk_load(sSFA + s * sfa_stage, wsf + (size_t)steps_per_stage * ks * kAtomBytes,
+                      (uint32_t)kk * kAtomBytes, fb);
+          }
           if (waited) {
             load_route_half(s, ks, tau, kk, gi);
           } else {
@@ -584,7 +715,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       int s = 0, uc = 0;
       uint32_t phase = 0;  // ring position: stage s, its current full phase
       bool stop = false;
-      for (int n = 0; !stop; ++n, ++uc) {
+      for (int n = 0; !stop; ++n) {
         int u;
         if constexpr (MODE == 3) {
           const int q = n % kUnitQ;
@@ -649,6 +780,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         }
         if (stop) break;
         tc_commit(smem_u32(&accf_bar[b]));
+        ++uc;
       }
     }
     __syncwarp();
@@ -708,7 +840,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
                    (warp - 2) * epi_cols_for(tile_m) * kEpiStride;
     int uc = 0;
-    for (int n = 0;; ++n, ++uc) {
+    bool gemm_end = false;  // MODE 3: the queue ended (not a wait that gave up)
+    for (int n = 0;; ++n) {
       int u;
       if constexpr (MODE == 3) {
         const int q = n % kUnitQ;
@@ -718,7 +851,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           mbar_arrive(smem_u32(&uq_empty[q]));
         }
         u = __shfl_sync(0xFFFFFFFFu, u, 0);
-        if (u < 0) break;
+        if (u < 0) {
+          gemm_end = u == -1;
+          break;
+        }
       } else {
         u = blockIdx.x + n * gridDim.x;
         if (u >= n_units) break;
@@ -880,6 +1016,82 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         __syncwarp();
         if (lane == 0) atomicAdd(p.done + tau, 1);
       }
+      if (MODE == 3 && !g1 && p.fin_out != nullptr) {
+        // This warp's share of the unit's rows and sums of squares is
+        // stored: publish it to the finalize units (release at GPU scope).
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.gemm2_done, 1);
+      }
+      ++uc;
+    }
+    if (MODE == 3 && p.fin_out != nullptr) {
+      // The finalize, once every GEMM2 unit has stored its rows: each warp
+      // with no GEMM work left draws finalize units (token, 256 columns) one
+      // at a time -- a warp draws only when free, so the units spread over
+      // the warps that finish first -- and reads the first one's routing
+      // meanwhile. The CTA's first epilogue warp alone polls the global
+      // count (with a back-off, so that the waiting CTAs do not crowd the L2
+      // slice that holds it) and posts the outcome in shared memory (1 go,
+      // -1 give up) for the others.
+      const int nvec = p.g[1].out_cols / 8;
+      const int slices = (nvec + 31) / 32;
+      const int n_fin = p.fin_T * slices;
+      auto draw = [&]() {
+        int f = 0;
+        if (lane == 0) f = atomicAdd(p.fin_ticket, 1);
+        return __shfl_sync(0xFFFFFFFFu, f, 0);
+      };
+      // the first unit, and what of it does not depend on GEMM2, while the
+      // last GEMM2 units finish
+      int f = gemm_end ? draw() : n_fin;
+      FinPre pre{};
+      if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * 32, lane);
+      if (warp == 2 && lane == 0) {
+        bool ok = gemm_end;
+        if (ok) {
+          const uint64_t t0 = global_timer_ns();
+          const int32_t target = ntiles * tw2 * EPW;
+          for (;;) {
+            int32_t v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.gemm2_done) : "memory");
+            if (v >= target) break;
+            if (abort_flag) {
+              ok = false;
+              break;
+            }
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              record_status(p.status, MOE_ERR_TIMEOUT);
+              abort_flag = 1;
+              ok = false;
+              break;
+            }
+            __nanosleep(256);
+          }
+        }
+        __threadfence();
+        *reinterpret_cast<volatile int*>(&fin_go) = ok ? 1 : -1;
+      }
+      int go = 0;
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while ((go = *reinterpret_cast<volatile int*>(&fin_go)) == 0) {
+          if (abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+            go = -1;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      go = __shfl_sync(0xFFFFFFFFu, go, 0);
+      if (go > 0) {
+        __threadfence();
+        while (f < n_fin) {
+          fin_finish(p, pre, lane);
+          f = draw();
+          if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * 32, lane);
+        }
+      }
     }
   }
 
@@ -949,10 +1161,12 @@ static cudaError_t launch_one(const CUtensorMap* maps, GemmParams& p, int max_ti
   // ctas_per_sm CTAs per SM (all resident at once); CTAs past the live unit
   // count exit at once.
   const long long units =
-      (long long)max_tiles * ((MODE != 2 ? p.g[0].rows_w : 0) + (MODE != 1 ? p.g[1].rows_w : 0)) / kWTile;
+      (long long)max_tiles * ((MODE != 2 ? p.g[0].rows_w : 0) + (MODE != 1 ? p.g[1].rows_w : 0)) / kWTile +
+      (p.fin_out != nullptr ? 1 : 0);
   long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
   if (MODE == 3) {
-    // The fused grid's waits end only if all of its CTAs are resident at once.
+    // No more CTAs than fit at once (more would only queue behind the
+    // resident ones for the tickets).
     int fit = 0;
     err = resident_ctas(reinterpret_cast<const void*>(kern), gemm_threads(MODE, TILE), smem, &fit);
     if (err != cudaSuccess) return err;
@@ -1070,7 +1284,9 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
                        const int32_t* tile_row_limit, const int32_t* totals, const uint8_t* a_codes,
                        const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, void* rows, float* row_ss,
                        const void* ss_gamma, int ss_wbn, int32_t* done, int E, int H, int I, int tile_m, int P,
-                       int max_tiles, int32_t* status, cudaStream_t stream, bool pdl, const char** why) {
+                       int max_tiles, const int32_t* fin_e2p, const float* fin_w, const void* fin_gamma,
+                       float fin_eps, void* fin_out, int fin_T, int fin_K, int32_t* status, cudaStream_t stream,
+                       bool pdl, const char** why) {
   CUtensorMap maps[4];
   GemmParams p{};
   if (!gemm1_side(p, &maps[0], &maps[1], p_w13, p_w13_sf, g1_alphas, g1_scale_c, a_codes, a_sf, E, H, I,
@@ -1094,6 +1310,21 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
   p.ticket = done + max_tiles;
   p.num_experts = E;
   p.max_tiles = max_tiles;
+  p.w_evict_first = 1;
+  if (fin_out != nullptr) {
+    // the GEMM2 completion count and the finalize units' ticket follow the
+    // unit ticket, each in a 128-byte line of its own
+    p.gemm2_done = done + max_tiles + 32;
+    p.fin_ticket = done + max_tiles + 64;
+    p.fin_e2p = fin_e2p;
+    p.fin_w = fin_w;
+    p.fin_gamma = reinterpret_cast<const __nv_bfloat16*>(fin_gamma);
+    p.fin_out = reinterpret_cast<__nv_bfloat16*>(fin_out);
+    p.fin_eps = fin_eps;
+    p.fin_T = fin_T;
+    p.fin_K = fin_K;
+    p.fin_rows = P;
+  }
   p.status = status;
   p.tile_m = tile_m;
   if (launch_mode<3>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {

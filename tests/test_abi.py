@@ -95,6 +95,13 @@ def test_null_pointers_refused_before_any_launch(lib):
     rc = lib.moe_nvfp4_experts_routed(C.byref(B.MoeWeights()), 16, 16, None, None, 16, 16, 4, 256, 128, 8, 2, 32,
                                       16, 16, 16, 16, 16, 16, 16, 16, 1024, 1 << 20, None, None)
     assert rc == -1
+    # the whole block: no output, then no row sums of squares
+    rc = lib.moe_nvfp4_moe_block(C.byref(w), 16, 16, 16, None, None, 16, 16, 16, 1e-6, 1, 4, 256, 128, 8, 2, 32,
+                                 16, 16, 16, 16, 16, 16, 16, 16, 16, None, 1024, 1 << 20, None, None)
+    assert rc == -1 and b"out" in lib.moe_last_error()
+    rc = lib.moe_nvfp4_moe_block(C.byref(w), 16, 16, 16, None, None, 16, 16, 16, 1e-6, 1, 4, 256, 128, 8, 2, 32,
+                                 16, 16, 16, 16, 16, 16, 16, 16, None, 16, 1024, 1 << 20, None, None)
+    assert rc == -1 and b"row_sumsq" in lib.moe_last_error()
 
 
 def test_experts_kernel_count():
@@ -129,6 +136,18 @@ def test_routed_experts_kernel_count():
     assert B.routed_experts_kernels(0, 8, 128, 32) == 1
     with pytest.raises(B.MoeError):
         B.routed_experts_kernels(8, 8, 128, 48)
+
+
+def test_moe_block_kernel_count():
+    """The whole block is 2 kernels where routing runs inside the quantizer
+    and K <= 8 (the finalize as the GEMMs' last units); otherwise the routed
+    body's kernels and the finalize kernel."""
+    assert B.moe_block_kernels(8, 8, 128, 32) == 2
+    assert B.moe_block_kernels(64, 8, 128, 32) == 2
+    assert B.moe_block_kernels(8, 12, 128, 32) == 2 + 1
+    assert B.moe_block_kernels(257, 8, 128, 32) == 1 + 2 + 1
+    assert B.moe_block_kernels(8192, 8, 128, 128) == 3 + 3 + 1
+    assert B.moe_block_kernels(0, 8, 128, 32) == 1
 
 
 def test_selftest_arguments_refused_before_launch(lib):

@@ -258,6 +258,124 @@ def test_routed_entry_unrouted_and_bad_ids(small_cases):
         assert torch.equal(rows_b[live], rows_a[live])
 
 
+BLOCK_EXTRA = ROUTED_EXTRA + [
+    (7, 256, 128, 16, 12, "uniform", 32, 4.0, 1e-3),    # K = 12 > 8: the finalize kernel after the body
+    (1, 640, 384, 8, 8, "uniform", 64, 4.0, 1e-3),      # one token, H = 640: a partial column slice
+]
+
+
+def _block_vs_parts(prep, ids_np, batch, tile, a1, a2, wbn, calls=2):
+    """(status, route, rows, row_sumsq, out) of route_permute +
+    nvfp4_experts_sumsq + post_expert_finalize_sumsq, and of moe_block called
+    `calls` times on the same buffers (its outputs of each call)."""
+    E, H, I = prep.E, prep.H, prep.I
+    ids = _dev(ids_np.astype(np.int32))
+    T, K = ids.shape
+    x = bf16_dev(batch["x"])
+    tw = _dev(batch["topk_weights"])
+    g1 = torch.tensor([a1], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([a2], dtype=torch.float32, device=DEV)
+    st_a = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r_a = B.route_permute(ids, E, tile, status=st_a)
+    rows_a, ss_a, _ = B.nvfp4_experts_sumsq(prep.w, r_a, x=x, a1_gscale=g1, a2_gscale=g2, T=T, H=H, I=I, E=E, K=K,
+                                            gamma=prep.gamma, weight_before_norm=wbn, status=st_a)
+    out_a = B.post_expert_finalize_sumsq(rows_a, ss_a, r_a.expanded_to_permuted, tw, prep.gamma, 1e-6, status=st_a)
+    st_b = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r_b = B.alloc_route(T, K, E, tile, DEV)
+    for f in _ROUTE_FIELDS:
+        getattr(r_b, f).fill_(12345)
+    ws = B.alloc_workspace(T, K, E, H, I, tile, DEV)
+    got = []
+    for _ in range(calls):
+        rows_b = torch.zeros_like(rows_a)
+        ss_b = torch.zeros_like(ss_a)
+        out_b = torch.full_like(out_a, 7.0)
+        B.moe_block(prep.w, ids, tw, r_b, x=x, a1_gscale=g1, a2_gscale=g2, gamma=prep.gamma, eps=1e-6,
+                    weight_before_norm=wbn, H=H, I=I, E=E, gemm2_rows=rows_b, row_sumsq=ss_b, out=out_b, ws=ws,
+                    status=st_b)
+        got.append((rows_b, ss_b, out_b))
+    torch.cuda.synchronize()
+    return (int(st_a.item()), r_a, rows_a, ss_a, out_a), (int(st_b.item()), r_b, got)
+
+
+def _check_block(parts, block):
+    (st_a, r_a, rows_a, ss_a, out_a), (st_b, r_b, got) = parts, block
+    assert st_a == st_b
+    for f in _ROUTE_FIELDS:
+        assert torch.equal(getattr(r_a, f), getattr(r_b, f)), f
+    live = r_a.expanded_to_permuted.reshape(-1)
+    live = live[live >= 0]
+    for rows_b, ss_b, out_b in got:
+        assert torch.equal(rows_b[live], rows_a[live])
+        assert torch.equal(ss_b[live], ss_a[live])
+        assert torch.equal(out_b, out_a)
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+@pytest.mark.parametrize("idx", range(len(SMALL) + len(BLOCK_EXTRA)))
+def test_block_entry_matches_its_parts(small_cases, idx, wbn):
+    """moe_nvfp4_moe_block equals moe_route_permute, moe_nvfp4_experts_sumsq
+    and moe_post_expert_finalize_sumsq bit for bit (metadata, live rows,
+    their sums of squares, the output), whether the finalize ran as the
+    one-launch GEMMs' last units (2 kernels) or as its own kernel, in both
+    norm readings (gamma ~ N(0, 1)), and again on a second call over the same
+    buffers."""
+    if idx < len(SMALL):
+        w, raw, batch, tile, a1, a2 = small_cases[idx]
+    else:
+        T, H, I, E, K, routing, tile, a1, a2 = BLOCK_EXTRA[idx - len(SMALL)]
+        w = _workload(T, H, I, E, K, routing, tile)
+        raw, batch = inputs.make_layer(w), inputs.make_batch(w)
+    raw = dict(raw)
+    raw["gamma"] = inputs._to_bf16_bits(np.random.default_rng(5).standard_normal(w.H))
+    prep = Prepared(raw)
+    fused = w.T * w.K <= 2048 and w.E <= 256 and tile <= 64 and w.K <= 8
+    n = B.moe_block_kernels(w.T, w.K, w.E, tile)
+    assert (n == 2) == fused
+    _check_block(*_block_vs_parts(prep, batch["topk_ids"], batch, tile, a1, a2, wbn))
+
+
+def test_block_entry_against_the_oracle(small_cases, record_property):
+    """The whole block (finalize units inside the GEMMs' launch) against the
+    oracle's layer: output within the end-to-end bar, and the oracle's
+    finalize of the block's own rows within 2e-3."""
+    w, raw, batch, tile, a1, a2 = small_cases[1]
+    raw = dict(raw)
+    raw["gamma"] = inputs._to_bf16_bits(np.random.default_rng(6).standard_normal(w.H))
+    prep = Prepared(raw)
+    assert B.moe_block_kernels(w.T, w.K, w.E, tile) == 2
+    for wbn in (True, False):
+        (_, r_a, _, _, _), (st, r_b, got) = _block_vs_parts(prep, batch["topk_ids"], batch, tile, a1, a2, wbn,
+                                                            calls=1)
+        assert st == 0
+        rows_b, _, out_b = got[0]
+        ref = olayer.moe_layer(batch["x"], batch["topk_ids"], batch["topk_weights"], raw, a1, a2, raw["gamma"],
+                               1e-6, tile, weight_before_norm=wbn)
+        err = rel_l2(bf16_host_f64(out_b), ref["out"])
+        e2p = r_b.expanded_to_permuted.cpu().numpy()
+        fin = olayer.finalize(bf16_host_f64(rows_b), e2p, batch["topk_weights"], raw["gamma"], 1e-6, wbn)
+        err_fin = rel_l2(bf16_host_f64(out_b), fin["out"])
+        record_property(f"out_rel_l2_wbn{int(wbn)}", err)
+        record_property(f"finalize_rel_l2_wbn{int(wbn)}", err_fin)
+        assert err < OUT_BAR and err_fin < 2e-3, (err, err_fin)
+
+
+def test_block_entry_unrouted_and_bad_ids(small_cases):
+    """Routes marked -1 contribute nothing and an id out of range is skipped
+    and reported, inside the fused block as in its parts; a token with no
+    routes at all gets a zero output row."""
+    w, raw, batch, tile, a1, a2 = small_cases[1]
+    ids = batch["topk_ids"].copy()
+    ids[::3, 0] = -1
+    ids[1, 1] = w.E
+    ids[2, :] = -1
+    prep = Prepared(raw)
+    parts, block = _block_vs_parts(prep, ids, batch, tile, a1, a2, True)
+    assert parts[0] == -6 and block[0] == -6
+    _check_block(parts, block)
+    assert not block[2][0][2][2].any()
+
+
 def test_fused_gemms_finish_while_other_work_holds_most_sms():
     """The one-launch GEMMs hand their units out by ticket to running CTAs
     only, so a GEMM2 unit never waits for a GEMM1 unit that no running CTA
@@ -506,6 +624,21 @@ def test_routed_entry_full_size(full, name):
     live = r_a.expanded_to_permuted.reshape(-1)
     for rows_b in outs:
         assert torch.equal(rows_b[live], rows_a[live])
+
+
+@pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf"])
+def test_block_entry_full_size(full, name):
+    """At full size the whole block in 2 kernels (routing inside the
+    quantizer, the finalize inside the GEMMs' launch) equals its parts bit
+    for bit."""
+    raw, prep = full
+    w = inputs.WORKLOADS[name]
+    a1, a2 = inputs.global_scales(w)
+    batch = inputs.make_batch(w)
+    assert B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 2
+    parts, block = _block_vs_parts(prep, batch["topk_ids"], batch, w.tile_m, a1, a2, True)
+    assert parts[0] == 0
+    _check_block(parts, block)
 
 
 def test_expert_tp_identity(full, record_property):
