@@ -307,9 +307,17 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
     stream = torch.cuda.current_stream(dev)
 
     fused = B.experts_kernels(tile) == 2
+    # the whole block in 2 kernels (routing inside the input quantizer, the
+    # finalize inside the GEMMs' launch) where it applies
+    block = B.moe_block_kernels(T, K, E, tile) == 2
 
     def step(i, ev=None, split=True):
         wts = copies[i % len(copies)]
+        if ev is None and block:
+            B.moe_block(wts, ids, tw, route, x=x, a1_gscale=moe.a1_gscale, a2_gscale=moe.a2_gscale,
+                        gamma=moe.gamma, eps=moe.eps, weight_before_norm=True, H=H, I=I, E=E, gemm2_rows=rows,
+                        row_sumsq=bufs["row_sumsq"], out=out, ws=ws, status=status)
+            return
         if ev is None:
             # Routing and the expert body as one call (for few routes the
             # routing runs inside the input quantizer); the GEMMs start as
@@ -339,10 +347,11 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         if ev is not None:
             ev[4].record(stream)
 
-    # routing + expert body (routing fused into the quantizer for few routes,
-    # else 1 or 3 routing kernels, the quantizer and one or two GEMM
-    # launches), then the finalize
-    launches_per_step = B.routed_experts_kernels(T, K, E, tile) + 1
+    # the whole block in 2 kernels where it applies; else routing + expert
+    # body (routing fused into the quantizer for few routes, else 1 or 3
+    # routing kernels, the quantizer and one or two GEMM launches), then the
+    # finalize
+    launches_per_step = B.moe_block_kernels(T, K, E, tile) if block else B.routed_experts_kernels(T, K, E, tile) + 1
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()

@@ -473,10 +473,10 @@ namespace moe {
 // weighted for the weight-before-norm reading): every route's coefficient
 // w[t, k] / sqrt(mean + eps) is known before any row is read, so the rows
 // stream through once with no reduction between a row's load and its use.
-// One CTA per token: route k's H / 32 partials are summed by the four lanes
-// 4 (k % 8) + j of warp k / 8, as float4s (lane j takes float4s j, j + 4,
-// ..., adding .x, .y, .z, .w in turn; then (s0 + s1) + (s2 + s3) by two xor
-// shuffles), the order the one-launch GEMMs' finalize units use too; then
+// One CTA per token: route k's H / 32 partials are summed by 16 lanes of
+// one warp, as float4s (lane j takes float4s j, j + 16, ..., adding .x, .y,
+// .z, .w in turn; then an xor butterfly over the 16 lanes), the order the
+// one-launch GEMMs' finalize units use too; then
 // every thread takes 8-element vectors of the hidden dimension, issues the
 // loads of all of its routes' vectors at once (up to eight in flight), and
 // accumulates coef_k * r_k in fp32; out = bf16(g * sum), g = 1 + gamma, in
@@ -494,29 +494,30 @@ __global__ void __launch_bounds__(kFinSsThreads) finalize_sumsq_kernel(
   const int t = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int G4 = H / 128;
-  {
-    const int k = 8 * warp + (lane >> 2);  // K <= 64 = 8 warps x 8 routes
+  // routes 16 r + 2 warp + (lane >> 4), over the 16 lanes lane & 15
+  for (int k0 = 0; k0 < K; k0 += 2 * (kFinSsThreads / 32)) {
+    const int k = k0 + 2 * warp + (lane >> 4), j = lane & 15;
     int p = -1;
     if (k < K) {
       p = e2p[(size_t)t * K + k];
       if (p < -1 || p >= num_rows) {
-        if ((lane & 3) == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
+        if (j == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
         p = -1;
       }
     }
     const float4* src = reinterpret_cast<const float4*>(row_ss + (size_t)(p >= 0 ? p : 0) * (H / 32));
     float ss = 0.f;
     if (p >= 0)
-      for (int m = lane & 3; m < G4; m += 4) {
+      for (int m = j; m < G4; m += 16) {
         const float4 x = src[m];
         ss += x.x;
         ss += x.y;
         ss += x.z;
         ss += x.w;
       }
-    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-    if (k < K && (lane & 3) == 0) {
+#pragma unroll
+    for (int d = 1; d < 16; d <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, d);
+    if (k < K && j == 0) {
       rowp[k] = p;
       coef[k] = p >= 0 ? topk_w[(size_t)t * K + k] / sqrtf(ss / (float)H + eps) : 0.f;
     }

@@ -312,20 +312,27 @@ __host__ __device__ constexpr int gemm_threads(int mode, int tile_m) {
 // fits at once). The tile's launch shape, pipeline depth and scale-atom
 // count are compile-time, so the MMA issuer's per-stage loops unroll and its
 // descriptors are base + constant.
-// Both GEMMs in one grid: one finalize unit, done by one epilogue warp (the
-// same arithmetic, in the same order, as the finalize from sums of squares,
-// finalize_sumsq_kernel): token t, hidden vectors (8 columns) v0 + lane.
+// Both GEMMs in one grid: the finalize units, each done by the CTA's four
+// epilogue warps together (the same arithmetic, in the same order, as the
+// finalize from sums of squares, finalize_sumsq_kernel): token t, 1024
+// columns, warp wi taking hidden vectors (8 columns) v0 + 32 wi + lane.
 // fin_prepare reads what does not depend on GEMM2 (the token's rows and
 // weights, lane k holding route k's; the lane's gain vector) and may run
 // before the GEMM2 units have completed. fin_finish then loads the lane's
-// vector of every route row, and route k's H/32 partial sums of squares as
-// float4s over the four lanes 4k + j (lane j takes float4s j, j + 4, ...,
-// adding .x, .y, .z, .w in turn; then (s0 + s1) + (s2 + s3) by two xor
-// shuffles): sum_sq_k_total, coef_k = w[t, k] / sqrt(total / H + eps), and
-// out = bf16((1 + gamma) * sum_k coef_k * r_k), accumulated in fp32 in
-// route order. Rows and sums are read from L2 (ld.cg): they were written
-// during this launch.
+// vector of every route row and, at the same time, warp wi's share of the
+// sums of squares: routes 2 wi and 2 wi + 1, each over 16 lanes, as the
+// float4s of its H/32 partials (lane j takes float4s j, j + 16, ...,
+// adding .x, .y, .z, .w in turn; then an xor butterfly over the 16 lanes);
+// coef_k = w[t, k] / sqrt(total / H + eps) goes through shared memory to
+// the other warps (a named barrier over the epilogue warps), and every lane
+// accumulates coef_k * r_k in fp32 in route order; out = bf16((1 + gamma)
+// * sum). Rows and sums are read from L2 (ld.cg): they were written during
+// this launch.
 constexpr int kFinFusedMaxK = 8;
+
+__device__ __forceinline__ void epi_bar_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
 
 struct FinPre {
   int t, v, pk;
@@ -333,11 +340,11 @@ struct FinPre {
   uint4 gain;
 };
 
-__device__ __forceinline__ FinPre fin_prepare(const GemmParams& p, int t, int v0, int lane) {
+__device__ __forceinline__ FinPre fin_prepare(const GemmParams& p, int t, int v, int lane) {
   const int K = p.fin_K, H = p.g[1].out_cols;
   FinPre f;
   f.t = t;
-  f.v = v0 + lane;
+  f.v = v;
   f.pk = -1;
   f.wk = 0.f;
   if (lane < K) {
@@ -352,32 +359,31 @@ __device__ __forceinline__ FinPre fin_prepare(const GemmParams& p, int t, int v0
   return f;
 }
 
-__device__ __noinline__ void fin_finish(const GemmParams& p, const FinPre& f, int lane) {
+__device__ __noinline__ void fin_finish(const GemmParams& p, const FinPre& f, int lane, int wi, float* coef_s,
+                                        int nthreads) {
   const int K = p.fin_K, H = p.g[1].out_cols, G4 = H / 128;
-  int rp[kFinFusedMaxK];
-#pragma unroll
-  for (int k = 0; k < kFinFusedMaxK; ++k) {
-    rp[k] = __shfl_sync(0xFFFFFFFFu, f.pk, k);
-    if (k >= K) rp[k] = -1;
-  }
   const bool on = f.v < H / 8;
   uint4 raw[kFinFusedMaxK];
 #pragma unroll
-  for (int k = 0; k < kFinFusedMaxK; ++k)
-    raw[k] = (on && rp[k] >= 0) ? __ldcg(reinterpret_cast<const uint4*>(p.rows + (size_t)rp[k] * H) + f.v)
-                                : make_uint4(0, 0, 0, 0);
-  // route lane / 4: this lane's float4s j, j + 4, ..., five at a time
-  const int my = __shfl_sync(0xFFFFFFFFu, f.pk, lane >> 2);
-  const bool mine = (lane >> 2) < K && my >= 0;
+  for (int k = 0; k < kFinFusedMaxK; ++k) {
+    const int rp = __shfl_sync(0xFFFFFFFFu, f.pk, k);
+    raw[k] = (on && k < K && rp >= 0) ? __ldcg(reinterpret_cast<const uint4*>(p.rows + (size_t)rp * H) + f.v)
+                                      : make_uint4(0, 0, 0, 0);
+  }
+  // this half-warp's route and its share of the partial sums
+  const int k = 2 * wi + (lane >> 4), j = lane & 15;
+  const int my = __shfl_sync(0xFFFFFFFFu, f.pk, k & 31);
+  const float wk = __shfl_sync(0xFFFFFFFFu, f.wk, k & 31);
+  const bool mine = k < K && my >= 0;
   const float4* src = reinterpret_cast<const float4*>(p.row_ss + (size_t)(mine ? my : 0) * (H / 32));
   float ss = 0.f;
-  for (int m0 = lane & 3; m0 < G4; m0 += 20) {
-    float4 x[5];
+  for (int m0 = j; m0 < G4; m0 += 64) {
+    float4 x[4];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) x[i] = (mine && m0 + 4 * i < G4) ? __ldcg(src + m0 + 4 * i) : make_float4(0, 0, 0, 0);
+    for (int i = 0; i < 4; ++i) x[i] = (mine && m0 + 16 * i < G4) ? __ldcg(src + m0 + 16 * i) : make_float4(0, 0, 0, 0);
 #pragma unroll
-    for (int i = 0; i < 5; ++i) {
-      if (m0 + 4 * i < G4) {
+    for (int i = 0; i < 4; ++i) {
+      if (m0 + 16 * i < G4) {
         ss += x[i].x;
         ss += x[i].y;
         ss += x[i].z;
@@ -385,19 +391,19 @@ __device__ __noinline__ void fin_finish(const GemmParams& p, const FinPre& f, in
       }
     }
   }
-  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-  const float wk = __shfl_sync(0xFFFFFFFFu, f.wk, lane >> 2);
-  const float coef = mine ? wk / sqrtf(ss / (float)H + p.fin_eps) : 0.f;
+#pragma unroll
+  for (int d = 1; d < 16; d <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, d);
+  if (j == 0 && k < K) coef_s[k] = mine ? wk / sqrtf(ss / (float)H + p.fin_eps) : 0.f;
+  epi_bar_sync(nthreads);
   float2 acc[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < kFinFusedMaxK; ++k) {
-    const float c = __shfl_sync(0xFFFFFFFFu, coef, 4 * k);
-    if (k >= K) break;
+  for (int kk = 0; kk < kFinFusedMaxK; ++kk) {
+    if (kk >= K) break;
+    const float c = coef_s[kk];
     const float2 ck = make_float2(c, c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[kk]);
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = ffma2(__bfloat1622float2(h[q]), ck, acc[q]);
   }
@@ -463,7 +469,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __shared__ __align__(8) uint64_t uq_empty[kUnitQ];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int fin_go;  // the finalize may start: 1, or -1 (gave up); 0 until known
+  __shared__ int fin_go;  // the finalize may start: 1, or -1 (gave up)
+  __shared__ int fin_unit;  // the finalize unit the epilogue warps do next
+  __shared__ float fin_coef[kFinFusedMaxK];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // weight tiles per route tile of each GEMM, and the units: GEMM1's, then GEMM2's
@@ -840,7 +848,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     float* stage = reinterpret_cast<float*>(dsmem + (sEpi - smem_u32(dsmem))) +
                    (warp - 2) * epi_cols_for(tile_m) * kEpiStride;
     int uc = 0;
-    bool gemm_end = false;  // MODE 3: the queue ended (not a wait that gave up)
     for (int n = 0;; ++n) {
       int u;
       if constexpr (MODE == 3) {
@@ -851,10 +858,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           mbar_arrive(smem_u32(&uq_empty[q]));
         }
         u = __shfl_sync(0xFFFFFFFFu, u, 0);
-        if (u < 0) {
-          gemm_end = u == -1;
-          break;
-        }
+        if (u < 0) break;
       } else {
         u = blockIdx.x + n * gridDim.x;
         if (u >= n_units) break;
@@ -1026,29 +1030,30 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       ++uc;
     }
     if (MODE == 3 && p.fin_out != nullptr) {
-      // The finalize, once every GEMM2 unit has stored its rows: each warp
-      // with no GEMM work left draws finalize units (token, 256 columns) one
-      // at a time -- a warp draws only when free, so the units spread over
-      // the warps that finish first -- and reads the first one's routing
-      // meanwhile. The CTA's first epilogue warp alone polls the global
-      // count (with a back-off, so that the waiting CTAs do not crowd the L2
-      // slice that holds it) and posts the outcome in shared memory (1 go,
-      // -1 give up) for the others.
+      // The finalize, once every GEMM2 unit has stored its rows. The CTA's
+      // epilogue warps, all past their GEMM work, draw finalize units (token,
+      // 1024 columns) from the finalize ticket one at a time and do each
+      // together -- a CTA draws only when free, so the units spread over the
+      // CTAs that finish first. The first unit is drawn, and what of it does
+      // not depend on GEMM2 read, while the last GEMM2 units finish. The
+      // first epilogue warp's lane 0 alone draws, and polls the global count
+      // (with a short back-off); the others learn both through shared memory
+      // after a named barrier over the epilogue warps, which every one of
+      // them reaches whether its GEMM work ended or gave up.
+      static_assert(EPW * 2 >= kFinFusedMaxK, "two routes' sums per epilogue warp");
+      constexpr int kEpiThreads = 32 * EPW;
+      const int wi = warp - 2;
       const int nvec = p.g[1].out_cols / 8;
-      const int slices = (nvec + 31) / 32;
+      const int slices = (nvec + kEpiThreads - 1) / kEpiThreads;
       const int n_fin = p.fin_T * slices;
-      auto draw = [&]() {
-        int f = 0;
-        if (lane == 0) f = atomicAdd(p.fin_ticket, 1);
-        return __shfl_sync(0xFFFFFFFFu, f, 0);
-      };
-      // the first unit, and what of it does not depend on GEMM2, while the
-      // last GEMM2 units finish
-      int f = gemm_end ? draw() : n_fin;
+      epi_bar_sync(kEpiThreads);
+      if (wi == 0 && lane == 0) fin_unit = *reinterpret_cast<volatile int*>(&abort_flag) ? n_fin : atomicAdd(p.fin_ticket, 1);
+      epi_bar_sync(kEpiThreads);
+      int f = *reinterpret_cast<volatile int*>(&fin_unit);
       FinPre pre{};
-      if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * 32, lane);
-      if (warp == 2 && lane == 0) {
-        bool ok = gemm_end;
+      if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * kEpiThreads + 32 * wi + lane, lane);
+      if (wi == 0 && lane == 0) {
+        bool ok = f < n_fin;
         if (ok) {
           const uint64_t t0 = global_timer_ns();
           const int32_t target = ntiles * tw2 * EPW;
@@ -1066,30 +1071,24 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
               ok = false;
               break;
             }
-            __nanosleep(256);
+            __nanosleep(32);
           }
         }
-        __threadfence();
-        *reinterpret_cast<volatile int*>(&fin_go) = ok ? 1 : -1;
+        fin_go = ok ? 1 : -1;
       }
-      int go = 0;
-      if (lane == 0) {
-        const uint64_t t0 = global_timer_ns();
-        while ((go = *reinterpret_cast<volatile int*>(&fin_go)) == 0) {
-          if (abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
-            go = -1;
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-      go = __shfl_sync(0xFFFFFFFFu, go, 0);
-      if (go > 0) {
+      epi_bar_sync(kEpiThreads);
+      if (*reinterpret_cast<volatile int*>(&fin_go) > 0) {
         __threadfence();
         while (f < n_fin) {
-          fin_finish(p, pre, lane);
-          f = draw();
-          if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * 32, lane);
+          // the next unit's ticket, drawn now so that the atomic's round trip
+          // overlaps this unit's loads
+          int next = 0;
+          if (wi == 0 && lane == 0) next = atomicAdd(p.fin_ticket, 1);
+          fin_finish(p, pre, lane, wi, fin_coef, kEpiThreads);
+          if (wi == 0 && lane == 0) fin_unit = next;
+          epi_bar_sync(kEpiThreads);
+          f = *reinterpret_cast<volatile int*>(&fin_unit);
+          if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * kEpiThreads + 32 * wi + lane, lane);
         }
       }
     }

@@ -1,9 +1,10 @@
 """The routed NVFP4 expert block as one object over the C ABI.
 
 ``NvFp4MoE`` holds one layer's prepared weights and scalars on the device and
-runs the entry points in order on the current stream: routing metadata and
-the expert body (input quantization, GEMM1 + SwiGLU + requant, GEMM2) in one
-call, then the post-expert finalize. It only allocates (once, then reuses) and passes
+runs the hot path on the current stream: routing metadata, the expert body
+(input quantization, GEMM1 + SwiGLU + requant, GEMM2) and the post-expert
+finalize, as one call (moe_nvfp4_moe_block) or as the routed body then the
+finalize. It only allocates (once, then reuses) and passes
 pointers; the work is the library's.
 """
 from __future__ import annotations
@@ -16,15 +17,17 @@ from . import binding as B
 
 class NvFp4MoE:
     def __init__(self, raw: dict, a1_gscale: float, a2_gscale: float, gamma_bits, eps: float = 1e-6,
-                 tile_m: int = 32, weight_before_norm: bool = True, device="cuda", fused_norm: bool = False):
+                 tile_m: int = 32, weight_before_norm: bool = True, device="cuda", fused_norm: bool | None = None):
         """``raw``: numpy or torch uint8 w13 [E,2I,H/2], w13_sf [E,2I,H/16],
         w2 [E,H,I/2], w2_sf [E,H,I/16]; fp32 g1_alphas, g1_scale_c, g2_alphas
         [E]. ``gamma_bits``: bf16 bit patterns [H] (uint16) or a bf16 tensor.
-        ``fused_norm``: GEMM2's epilogue also writes the rows' sums of squares
-        and the finalize streams the rows once (moe_nvfp4_experts_sumsq and
-        moe_post_expert_finalize_sumsq); otherwise (the default, faster on
-        GB300 at every measured batch size) the plain pair moe_nvfp4_experts_routed
-        and moe_post_expert_finalize."""
+        ``fused_norm``: True: the whole block through moe_nvfp4_moe_block
+        (GEMM2's epilogue also writes the rows' sums of squares; the finalize
+        runs from them, inside the GEMMs' launch where the sizes allow);
+        False: moe_nvfp4_experts_routed, then moe_post_expert_finalize; None
+        (the default): the first where it is 2 kernels (decode batches), the
+        second otherwise (at prefill the sums of squares slow GEMM2 more than
+        they save in the finalize)."""
         dev = torch.device(device)
         t = {k: torch.as_tensor(raw[k]).to(dev) for k in ("w13", "w13_sf", "w2", "w2_sf")}
         self.E, twoI, half_h = t["w13"].shape
@@ -73,14 +76,14 @@ class NvFp4MoE:
         b = self.buffers(T, K)
         st = b["status"] if status is None else status
         o = b["out"] if out is None else out
-        if self.fused_norm:
-            B.route_permute(topk_ids, self.E, self.tile_m, route=b["route"], status=st)
-            B.nvfp4_experts_sumsq(self.weights, b["route"], x=x, a1_gscale=self.a1_gscale,
-                                  a2_gscale=self.a2_gscale, T=T, H=self.H, I=self.I, E=self.E, K=K,
-                                  gamma=self.gamma, weight_before_norm=self.weight_before_norm,
-                                  gemm2_rows=b["rows"], row_sumsq=b["row_sumsq"], ws=b["ws"], status=st)
-            B.post_expert_finalize_sumsq(b["rows"], b["row_sumsq"], b["route"].expanded_to_permuted, topk_weights,
-                                         self.gamma, self.eps, out=o, status=st)
+        fused = self.fused_norm
+        if fused is None:
+            fused = B.moe_block_kernels(T, K, self.E, self.tile_m) == 2
+        if fused:
+            B.moe_block(self.weights, topk_ids, topk_weights, b["route"], x=x, a1_gscale=self.a1_gscale,
+                        a2_gscale=self.a2_gscale, gamma=self.gamma, eps=self.eps,
+                        weight_before_norm=self.weight_before_norm, H=self.H, I=self.I, E=self.E,
+                        gemm2_rows=b["rows"], row_sumsq=b["row_sumsq"], out=o, ws=b["ws"], status=st)
             return o, b
         # routing and the expert body in one call (for few routes the routing
         # runs inside the input quantizer)

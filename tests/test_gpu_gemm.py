@@ -843,14 +843,16 @@ def test_graphed_serving_path_matches_eager():
 
 @pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf", "prefill_t8192_zipf"])
 def test_timed_launch_path_matches_split_path(full, name):
-    """The path bench.py times (route_permute, moe_nvfp4_experts -- the
-    quantizer, then for decode tiles one persistent launch of both GEMMs,
-    for prefill tiles two GEMM launches, each a programmatic dependent that
-    prefetches weights -- the finalize; eager and as a graph replay) gives
-    exactly the split entry points' output at full size; those are held to
-    the oracle above; so does the host-staged serving call (its copies inside
-    the graph). moe_experts_gemms at that size gives the split GEMM2 rows
-    too."""
+    """The routed body then the plain finalize (for decode tiles the routing
+    inside the quantizer and one persistent launch of both GEMMs, for
+    prefill tiles the routing kernels, the quantizer and two GEMM launches,
+    each a programmatic dependent that prefetches weights; eager and as a
+    graph replay) gives exactly the split entry points' output at full size;
+    those are held to the oracle above; so does the host-staged serving call
+    (its copies inside the graph). moe_experts_gemms at that size gives the
+    split GEMM2 rows too. The whole-block call (bench.py's step at decode
+    sizes) gives the same rows and the output up to the order of fp32
+    sums."""
     from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
 
     raw, prep = full
@@ -859,7 +861,7 @@ def test_timed_launch_path_matches_split_path(full, name):
     batch = inputs.make_batch(w)
     split = run_gpu(prep, batch, w.tile_m, a1, a2, export=False)
     assert split["status"] == 0
-    moe = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=w.tile_m)
+    moe = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=w.tile_m, fused_norm=False)
     x = bf16_dev(batch["x"])
     ids = torch.from_numpy(batch["topk_ids"]).to(DEV)
     tw = torch.from_numpy(batch["topk_weights"]).to(DEV)
@@ -879,10 +881,12 @@ def test_timed_launch_path_matches_split_path(full, name):
     assert np.array_equal(bf16_host_f64(host), split["out"])
     status, fused = _fused_rows(prep, batch, w.tile_m, a1, a2, calls=1)
     assert status == 0 and np.array_equal(fused[0], split["rows"])
-    # The layer with the norm's sums of squares fused into GEMM2 and the
-    # finalize streaming the rows once: the same rows bit for bit; the output
-    # equal up to the order of the fp32 sums; its graph replays equal its
-    # eager call.
+    # The layer through the whole-block call (the norm's sums of squares
+    # fused into GEMM2, the finalize from them, inside the GEMMs' launch at
+    # decode sizes: what bench.py times there): the same rows bit for bit;
+    # the output equal up to the order of the fp32 sums; its graph replays
+    # equal its eager call; the layer's default picks it exactly where it is
+    # 2 kernels.
     del moe
     torch.cuda.empty_cache()
     fn = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=w.tile_m, fused_norm=True)
@@ -906,3 +910,6 @@ def test_timed_launch_path_matches_split_path(full, name):
     host = fn.replay_host(w.T, w.K)
     torch.cuda.synchronize()
     assert np.array_equal(bf16_host_f64(host), got)
+    fn.fused_norm = None
+    auto = bf16_host_f64(fn.forward(x, ids, tw)[0])
+    assert np.array_equal(auto, got if B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 2 else split["out"])
