@@ -407,13 +407,15 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
 
     # e2e: the public serving call NvFp4MoE.replay_host: one CUDA graph per
-    # step that copies the step's inputs from the layer's pinned host buffer
-    # to the device (x, topk_ids and topk_weights in one copy, laid out by
-    # input_layout), runs routing, expert body and finalize, and copies the
-    # output back into pinned host memory; the copies are inside the timed
-    # region. One weight copy: a step streams the touched experts' weights
-    # (far larger than L2) from HBM anyway. --no-graph times the eager public
-    # call (NvFp4MoE.forward) with the same two copies around it.
+    # step whose inputs are the layer's pinned host buffer (x, topk_ids and
+    # topk_weights, laid out by input_layout) and whose output lands in
+    # pinned host memory. At decode sizes it is zero-copy (the step's kernels
+    # read the inputs and the finalize writes the output over the host link
+    # themselves); otherwise one copy in, routing, expert body and finalize,
+    # one copy out. Either way the transfers are inside the timed region.
+    # One weight copy: a step streams the touched experts' weights (far
+    # larger than L2) from HBM anyway. --no-graph times the eager public call
+    # (NvFp4MoE.forward) with two copies around it.
     offs, nbytes = moe.input_layout(T, K)
     moe.weights = copies[0]
     hb = moe.host_buffers(T, K)
@@ -500,7 +502,9 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         "clocks": clocks.summary(),
         "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": in_h.numel(),
-                "d2h_bytes_per_step": out_h.numel() * 2},
+                "d2h_bytes_per_step": out_h.numel() * 2,
+                "transfer": ("zero-copy: the kernels read the pinned inputs and write the pinned output"
+                             if args.graph and moe.zero_copy(T, K) else "one copy in, one copy out")},
         "gpu_launches": launches_per_step * args.steps,
     }
     if tensor_bound:

@@ -65,6 +65,13 @@ const char* moe_last_error(void);
 /* ABI version, bumped on any incompatible change. */
 int moe_abi_version(void);
 
+/* 1 if kernels of this library may read and write the host memory at p
+ * through p itself (page-locked or managed memory that the current device
+ * maps at the same address, as unified addressing gives cudaHostAlloc
+ * memory), else 0. Callers use it before passing host pointers as step
+ * inputs or outputs (zero-copy serving); no error is recorded. */
+int moe_device_reads_host(const void* p);
+
 /* ------------------------------------------------------------------------
  * Weight preparation (runs once per layer, at load).
  *

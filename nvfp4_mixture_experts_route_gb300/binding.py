@@ -62,6 +62,7 @@ _I = C.c_int
 _SIGNATURES = {
     "moe_last_error": ([], C.c_char_p),
     "moe_abi_version": ([], _I),
+    "moe_device_reads_host": ([_P], _I),
     "moe_route_kernels": ([_I, _I, _I], _I),
     "moe_experts_kernels": ([_I], _I),
     "moe_prepared_sizes": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
@@ -236,6 +237,12 @@ def routed_experts_kernels(T: int, K: int, E: int, tile_m: int) -> int:
     if n < 0:
         _check(n)
     return n
+
+
+def device_reads_host(t) -> bool:
+    """Whether the library's kernels may read / write the host tensor `t`
+    through its own address (page-locked, mapped at the same address)."""
+    return bool(load().moe_device_reads_host(_ptr(t)))
 
 
 def moe_block_kernels(T: int, K: int, E: int, tile_m: int) -> int:

@@ -188,7 +188,17 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-int moe_abi_version(void) { return 3; }
+int moe_abi_version(void) { return 4; }
+
+int moe_device_reads_host(const void* p) {
+  if (!p) return 0;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // an unregistered pointer is an answer, not an error
+    return 0;
+  }
+  return (a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeManaged) && a.devicePointer == p ? 1 : 0;
+}
 
 int moe_prepared_sizes(int E, int H, int I, size_t out_bytes[4]) {
   if (!out_bytes) return fail(MOE_ERR_INVALID_ARG, "out_bytes is null");

@@ -135,19 +135,42 @@ class NvFp4MoE:
             }
         return self._buffers[key]
 
+    def zero_copy(self, T: int, K: int) -> bool:
+        """Whether ``replay_host(T, K)`` runs zero-copy: at decode sizes (the
+        whole block in 2 kernels) its kernels read the step's inputs straight
+        from ``host_inputs`` and the finalize writes ``host_out`` directly,
+        where the device maps that page-locked memory at its own address;
+        otherwise two copies run around the step."""
+        h = self.host_buffers(T, K)
+        fused = self.fused_norm if self.fused_norm is not None else B.moe_block_kernels(T, K, self.E, self.tile_m) == 2
+        return bool(fused and B.moe_block_kernels(T, K, self.E, self.tile_m) == 2 and
+                    B.device_reads_host(h["host_inputs"]) and B.device_reads_host(h["host_out"]))
+
     def replay_host(self, T: int, K: int) -> torch.Tensor:
-        """One CUDA graph replay that copies ``host_buffers(T, K)["host_inputs"]``
-        to the device, runs the step (routing, expert body, finalize) and
-        copies the output into ``host_out``, all on the current stream: a
-        serving step with one launch. Returns ``host_out``; read it after the
+        """One CUDA graph replay of a serving step from pinned host memory:
+        the step's inputs come from ``host_buffers(T, K)["host_inputs"]``
+        and its output lands in ``host_out``, all on the current stream.
+        Zero-copy at decode sizes (``zero_copy``: the kernels read and write
+        the pinned buffers over the host link themselves), else a copy in,
+        the step, and a copy out. Returns ``host_out``; read it after the
         stream is synchronised."""
         h = self.host_buffers(T, K)
-        g = self.graph_buffers(T, K)
+        if self.zero_copy(T, K):
+            offs, _ = self.input_layout(T, K)
+            hi = h["host_inputs"]
+            x = hi[offs["x"]:offs["x"] + T * self.H * 2].view(torch.bfloat16).view(T, self.H)
+            ids = hi[offs["topk_ids"]:offs["topk_ids"] + T * K * 4].view(torch.int32).view(T, K)
+            tw = hi[offs["topk_weights"]:offs["topk_weights"] + T * K * 4].view(torch.float32).view(T, K)
 
-        def step():
-            g["inputs"].copy_(h["host_inputs"], non_blocking=True)
-            self.forward(g["x"], g["topk_ids"], g["topk_weights"], out=g["out"])
-            h["host_out"].copy_(g["out"], non_blocking=True)
+            def step():
+                self.forward(x, ids, tw, out=h["host_out"])
+        else:
+            g = self.graph_buffers(T, K)
+
+            def step():
+                g["inputs"].copy_(h["host_inputs"], non_blocking=True)
+                self.forward(g["x"], g["topk_ids"], g["topk_weights"], out=g["out"])
+                h["host_out"].copy_(g["out"], non_blocking=True)
 
         if h["graph"] is None:
             step()  # warm-up, outside capture

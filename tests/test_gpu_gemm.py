@@ -841,6 +841,38 @@ def test_graphed_serving_path_matches_eager():
         assert torch.equal(got, eager)
 
 
+def test_zero_copy_serving_step_matches_device_step():
+    """The zero-copy serving step (its kernels read x, topk_ids and
+    topk_weights from pinned host memory and the finalize writes the output
+    there) gives the device-buffer step's output bit for bit, for two batches
+    written into the same pinned inputs between replays of one graph."""
+    from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
+
+    w = inputs.WORKLOADS["tiny_t4"]
+    raw = inputs.make_layer(w)
+    moe = NvFp4MoE(raw, 1.0, 1.0, raw["gamma"], tile_m=w.tile_m)
+    hb = moe.host_buffers(w.T, w.K)
+    assert B.device_reads_host(hb["host_inputs"]) and B.device_reads_host(hb["host_out"])
+    assert not B.device_reads_host(torch.zeros(16, dtype=torch.uint8))  # pageable: not registered
+    assert moe.zero_copy(w.T, w.K)
+    offs, _ = moe.input_layout(w.T, w.K)
+    for seed in (0, 1):
+        batch = inputs.make_batch(w, seed=seed)
+        x = bf16_dev(batch["x"])
+        ids = torch.from_numpy(batch["topk_ids"]).to("cuda")
+        tw = torch.from_numpy(batch["topk_weights"]).to("cuda")
+        want = moe.forward(x, ids, tw)[0].cpu()
+        hi = hb["host_inputs"]
+        hi[offs["x"]:offs["x"] + x.numel() * 2].copy_(torch.from_numpy(batch["x"].view(np.uint8).reshape(-1)))
+        hi[offs["topk_ids"]:offs["topk_ids"] + ids.numel() * 4].copy_(
+            torch.from_numpy(batch["topk_ids"].view(np.uint8).reshape(-1)))
+        hi[offs["topk_weights"]:offs["topk_weights"] + tw.numel() * 4].copy_(
+            torch.from_numpy(batch["topk_weights"].view(np.uint8).reshape(-1)))
+        got = moe.replay_host(w.T, w.K)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+
+
 @pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf", "prefill_t8192_zipf"])
 def test_timed_launch_path_matches_split_path(full, name):
     """The routed body then the plain finalize (for decode tiles the routing
@@ -907,6 +939,7 @@ def test_timed_launch_path_matches_split_path(full, name):
     assert np.array_equal(bf16_host_f64(fn.replay(w.T, w.K)), got)
     hb = fn.host_buffers(w.T, w.K)
     hb["host_inputs"].copy_(gb["inputs"].cpu())
+    assert fn.zero_copy(w.T, w.K) == (B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 2)
     host = fn.replay_host(w.T, w.K)
     torch.cuda.synchronize()
     assert np.array_equal(bf16_host_f64(host), got)
