@@ -3,15 +3,19 @@
 
 One step = the whole hot path over one batch: routing metadata, NVFP4 input
 quantization into permuted order, GEMM1 with the fused SwiGLU + requant
-epilogue, GEMM2, and the post-expert finalize -- four to six kernel launches
-through the C ABI (for decode-sized route tiles both GEMMs are one persistent
-launch), inputs resident in HBM. The default workload is the b = 8 decode
-batch (T = 8, H = 5120, I = 2048, E = 128, top-8, uniform routing).
+epilogue, GEMM2, and the post-expert finalize -- two kernel launches through
+the C ABI at decode sizes (routing inside the quantizer; both GEMMs and the
+finalize in one persistent launch), up to seven at prefill, inputs resident
+in HBM. The default workload is the b = 8 decode batch (T = 8, H = 5120,
+I = 2048, E = 128, top-8, uniform routing).
 
 Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
 the launching stream, bracketed by a barrier and a device synchronize; the
 layer's prepared weights rotate over several copies whose total exceeds L2,
-so no step reads the previous step's weights from L2. For the roofline, the
+so no step reads the previous step's weights from L2. The steps are replayed
+from CUDA graphs that each hold one step per weight copy in a row, as
+consecutive layers' blocks sit in a captured forward (--no-chain: one graph
+per step). For the roofline, the
 same steps run once more with the dominant kernel -- the one-launch GEMMs at
 decode, GEMM1 at prefill -- bracketed by its own events. `e2e` repeats the
 measurement through the public layer call with host (pinned) inputs and
@@ -358,17 +362,29 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} during warm-up")
 
-    # One CUDA graph per weight copy holds the launches of a step (the ABI
-    # calls allocate nothing and never synchronise, so they capture as is).
-    graphs = []
+    # CUDA graphs of the step's launches (the ABI calls allocate nothing and
+    # never synchronise, so they capture as is): one graph holding len(copies)
+    # consecutive steps, one per weight copy, as consecutive layers' blocks
+    # sit in a model's captured forward (each step's first kernel is a
+    # programmatic dependent of the step before, whose outputs it waits for
+    # before touching memory); and one graph per copy holding a single step,
+    # for a step count that is not a multiple of len(copies).
+    graphs, chain = [], None
     if args.graph:
         for c in range(len(copies)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 step(c)
             graphs.append(g)
+        if getattr(args, "chain", False) and len(copies) > 1:
+            chain = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(chain):
+                for c in range(len(copies)):
+                    step(c)
         for i in range(args.warmup):
             graphs[i % len(graphs)].replay()
+        if chain is not None:
+            chain.replay()
         torch.cuda.synchronize()
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -376,17 +392,23 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
     torch.cuda.synchronize()
     with ClockSampler(dev.index or 0) as clocks:
         start.record(stream)
-        for i in range(args.steps):
+        i = 0
+        if chain is not None:
+            while i + len(copies) <= args.steps:
+                chain.replay()
+                i += len(copies)
+        while i < args.steps:
             if graphs:
                 graphs[i % len(graphs)].replay()
             else:
                 step(i)
+            i += 1
         end.record(stream)
         torch.cuda.synchronize()
     total_ms = _max_over_ranks(world, start.elapsed_time(end))
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(int(status.item()))} in the timed region")
-    del graphs
+    del graphs, chain
 
     # The same steps launched one by one, GEMM launches between events on the
     # launching stream: the per-kernel durations of the roofline.
@@ -490,7 +512,10 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         "value": tokens_total / (total_ms * 1e-3), "ms_per_step": step_ms,
         "config": {**_config(w), "l2": f"{len(copies)} rotating prepared weight copies "
                                         f"({len(copies) * layer.layer_bytes / 1e9:.2f} GB > L2)",
-                   "launch": (f"CUDA graph per step ({launches_per_step} kernels)" if args.graph
+                   "launch": ((f"CUDA graphs of {len(copies)} consecutive steps ({launches_per_step} kernels "
+                               f"per step, chained by programmatic dependent launch)"
+                               if getattr(args, "chain", False) and len(copies) > 1
+                               else f"CUDA graph per step ({launches_per_step} kernels)") if args.graph
                               else f"eager ({launches_per_step} kernels per step)")},
         "roofline": roof,
         "step_roofline": {"bytes": weight_bytes, "touched_experts": int(n_touch),
@@ -737,6 +762,8 @@ def main() -> None:
                     help="comma-separated further workloads of the same layer, timed in the same run and "
                          "reported under 'workloads' (default with decode_b8: decode_b64_zipf,prefill_t8192_zipf; "
                          "'' for none)")
+    ap.add_argument("--no-chain", dest="chain", action="store_false",
+                    help="time one graph replay per step instead of graphs of one step per weight copy in a row")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps one by one instead of replaying CUDA graphs")
     args = ap.parse_args()
