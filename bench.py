@@ -3,10 +3,10 @@
 
 One step = the whole hot path over one batch: routing metadata, NVFP4 input
 quantization into permuted order, GEMM1 with the fused SwiGLU + requant
-epilogue, GEMM2, and the post-expert finalize -- two kernel launches through
-the C ABI at decode sizes (routing inside the quantizer; both GEMMs and the
-finalize in one persistent launch), up to seven at prefill, inputs resident
-in HBM. The default workload is the b = 8 decode batch (T = 8, H = 5120,
+epilogue, GEMM2, and the post-expert finalize -- four kernel launches
+through the C ABI at decode sizes (routing; the quantizer; both GEMMs in one
+persistent launch; the finalize), up to seven at prefill, inputs resident in
+HBM. The default workload is the b = 8 decode batch (T = 8, H = 5120,
 I = 2048, E = 128, top-8, uniform routing).
 
 Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
@@ -311,9 +311,10 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
     stream = torch.cuda.current_stream(dev)
 
     fused = B.experts_kernels(tile) == 2
-    # the whole block in 2 kernels (routing inside the input quantizer, the
-    # finalize inside the GEMMs' launch) where it applies
-    block = B.moe_block_kernels(T, K, E, tile) == 2
+    # the whole block in one call at decode sizes (routing, the quantizer,
+    # both GEMMs in one launch with the norm's sums of squares in GEMM2's
+    # epilogue, then the finalize from them: 4 kernels)
+    block = fused
 
     def step(i, ev=None, split=True):
         wts = copies[i % len(copies)]
@@ -351,10 +352,9 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         if ev is not None:
             ev[4].record(stream)
 
-    # the whole block in 2 kernels where it applies; else routing + expert
-    # body (routing fused into the quantizer for few routes, else 1 or 3
-    # routing kernels, the quantizer and one or two GEMM launches), then the
-    # finalize
+    # routing + expert body (routing fused into the quantizer for few
+    # routes, else 1 or 3 routing kernels, the quantizer and one or two GEMM
+    # launches), then the finalize
     launches_per_step = B.moe_block_kernels(T, K, E, tile) if block else B.routed_experts_kernels(T, K, E, tile) + 1
     for i in range(args.warmup):
         step(i)

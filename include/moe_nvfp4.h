@@ -248,13 +248,10 @@ int moe_routed_experts_kernels(int T, int K, int E, int tile_m);
  * for bit, moe_route_permute, then moe_nvfp4_experts_sumsq, then
  * moe_post_expert_finalize_sumsq on the same buffers (the routing buffers,
  * gemm2_rows and row_sumsq [max_padded_rows, H/32] fp32 hold what those
- * calls leave). With few routes (T*K <= 2048, E <= 256), tile_m <= 64 and
- * K <= 8 it is 2 kernels: the routing inside the input quantizer, then one
- * persistent launch of both GEMMs whose last units are the finalize, one per
- * (token, column slice), each started as soon as every GEMM2 tile of its
- * token's routes has stored its rows; otherwise the routing kernels, the
- * expert body and the finalize kernel (moe_moe_block_kernels). topk_weights
- * fp32 [T, K]; gamma bf16 [H] (zero-centred gain, 16-byte aligned), eps,
+ * calls leave). For tile_m <= 64: the routing kernel, then the input
+ * quantizer, one persistent launch of both GEMMs and the finalize, each a
+ * programmatic dependent of the kernel before it (moe_moe_block_kernels). topk_weights fp32
+ * [T, K]; gamma bf16 [H] (zero-centred gain, 16-byte aligned), eps,
  * weight_before_norm as for moe_post_expert_finalize; out 16-byte aligned;
  * the rest as for moe_nvfp4_experts_routed. */
 int moe_nvfp4_moe_block(const moe_weights* w, const int32_t* topk_ids,

@@ -246,8 +246,8 @@ def device_reads_host(t) -> bool:
 
 
 def moe_block_kernels(T: int, K: int, E: int, tile_m: int) -> int:
-    """Kernels moe_block launches for these sizes (2 when routing runs inside
-    the input quantizer and the finalize inside the GEMMs' launch)."""
+    """Kernels moe_block launches for these sizes (3 when routing runs inside
+    the input quantizer)."""
     n = load().moe_moe_block_kernels(T, K, E, tile_m)
     if n < 0:
         _check(n)

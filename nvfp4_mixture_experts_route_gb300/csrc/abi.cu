@@ -44,8 +44,7 @@ int launch_gemm2(const void*, const void*, const float*, const int32_t*, const i
 int launch_gemms_fused(const void*, const void*, const float*, const float*, const float*, const void*,
                        const void*, const float*, const int32_t*, const int32_t*, const int32_t*,
                        const uint8_t*, const uint8_t*, uint8_t*, uint8_t*, void*, float*, const void*, int,
-                       int32_t*, int, int, int, int, int, int, const int32_t*, const float*, const void*, float,
-                       void*, int, int, int32_t*, cudaStream_t, bool, const char**);
+                       int32_t*, int, int, int, int, int, int, int32_t*, cudaStream_t, bool, const char**);
 cudaError_t launch_finalize_sumsq(const void*, const float*, int, const int32_t*, const float*, const void*,
                                   float, int, int, int, void*, int32_t*, cudaStream_t);
 int launch_dense_bf16(const void*, const void*, int, int, int, void*, void*, int32_t*, cudaStream_t,
@@ -101,9 +100,8 @@ int route_dims(int T, int K, int E, int tile_m, RouteDims* d) {
 
 // Workspace of the expert body: permuted NVFP4 activations and the quantized
 // intermediate (codes row-major, scales as per-tile atoms; see quant.cu).
-// Counters after the per-route-tile ones: the unit ticket, the GEMM2
-// completion count and the finalize ticket, 128 bytes apart.
-constexpr int kDoneExtra = 65;
+// Counters after the per-route-tile ones: the one-launch GEMMs' unit ticket.
+constexpr int kDoneExtra = 1;
 
 struct WsLayout {
   size_t a_codes = 0, a_sf = 0, h_codes = 0, h_sf = 0, done = 0, total = 0;
@@ -129,8 +127,7 @@ int ws_layout(int T, int K, int E, int H, int I, int tile_m, WsLayout* w) {
   w->h_sf = off;
   off = round_up(off + (size_t)d.MT * (I / 64) * S * moe::kAtomBytes, 1024);
   // per route tile: GEMM1 completions the fused GEMM2 units wait for, then
-  // the fused GEMMs' unit ticket, the GEMM2 completion count (at MT + 32) and
-  // the ticket of the fused finalize units (at MT + 64)
+  // the fused GEMMs' unit ticket
   w->done = off;
   off = round_up(off + (size_t)(d.MT + kDoneExtra) * sizeof(int32_t), 1024);
   w->total = off;
@@ -340,17 +337,6 @@ struct SumSq {
   int wbn = 0;
 };
 
-// The post-expert finalize as the one-launch GEMMs' last units (with the
-// sums of squares above): out set.
-struct FusedFin {
-  const int32_t* e2p = nullptr;
-  const float* w = nullptr;
-  const void* gamma = nullptr;
-  float eps = 0.f;
-  void* out = nullptr;
-  int T = 0, K = 0;
-};
-
 static int experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, int I, int E,
                          int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
                          int32_t* status, void* stream, bool pdl, SumSq ss = SumSq()) {
@@ -382,8 +368,7 @@ int moe_experts_gemm2(const moe_weights* w, const moe_route* r, int T, int H, in
 // moe_nvfp4_experts).
 static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe_route* r, int T, int H,
                          int I, int E, int K, int tile_m, void* gemm2_rows, void* ws, size_t ws_bytes,
-                         int32_t* status, void* stream, bool pdl, bool zero_counters, SumSq ss = SumSq(),
-                         FusedFin fin = FusedFin()) {
+                         int32_t* status, void* stream, bool pdl, bool zero_counters, SumSq ss = SumSq()) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -405,7 +390,7 @@ static int experts_fused(const moe_weights* w, const float* a2_gscale, const moe
                                w->g2_alphas, r->tile_expert, r->tile_row_limit, r->totals,
                                base + L.a_codes, base + L.a_sf, base + L.h_codes, base + L.h_sf, gemm2_rows,
                                ss.row_ss, ss.gamma, ss.wbn, reinterpret_cast<int32_t*>(base + L.done), E, H, I,
-                               tile_m, L.P, L.MT, fin.e2p, fin.w, fin.gamma, fin.eps, fin.out, fin.T, fin.K, status,
+                               tile_m, L.P, L.MT, status,
                                as_stream(stream), pdl, &why);
   return rc ? fail(rc, "%s", why) : MOE_OK;
 }
@@ -507,7 +492,7 @@ static int routed_body(const moe_weights* w, const int32_t* topk_ids, const void
                        int E, int K, int tile_m, int32_t* expert_counts, int32_t* expert_offsets,
                        int32_t* expanded_to_permuted, int32_t* permuted_to_token, int32_t* tile_expert,
                        int32_t* tile_row_limit, int32_t* totals, void* gemm2_rows, void* ws, size_t ws_bytes,
-                       int32_t* status, void* stream, SumSq ss, FusedFin fin) {
+                       int32_t* status, void* stream, SumSq ss) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc || (rc = check_weights(w, true)) || (rc = check_weights(w, false))) return rc;
@@ -541,7 +526,7 @@ static int routed_body(const moe_weights* w, const int32_t* topk_ids, const void
       base + L.a_sf, reinterpret_cast<int32_t*>(base + L.done), status, as_stream(stream));
   if (err != cudaSuccess) return cuda_fail(err, "routing + input quantization");
   return experts_fused(w, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true,
-                       false, ss, fin);
+                       false, ss);
 }
 
 int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
@@ -552,17 +537,21 @@ int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, cons
                              size_t ws_bytes, int32_t* status, void* stream) {
   return routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
                      expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
-                     gemm2_rows, ws, ws_bytes, status, stream, SumSq(), FusedFin());
+                     gemm2_rows, ws, ws_bytes, status, stream, SumSq());
 }
 
-// The whole block: the finalize runs as the one-launch GEMMs' last units
-// where routing runs inside the quantizer and K fits the finalize units.
-static bool block_fused(int T, int K, int E, int tile_m) { return routed_fused(T, K, E, tile_m) && K <= 8; }
-
+// The whole block: the routing kernels, the expert body with the sums of
+// squares fused into GEMM2, then the finalize from them. (Routing inside the
+// quantizer, as moe_nvfp4_experts_routed does, measured no faster here.)
 int moe_moe_block_kernels(int T, int K, int E, int tile_m) {
-  const int n = moe_routed_experts_kernels(T, K, E, tile_m);
+  const int n = moe_route_kernels(T, K, E);
   if (n < 0) return n;
-  return block_fused(T, K, E, tile_m) ? n : n + (T > 0 ? 1 : 0);
+  const int b = moe_experts_kernels(tile_m);
+  if (b < 0) return b;
+  RouteDims d;
+  int rc = route_dims(T, K, E, tile_m, &d);
+  if (rc) return rc;
+  return n + (d.P > 0 ? b + 1 : 0);
 }
 
 int moe_nvfp4_moe_block(const moe_weights* w, const int32_t* topk_ids, const float* topk_weights, const void* x,
@@ -581,22 +570,27 @@ int moe_nvfp4_moe_block(const moe_weights* w, const int32_t* topk_ids, const flo
     return fail(MOE_ERR_INVALID_ARG, "topk_weights, gamma and out must be given; gamma and out 16-byte aligned");
   SumSq ss;
   if ((rc = sumsq_args(gamma, weight_before_norm, row_sumsq, &ss))) return rc;
-  if (block_fused(T, K, E, tile_m)) {
-    FusedFin fin;
-    fin.e2p = expanded_to_permuted;
-    fin.w = topk_weights;
-    fin.gamma = gamma;
-    fin.eps = eps;
-    fin.out = out;
-    fin.T = T;
-    fin.K = K;
-    return routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
-                       expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
-                       gemm2_rows, ws, ws_bytes, status, stream, ss, fin);
+  if ((rc = check_weights(w, true)) || (rc = check_weights(w, false)) || (rc = check_ws(ws, ws_bytes, L)))
+    return rc;
+  if (L.P > 0) {  // what the body checks, before anything is enqueued
+    if (x) {
+      if (!a1_gscale) return fail(MOE_ERR_INVALID_ARG, "a1_gscale is null");
+      if (!aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    } else {
+      if (!a || !a_sf) return fail(MOE_ERR_INVALID_ARG, "give x, or a and a_sf");
+      if (!aligned(a, 16) || !aligned(a_sf, 4))
+        return fail(MOE_ERR_INVALID_ARG, "a must be 16-byte and a_sf 4-byte aligned");
+    }
+    if (!a2_gscale) return fail(MOE_ERR_INVALID_ARG, "a2_gscale is null");
+    if (!gemm2_rows || !aligned(gemm2_rows, 16))
+      return fail(MOE_ERR_INVALID_ARG, "gemm2_rows must be non-null and 16-byte aligned");
   }
-  rc = routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
-                   expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
-                   gemm2_rows, ws, ws_bytes, status, stream, ss, FusedFin());
+  rc = moe_route_permute(topk_ids, T, K, E, tile_m, expert_counts, expert_offsets, expanded_to_permuted,
+                         permuted_to_token, tile_expert, tile_row_limit, totals, status, stream);
+  if (rc || L.P == 0) return rc;
+  const moe_route r{permuted_to_token, tile_expert, tile_row_limit, totals, expanded_to_permuted};
+  rc = experts_body(w, x, a, a_sf, a1_gscale, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status,
+                    stream, ss);
   if (rc) return rc;
   return moe_post_expert_finalize_sumsq(gemm2_rows, row_sumsq, L.P, expanded_to_permuted, topk_weights, gamma, eps,
                                         T, K, H, out, status, stream);

@@ -10,6 +10,7 @@
 // reduction, then adds w * u / rms into fp32 registers. HBM traffic: K rows
 // of H bf16 in, one row out.
 #include "common.cuh"
+#include "finalize_units.cuh"
 
 namespace moe {
 
@@ -560,11 +561,72 @@ __global__ void __launch_bounds__(kFinSsThreads) finalize_sumsq_kernel(
   }
 }
 
+// The same finalize for K <= 8 in units of (token, 1024 columns), four warps
+// each (finalize_units.cuh, the arithmetic and order the one-launch GEMMs'
+// finalize units use): a persistent grid walks the units, reading the next
+// unit's routing while it finishes the current one, so that no CTA waits
+// through a coefficient phase with nothing else in flight.
+__global__ void __launch_bounds__(32 * kFinUnitWarps) finalize_sumsq_units_kernel(FinArgs a, int T) {
+  __shared__ float coef[kFinUnitMaxK];
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kThreads = 32 * kFinUnitWarps;
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int slices = (a.H / 8 + kThreads - 1) / kThreads, n = T * slices;
+  int u = blockIdx.x;
+  FinPre f{};
+  if (u < n) f = fin_prepare(a, u / slices, (u % slices) * kThreads + 32 * wi + lane, lane);
+  while (u < n) {
+    const int un = u + gridDim.x;
+    FinPre g{};
+    if (un < n) g = fin_prepare(a, un / slices, (un % slices) * kThreads + 32 * wi + lane, lane);
+    fin_finish_inl(a, f, lane, wi, coef, kThreads);
+    fin_bar_sync(kThreads);  // every warp has read coef before the next unit writes it
+    f = g;
+    u = un;
+  }
+}
+
 cudaError_t launch_finalize_sumsq(const void* rows, const float* row_ss, int num_rows, const int32_t* e2p,
                                   const float* w, const void* gamma, float eps, int T, int K, int H, void* out,
                                   int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   if (K > kFinMaxK) return cudaErrorInvalidValue;
+  if (K <= kFinUnitMaxK) {
+    FinArgs a;
+    a.rows = reinterpret_cast<const __nv_bfloat16*>(rows);
+    a.row_ss = row_ss;
+    a.e2p = e2p;
+    a.w = w;
+    a.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
+    a.out = reinterpret_cast<__nv_bfloat16*>(out);
+    a.status = status;
+    a.eps = eps;
+    a.K = K;
+    a.H = H;
+    a.num_rows = num_rows;
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0, n = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 148;
+      sms = n;
+    }
+    static int per_sm = 0;
+    if (per_sm == 0) {
+      int b = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, finalize_sumsq_units_kernel, 32 * kFinUnitWarps, 0) !=
+              cudaSuccess ||
+          b < 1)
+        b = 4;
+      per_sm = b;
+    }
+    const long long units = (long long)T * ((H / 8 + 32 * kFinUnitWarps - 1) / (32 * kFinUnitWarps));
+    const long long slots = (long long)sms * per_sm;
+    const int grid = (int)(units < slots ? units : slots);
+    return launch_kernel(finalize_sumsq_units_kernel, dim3(grid), dim3(32 * kFinUnitWarps), 0, stream, true, a, T);
+  }
   return launch_kernel(finalize_sumsq_kernel, dim3(T), dim3(kFinSsThreads), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(rows), row_ss, num_rows, e2p, w,
                        reinterpret_cast<const __nv_bfloat16*>(gamma), eps, K, H,

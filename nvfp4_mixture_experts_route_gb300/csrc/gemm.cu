@@ -110,20 +110,6 @@ struct GemmParams {
   // both GEMMs in one grid: the experts and the route tiles the buffers hold
   // (bounds for the head prefetch, which reads the routing as a hint)
   int num_experts, max_tiles;
-  // Both GEMMs in one grid, optional (fin_out set; row_ss set too): the
-  // post-expert finalize of fin_T tokens, after the GEMM units, in units of
-  // (token, 256 columns) that epilogue warps with no GEMM work left draw from
-  // fin_ticket. A unit starts once every GEMM2 unit has stored its rows and
-  // sums of squares: gemm2_done counts the epilogue warps of GEMM2 units that
-  // have (both zeroed with done).
-  int32_t* gemm2_done;
-  int32_t* fin_ticket;
-  const int32_t* fin_e2p;      // expanded_to_permuted [fin_T, fin_K]
-  const float* fin_w;          // topk_weights [fin_T, fin_K]
-  const __nv_bfloat16* fin_gamma;  // [H]: out = bf16((1 + gamma) * sum)
-  __nv_bfloat16* fin_out;      // [fin_T, H]
-  float fin_eps;
-  int fin_T, fin_K, fin_rows;  // fin_rows: rows of the GEMM2 row buffer
   // Load the weights and their scales with an L2 evict_first policy (they
   // stream through once), so that the rows, sums and intermediate the grid
   // writes and reads again stay in L2.
@@ -145,22 +131,6 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
     }
   }
   return x[0];
-}
-
-// The norm's gain for 32 consecutive columns (uniform across the warp).
-__device__ __forceinline__ void gain32(const __nv_bfloat16* gamma, int col0, float (&g)[32]) {
-  const uint4* src = reinterpret_cast<const uint4*>(gamma + col0);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 u = __ldg(src + j);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 f = __bfloat1622float2(h[q]);
-      g[8 * j + 2 * q] = 1.f + f.x;
-      g[8 * j + 2 * q + 1] = 1.f + f.y;
-    }
-  }
 }
 
 // Launch shape per route-tile size: CTAs per SM, accumulator buffers, K=256
@@ -312,114 +282,6 @@ __host__ __device__ constexpr int gemm_threads(int mode, int tile_m) {
 // fits at once). The tile's launch shape, pipeline depth and scale-atom
 // count are compile-time, so the MMA issuer's per-stage loops unroll and its
 // descriptors are base + constant.
-// Both GEMMs in one grid: the finalize units, each done by the CTA's four
-// epilogue warps together (the same arithmetic, in the same order, as the
-// finalize from sums of squares, finalize_sumsq_kernel): token t, 1024
-// columns, warp wi taking hidden vectors (8 columns) v0 + 32 wi + lane.
-// fin_prepare reads what does not depend on GEMM2 (the token's rows and
-// weights, lane k holding route k's; the lane's gain vector) and may run
-// before the GEMM2 units have completed. fin_finish then loads the lane's
-// vector of every route row and, at the same time, warp wi's share of the
-// sums of squares: routes 2 wi and 2 wi + 1, each over 16 lanes, as the
-// float4s of its H/32 partials (lane j takes float4s j, j + 16, ...,
-// adding .x, .y, .z, .w in turn; then an xor butterfly over the 16 lanes);
-// coef_k = w[t, k] / sqrt(total / H + eps) goes through shared memory to
-// the other warps (a named barrier over the epilogue warps), and every lane
-// accumulates coef_k * r_k in fp32 in route order; out = bf16((1 + gamma)
-// * sum). Rows and sums are read from L2 (ld.cg): they were written during
-// this launch.
-constexpr int kFinFusedMaxK = 8;
-
-__device__ __forceinline__ void epi_bar_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-struct FinPre {
-  int t, v, pk;
-  float wk;
-  uint4 gain;
-};
-
-__device__ __forceinline__ FinPre fin_prepare(const GemmParams& p, int t, int v, int lane) {
-  const int K = p.fin_K, H = p.g[1].out_cols;
-  FinPre f;
-  f.t = t;
-  f.v = v;
-  f.pk = -1;
-  f.wk = 0.f;
-  if (lane < K) {
-    f.pk = __ldcg(p.fin_e2p + (size_t)t * K + lane);
-    if (f.pk < -1 || f.pk >= p.fin_rows) {
-      record_status(p.status, MOE_ERR_INVALID_ROUTE);
-      f.pk = -1;
-    }
-    f.wk = __ldcg(p.fin_w + (size_t)t * K + lane);
-  }
-  f.gain = f.v < H / 8 ? __ldg(reinterpret_cast<const uint4*>(p.fin_gamma + 8 * f.v)) : make_uint4(0, 0, 0, 0);
-  return f;
-}
-
-__device__ __noinline__ void fin_finish(const GemmParams& p, const FinPre& f, int lane, int wi, float* coef_s,
-                                        int nthreads) {
-  const int K = p.fin_K, H = p.g[1].out_cols, G4 = H / 128;
-  const bool on = f.v < H / 8;
-  uint4 raw[kFinFusedMaxK];
-#pragma unroll
-  for (int k = 0; k < kFinFusedMaxK; ++k) {
-    const int rp = __shfl_sync(0xFFFFFFFFu, f.pk, k);
-    raw[k] = (on && k < K && rp >= 0) ? __ldcg(reinterpret_cast<const uint4*>(p.rows + (size_t)rp * H) + f.v)
-                                      : make_uint4(0, 0, 0, 0);
-  }
-  // this half-warp's route and its share of the partial sums
-  const int k = 2 * wi + (lane >> 4), j = lane & 15;
-  const int my = __shfl_sync(0xFFFFFFFFu, f.pk, k & 31);
-  const float wk = __shfl_sync(0xFFFFFFFFu, f.wk, k & 31);
-  const bool mine = k < K && my >= 0;
-  const float4* src = reinterpret_cast<const float4*>(p.row_ss + (size_t)(mine ? my : 0) * (H / 32));
-  float ss = 0.f;
-  for (int m0 = j; m0 < G4; m0 += 64) {
-    float4 x[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = (mine && m0 + 16 * i < G4) ? __ldcg(src + m0 + 16 * i) : make_float4(0, 0, 0, 0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (m0 + 16 * i < G4) {
-        ss += x[i].x;
-        ss += x[i].y;
-        ss += x[i].z;
-        ss += x[i].w;
-      }
-    }
-  }
-#pragma unroll
-  for (int d = 1; d < 16; d <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, d);
-  if (j == 0 && k < K) coef_s[k] = mine ? wk / sqrtf(ss / (float)H + p.fin_eps) : 0.f;
-  epi_bar_sync(nthreads);
-  float2 acc[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int kk = 0; kk < kFinFusedMaxK; ++kk) {
-    if (kk >= K) break;
-    const float c = coef_s[kk];
-    const float2 ck = make_float2(c, c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[kk]);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = ffma2(__bfloat1622float2(h[q]), ck, acc[q]);
-  }
-  if (!on) return;
-  const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&f.gain);
-  uint4 o;
-  __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 gf = __bfloat1622float2(gh[q]);
-    const float2 r = fmul2(acc[q], make_float2(1.f + gf.x, 1.f + gf.y));  // gain centre added in fp32
-    oh[q] = __floats2bfloat162_rn(r.x, r.y);
-  }
-  *reinterpret_cast<uint4*>(p.fin_out + (size_t)f.t * H + 8 * f.v) = o;
-}
-
 // Both GEMMs in one grid: L2 prefetch of the first kHeadPrefetchStages
 // stages of weights and weight scales of unit blockIdx.x, from a routing
 // read before the previous kernel has completed (a hint: the route-tile
@@ -469,9 +331,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __shared__ __align__(8) uint64_t uq_empty[kUnitQ];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int fin_go;  // the finalize may start: 1, or -1 (gave up)
-  __shared__ int fin_unit;  // the finalize unit the epilogue warps do next
-  __shared__ float fin_coef[kFinFusedMaxK];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // weight tiles per route tile of each GEMM, and the units: GEMM1's, then GEMM2's
@@ -492,7 +351,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     if (tid == 0) pdl_trigger();
   }
   const int ntiles_early = late ? 0 : __ldcg(p.totals);
-  if (!late && p.fin_out == nullptr && (int)blockIdx.x >= ntiles_early * (tw1 + tw2)) {
+  if (!late && (int)blockIdx.x >= ntiles_early * (tw1 + tw2)) {
     // Even an idle CTA must not let this grid complete before its
     // predecessor: the kernels after it rely on that ordering.
     if (p.prefetch) pdl_wait();
@@ -537,7 +396,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       mbar_init(smem_u32(&uq_empty[q]), 1 + EPW);  // the MMA issuer and every epilogue warp
     }
     abort_flag = 0;
-    fin_go = 0;
     fence_barrier_init();
     if (MODE != 2) {
       tma_prefetch_desc(&tmA1);
@@ -926,6 +784,15 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const int cc = 2 * half + k;
+              // the gain of these 32 columns (weight-before-norm sums of
+              // squares), loaded as packed bf16 before the conversions so
+              // that they hide the loads' latency
+              uint4 gu[4];
+              if (p.row_ss != nullptr && p.ss_wbn) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.ss_gamma + mt * kWTile + 32 * cc);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) gu[j] = __ldg(src + j);
+              }
               uint32_t w[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -934,15 +801,17 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
                 w[i] = *reinterpret_cast<const uint32_t*>(&h2);
               }
               if (p.row_ss != nullptr) {
-                // of the stored (bf16) values, gain-weighted for the
-                // weight-before-norm reading
-                float gn[32];
-                if (p.ss_wbn) gain32(p.ss_gamma, mt * kWTile + 32 * cc, gn);
+                // of the stored (bf16) values, gain-weighted (g = 1 + gamma)
+                // for the weight-before-norm reading
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                   const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-                  const float a = p.ss_wbn ? f.x * gn[2 * i] : f.x;
-                  const float c = p.ss_wbn ? f.y * gn[2 * i + 1] : f.y;
+                  float a = f.x, c = f.y;
+                  if (p.ss_wbn) {
+                    const float2 gf = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&gu[i >> 2])[i & 3]);
+                    a = f.x * (1.f + gf.x);
+                    c = f.y * (1.f + gf.y);
+                  }
                   ss2[k] = fmaf(a, a, ss2[k]);
                   ss2[k] = fmaf(c, c, ss2[k]);
                 }
@@ -1020,77 +889,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         __syncwarp();
         if (lane == 0) atomicAdd(p.done + tau, 1);
       }
-      if (MODE == 3 && !g1 && p.fin_out != nullptr) {
-        // This warp's share of the unit's rows and sums of squares is
-        // stored: publish it to the finalize units (release at GPU scope).
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(p.gemm2_done, 1);
-      }
       ++uc;
-    }
-    if (MODE == 3 && p.fin_out != nullptr) {
-      // The finalize, once every GEMM2 unit has stored its rows. The CTA's
-      // epilogue warps, all past their GEMM work, draw finalize units (token,
-      // 1024 columns) from the finalize ticket one at a time and do each
-      // together -- a CTA draws only when free, so the units spread over the
-      // CTAs that finish first. The first unit is drawn, and what of it does
-      // not depend on GEMM2 read, while the last GEMM2 units finish. The
-      // first epilogue warp's lane 0 alone draws, and polls the global count
-      // (with a short back-off); the others learn both through shared memory
-      // after a named barrier over the epilogue warps, which every one of
-      // them reaches whether its GEMM work ended or gave up.
-      static_assert(EPW * 2 >= kFinFusedMaxK, "two routes' sums per epilogue warp");
-      constexpr int kEpiThreads = 32 * EPW;
-      const int wi = warp - 2;
-      const int nvec = p.g[1].out_cols / 8;
-      const int slices = (nvec + kEpiThreads - 1) / kEpiThreads;
-      const int n_fin = p.fin_T * slices;
-      epi_bar_sync(kEpiThreads);
-      if (wi == 0 && lane == 0) fin_unit = *reinterpret_cast<volatile int*>(&abort_flag) ? n_fin : atomicAdd(p.fin_ticket, 1);
-      epi_bar_sync(kEpiThreads);
-      int f = *reinterpret_cast<volatile int*>(&fin_unit);
-      FinPre pre{};
-      if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * kEpiThreads + 32 * wi + lane, lane);
-      if (wi == 0 && lane == 0) {
-        bool ok = f < n_fin;
-        if (ok) {
-          const uint64_t t0 = global_timer_ns();
-          const int32_t target = ntiles * tw2 * EPW;
-          for (;;) {
-            int32_t v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.gemm2_done) : "memory");
-            if (v >= target) break;
-            if (abort_flag) {
-              ok = false;
-              break;
-            }
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-              record_status(p.status, MOE_ERR_TIMEOUT);
-              abort_flag = 1;
-              ok = false;
-              break;
-            }
-            __nanosleep(32);
-          }
-        }
-        fin_go = ok ? 1 : -1;
-      }
-      epi_bar_sync(kEpiThreads);
-      if (*reinterpret_cast<volatile int*>(&fin_go) > 0) {
-        __threadfence();
-        while (f < n_fin) {
-          // the next unit's ticket, drawn now so that the atomic's round trip
-          // overlaps this unit's loads
-          int next = 0;
-          if (wi == 0 && lane == 0) next = atomicAdd(p.fin_ticket, 1);
-          fin_finish(p, pre, lane, wi, fin_coef, kEpiThreads);
-          if (wi == 0 && lane == 0) fin_unit = next;
-          epi_bar_sync(kEpiThreads);
-          f = *reinterpret_cast<volatile int*>(&fin_unit);
-          if (f < n_fin) pre = fin_prepare(p, f / slices, (f % slices) * kEpiThreads + 32 * wi + lane, lane);
-        }
-      }
     }
   }
 
@@ -1160,8 +959,7 @@ static cudaError_t launch_one(const CUtensorMap* maps, GemmParams& p, int max_ti
   // ctas_per_sm CTAs per SM (all resident at once); CTAs past the live unit
   // count exit at once.
   const long long units =
-      (long long)max_tiles * ((MODE != 2 ? p.g[0].rows_w : 0) + (MODE != 1 ? p.g[1].rows_w : 0)) / kWTile +
-      (p.fin_out != nullptr ? 1 : 0);
+      (long long)max_tiles * ((MODE != 2 ? p.g[0].rows_w : 0) + (MODE != 1 ? p.g[1].rows_w : 0)) / kWTile;
   long long slots = (long long)ctas_per_sm(p.tile_m) * sm_count();
   if (MODE == 3) {
     // No more CTAs than fit at once (more would only queue behind the
@@ -1283,9 +1081,7 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
                        const int32_t* tile_row_limit, const int32_t* totals, const uint8_t* a_codes,
                        const uint8_t* a_sf, uint8_t* h_codes, uint8_t* h_sf, void* rows, float* row_ss,
                        const void* ss_gamma, int ss_wbn, int32_t* done, int E, int H, int I, int tile_m, int P,
-                       int max_tiles, const int32_t* fin_e2p, const float* fin_w, const void* fin_gamma,
-                       float fin_eps, void* fin_out, int fin_T, int fin_K, int32_t* status, cudaStream_t stream,
-                       bool pdl, const char** why) {
+                       int max_tiles, int32_t* status, cudaStream_t stream, bool pdl, const char** why) {
   CUtensorMap maps[4];
   GemmParams p{};
   if (!gemm1_side(p, &maps[0], &maps[1], p_w13, p_w13_sf, g1_alphas, g1_scale_c, a_codes, a_sf, E, H, I,
@@ -1310,20 +1106,6 @@ int launch_gemms_fused(const void* p_w13, const void* p_w13_sf, const float* g1_
   p.num_experts = E;
   p.max_tiles = max_tiles;
   p.w_evict_first = 1;
-  if (fin_out != nullptr) {
-    // the GEMM2 completion count and the finalize units' ticket follow the
-    // unit ticket, each in a 128-byte line of its own
-    p.gemm2_done = done + max_tiles + 32;
-    p.fin_ticket = done + max_tiles + 64;
-    p.fin_e2p = fin_e2p;
-    p.fin_w = fin_w;
-    p.fin_gamma = reinterpret_cast<const __nv_bfloat16*>(fin_gamma);
-    p.fin_out = reinterpret_cast<__nv_bfloat16*>(fin_out);
-    p.fin_eps = fin_eps;
-    p.fin_T = fin_T;
-    p.fin_K = fin_K;
-    p.fin_rows = P;
-  }
   p.status = status;
   p.tile_m = tile_m;
   if (launch_mode<3>(maps, p, max_tiles, stream, pdl) != cudaSuccess) {

@@ -64,9 +64,8 @@ __device__ __forceinline__ void quantize_permute_items(
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale, const int32_t* e2p,
     const int32_t* tile_row_limit, int n_tiles, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done) {
-  // the per-tile GEMM1 completion counters, the unit ticket, the GEMM2
-  // completion count and the finalize ticket of the one-launch expert GEMMs
-  // that follow
+  // the per-tile GEMM1 completion counters and the unit ticket of the
+  // one-launch expert GEMMs that follow
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_done; i += gridDim.x * blockDim.x) done[i] = 0;
   const int ng = H / 64;  // four-block groups per row
   const int nb = H / 16;
@@ -191,7 +190,7 @@ __global__ void __launch_bounds__(256) route_quantize_kernel(
   if (writer) __threadfence();
   pdl_trigger();
   quantize_permute_items(x, a_in, a_sf_in, gscale, e2p_s, limit_s, totals_s[0], T, K, H, tile_m, codes, scales, done,
-                         MT + 65);
+                         MT + 1);
 }
 
 // Scale atoms <-> row-major scales [rows, K/16].
@@ -223,9 +222,8 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                                     int K, int H, int tile_m, int P, int n_done, uint8_t* codes,
                                     uint8_t* scales, int32_t* done, cudaStream_t stream) {
   (void)P;
-  // per route tile a GEMM1 counter, then the unit ticket, the GEMM2 count
-  // and the finalize ticket (65 ints)
-  const int MT = n_done - 65;
+  // per route tile a GEMM1 counter, then the unit ticket
+  const int MT = n_done - 1;
   // enough warps for one padding item each (one global read then one store
   // per lane), and one warp per token item
   const long long pad_threads = (long long)MT * (H / 64) * 32,

@@ -23,11 +23,11 @@ class NvFp4MoE:
         [E]. ``gamma_bits``: bf16 bit patterns [H] (uint16) or a bf16 tensor.
         ``fused_norm``: True: the whole block through moe_nvfp4_moe_block
         (GEMM2's epilogue also writes the rows' sums of squares; the finalize
-        runs from them, inside the GEMMs' launch where the sizes allow);
-        False: moe_nvfp4_experts_routed, then moe_post_expert_finalize; None
-        (the default): the first where it is 2 kernels (decode batches), the
-        second otherwise (at prefill the sums of squares slow GEMM2 more than
-        they save in the finalize)."""
+        runs from them); False: moe_nvfp4_experts_routed, then
+        moe_post_expert_finalize; None (the default): the first for route
+        tiles of at most 64 rows (decode batches), the second otherwise (at
+        prefill the sums of squares cost GEMM2 more than they save in the
+        finalize)."""
         dev = torch.device(device)
         t = {k: torch.as_tensor(raw[k]).to(dev) for k in ("w13", "w13_sf", "w2", "w2_sf")}
         self.E, twoI, half_h = t["w13"].shape
@@ -78,7 +78,7 @@ class NvFp4MoE:
         o = b["out"] if out is None else out
         fused = self.fused_norm
         if fused is None:
-            fused = B.moe_block_kernels(T, K, self.E, self.tile_m) == 2
+            fused = B.experts_kernels(self.tile_m) == 2
         if fused:
             B.moe_block(self.weights, topk_ids, topk_weights, b["route"], x=x, a1_gscale=self.a1_gscale,
                         a2_gscale=self.a2_gscale, gamma=self.gamma, eps=self.eps,
@@ -136,14 +136,15 @@ class NvFp4MoE:
         return self._buffers[key]
 
     def zero_copy(self, T: int, K: int) -> bool:
-        """Whether ``replay_host(T, K)`` runs zero-copy: at decode sizes (the
-        whole block in 2 kernels) its kernels read the step's inputs straight
+        """Whether ``replay_host(T, K)`` runs zero-copy: at decode sizes (route
+        tiles of at most 64 rows) its kernels read the step's inputs straight
         from ``host_inputs`` and the finalize writes ``host_out`` directly,
         where the device maps that page-locked memory at its own address;
         otherwise two copies run around the step."""
         h = self.host_buffers(T, K)
-        fused = self.fused_norm if self.fused_norm is not None else B.moe_block_kernels(T, K, self.E, self.tile_m) == 2
-        return bool(fused and B.moe_block_kernels(T, K, self.E, self.tile_m) == 2 and
+        decode = B.experts_kernels(self.tile_m) == 2
+        fused = self.fused_norm if self.fused_norm is not None else decode
+        return bool(fused and decode and
                     B.device_reads_host(h["host_inputs"]) and B.device_reads_host(h["host_out"]))
 
     def replay_host(self, T: int, K: int) -> torch.Tensor:

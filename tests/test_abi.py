@@ -139,15 +139,16 @@ def test_routed_experts_kernel_count():
 
 
 def test_moe_block_kernel_count():
-    """The whole block is 2 kernels where routing runs inside the quantizer
-    and K <= 8 (the finalize as the GEMMs' last units); otherwise the routed
-    body's kernels and the finalize kernel."""
-    assert B.moe_block_kernels(8, 8, 128, 32) == 2
-    assert B.moe_block_kernels(64, 8, 128, 32) == 2
-    assert B.moe_block_kernels(8, 12, 128, 32) == 2 + 1
-    assert B.moe_block_kernels(257, 8, 128, 32) == 1 + 2 + 1
+    """The whole block is the routing kernels (1 or 3), the body's (2 for
+    tiles of at most 64 rows, else 3) and the finalize; nothing but the
+    routing kernel when there are no routes."""
+    assert B.moe_block_kernels(8, 8, 128, 32) == 1 + 2 + 1
+    assert B.moe_block_kernels(64, 8, 128, 32) == 1 + 2 + 1
+    assert B.moe_block_kernels(8, 12, 128, 32) == 1 + 2 + 1
     assert B.moe_block_kernels(8192, 8, 128, 128) == 3 + 3 + 1
     assert B.moe_block_kernels(0, 8, 128, 32) == 1
+    with pytest.raises(B.MoeError):
+        B.moe_block_kernels(8, 8, 128, 48)
 
 
 def test_selftest_arguments_refused_before_launch(lib):

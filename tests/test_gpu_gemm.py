@@ -316,10 +316,9 @@ def _check_block(parts, block):
 def test_block_entry_matches_its_parts(small_cases, idx, wbn):
     """moe_nvfp4_moe_block equals moe_route_permute, moe_nvfp4_experts_sumsq
     and moe_post_expert_finalize_sumsq bit for bit (metadata, live rows,
-    their sums of squares, the output), whether the finalize ran as the
-    one-launch GEMMs' last units (2 kernels) or as its own kernel, in both
-    norm readings (gamma ~ N(0, 1)), and again on a second call over the same
-    buffers."""
+    their sums of squares, the output), with the finalize by units (K <= 8)
+    or per token (K = 12), in both norm readings (gamma ~ N(0, 1)), and again
+    on a second call over the same buffers."""
     if idx < len(SMALL):
         w, raw, batch, tile, a1, a2 = small_cases[idx]
     else:
@@ -329,21 +328,19 @@ def test_block_entry_matches_its_parts(small_cases, idx, wbn):
     raw = dict(raw)
     raw["gamma"] = inputs._to_bf16_bits(np.random.default_rng(5).standard_normal(w.H))
     prep = Prepared(raw)
-    fused = w.T * w.K <= 2048 and w.E <= 256 and tile <= 64 and w.K <= 8
     n = B.moe_block_kernels(w.T, w.K, w.E, tile)
-    assert (n == 2) == fused
+    assert n == B.route_kernels(w.T, w.K, w.E) + B.experts_kernels(tile) + 1
     _check_block(*_block_vs_parts(prep, batch["topk_ids"], batch, tile, a1, a2, wbn))
 
 
 def test_block_entry_against_the_oracle(small_cases, record_property):
-    """The whole block (finalize units inside the GEMMs' launch) against the
-    oracle's layer: output within the end-to-end bar, and the oracle's
-    finalize of the block's own rows within 2e-3."""
+    """The whole block (sums of squares in GEMM2, the finalize from them)
+    against the oracle's layer: output within the end-to-end bar, and the
+    oracle's finalize of the block's own rows within 2e-3."""
     w, raw, batch, tile, a1, a2 = small_cases[1]
     raw = dict(raw)
     raw["gamma"] = inputs._to_bf16_bits(np.random.default_rng(6).standard_normal(w.H))
     prep = Prepared(raw)
-    assert B.moe_block_kernels(w.T, w.K, w.E, tile) == 2
     for wbn in (True, False):
         (_, r_a, _, _, _), (st, r_b, got) = _block_vs_parts(prep, batch["topk_ids"], batch, tile, a1, a2, wbn,
                                                             calls=1)
@@ -628,14 +625,14 @@ def test_routed_entry_full_size(full, name):
 
 @pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf"])
 def test_block_entry_full_size(full, name):
-    """At full size the whole block in 2 kernels (routing inside the
-    quantizer, the finalize inside the GEMMs' launch) equals its parts bit
-    for bit."""
+    """At full size the whole block in 4 kernels (routing, the quantizer,
+    both GEMMs with the sums of squares in one launch, the finalize) equals
+    its parts bit for bit."""
     raw, prep = full
     w = inputs.WORKLOADS[name]
     a1, a2 = inputs.global_scales(w)
     batch = inputs.make_batch(w)
-    assert B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 2
+    assert B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 4
     parts, block = _block_vs_parts(prep, batch["topk_ids"], batch, w.tile_m, a1, a2, True)
     assert parts[0] == 0
     _check_block(parts, block)
@@ -914,11 +911,10 @@ def test_timed_launch_path_matches_split_path(full, name):
     status, fused = _fused_rows(prep, batch, w.tile_m, a1, a2, calls=1)
     assert status == 0 and np.array_equal(fused[0], split["rows"])
     # The layer through the whole-block call (the norm's sums of squares
-    # fused into GEMM2, the finalize from them, inside the GEMMs' launch at
-    # decode sizes: what bench.py times there): the same rows bit for bit;
-    # the output equal up to the order of the fp32 sums; its graph replays
-    # equal its eager call; the layer's default picks it exactly where it is
-    # 2 kernels.
+    # fused into GEMM2, the finalize from them: what bench.py times at decode
+    # sizes): the same rows bit for bit; the output equal up to the order of
+    # the fp32 sums; its graph replays equal its eager call; the layer's
+    # default picks it exactly for route tiles of at most 64 rows.
     del moe
     torch.cuda.empty_cache()
     fn = NvFp4MoE(raw, a1, a2, raw["gamma"], tile_m=w.tile_m, fused_norm=True)
@@ -939,10 +935,10 @@ def test_timed_launch_path_matches_split_path(full, name):
     assert np.array_equal(bf16_host_f64(fn.replay(w.T, w.K)), got)
     hb = fn.host_buffers(w.T, w.K)
     hb["host_inputs"].copy_(gb["inputs"].cpu())
-    assert fn.zero_copy(w.T, w.K) == (B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 2)
+    assert fn.zero_copy(w.T, w.K) == (B.experts_kernels(w.tile_m) == 2)
     host = fn.replay_host(w.T, w.K)
     torch.cuda.synchronize()
     assert np.array_equal(bf16_host_f64(host), got)
     fn.fused_norm = None
     auto = bf16_host_f64(fn.forward(x, ids, tw)[0])
-    assert np.array_equal(auto, got if B.moe_block_kernels(w.T, w.K, w.E, w.tile_m) == 2 else split["out"])
+    assert np.array_equal(auto, got if B.experts_kernels(w.tile_m) == 2 else split["out"])
