@@ -54,10 +54,10 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # and the SHA-256 of the kernel sources it was taken on (gemm.cu,
 # common.cuh, layout.cuh in that order): once those change, traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_343_232 + 5_146_368,
-                  "sources": "70999906871602a428c3b1ef5cb63ff6c8a0c4117862f409e17bc6d407d9b4c5"},
-    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_721_594_880 + 86_582_784,
-                           "sources": "70999906871602a428c3b1ef5cb63ff6c8a0c4117862f409e17bc6d407d9b4c5"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_330_432 + 5_168_896,
+                  "sources": "cf565adca50bc94e8f51649b6d17c30b8f6d926057999492f03b6386bf143c83"},
+    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_722_795_008 + 85_284_096,
+                           "sources": "cf565adca50bc94e8f51649b6d17c30b8f6d926057999492f03b6386bf143c83"},
 }
 
 
