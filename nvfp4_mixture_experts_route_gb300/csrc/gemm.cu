@@ -13,7 +13,7 @@
 // rows are permuted route rows of one routing tile (all of one expert). A
 // work unit is one (route tile tau, weight tile mt) pair over the whole K.
 //
-// Persistent, warp-specialised kernel, one to three CTAs per SM (tile_cfg
+// Persistent, warp-specialised kernel, one or two CTAs per SM (tile_cfg
 // below), 2 + 4 or 2 + 8 warps (+ 1 for GEMM1 over 128-row tiles):
 //   - warp 0 / lane 0: TMA producer. Walks this CTA's units in order and, per
 //     pipeline stage (K = 256 elements = 128 bytes per row per chunk), loads
@@ -64,7 +64,7 @@ constexpr int kMaxStages = 8;
 // Stages of its first unit's weights a CTA of the one-launch GEMMs prefetches
 // into L2 while the previous kernel (the quantizer) finishes.
 #ifndef MOE_HEAD_PREFETCH_STAGES
-#define MOE_HEAD_PREFETCH_STAGES 2
+#define MOE_HEAD_PREFETCH_STAGES 4
 #endif
 constexpr int kHeadPrefetchStages = MOE_HEAD_PREFETCH_STAGES;
 constexpr int kEpiStride = 33;  // floats per staged route column (32 + pad)
@@ -139,9 +139,10 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 // each instruction occupies that thread for a fixed time whatever its size
 // (measured with a pipe probe: about 26 ns per copy or MMA and 175 ns per
 // commit), so the tensor core is fed by several CTAs per SM wherever tensor
-// memory and shared memory allow; the decode tiles (32 rows) run three CTAs
-// per SM (GEMM1 on the b = 8 decode: 254 us with one CTA per SM, 136 us with
-// two, 121 us with three). Each epilogue warp works through its accumulator
+// memory and shared memory allow; the decode tiles (32 and 64 rows) run two
+// CTAs per SM with a 4- or 3-stage ring (one CTA per SM: 1.5 x slower; three
+// with 2-stage rings: 1-2 % slower at b = 8, 2 % at b = 64, once the weights
+// are loaded evict_first). Each epilogue warp works through its accumulator
 // columns as one dependent instruction stream, so the larger tiles take two
 // warps per TMEM lane quadrant (8 in all) that split the route columns.
 //
@@ -156,7 +157,7 @@ struct TileCfg {
   bool route_m;
 };
 __host__ __device__ constexpr TileCfg tile_cfg(int tile_m) {
-  return tile_m <= 32    ? TileCfg{3, 2, 1, 4, 16, false}
+  return tile_m <= 32    ? TileCfg{2, 2, 1, 4, 16, false}
          : tile_m <= 64  ? TileCfg{2, 2, 1, 4, 16, false}
          : tile_m <= 128 ? TileCfg{2, 1, 1, 8, 32, true}
                          : TileCfg{1, 1, 1, 8, 32, false};
