@@ -33,7 +33,8 @@ cudaError_t launch_musespark1x_routing(const float*, const float*, const uint8_t
 cudaError_t launch_rmsnorm_nvfp4(const void*, const void*, float, const float*, int, int, void*, void*,
                                  cudaStream_t);
 cudaError_t launch_rmsnorm_nvfp4_permuted(const void*, const void*, float, const float*, const int32_t*,
-                                          const int32_t*, int, int, int, uint8_t*, uint8_t*, cudaStream_t);
+                                          const int32_t*, const int32_t*, const int32_t*, int, int, int, int, int,
+                                          int, uint8_t*, uint8_t*, cudaStream_t);
 int launch_gemm1(const void*, const void*, const float*, const float*, const float*,
                  const int32_t*, const int32_t*, const int32_t*, const uint8_t*, const uint8_t*,
                  uint8_t*, uint8_t*, int, int, int, int, int, int, int32_t*, cudaStream_t, bool,
@@ -749,9 +750,10 @@ int moe_experts_norm_quantize(const void* x, const void* gamma, float eps, const
     return fail(MOE_ERR_INVALID_ARG, "x and gamma must be 16-byte aligned");
   if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
-  cudaError_t err = moe::launch_rmsnorm_nvfp4_permuted(x, gamma, eps, a1_gscale, r->permuted_to_token,
-                                                       r->totals, H, tile_m, L.P, base + L.a_codes,
-                                                       base + L.a_sf, as_stream(stream));
+  if (!r->expanded_to_permuted) return fail(MOE_ERR_INVALID_ARG, "route expanded_to_permuted is null");
+  cudaError_t err = moe::launch_rmsnorm_nvfp4_permuted(
+      x, gamma, eps, a1_gscale, r->permuted_to_token, r->expanded_to_permuted, r->tile_row_limit, r->totals, T, K,
+      H, tile_m, L.P, L.MT, base + L.a_codes, base + L.a_sf, as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_norm_quantize");
 }
 

@@ -58,7 +58,8 @@ def test_routing_feeds_the_block_end_to_end():
     assert rel_l2(bf16_host_f64(out), ref["out"]) < 1e-2
 
 
-@pytest.mark.parametrize("T,H,gs,scale", [(4, 256, 1.0, 1.0), (37, 5120, 618.8201293945312, 3.0), (9, 1024, 2.0, 1e3)])
+@pytest.mark.parametrize("T,H,gs,scale", [(4, 256, 1.0, 1.0), (37, 5120, 618.8201293945312, 3.0), (9, 1024, 2.0, 1e3),
+                                          (5, 6144, 4.0, 1.0)])  # H > 5120: one CTA per row
 def test_rmsnorm_nvfp4_quant_parity(T, H, gs, scale):
     rng = np.random.default_rng(T * H)
     x = inputs._to_bf16_bits(rng.standard_normal((T, H)) * scale)
@@ -77,13 +78,21 @@ def test_rmsnorm_nvfp4_quant_parity(T, H, gs, scale):
     assert rel_l2(deq, want) < 1e-3
 
 
-def test_norm_quantize_into_permuted_workspace_equals_gathered_linear():
-    T, H, I, E, K, tile = 21, 512, 128, 8, 4, 32
+@pytest.mark.parametrize("T,H,I,E,K,tile,routing", [
+    (21, 512, 128, 8, 4, 32, "uniform"),
+    (300, 5120, 256, 16, 8, 128, "zipf"),     # a CTA per permuted row, 128-row tiles
+    (600, 5120, 256, 16, 8, 128, "zipf"),     # one warp per token
+    (9, 6144, 128, 8, 2, 64, "uniform"),      # H > 5120: one CTA per permuted row
+])
+def test_norm_quantize_into_permuted_workspace_equals_gathered_linear(T, H, I, E, K, tile, routing):
+    """moe_experts_norm_quantize writes exactly the row-major kernel's codes
+    and scales of each route's token into its permuted row, and zero scales
+    into every padding row of the tiles in use."""
     rng = np.random.default_rng(4)
     x = bf16_dev(inputs._to_bf16_bits(rng.standard_normal((T, H))))
     gamma = bf16_dev(inputs._to_bf16_bits(rng.standard_normal(H) * 0.1))
     g = torch.tensor([3.0], dtype=torch.float32, device=DEV)
-    ids = torch.from_numpy(inputs.draw_topk(rng, T, E, K, "uniform")).to(DEV)
+    ids = torch.from_numpy(inputs.draw_topk(rng, T, E, K, routing)).to(DEV)
     r = B.route_permute(ids, E, tile)
     ws = B.alloc_workspace(T, K, E, H, I, tile, DEV)
     B.experts_norm_quantize(r, ws, x=x, gamma=gamma, eps=1e-6, a1_gscale=g, T=T, H=H, I=I, E=E, K=K)
