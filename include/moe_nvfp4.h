@@ -216,7 +216,9 @@ int moe_nvfp4_experts(const moe_weights* w, const void* x, const void* a,
                       void* gemm2_rows, void* ws, size_t ws_bytes,
                       int32_t* status, void* stream);
 
-/* Routing and the whole expert body in one call: the result of
+/* Routing and the whole expert body in one call (steps a2, a1, a3-a6 as the
+ * flashinfer_ops page's FlashInferOps.slot runs them: metadata, then the
+ * experts): the result of
  * moe_route_permute (same buffers, same contents, readable after the call,
  * e.g. by the finalize) followed by moe_nvfp4_experts on that route. With few
  * routes (T*K <= 2048, E <= 256) and tile_m <= 64 the routing runs inside the
@@ -241,7 +243,9 @@ int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids,
  * status for invalid ones). */
 int moe_routed_experts_kernels(int T, int K, int E, int tile_m);
 
-/* The whole routed expert block in one call: routing, the expert body with
+/* The whole routed expert block in one call (steps a1-a7: the
+ * muse_moe_runner page's apply_routed with do_finalize=False followed by
+ * MusePostExpertFinalize): routing, the expert body with
  * the post-expert norm's sums of squares fused into GEMM2's epilogue
  * (moe_nvfp4_experts_sumsq), and the finalize from those sums
  * (moe_post_expert_finalize_sumsq): out bf16 [T, H]. The result equals, bit
