@@ -484,16 +484,14 @@ int moe_routed_experts_kernels(int T, int K, int E, int tile_m) {
   return moe::route_kernel_count(T, K, E) + (d.P > 0 ? moe_experts_kernels(tile_m) : 0);
 }
 
-// The body of the routed entry points: routing inside the quantizer when
-// routed_fused, else the routing kernels then experts_body. ss / fin: the
-// sums of squares and the finalize units of the one-launch GEMMs (fin only
-// on the fused path; the caller checked their pointers).
+// moe_nvfp4_experts_routed: routing inside the quantizer when routed_fused,
+// else the routing kernels then experts_body.
 static int routed_body(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
                        const void* a_sf, const float* a1_gscale, const float* a2_gscale, int T, int H, int I,
                        int E, int K, int tile_m, int32_t* expert_counts, int32_t* expert_offsets,
                        int32_t* expanded_to_permuted, int32_t* permuted_to_token, int32_t* tile_expert,
                        int32_t* tile_row_limit, int32_t* totals, void* gemm2_rows, void* ws, size_t ws_bytes,
-                       int32_t* status, void* stream, SumSq ss) {
+                       int32_t* status, void* stream) {
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc || (rc = check_weights(w, true)) || (rc = check_weights(w, false))) return rc;
@@ -503,7 +501,7 @@ static int routed_body(const moe_weights* w, const int32_t* topk_ids, const void
                            permuted_to_token, tile_expert, tile_row_limit, totals, status, stream);
     if (rc) return rc;
     return experts_body(w, x, a, a_sf, a1_gscale, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes,
-                        status, stream, ss);
+                        status, stream, SumSq());
   }
   if (!expert_counts || !expert_offsets || !topk_ids || !expanded_to_permuted || !permuted_to_token ||
       !tile_expert || !tile_row_limit || !totals)
@@ -527,7 +525,7 @@ static int routed_body(const moe_weights* w, const int32_t* topk_ids, const void
       base + L.a_sf, reinterpret_cast<int32_t*>(base + L.done), status, as_stream(stream));
   if (err != cudaSuccess) return cuda_fail(err, "routing + input quantization");
   return experts_fused(w, a2_gscale, &r, T, H, I, E, K, tile_m, gemm2_rows, ws, ws_bytes, status, stream, true,
-                       false, ss);
+                       false);
 }
 
 int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, const void* x, const void* a,
@@ -538,7 +536,7 @@ int moe_nvfp4_experts_routed(const moe_weights* w, const int32_t* topk_ids, cons
                              size_t ws_bytes, int32_t* status, void* stream) {
   return routed_body(w, topk_ids, x, a, a_sf, a1_gscale, a2_gscale, T, H, I, E, K, tile_m, expert_counts,
                      expert_offsets, expanded_to_permuted, permuted_to_token, tile_expert, tile_row_limit, totals,
-                     gemm2_rows, ws, ws_bytes, status, stream, SumSq());
+                     gemm2_rows, ws, ws_bytes, status, stream);
 }
 
 // The whole block: the routing kernels, the expert body with the sums of

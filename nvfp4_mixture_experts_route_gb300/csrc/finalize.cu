@@ -477,7 +477,7 @@ namespace moe {
 // One CTA per token: route k's H / 32 partials are summed by 16 lanes of
 // one warp, as float4s (lane j takes float4s j, j + 16, ..., adding .x, .y,
 // .z, .w in turn; then an xor butterfly over the 16 lanes), the order the
-// one-launch GEMMs' finalize units use too; then
+// finalize_sumsq_units_kernel uses too; then
 // every thread takes 8-element vectors of the hidden dimension, issues the
 // loads of all of its routes' vectors at once (up to eight in flight), and
 // accumulates coef_k * r_k in fp32; out = bf16(g * sum), g = 1 + gamma, in
@@ -562,8 +562,7 @@ __global__ void __launch_bounds__(kFinSsThreads) finalize_sumsq_kernel(
 }
 
 // The same finalize for K <= 8 in units of (token, 1024 columns), four warps
-// each (finalize_units.cuh, the arithmetic and order the one-launch GEMMs'
-// finalize units use): a persistent grid walks the units, reading the next
+// each (finalize_units.cuh): a persistent grid walks the units, reading the next
 // unit's routing while it finishes the current one, so that no CTA waits
 // through a coefficient phase with nothing else in flight.
 __global__ void __launch_bounds__(32 * kFinUnitWarps) finalize_sumsq_units_kernel(FinArgs a, int T) {

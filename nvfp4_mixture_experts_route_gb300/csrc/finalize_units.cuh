@@ -1,7 +1,6 @@
 // The post-expert finalize from GEMM2's sums of squares, in units of
-// (token, 256 columns per warp) done by four warps together: shared by the
-// one-launch GEMMs' last units (gemm.cu) and the standalone finalize from
-// sums of squares (finalize.cu), so that both give the same bits.
+// (token, 256 columns per warp) done by four warps together
+// (finalize_sumsq_units_kernel).
 //
 // Per token t and route k (row p = expanded_to_permuted[t, k]):
 //   coef_k = w[t, k] / sqrt(sum_c row_ss[p][c] / H + eps)
@@ -17,7 +16,7 @@
 namespace moe {
 
 constexpr int kFinUnitMaxK = 8;    // routes per token the units take
-constexpr int kFinUnitWarps = 4;   // warps of a standalone unit (warps 0-3 sum 2 routes each)
+constexpr int kFinUnitWarps = 4;   // warps of a unit (each sums 2 routes' partials)
 
 struct FinArgs {
   const __nv_bfloat16* rows;  // [num_rows, H]
@@ -67,8 +66,7 @@ namespace moe {
 
 // The rest of a unit: warp wi of its kFinUnitWarps, all reaching the named
 // barrier once (nthreads = 32 * kFinUnitWarps). The loads of the rows and of
-// the warp's share of the partial sums are in flight together. Rows and sums
-// are read through L2 (ld.cg): they may have been written during the launch.
+// the warp's share of the partial sums are in flight together.
 static __device__ __forceinline__ void fin_finish_inl(const FinArgs& a, const FinPre& f, int lane, int wi,
                                                      float* coef_s, int nthreads) {
   const int K = a.K, H = a.H, G4 = H / 128;
@@ -129,12 +127,6 @@ static __device__ __forceinline__ void fin_finish_inl(const FinArgs& a, const Fi
     oh[q] = __floats2bfloat162_rn(r.x, r.y);
   }
   *reinterpret_cast<uint4*>(a.out + (size_t)f.t * H + 8 * f.v) = o;
-}
-
-// Out of line, for callers whose own registers must not grow with it.
-static __device__ __noinline__ void fin_finish(const FinArgs& a, const FinPre& f, int lane, int wi, float* coef_s,
-                                               int nthreads) {
-  fin_finish_inl(a, f, lane, wi, coef_s, nthreads);
 }
 
 }  // namespace moe
