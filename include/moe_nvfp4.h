@@ -514,17 +514,21 @@ int moe_dense_bf16(const void* x, const void* w, int T, int Din, int Dout, void*
  * mbarrier; 3 by two more warps, one per operand; 4 every stage by the MMA
  * thread with 128x256b copies (two K = 64 steps per copy) for both operands;
  * 5 the same for A only. Modes 4 and 5 time the copies, not a scale layout:
- * every scale byte is 1.0 here. Supported: n = 128 (ctas_per_sm 1 or 2) or
+ * every scale byte is 1.0 here. warp_issue selects how the issuing warps run
+ * their loops: 0 lane 0 alone; 1 the whole warp, converged, with lane 0
+ * issuing each tcgen05 instruction under a predicate (the expert GEMM1's
+ * form). Supported: n = 128 (ctas_per_sm 1 or 2) or
  * 256 (ctas_per_sm 1); mmas_per_commit 4, or 16 with sf_copies = 0; ring 5
- * only with ctas_per_sm = 1 and sf_copies != 0; stages 1 .. 2^24. *flops
+ * only with ctas_per_sm = 1 and sf_copies != 0; warp_issue 0 or 1; stages
+ * 1 .. 2^24. *flops
  * (host) receives the launch's FLOPs,
  * 2 * 128 * n * 64 * mmas_per_commit * stages * CTAs; time the launch with
  * events on `stream`. A wait that gives up records MOE_ERR_TIMEOUT in *status
  * (optional device word). Operands and outputs are scratch inside the kernel.
  * ---------------------------------------------------------------------- */
 int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm,
-                     int ring, int stages, double* flops, int32_t* status,
-                     void* stream);
+                     int ring, int warp_issue, int stages, double* flops,
+                     int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * Self-test of the failure path: runs the library's bounded mbarrier wait on

@@ -129,7 +129,7 @@ _SIGNATURES = {
     "moe_rmsnorm_nvfp4_quant": ([_P, _P, C.c_float, _P, _I, _I, _P, _P, _P], _I),
     "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
-    "moe_fp4_mma_rate": ([_I, _I, _I, _I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
+    "moe_fp4_mma_rate": ([_I, _I, _I, _I, _I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
     "moe_selftest_wait_timeout": ([C.c_uint64, _P, _P, _P], _I),
     "moe_selftest_occupy": ([_I, _I, C.c_uint64, _P], _I),
     "moe_selftest_counter_timeout": ([C.c_uint64, _P, _P, _P, _P], _I),
@@ -598,12 +598,12 @@ def dense_bf16(x, w, *, out=None, ws=None, status=None, stream=None):
 
 
 def fp4_mma_rate(n: int, sf_copies: int, mmas_per_commit: int, ctas_per_sm: int, stages: int, status=None,
-                 stream=None, ring: int = 3) -> float:
+                 stream=None, ring: int = 3, warp_issue: bool = False) -> float:
     """Launch the dense NVFP4 tensor-core rate probe (see the header);
     returns the launch's FLOPs. Time it with events on the same stream."""
     f = C.c_double()
-    _check(load().moe_fp4_mma_rate(n, int(sf_copies), mmas_per_commit, ctas_per_sm, ring, stages, C.byref(f),
-                                   _ptr(status), _stream(stream)))
+    _check(load().moe_fp4_mma_rate(n, int(sf_copies), mmas_per_commit, ctas_per_sm, ring, int(warp_issue), stages,
+                                   C.byref(f), _ptr(status), _stream(stream)))
     return f.value
 
 

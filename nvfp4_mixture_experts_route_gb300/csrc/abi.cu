@@ -186,7 +186,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-int moe_abi_version(void) { return 4; }
+int moe_abi_version(void) { return 5; }
 
 int moe_device_reads_host(const void* p) {
   if (!p) return 0;

@@ -14,22 +14,21 @@
 // work unit is one (route tile tau, weight tile mt) pair over the whole K.
 //
 // Persistent, warp-specialised kernel, one or two CTAs per SM (tile_cfg
-// below), 2 + 4 or 2 + 8 warps (+ 1 for GEMM1 over 128-row tiles):
+// below), 2 + 4 or 2 + 8 warps:
 //   - warp 0 / lane 0: TMA producer. Walks this CTA's units in order and, per
 //     pipeline stage (K = 256 elements = 128 bytes per row per chunk), loads
 //     the 128 x 128 B weight box and the tile_m x 128 B route box (both
 //     128-byte swizzled) and the stage's scale atoms for both operands (plain
 //     bulk copies), all completing one mbarrier. The ring of ST stages runs
 //     across unit boundaries, so HBM streaming never stops between units.
-//   - warp 1 / lane 0: MMA issuer. Copies each stage's scale atoms into that
-//     stage's own tensor-memory columns (tcgen05.cp 32x128b.warpx4), issues
-//     the stage's MMAs of K = 64 into the unit's accumulator buffer, and
-//     commits the stage back to the producer; after a unit's last stage it
-//     commits the accumulator to the epilogue.
-//   - GEMM1 over 128-row tiles (prefill, where the MMA thread's issue rate
-//     bounds the kernel): a last warp's lane 0 makes the scale copies of each
-//     landed stage instead and commits them to the stage's sfready barrier,
-//     on which the MMA thread then waits.
+//   - warp 1: MMA issuer. Copies each stage's scale atoms into that stage's
+//     own tensor-memory columns (tcgen05.cp 32x128b.warpx4), issues the
+//     stage's MMAs of K = 64 into the unit's accumulator buffer, and commits
+//     the stage back to the producer; after a unit's last stage it commits
+//     the accumulator to the epilogue. GEMM1 runs this loop on the whole
+//     warp, converged, with lane 0 issuing under a predicate (a faster
+//     instruction stream where the issue rate bounds the kernel, at
+//     prefill); GEMM2 and the one-launch pair run it on lane 0 alone.
 //   - warps 2..: epilogue. Warp w reads TMEM lane quadrant w % 4 (32 weight
 //     rows) of the finished accumulator (with 8 warps, two per quadrant split
 //     the route columns), then hands the buffer back. With two accumulator
@@ -137,8 +136,9 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 // chunks per pipeline stage, epilogue warps and GEMM1 epilogue staging
 // columns. One thread per CTA issues all of its tcgen05 copies and MMAs, and
 // each instruction occupies that thread for a fixed time whatever its size
-// (measured with a pipe probe: about 26 ns per copy or MMA and 175 ns per
-// commit), so the tensor core is fed by several CTAs per SM wherever tensor
+// (measured with a pipe probe, issued by lane 0 alone: about 28 ns per copy
+// or MMA and 140 ns per commit; by a converged warp, lane 0 issuing, about a
+// third less), so the tensor core is fed by several CTAs per SM wherever tensor
 // memory and shared memory allow; the decode tiles (32 and 64 rows) run two
 // CTAs per SM with a 4- or 3-stage ring (one CTA per SM: 1.5 x slower; three
 // with 2-stage rings: 1-2 % slower at b = 8, 2 % at b = 64, once the weights
@@ -262,12 +262,17 @@ __device__ __forceinline__ void gemm1_epilogue_chunk(uint32_t taddr, float* stag
   __syncwarp();
 }
 
-// GEMM1 over 128-row tiles (issue-bound at prefill) gives the scale-factor
-// copies their own warp, so the MMA thread issues only MMAs and commits.
-// (GEMM2's shorter units measured slower that way.)
-__host__ __device__ constexpr bool scale_warp_for(int mode, int tile_m) { return mode == 1 && tile_m == 128; }
+// How the MMA issuer runs (measured at T = 8192, 128-row tiles, one GB300):
+// GEMM1 with the loop on the whole warp, converged, lane 0 issuing under a
+// predicate, and the scale copies on that same warp: 0.694 ms, against 0.738
+// with the copies on a warp of their own (either issue form) and 0.755 with
+// lane 0 alone running the loop. GEMM2 measured the other way: 0.474 ms
+// converged against 0.433 on lane 0 alone, and the decode pair the same
+// either way, so those keep lane 0. (A converged loop in which lane 0 alone
+// polled the barriers and broadcast the outcome: 0.875 ms for GEMM1.)
+__host__ __device__ constexpr bool warp_issue_for(int mode) { return mode == 1; }
 __host__ __device__ constexpr int gemm_threads(int mode, int tile_m) {
-  return 64 + 32 * tile_cfg(tile_m).epi_warps + (scale_warp_for(mode, tile_m) ? 32 : 0);
+  return 64 + 32 * tile_cfg(tile_m).epi_warps;
 }
 
 // One instantiation per (mode, route-tile size). MODE 1 runs GEMM1 units, 2
@@ -322,8 +327,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   __shared__ __align__(8) uint64_t accf_bar[2];
   __shared__ __align__(8) uint64_t acce_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
-  __shared__ __align__(8) uint64_t sfready_bar[kMaxStages];  // a stage's scales are in tensor memory
-  __shared__ __align__(8) uint64_t sfdrain_bar;
   // Both GEMMs in one grid: the units this CTA drew, in order, from the
   // producer to the MMA issuer and the epilogue warps.
   constexpr int kUnitQ = 8;
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
   constexpr int tile_m = TILE, S = sf_atoms_for(TILE), ST = stages_for(TILE, MODE == 2 ? 2 : 1);
   constexpr int NB = acc_bufs_for(TILE), CH = chunks_for(TILE), EPW = epi_warps_for(TILE);
   constexpr bool kRouteM = tile_cfg(TILE).route_m;
-  constexpr bool kSW = scale_warp_for(MODE, TILE);
+  constexpr bool kWI = warp_issue_for(MODE);
   // Per stage: CH chunks of K = 256, i.e. up to 4 * CH MMA steps of K = 64.
   constexpr uint32_t b_bytes = (uint32_t)tile_m * kStageRowBytes;  // one chunk of the route box
   constexpr uint32_t a_stage = CH * kABytes, b_stage = CH * b_bytes;
@@ -390,8 +393,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
       mbar_init(smem_u32(&acce_bar[b]), EPW);
     }
     mbar_init(smem_u32(&drain_bar), 1);
-    for (int s = 0; s < ST; ++s) mbar_init(smem_u32(&sfready_bar[s]), 1);
-    mbar_init(smem_u32(&sfdrain_bar), 1);
     for (int q = 0; q < kUnitQ; ++q) {
       mbar_init(smem_u32(&uq_full[q]), 1);
       mbar_init(smem_u32(&uq_empty[q]), 1 + EPW);  // the MMA issuer and every epilogue warp
@@ -570,7 +571,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
-    if (lane == 0) {
+    // kWI: the whole warp runs the loop, converged, and lane 0 issues;
+    // otherwise lane 0 alone runs it.
+    if (kWI || lane == 0) {
       constexpr uint32_t idesc = idesc_nvf4(kWTile, (uint32_t)tile_m);
       // Descriptors of stage 0's first K = 64 step; another stage or step adds
       // its byte offset >> 4 to the start-address field (shared-memory
@@ -586,9 +589,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         int u;
         if constexpr (MODE == 3) {
           const int q = n % kUnitQ;
-          if (!mbar_wait(smem_u32(&uq_full[q]), (n / kUnitQ) & 1, &abort_flag, p.status)) break;
+          if (!mbar_wait_f<kWI>(smem_u32(&uq_full[q]), (n / kUnitQ) & 1, &abort_flag, p.status)) break;
           u = *reinterpret_cast<volatile int*>(&unit_q[q]);
-          mbar_arrive(smem_u32(&uq_empty[q]));
+          if constexpr (kWI) __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&uq_empty[q]));
           if (u < 0) break;
         } else {
           u = blockIdx.x + n * gridDim.x;
@@ -598,13 +602,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
         const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2;
         const int b = uc % NB, use = uc / NB;
         if (use > 0 &&
-            !mbar_wait(smem_u32(&acce_bar[b]), (use - 1) & 1, &abort_flag, p.status))
+            !mbar_wait_f<kWI>(smem_u32(&acce_bar[b]), (use - 1) & 1, &abort_flag, p.status))
           break;
         tc_fence_after();
         const uint32_t dacc = tmem + (uint32_t)(b * tile_m);
         for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait(smem_u32(&full_bar[s]), phase, &abort_flag, p.status) ||
-              (kSW && !mbar_wait(smem_u32(&sfready_bar[s]), phase, &abort_flag, p.status))) {
+          if (!mbar_wait_f<kWI>(smem_u32(&full_bar[s]), phase, &abort_flag, p.status)) {
             stop = true;
             break;
           }
@@ -618,11 +621,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
           const uint64_t sbd = sfb_desc0 + ((s * sfb_stage) >> 4);
 #pragma unroll
           for (int j = 0; j < steps_per_stage; ++j) {
-            if (j < kk && !kSW) {
-              tc_copy_scale_atom(fa + 4 * j, sad + j * (kAtomBytes >> 4));
+            if (j < kk) {
+              tc_copy_scale_atom_f<kWI>(fa + 4 * j, sad + j * (kAtomBytes >> 4));
 #pragma unroll
               for (int sub = 0; sub < S; ++sub)
-                tc_copy_scale_atom(fbc + 4 * (j * S + sub), sbd + (j * S + sub) * (kAtomBytes >> 4));
+                tc_copy_scale_atom_f<kWI>(fbc + 4 * (j * S + sub), sbd + (j * S + sub) * (kAtomBytes >> 4));
             }
           }
 #pragma unroll
@@ -632,70 +635,23 @@ __global__ void __launch_bounds__(gemm_threads(MODE, TILE), tile_cfg(TILE).ctas)
               const uint32_t a_off = ((j >> 2) * kABytes + 32 * (j & 3)) >> 4;
               const uint32_t b_off = ((j >> 2) * b_bytes + 32 * (j & 3)) >> 4;
               if constexpr (kRouteM)  // A = route rows, B = weight rows
-                tc_mma_nvf4(dacc, bd + b_off, ad + a_off, idesc, fbc + 4 * j * S, fa + 4 * j,
+                tc_mma_nvf4_f<kWI>(dacc, bd + b_off, ad + a_off, idesc, fbc + 4 * j * S, fa + 4 * j,
                             (ks | j) != 0);
               else  // A = weight rows, B = route rows
-                tc_mma_nvf4(dacc, ad + a_off, bd + b_off, idesc, fa + 4 * j, fbc + 4 * j * S,
+                tc_mma_nvf4_f<kWI>(dacc, ad + a_off, bd + b_off, idesc, fa + 4 * j, fbc + 4 * j * S,
                             (ks | j) != 0);
             }
           }
-          tc_commit(smem_u32(&empty_bar[s]));
+          tc_commit_f<kWI>(smem_u32(&empty_bar[s]));
           if (++s == ST) {
             s = 0;
             phase ^= 1u;
           }
         }
         if (stop) break;
-        tc_commit(smem_u32(&accf_bar[b]));
+        tc_commit_f<kWI>(smem_u32(&accf_bar[b]));
         ++uc;
       }
-    }
-    __syncwarp();
-  } else if (kSW && warp == 2 + EPW) {
-    // --------------------------- scale-factor copies -------------------------
-    // Waits for each stage to land, copies its scale atoms into the stage's
-    // tensor-memory columns and commits to the stage's sfready barrier, on
-    // which the MMA thread waits. A stage's columns are rewritten only after
-    // its next full phase, i.e. after the producer refilled it, which it does
-    // only once the MMAs that read the columns have completed.
-    if (lane == 0) {
-      const uint64_t sfa_desc0 = smem_desc(sSFA, 0, 128, 0);
-      const uint64_t sfb_desc0 = smem_desc(sSFB, 0, 128, 0);
-      int s = 0;
-      uint32_t phase = 0;
-      bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const int gi = u < n1 ? 0 : 1;
-        const int KC = gi == 0 ? KC1 : KC2, nks = gi == 0 ? nks1 : nks2;
-        for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait(smem_u32(&full_bar[s]), phase, &abort_flag, p.status)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const int kk = min(steps_per_stage, KC - steps_per_stage * ks);
-          const uint32_t fa = t_sfa + s * 16 * CH, fbc = t_sfb + s * 16 * CH * S;
-          const uint64_t sad = sfa_desc0 + ((s * sfa_stage) >> 4);
-          const uint64_t sbd = sfb_desc0 + ((s * sfb_stage) >> 4);
-#pragma unroll
-          for (int j = 0; j < steps_per_stage; ++j) {
-            if (j < kk) {
-              tc_copy_scale_atom(fa + 4 * j, sad + j * (kAtomBytes >> 4));
-#pragma unroll
-              for (int sub = 0; sub < S; ++sub)
-                tc_copy_scale_atom(fbc + 4 * (j * S + sub), sbd + (j * S + sub) * (kAtomBytes >> 4));
-            }
-          }
-          tc_commit(smem_u32(&sfready_bar[s]));
-          if (++s == ST) {
-            s = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // every copy this thread issued has landed before tensor memory is freed
-      tc_commit(smem_u32(&sfdrain_bar));
-      mbar_wait_cleanup(smem_u32(&sfdrain_bar), 0);
     }
     __syncwarp();
   } else {

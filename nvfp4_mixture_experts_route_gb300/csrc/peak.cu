@@ -12,7 +12,9 @@
 // step), then the stage's MMAs, then one tcgen05.commit to the stage's
 // mbarrier; a stage's tensor-memory scale columns are rewritten only after
 // the commit of their previous use has arrived (a ring of stages). Variants
-// separate the cost of the MMAs, of the scale copies and of the commits.
+// separate the cost of the MMAs, of the scale copies and of the commits, and
+// of the issue form: lane 0 alone running the issue loops, or the whole warp
+// running them converged with lane 0 issuing under a predicate.
 //
 // Every wait is bounded (1 s) and reports MOE_ERR_TIMEOUT; no trap.
 #include "common.cuh"
@@ -34,9 +36,17 @@ __host__ __device__ constexpr uint32_t rate_tmem_cols(int n, int sfcp, int mpc, 
 
 // One tcgen05.cp of a 128-row x 32-byte shared-memory matrix into 128 lanes
 // x 8 columns (no replication): the cost of a wider copy, timed against the
-// 512-byte 32x128b.warpx4 atoms.
-__device__ __forceinline__ void tc_copy_128x256b(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+// 512-byte 32x128b.warpx4 atoms. WI: issued by lane 0 of a converged warp.
+template <bool WI>
+__device__ __forceinline__ void tc_copy_128x256b_f(uint32_t taddr, uint64_t desc) {
+  if constexpr (WI)
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(desc)
+        : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 // Shared memory: one 128-byte-swizzled K = 256 chunk of A (128 rows) and of
 // B (N rows), and four K = 64 steps of scale atoms for each.
@@ -53,7 +63,7 @@ __host__ __device__ constexpr uint32_t rate_smem_bytes(int n) {
 // the same, so the columns' layout does not matter to the MMAs here.
 __host__ __device__ constexpr int rate_threads(int sfcp) { return sfcp == 2 ? 64 : sfcp == 3 ? 96 : 32; }
 
-template <int N, int SFCP, int MPC, int RING>
+template <int N, int SFCP, int MPC, int RING, bool WI>
 __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int stages, int32_t* status) {
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bar[RING];
@@ -104,7 +114,7 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
   const uint32_t tmem = tmem_slot;
   const uint32_t t_sf = tmem + N;
 
-  if (lane == 0) {
+  if (WI || lane == 0) {
     constexpr uint32_t idesc = idesc_nvf4(128, N);
     const uint64_t a_desc = smem_desc(sA, 16, 1024, 2), b_desc = smem_desc(sB, 16, 1024, 2);
     const uint64_t sfa_desc = smem_desc(sSFA, 0, 128, 0), sfb_desc = smem_desc(sSFB, 0, 128, 0);
@@ -113,22 +123,22 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
     auto sfa_col = [&](int r, int j) { return t_sf + (uint32_t)(r * SL * 4 * (1 + S) + 4 * j); };
     auto sfb_col = [&](int r, int j) { return t_sf + (uint32_t)(r * SL * 4 * (1 + S) + 4 * SL + 4 * j * S); };
     auto copy_a = [&](int r, int j) {
-      tc_copy_scale_atom(sfa_col(r, j), sfa_desc + (uint64_t)((j & 3) * (kAtomBytes >> 4)));
+      tc_copy_scale_atom_f<WI>(sfa_col(r, j), sfa_desc + (uint64_t)((j & 3) * (kAtomBytes >> 4)));
     };
     auto copy_b = [&](int r, int j) {
 #pragma unroll
       for (int sub = 0; sub < S; ++sub)
-        tc_copy_scale_atom(sfb_col(r, j) + 4 * sub, sfb_desc + (uint64_t)(((j & 3) * S + sub) * (kAtomBytes >> 4)));
+        tc_copy_scale_atom_f<WI>(sfb_col(r, j) + 4 * sub, sfb_desc + (uint64_t)(((j & 3) * S + sub) * (kAtomBytes >> 4)));
     };
     auto copy_scales = [&](int r, int j) {
       if (SFCP >= 4) {
         // 128 rows x 32 bytes from the scale region (4 KB inside the
         // operand buffer) into the 8 columns of steps j and j + 1
         if ((j & 1) == 0) {
-          tc_copy_128x256b(sfa_col(r, j), smem_desc(sSFA, 128, 256, 0));
+          tc_copy_128x256b_f<WI>(sfa_col(r, j), smem_desc(sSFA, 128, 256, 0));
           if (SFCP == 4) {
 #pragma unroll
-            for (int sub = 0; sub < S; ++sub) tc_copy_128x256b(sfb_col(r, j) + 8 * sub, smem_desc(sSFA, 128, 256, 0));
+            for (int sub = 0; sub < S; ++sub) tc_copy_128x256b_f<WI>(sfb_col(r, j) + 8 * sub, smem_desc(sSFA, 128, 256, 0));
           }
         }
         if (SFCP == 5) copy_b(r, j);
@@ -143,7 +153,7 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
       bool do_a = SFCP == 2 || warp == 1, do_b = SFCP == 2 || warp == 2;
       for (int s = 0; s < stages; ++s) {
         const int r = s % RING;
-        if (s >= RING && !mbar_wait(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status))
+        if (s >= RING && !mbar_wait_f<WI>(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status))
           break;
         tc_fence_after();
 #pragma unroll
@@ -151,9 +161,9 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
           if (do_a) copy_a(r, j);
           if (do_b) copy_b(r, j);
         }
-        tc_commit(smem_u32(warp == 2 ? &sfb_ready[r] : &sfa_ready[r]));
+        tc_commit_f<WI>(smem_u32(warp == 2 ? &sfb_ready[r] : &sfa_ready[r]));
       }
-      tc_commit(smem_u32(&cp_drain[warp - 1]));
+      tc_commit_f<WI>(smem_u32(&cp_drain[warp - 1]));
       mbar_wait_cleanup(smem_u32(&cp_drain[warp - 1]), 0);
     } else {
     if (!SFCP) {
@@ -163,10 +173,10 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
     for (int s = 0; s < stages; ++s) {
       const int r = s % RING;
       const bool copy_warps = SFCP == 2 || SFCP == 3;
-      if (!copy_warps && s >= RING && !mbar_wait(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status))
+      if (!copy_warps && s >= RING && !mbar_wait_f<WI>(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status))
         break;
-      if (copy_warps && !mbar_wait(smem_u32(&sfa_ready[r]), (s / RING) & 1, &abort_flag, status)) break;
-      if (SFCP == 3 && !mbar_wait(smem_u32(&sfb_ready[r]), (s / RING) & 1, &abort_flag, status)) break;
+      if (copy_warps && !mbar_wait_f<WI>(smem_u32(&sfa_ready[r]), (s / RING) & 1, &abort_flag, status)) break;
+      if (SFCP == 3 && !mbar_wait_f<WI>(smem_u32(&sfb_ready[r]), (s / RING) & 1, &abort_flag, status)) break;
       tc_fence_after();
       if (SFCP == 1 || SFCP >= 4) {
 #pragma unroll
@@ -176,12 +186,12 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
       for (int j = 0; j < MPC; ++j) {
         const uint64_t koff = (uint64_t)((32 * (j & 3)) >> 4);
         const int rs = SFCP ? r : 0, js = SFCP ? j : (j & 3);
-        tc_mma_nvf4(tmem, a_desc + koff, b_desc + koff, idesc, sfa_col(rs, js), sfb_col(rs, js),
+        tc_mma_nvf4_f<WI>(tmem, a_desc + koff, b_desc + koff, idesc, sfa_col(rs, js), sfb_col(rs, js),
                     (s | j) != 0);
       }
-      tc_commit(smem_u32(&bar[r]));
+      tc_commit_f<WI>(smem_u32(&bar[r]));
     }
-    tc_commit(smem_u32(&drain_bar));
+    tc_commit_f<WI>(smem_u32(&drain_bar));
     mbar_wait_cleanup(smem_u32(&drain_bar), 0);
     }
   }
@@ -191,9 +201,9 @@ __global__ void __launch_bounds__(rate_threads(SFCP)) fp4_mma_rate_kernel(int st
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
-template <int N, int SFCP, int MPC, int RING = 3>
+template <int N, int SFCP, int MPC, int RING, bool WI>
 static cudaError_t launch_rate(int grid, int smem, int stages, int32_t* status, cudaStream_t stream) {
-  auto kern = fp4_mma_rate_kernel<N, SFCP, MPC, RING>;
+  auto kern = fp4_mma_rate_kernel<N, SFCP, MPC, RING, WI>;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, rate_threads(SFCP), smem, stream>>>(stages, status);
@@ -201,12 +211,13 @@ static cudaError_t launch_rate(int grid, int smem, int stages, int32_t* status, 
 }
 
 // Host check of a variant: MOE_OK, or an error code with the reason.
-int fp4_mma_rate_check(int n, int sf_copies, int mpc, int ctas_per_sm, int ring, int stages, const char** why) {
+int fp4_mma_rate_check(int n, int sf_copies, int mpc, int ctas_per_sm, int ring, int warp_issue, int stages,
+                       const char** why) {
   if (!((n == 128 || n == 256) && sf_copies >= 0 && sf_copies <= 5 && (mpc == 4 || mpc == 16) &&
-        (ctas_per_sm == 1 || ctas_per_sm == 2) && (ring == 3 || ring == 5) && stages >= 1 &&
-        stages <= (1 << 24))) {
+        (ctas_per_sm == 1 || ctas_per_sm == 2) && (ring == 3 || ring == 5) && (warp_issue == 0 || warp_issue == 1) &&
+        stages >= 1 && stages <= (1 << 24))) {
     *why = "fp4 rate: n in {128, 256}, sf_copies in 0..5, mmas_per_commit in {4, 16}, ctas_per_sm in {1, 2}, "
-           "ring in {3, 5}";
+           "ring in {3, 5}, warp_issue in {0, 1}";
     return MOE_ERR_INVALID_ARG;
   }
   if ((n == 256 && ctas_per_sm == 2) || (sf_copies && mpc == 16) || (ring == 5 && (ctas_per_sm == 2 || !sf_copies))) {
@@ -220,10 +231,11 @@ int fp4_mma_rate_check(int n, int sf_copies, int mpc, int ctas_per_sm, int ring,
 // the MMA thread (1), by one copy warp (2) or by two (3);
 // mpc: MMAs per commit (4: a K = 256 stage; 16: a K = 1024 stage, only
 // without per-stage copies); ctas_per_sm: 1 or 2 (2 only for n = 128, whose
-// tensor memory then fits two CTAs).
-int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring, int stages, int sms,
-                        int32_t* status, cudaStream_t stream, double* flops, const char** why) {
-  const int rc = fp4_mma_rate_check(n, sf_copies, mpc, ctas_per_sm, ring, stages, why);
+// tensor memory then fits two CTAs); warp_issue: 0 lane 0 alone runs the
+// issue loops, 1 the whole warp runs them converged, lane 0 issuing.
+int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring, int warp_issue, int stages,
+                        int sms, int32_t* status, cudaStream_t stream, double* flops, const char** why) {
+  const int rc = fp4_mma_rate_check(n, sf_copies, mpc, ctas_per_sm, ring, warp_issue, stages, why);
   if (rc) return rc;
   // Shared memory requested per CTA so that exactly ctas_per_sm fit an SM:
   // their tensor memory (at most 512 / ctas_per_sm columns each) then never
@@ -232,10 +244,12 @@ int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring
   const int grid = sms * ctas_per_sm;
   *flops = 2.0 * 128.0 * n * 64.0 * (double)mpc * (double)stages * (double)grid;
   cudaError_t err;
-  const int key = (n == 256 ? 1000 : 0) + (ring == 5 ? 100 : 0) + 10 * sf_copies + (mpc == 16 ? 1 : 0);
+  const int key =
+      (warp_issue ? 10000 : 0) + (n == 256 ? 1000 : 0) + (ring == 5 ? 100 : 0) + 10 * sf_copies + (mpc == 16 ? 1 : 0);
   switch (key) {
-#define MOE_RATE(k, nn, cp, mpcv, rg) \
-  case k: err = launch_rate<nn, cp, mpcv, rg>(grid, smem, stages, status, stream); break;
+#define MOE_RATE1(k, nn, cp, mpcv, rg, wi) \
+  case k: err = launch_rate<nn, cp, mpcv, rg, wi>(grid, smem, stages, status, stream); break;
+#define MOE_RATE(k, nn, cp, mpcv, rg) MOE_RATE1(k, nn, cp, mpcv, rg, false) MOE_RATE1(10000 + k, nn, cp, mpcv, rg, true)
     MOE_RATE(0, 128, 0, 4, 3)
     MOE_RATE(1, 128, 0, 16, 3)
     MOE_RATE(10, 128, 1, 4, 3)
@@ -259,6 +273,7 @@ int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring
     MOE_RATE(1140, 256, 4, 4, 5)
     MOE_RATE(1150, 256, 5, 4, 5)
 #undef MOE_RATE
+#undef MOE_RATE1
     default:
       *why = "fp4 rate: variant not built";
       return MOE_ERR_UNSUPPORTED;
@@ -283,17 +298,17 @@ int report_error(int code, const char* fmt, ...);
 }
 
 extern "C" int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm, int ring,
-                                int stages, double* flops, int32_t* status, void* stream) {
+                                int warp_issue, int stages, double* flops, int32_t* status, void* stream) {
   if (!flops) return moe::report_error(MOE_ERR_INVALID_ARG, "flops is null");
   const char* why = "";
-  int rc = moe::fp4_mma_rate_check(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, stages, &why);
+  int rc = moe::fp4_mma_rate_check(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, warp_issue, stages, &why);
   if (rc) return moe::report_error(rc, "%s", why);
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess || sms < 1)
     return moe::report_error(MOE_ERR_CUDA, "fp4 rate: no device (%s)", cudaGetErrorString(err));
-  rc = moe::launch_fp4_mma_rate(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, stages, sms, status,
+  rc = moe::launch_fp4_mma_rate(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, warp_issue, stages, sms, status,
                                           reinterpret_cast<cudaStream_t>(stream), flops, &why);
   return rc ? moe::report_error(rc, "%s", why) : MOE_OK;
 }

@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_sizes(lib):
-    assert lib.moe_abi_version() == 4
+    assert lib.moe_abi_version() == 5
     assert B.prepared_sizes(128, 5120, 2048) == [
         128 * 4096 * 2560, 128 * 4096 * 320, 128 * 5120 * 1024, 128 * 5120 * 128]
     assert B.route_sizes(8, 8, 128, 32) == (2048, 64)

@@ -23,19 +23,21 @@ def test_unfitting_variants_refused_on_host():
     for n, sf, mpc, ctas, ring, want in ((256, 0, 4, 2, 3, -2), (128, 1, 16, 1, 3, -2), (128, 3, 16, 1, 3, -2),
                                          (128, 1, 4, 2, 5, -2), (64, 0, 4, 1, 3, -1), (128, 0, 4, 3, 3, -1),
                                          (128, 6, 4, 1, 3, -1), (128, 1, 4, 1, 4, -1)):
-        assert lib.moe_fp4_mma_rate(n, sf, mpc, ctas, ring, 8, C.byref(f), None, None) == want
+        assert lib.moe_fp4_mma_rate(n, sf, mpc, ctas, ring, 0, 8, C.byref(f), None, None) == want
         assert b"fp4 rate" in lib.moe_last_error()
+    assert lib.moe_fp4_mma_rate(128, 0, 4, 1, 3, 2, 8, C.byref(f), None, None) == -1  # warp_issue 0 or 1
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("warp_issue", [False, True])
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_rate_probe_runs(variant, record_property):
+def test_rate_probe_runs(variant, warp_issue, record_property):
     n, sf, mpc, ctas, ring = variant
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.fp4_mma_rate(n, sf, mpc, ctas, 64, status=status, ring=ring)  # warm-up
+    B.fp4_mma_rate(n, sf, mpc, ctas, 64, status=status, ring=ring, warp_issue=warp_issue)  # warm-up
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    flops = B.fp4_mma_rate(n, sf, mpc, ctas, 2048 // mpc * 4, status=status, ring=ring)
+    flops = B.fp4_mma_rate(n, sf, mpc, ctas, 2048 // mpc * 4, status=status, ring=ring, warp_issue=warp_issue)
     e1.record()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -46,3 +48,16 @@ def test_rate_probe_runs(variant, record_property):
     # a rate above the part's nominal dense FP4 figure would mean the MMAs
     # did not run
     assert 0 < tflops < 20000
+
+
+@pytest.mark.gpu
+def test_same_kernel_with_more_shared_memory_later():
+    # n = 128, one stage of copies once, 4 MMAs per commit: the same kernel
+    # runs with 96 KB of shared memory at two CTAs per SM and 160 KB at one;
+    # the larger request after the smaller one raises the kernel's limit again
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for warp_issue in (False, True):
+        for ctas in (2, 1):
+            B.fp4_mma_rate(128, 0, 4, ctas, 64, status=status, warp_issue=warp_issue)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
