@@ -9,6 +9,8 @@
 // overlap), then reduces all of the chunk's sums of squares in one block
 // reduction, then adds w * u / rms into fp32 registers. HBM traffic: K rows
 // of H bf16 in, one row out.
+#include <algorithm>
+
 #include "common.cuh"
 #include "finalize_units.cuh"
 
@@ -301,6 +303,177 @@ __global__ void __launch_bounds__(kFinThreads, 2) finalize_staged_kernel(
   }
 }
 
+// The finalize made persistent for many tokens: a CTA takes tokens
+// blockIdx.x, + gridDim.x, ... and streams their route rows through a ring
+// of row buffers in shared memory (as many as kFinRingBytes hold, at most
+// kFinRingMaxSlots). A producer warp's lane 0 issues the bulk copy of each
+// valid route row into the next free slot (one full and one empty mbarrier
+// per slot), running up to a ring ahead across token boundaries, so the rows
+// of the next token are in flight while this one is reduced. The
+// kFinRingThreads consumer threads take the rows in the same order: each
+// loads its VPT 8-element vectors of the row into registers (kept as bf16,
+// converted where used), hands the slot back (one arrival per consumer
+// warp), reduces the row's sum of squares (one barrier of the consumer warps
+// per route) and adds coef_k r_k; after a
+// token's last route it applies the gain and stores the output row. A route's
+// reduction is a chain of dependent steps; the SM's kFinRingCtas CTAs run as
+// many such chains at once.
+// Both sides read expanded_to_permuted and skip the same entries (-1, and
+// out-of-range ones, which the producer records as MOE_ERR_INVALID_ROUTE).
+// Every wait is bounded. A producer that gives up stops issuing and lets its
+// copies in flight land; the consumers then run through their remaining
+// routes without waiting (every wait returns at once once the CTA's abort
+// flag is up), so that each of them passes the same per-route barriers, and
+// a thread whose wait gave up stores nothing.
+constexpr int kFinRingThreads = 128;
+constexpr int kFinRingWarps = kFinRingThreads / 32;
+// Three CTAs per SM with the gain held in registers: 149.9 us at T = 8192,
+// H = 5120, top-8 (the copies alone, timed without the arithmetic, 110 us);
+// two CTAs of eight consumer warps 203 us; four CTAs of four warps re-reading
+// the gain per row 201 us, holding it in registers (spills) 396 us.
+constexpr int kFinRingCtas = 3;  // per SM
+constexpr int kFinRingMaxSlots = 16;
+constexpr int kFinRingBytes = 60 * 1024;
+constexpr int kFinRingMinTokens = 1024;
+
+template <int VPT>
+__global__ void __launch_bounds__(kFinRingThreads + 32, kFinRingCtas) finalize_ring_kernel(
+    const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ e2p,
+    const float* __restrict__ topk_w, const __nv_bfloat16* __restrict__ gamma, float eps,
+    int weight_before_norm, int T, int K, int H, int num_rows, int R, __nv_bfloat16* __restrict__ out,
+    int32_t* status) {
+  extern __shared__ __align__(16) uint8_t ring[];  // R rows of H bf16
+  __shared__ __align__(8) uint64_t full[kFinRingMaxSlots];
+  __shared__ __align__(8) uint64_t empty[kFinRingMaxSlots];
+  __shared__ float red[2][kFinRingWarps];
+  __shared__ int abort_flag;
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = H / 8;
+  const uint32_t row_bytes = (uint32_t)H * 2;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kFinRingWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp == kFinRingWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      int n = 0;  // rows issued
+      bool stop = false;
+      for (int t = blockIdx.x; t < T && !stop; t += gridDim.x) {
+        for (int k = 0; k < K; ++k) {
+          int p = e2p[(size_t)t * K + k];
+          if (p < -1 || p >= num_rows) {
+            record_status(status, MOE_ERR_INVALID_ROUTE);
+            p = -1;
+          }
+          if (p < 0) continue;
+          const int slot = n % R, use = n / R;
+          if (use > 0 && !mbar_wait(smem_u32(&empty[slot]), (use - 1) & 1, &abort_flag, status)) {
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(smem_u32(&full[slot]), row_bytes);
+          bulk_load(smem_u32(ring) + slot * row_bytes, rows + (size_t)p * H, row_bytes, smem_u32(&full[slot]));
+          ++n;
+        }
+      }
+      // every copy issued has landed before the CTA's shared memory goes
+      for (int j = max(0, n - R); j < n; ++j) mbar_wait_cleanup(smem_u32(&full[j % R]), (j / R) & 1);
+    }
+    return;
+  }
+  // ------------------------------ consumers ------------------------------
+  // gain g = 1 + gamma (fp32), pairs of hidden-dimension elements
+  float2 g[VPT][4];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * kFinRingThreads;
+    const uint4 u = v < nvec ? __ldg(reinterpret_cast<const uint4*>(gamma + 8 * v)) : make_uint4(0, 0, 0, 0);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      g[i][q] = make_float2(1.f + f.x, 1.f + f.y);  // gain centre added in fp32
+    }
+  }
+  const float inv_h = 1.0f / (float)H;
+  int n = 0;       // rows consumed
+  bool ok = true;  // every wait of this thread ended with its row landed
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    float2 acc[VPT][4];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+      const int p = e2p[(size_t)t * K + k];
+      if (p < 0 || p >= num_rows) continue;  // the producer's decision, uniform across the CTA
+      const float wk = topk_w[(size_t)t * K + k];
+      const int slot = n % R;
+      ok = mbar_wait(smem_u32(&full[slot]), (n / R) & 1, &abort_flag, status) && ok;
+      const __nv_bfloat16* srow = reinterpret_cast<const __nv_bfloat16*>(ring + slot * row_bytes);
+      uint4 raw[VPT];  // route k's row, kept as bf16 (converted again when added)
+      float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = threadIdx.x + i * kFinRingThreads;
+        raw[i] = v < nvec ? *reinterpret_cast<const uint4*>(srow + 8 * v) : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(h[q]);
+          const float2 a = weight_before_norm ? fmul2(f, g[i][q]) : f;
+          ss2 = ffma2(a, a, ss2);
+        }
+      }
+      // the slot's bytes are in registers: hand it back to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+      float ss = ss2.x + ss2.y;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+      if (lane == 0) red[n & 1][warp] = ss;  // two buffers: one barrier per route
+      fin_bar_sync(kFinRingThreads);
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kFinRingWarps; ++w) total += red[n & 1][w];  // fixed order
+      // w / sqrt(ms + eps) as w * rsqrt(ms + eps): within 2 ulp in fp32, far
+      // below the bf16 output's step, and fewer instructions on the route's
+      // chain (142.7 against 149.9 us at T = 8192)
+      const float ck = wk * rsqrtf(total * inv_h + eps);
+      const float2 ck2 = make_float2(ck, ck);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = ffma2(__bfloat1622float2(h[q]), ck2, acc[i][q]);
+      }
+      ++n;
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kFinRingThreads;
+      if (v < nvec && ok) {
+        uint4 o;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 r = fmul2(acc[i][q], g[i][q]);
+          h[q] = __floats2bfloat162_rn(r.x, r.y);
+        }
+        *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * v) = o;
+      }
+    }
+  }
+}
+
 // The finalize for few tokens (decode batches), where its latency counts:
 // one CTA per token and one thread per 8-element vector of the hidden
 // dimension (H / 8 threads, H up to 5120), each loading its vector of all K
@@ -412,6 +585,39 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, int num_
     return launch_kernel(finalize_few_kernel, dim3(T), dim3((H / 8 + 31) / 32 * 32), 0, stream, true,
                          reinterpret_cast<const __nv_bfloat16*>(parts[0]), num_rows, e2p, w, gp, eps,
                          weight_before_norm, K, H, op, status);
+  const int ring_slots = (int)std::min<size_t>(kFinRingMaxSlots, (size_t)kFinRingBytes / ((size_t)H * 2));
+  const int ring_vpt = ceil_div(H / 8, kFinRingThreads);
+  if (nparts == 1 && T >= kFinRingMinTokens && ring_slots >= 2 && ring_vpt <= 5) {
+    auto rows = reinterpret_cast<const __nv_bfloat16*>(parts[0]);
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0, n = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 148;
+      sms = n;
+    }
+    const int grid = std::min(T, kFinRingCtas * sms);
+    const size_t smem = (size_t)ring_slots * H * 2;
+#define MOE_FIN_RING(n)                                                                                       \
+  case n:                                                                                                     \
+    err = ensure_smem_limit(reinterpret_cast<const void*>(finalize_ring_kernel<n>), kFinRingBytes);            \
+    if (err == cudaSuccess)                                                                                   \
+      err = launch_kernel(finalize_ring_kernel<n>, dim3(grid), dim3(kFinRingThreads + 32), smem, stream, true, \
+                          rows, e2p, w, gp, eps, weight_before_norm, T, K, H, num_rows, ring_slots, op,        \
+                          status);                                                                            \
+    return err;
+    switch (ring_vpt) {
+      MOE_FIN_RING(1)
+      MOE_FIN_RING(2)
+      MOE_FIN_RING(3)
+      MOE_FIN_RING(4)
+      MOE_FIN_RING(5)
+      default:
+        return cudaErrorInvalidValue;
+    }
+#undef MOE_FIN_RING
+  }
   if (nparts == 1 && K <= kFinMaxK && staged <= (size_t)kFinStagedMaxBytes && vpt <= 5) {
     auto rows = reinterpret_cast<const __nv_bfloat16*>(parts[0]);
 #define MOE_FIN_STAGED(n)                                                                       \

@@ -261,6 +261,12 @@ def test_tp_slice_layout_identity_on_gpu():
     (5, 8, 8192, 0.5, 1.0),
     (9, 4, 48, 1.0, 1.0),
     (7, 12, 1024, 1.0, 1.0),
+    # many tokens: the persistent kernel whose rows stream through a ring of
+    # shared-memory slots (several tokens per CTA, fewer slots than K for
+    # the widest row)
+    (1024, 8, 5120, 1.0, 1.0),
+    (1500, 6, 2048, 0.5, 1e2),
+    (1030, 8, 4096, 1.0, 1.0),
 ])
 @pytest.mark.parametrize("wbn", [True, False])
 def test_finalize_parity(T, K, H, gamma_sd, scale, wbn):
@@ -282,16 +288,15 @@ def test_finalize_parity(T, K, H, gamma_sd, scale, wbn):
     assert (np.abs(got - want["out_bf16"]) <= bound).all()
 
 
-@pytest.mark.parametrize("K,H", [(8, 5120), (3, 1024), (4, 16384)])
-def test_finalize_skips_out_of_range_rows(K, H):
+@pytest.mark.parametrize("K,H,T", [(8, 5120, 6), (3, 1024, 6), (4, 16384, 6), (8, 5120, 1024)])
+def test_finalize_skips_out_of_range_rows(K, H, T):
     """Entries of expanded_to_permuted past the rows buffer (num_rows and
     beyond) or below -1 are never read: the route adds nothing, as a -1 route
     does (the muse_moe_runner page, _finalize_native: unrouted routes read as
     zero rows), and the status word holds MOE_ERR_INVALID_ROUTE. The staged
     (K * H * 2 bytes in shared memory) and the register kernels are both
-    covered."""
+    covered, and the persistent ring kernel of many tokens."""
     rng = np.random.default_rng(K * H)
-    T = 6
     P = T * K
     rows_bits = inputs._to_bf16_bits(rng.standard_normal((P, H)))
     gamma = inputs._to_bf16_bits(rng.standard_normal(H) * 0.1)
@@ -326,6 +331,31 @@ def test_finalize_skips_out_of_range_rows(K, H):
                            bf16_dev(gamma), 1e-6, True, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+def test_finalize_ring_kernel_against_staged_kernel(wbn):
+    """The persistent ring kernel (1024 tokens and more) and the one-CTA-per-
+    token staged kernel (fewer) compute the same values in different
+    reduction orders: on the same tokens they agree to within one bf16 step
+    per element, and a token with no route gives a zero row in both."""
+    rng = np.random.default_rng(77)
+    T, K, H = 1024, 8, 5120
+    P = T * K + 64
+    rows = bf16_dev(inputs._to_bf16_bits(rng.standard_normal((P, H))))
+    gamma = bf16_dev(inputs._to_bf16_bits(rng.standard_normal(H) * 0.3))
+    e2p_np = rng.permutation(P)[: T * K].reshape(T, K).astype(np.int32)
+    e2p_np[5, 2] = -1
+    e2p_np[900, :] = -1  # a token with no route at all
+    e2p = torch.from_numpy(e2p_np).to(DEV)
+    w = torch.from_numpy(rng.random((T, K)).astype(np.float32)).to(DEV)
+    many = B.post_expert_finalize(rows, e2p, w, gamma, 1e-6, wbn)
+    few = B.post_expert_finalize(rows, e2p[: T - 1].contiguous(), w[: T - 1].contiguous(), gamma, 1e-6, wbn)
+    torch.cuda.synchronize()
+    a, b = many[: T - 1].double(), few.double()
+    assert ((a - b).abs() <= b.abs() * 2.0**-7 + 1e-6).all()
+    assert rel_l2(a.cpu().numpy(), b.cpu().numpy()) < 1e-3
+    assert not many[900].float().abs().any() and not few[900].float().abs().any()
 
 
 def test_finalize_readings_are_distinguished():
