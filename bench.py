@@ -54,10 +54,10 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # and the SHA-256 of the kernel sources it was taken on (gemm.cu,
 # common.cuh, layout.cuh in that order): once those change, traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_306_112 + 5_121_024,
-                  "sources": "675c0c01ececfcfb132625634a2c56377a2d99324716d660a59c0f6bd58de20a"},
-    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_723_019_008 + 85_335_040,
-                           "sources": "675c0c01ececfcfb132625634a2c56377a2d99324716d660a59c0f6bd58de20a"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_309_184 + 5_178_880,
+                  "sources": "2f0cc9c5dd0b680af0bfe378567e0e3caa11e0b2ba7cf6a9f0108fb595c8fb28"},
+    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_721_852_672 + 84_444_160,
+                           "sources": "2f0cc9c5dd0b680af0bfe378567e0e3caa11e0b2ba7cf6a9f0108fb595c8fb28"},
 }
 
 
