@@ -530,6 +530,19 @@ int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int ctas_per_sm,
                      int ring, int warp_issue, int stages, double* flops,
                      int32_t* status, void* stream);
 
+/* The pair form of the same measurement: tcgen05.mma.cta_group::2 (M = 256
+ * across the two CTAs of a cluster, on two SMs, A rows 128-255 read from the
+ * peer CTA's shared memory), one CTA per SM on an even number of SMs. Rank 0
+ * of each pair issues `stages` stages of 4 MMAs of N = n (128 or 256), with
+ * the scale atoms copied once (sf_copies 0) or every stage into both CTAs'
+ * tensor memory (1: tcgen05.cp.cta_group::2 32x128b.warpx4, one per 128 rows
+ * of A's and of B's scales per K = 64 step), a ring of 3 stages in flight.
+ * *flops (host) receives 2 * 256 * n * 64 * 4 * stages * pairs. Waits are
+ * bounded and report MOE_ERR_TIMEOUT in *status (optional device word);
+ * other arguments outside the ranges return MOE_ERR_INVALID_ARG. */
+int moe_fp4_mma_rate_pair(int n, int sf_copies, int stages, double* flops,
+                          int32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------
  * Self-test of the failure path: runs the library's bounded mbarrier wait on
  * a barrier that nothing completes, with limit_ns (1 us .. 1 s). On return

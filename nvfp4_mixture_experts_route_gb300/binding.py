@@ -130,6 +130,7 @@ _SIGNATURES = {
     "moe_dense_bf16_workspace_size": ([_I, _I, _I, C.POINTER(C.c_size_t)], _I),
     "moe_dense_bf16": ([_P, _P, _I, _I, _I, _P, _P, C.c_size_t, _P, _P], _I),
     "moe_fp4_mma_rate": ([_I, _I, _I, _I, _I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
+    "moe_fp4_mma_rate_pair": ([_I, _I, _I, C.POINTER(C.c_double), _P, _P], _I),
     "moe_selftest_wait_timeout": ([C.c_uint64, _P, _P, _P], _I),
     "moe_selftest_occupy": ([_I, _I, C.c_uint64, _P], _I),
     "moe_selftest_counter_timeout": ([C.c_uint64, _P, _P, _P, _P], _I),
@@ -604,6 +605,14 @@ def fp4_mma_rate(n: int, sf_copies: int, mmas_per_commit: int, ctas_per_sm: int,
     f = C.c_double()
     _check(load().moe_fp4_mma_rate(n, int(sf_copies), mmas_per_commit, ctas_per_sm, ring, int(warp_issue), stages,
                                    C.byref(f), _ptr(status), _stream(stream)))
+    return f.value
+
+
+def fp4_mma_rate_pair(n: int, sf_copies: int, stages: int, status=None, stream=None) -> float:
+    """Launch the pair-form (cta_group::2) rate probe (see the header);
+    returns the launch's FLOPs. Time it with events on the same stream."""
+    f = C.c_double()
+    _check(load().moe_fp4_mma_rate_pair(n, int(sf_copies), stages, C.byref(f), _ptr(status), _stream(stream)))
     return f.value
 
 

@@ -285,6 +285,126 @@ int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring
   return MOE_OK;
 }
 
+// Cluster helpers and the cta_group::2 forms of the copy, MMA and commit
+// (issued by lane 0 of a converged warp) for the pair-form probe below.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+#define MOE_PAIR_PRED "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+__device__ __forceinline__ void pair_copy_atom(uint32_t taddr, uint64_t desc) {
+  asm volatile(MOE_PAIR_PRED "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(desc) : "memory");
+}
+__device__ __forceinline__ void pair_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t acc) {
+  asm volatile(MOE_PAIR_PRED ".reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+               " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+               : "memory");
+}
+__device__ __forceinline__ void pair_commit(uint32_t bar) {
+  asm volatile(MOE_PAIR_PRED "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+               : "memory");
+}
+#undef MOE_PAIR_PRED
+
+// The pair form (cta_group::2) of the same MMA stream: clusters of two CTAs,
+// one CTA per SM. Both CTAs fill their operand tiles and allocate tensor
+// memory together (the pair allocation is collective); rank 0 alone issues,
+// as a converged warp with lane 0 issuing: M = 256 MMAs whose A rows 0-127
+// come from its own shared memory and 128-255 from its peer's (the same
+// offsets), each scale-atom copy into both CTAs' tensor memory, and the
+// commits to its own ring barriers. A cluster barrier before the teardown
+// keeps the peer's shared and tensor memory until rank 0's MMAs have landed.
+// FLOPs per pair MMA: 2 * 256 * N * 64.
+template <int N, int SFCP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32, 1) fp4_mma_pair_kernel(int stages, int32_t* status) {
+  constexpr int RING = 3, MPC = 4;
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bar[RING];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  constexpr int S = N / 128;
+  constexpr int SL = SFCP ? MPC : 4;
+  constexpr uint32_t ncols = rate_tmem_cols(N, SFCP, MPC, RING);
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const uint32_t sA = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t sB = sA + 128 * 128;
+  const uint32_t sSFA = sB + N * 128;
+  const uint32_t sSFB = sSFA + 4 * kAtomBytes;
+  uint8_t* base = dsmem + (sA - smem_u32(dsmem));
+  const uint32_t op_bytes = 128 * 128 + N * 128;
+  for (uint32_t i = lane * 4; i < op_bytes; i += 128)
+    *reinterpret_cast<uint32_t*>(base + i) = (i * 2654435761u) ^ 0x5A3C9617u ^ rank;
+  for (uint32_t i = op_bytes + lane * 4; i < op_bytes + 4 * kAtomBytes * (1 + S); i += 128)
+    *reinterpret_cast<uint32_t*>(base + i) = 0x38383838u;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (lane == 0) {
+    for (int r = 0; r < RING; ++r) mbar_init(smem_u32(&bar[r]), 1);
+    mbar_init(smem_u32(&drain_bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  cluster_sync_all();  // both CTAs' operands and barriers are ready
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  tc_fence_before();
+  __syncwarp();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t t_sf = tmem + N;
+  if (rank == 0) {
+    constexpr uint32_t idesc = idesc_nvf4(256, N);
+    const uint64_t a_desc = smem_desc(sA, 16, 1024, 2), b_desc = smem_desc(sB, 16, 1024, 2);
+    const uint64_t sfa_desc = smem_desc(sSFA, 0, 128, 0), sfb_desc = smem_desc(sSFB, 0, 128, 0);
+    auto sfa_col = [&](int r, int j) { return t_sf + (uint32_t)(r * SL * 4 * (1 + S) + 4 * j); };
+    auto sfb_col = [&](int r, int j) { return t_sf + (uint32_t)(r * SL * 4 * (1 + S) + 4 * SL + 4 * j * S); };
+    auto copies = [&](int r, int j) {
+      pair_copy_atom(sfa_col(r, j), sfa_desc + (uint64_t)((j & 3) * (kAtomBytes >> 4)));
+#pragma unroll
+      for (int sub = 0; sub < S; ++sub)
+        pair_copy_atom(sfb_col(r, j) + 4 * sub, sfb_desc + (uint64_t)(((j & 3) * S + sub) * (kAtomBytes >> 4)));
+    };
+    if (!SFCP) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) copies(0, j);
+    }
+    for (int s = 0; s < stages; ++s) {
+      const int r = s % RING;
+      if (s >= RING && !mbar_wait_warp(smem_u32(&bar[r]), ((s / RING) - 1) & 1, &abort_flag, status)) break;
+      tc_fence_after();
+      if (SFCP) {
+#pragma unroll
+        for (int j = 0; j < MPC; ++j) copies(r, j);
+      }
+#pragma unroll
+      for (int j = 0; j < MPC; ++j) {
+        const uint64_t koff = (uint64_t)((32 * (j & 3)) >> 4);
+        const int rs = SFCP ? r : 0, js = SFCP ? j : (j & 3);
+        pair_mma(tmem, a_desc + koff, b_desc + koff, idesc, sfa_col(rs, js), sfb_col(rs, js), (s | j) != 0);
+      }
+      pair_commit(smem_u32(&bar[r]));
+    }
+    pair_commit(smem_u32(&drain_bar));
+    mbar_wait_cleanup(smem_u32(&drain_bar), 0);
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();  // the peer's tensor memory and shared memory are no longer read
+  tc_fence_after();
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+}
+
 static_assert(rate_tmem_cols(128, 1, 4, 3) <= 256 && rate_tmem_cols(128, 0, 16, 3) <= 256 &&
                   rate_tmem_cols(256, 1, 4, 5) <= 512 && rate_tmem_cols(256, 0, 16, 3) <= 512 &&
                   rate_tmem_cols(128, 1, 4, 5) <= 512,
@@ -311,4 +431,34 @@ extern "C" int moe_fp4_mma_rate(int n, int sf_copies, int mmas_per_commit, int c
   rc = moe::launch_fp4_mma_rate(n, sf_copies, mmas_per_commit, ctas_per_sm, ring, warp_issue, stages, sms, status,
                                           reinterpret_cast<cudaStream_t>(stream), flops, &why);
   return rc ? moe::report_error(rc, "%s", why) : MOE_OK;
+}
+
+extern "C" int moe_fp4_mma_rate_pair(int n, int sf_copies, int stages, double* flops, int32_t* status, void* stream) {
+  if (!flops) return moe::report_error(MOE_ERR_INVALID_ARG, "flops is null");
+  if (!((n == 128 || n == 256) && (sf_copies == 0 || sf_copies == 1) && stages >= 1 && stages <= (1 << 24)))
+    return moe::report_error(MOE_ERR_INVALID_ARG, "fp4 rate pair: n in {128, 256}, sf_copies in {0, 1}, stages 1..2^24");
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess || sms < 2)
+    return moe::report_error(MOE_ERR_CUDA, "fp4 rate pair: no device (%s)", cudaGetErrorString(err));
+  const int grid = sms & ~1;  // one CTA per SM, clusters of two
+  const int smem = 160 * 1024;  // more than half an SM's shared memory: one CTA per SM
+  *flops = 2.0 * 256.0 * n * 64.0 * 4.0 * (double)stages * (double)(grid / 2);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+#define MOE_PAIR(nn, cp)                                                               \
+  if (n == nn && sf_copies == cp) {                                                    \
+    auto k = moe::fp4_mma_pair_kernel<nn, cp>;                                         \
+    err = moe::ensure_smem_limit(reinterpret_cast<const void*>(k), smem);              \
+    if (err == cudaSuccess) {                                                          \
+      k<<<grid, 32, smem, st>>>(stages, status);                                       \
+      err = cudaGetLastError();                                                        \
+    }                                                                                  \
+  }
+  MOE_PAIR(128, 0)
+  MOE_PAIR(128, 1)
+  MOE_PAIR(256, 0)
+  MOE_PAIR(256, 1)
+#undef MOE_PAIR
+  return err == cudaSuccess ? MOE_OK : moe::report_error(MOE_ERR_CUDA, "fp4 rate pair: %s", cudaGetErrorString(err));
 }

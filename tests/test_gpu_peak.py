@@ -26,6 +26,9 @@ def test_unfitting_variants_refused_on_host():
         assert lib.moe_fp4_mma_rate(n, sf, mpc, ctas, ring, 0, 8, C.byref(f), None, None) == want
         assert b"fp4 rate" in lib.moe_last_error()
     assert lib.moe_fp4_mma_rate(128, 0, 4, 1, 3, 2, 8, C.byref(f), None, None) == -1  # warp_issue 0 or 1
+    for n, sf, stages in ((64, 0, 8), (128, 2, 8), (256, 1, 0)):
+        assert lib.moe_fp4_mma_rate_pair(n, sf, stages, C.byref(f), None, None) == -1
+        assert b"fp4 rate pair" in lib.moe_last_error()
 
 
 @pytest.mark.gpu
@@ -61,3 +64,24 @@ def test_same_kernel_with_more_shared_memory_later():
             B.fp4_mma_rate(128, 0, 4, ctas, 64, status=status, warp_issue=warp_issue)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n,sf", [(128, 0), (128, 1), (256, 0), (256, 1)])
+def test_pair_rate_probe_runs(n, sf, record_property):
+    """The cta_group::2 form: clusters of two CTAs allocate tensor memory
+    together and rank 0 issues M = 256 MMAs over both; every variant ends
+    with a clean status word."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.fp4_mma_rate_pair(n, sf, 16, status=status)  # warm-up
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    flops = B.fp4_mma_rate_pair(n, sf, 2048, status=status)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count & ~1
+    assert flops == 2.0 * 256 * n * 64 * 4 * 2048 * (sms // 2)
+    tflops = flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    record_property("tflops", tflops)
+    assert 0 < tflops < 20000
