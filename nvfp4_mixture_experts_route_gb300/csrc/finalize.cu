@@ -474,6 +474,172 @@ __global__ void __launch_bounds__(kFinRingThreads + 32, kFinRingCtas) finalize_r
   }
 }
 
+// The expert-TP tail's form of the ring kernel: a route's row is the sum of
+// nparts partial row buffers (fp32 sum in part order, one bf16 rounding:
+// load_row_vec's arithmetic), so the producer copies each route's nparts
+// part rows into consecutive slots, and the consumers add them up (the slot
+// goes back as soon as its part is in registers) before the route's norm.
+// Two CTAs per SM: the fp32 sums of a route's vectors take registers that
+// three CTAs would not have.
+constexpr int kFinRingPartsCtas = 2;
+constexpr int kFinRingPartsBytes = 96 * 1024;
+
+template <int VPT>
+__global__ void __launch_bounds__(kFinRingThreads + 32, kFinRingPartsCtas) finalize_ring_parts_kernel(
+    const RowParts parts, const int32_t* __restrict__ e2p, const float* __restrict__ topk_w,
+    const __nv_bfloat16* __restrict__ gamma, float eps, int weight_before_norm, int T, int K, int H, int num_rows,
+    int R, __nv_bfloat16* __restrict__ out, int32_t* status) {
+  extern __shared__ __align__(16) uint8_t ring[];  // R part rows of H bf16
+  __shared__ __align__(8) uint64_t full[kFinRingMaxSlots];
+  __shared__ __align__(8) uint64_t empty[kFinRingMaxSlots];
+  __shared__ float red[2][kFinRingWarps];
+  __shared__ int abort_flag;
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = H / 8, np = parts.n;
+  const uint32_t row_bytes = (uint32_t)H * 2;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kFinRingWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp == kFinRingWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      int n = 0;  // part rows issued
+      bool stop = false;
+      for (int t = blockIdx.x; t < T && !stop; t += gridDim.x) {
+        for (int k = 0; k < K && !stop; ++k) {
+          int p = e2p[(size_t)t * K + k];
+          if (p < -1 || p >= num_rows) {
+            record_status(status, MOE_ERR_INVALID_ROUTE);
+            p = -1;
+          }
+          if (p < 0) continue;
+          for (int j = 0; j < np; ++j) {
+            const int slot = n % R, use = n / R;
+            if (use > 0 && !mbar_wait(smem_u32(&empty[slot]), (use - 1) & 1, &abort_flag, status)) {
+              stop = true;
+              break;
+            }
+            mbar_arrive_expect_tx(smem_u32(&full[slot]), row_bytes);
+            bulk_load(smem_u32(ring) + slot * row_bytes, parts.p[j] + (size_t)p * H, row_bytes,
+                      smem_u32(&full[slot]));
+            ++n;
+          }
+        }
+      }
+      // every copy issued has landed before the CTA's shared memory goes
+      for (int j = max(0, n - R); j < n; ++j) mbar_wait_cleanup(smem_u32(&full[j % R]), (j / R) & 1);
+    }
+    return;
+  }
+  // ------------------------------ consumers ------------------------------
+  float2 g[VPT][4];  // gain g = 1 + gamma (fp32)
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * kFinRingThreads;
+    const uint4 u = v < nvec ? __ldg(reinterpret_cast<const uint4*>(gamma + 8 * v)) : make_uint4(0, 0, 0, 0);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      g[i][q] = make_float2(1.f + f.x, 1.f + f.y);
+    }
+  }
+  const float inv_h = 1.0f / (float)H;
+  int n = 0;       // part rows consumed
+  int nr = 0;      // routes reduced
+  bool ok = true;  // every wait of this thread ended with its row landed
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    float2 acc[VPT][4];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+      const int p = e2p[(size_t)t * K + k];
+      if (p < 0 || p >= num_rows) continue;  // the producer's decision, uniform across the CTA
+      const float wk = topk_w[(size_t)t * K + k];
+      // the route's row: fp32 sum of its parts in part order, one bf16 rounding
+      float2 sum[VPT][4];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum[i][q] = make_float2(0.f, 0.f);
+      for (int j = 0; j < np; ++j) {
+        const int slot = n % R;
+        ok = mbar_wait(smem_u32(&full[slot]), (n / R) & 1, &abort_flag, status) && ok;
+        const __nv_bfloat16* srow = reinterpret_cast<const __nv_bfloat16*>(ring + slot * row_bytes);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = threadIdx.x + i * kFinRingThreads;
+          const uint4 u = v < nvec ? *reinterpret_cast<const uint4*>(srow + 8 * v) : make_uint4(0, 0, 0, 0);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(h[q]);
+            sum[i][q].x += f.x;
+            sum[i][q].y += f.y;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+        ++n;
+      }
+      uint4 raw[VPT];  // the route's row, bf16
+      float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw[i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          h[q] = __floats2bfloat162_rn(sum[i][q].x, sum[i][q].y);
+          const float2 f = __bfloat1622float2(h[q]);
+          const float2 a = weight_before_norm ? fmul2(f, g[i][q]) : f;
+          ss2 = ffma2(a, a, ss2);
+        }
+      }
+      float ss = ss2.x + ss2.y;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+      if (lane == 0) red[nr & 1][warp] = ss;  // two buffers: one barrier per route
+      fin_bar_sync(kFinRingThreads);
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kFinRingWarps; ++w) total += red[nr & 1][w];  // fixed order
+      const float ck = wk * rsqrtf(total * inv_h + eps);
+      const float2 ck2 = make_float2(ck, ck);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = ffma2(__bfloat1622float2(h[q]), ck2, acc[i][q]);
+      }
+      ++nr;
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kFinRingThreads;
+      if (v < nvec && ok) {
+        uint4 o;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 r = fmul2(acc[i][q], g[i][q]);
+          h[q] = __floats2bfloat162_rn(r.x, r.y);
+        }
+        *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * v) = o;
+      }
+    }
+  }
+}
+
 // The finalize for few tokens (decode batches), where its latency counts:
 // one CTA per token and one thread per 8-element vector of the hidden
 // dimension (H / 8 threads, H up to 5120), each loading its vector of all K
@@ -587,6 +753,37 @@ cudaError_t launch_finalize_parts(const void* const* parts, int nparts, int num_
                          weight_before_norm, K, H, op, status);
   const int ring_slots = (int)std::min<size_t>(kFinRingMaxSlots, (size_t)kFinRingBytes / ((size_t)H * 2));
   const int ring_vpt = ceil_div(H / 8, kFinRingThreads);
+  const int parts_slots = (int)std::min<size_t>(kFinRingMaxSlots, (size_t)kFinRingPartsBytes / ((size_t)H * 2));
+  if (nparts > 1 && T >= kFinRingMinTokens && parts_slots >= 2 && ring_vpt <= 5) {
+    static int psms = 0;
+    if (psms == 0) {
+      int dev = 0, n = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 148;
+      psms = n;
+    }
+    const int grid = std::min(T, kFinRingPartsCtas * psms);
+    const size_t smem = (size_t)parts_slots * H * 2;
+#define MOE_FIN_RING_PARTS(n)                                                                                   \
+  case n:                                                                                                       \
+    err = ensure_smem_limit(reinterpret_cast<const void*>(finalize_ring_parts_kernel<n>), kFinRingPartsBytes);   \
+    if (err == cudaSuccess)                                                                                     \
+      err = launch_kernel(finalize_ring_parts_kernel<n>, dim3(grid), dim3(kFinRingThreads + 32), smem, stream,   \
+                          true, rp, e2p, w, gp, eps, weight_before_norm, T, K, H, num_rows, parts_slots, op,     \
+                          status);                                                                              \
+    return err;
+    switch (ring_vpt) {
+      MOE_FIN_RING_PARTS(1)
+      MOE_FIN_RING_PARTS(2)
+      MOE_FIN_RING_PARTS(3)
+      MOE_FIN_RING_PARTS(4)
+      MOE_FIN_RING_PARTS(5)
+      default:
+        return cudaErrorInvalidValue;
+    }
+#undef MOE_FIN_RING_PARTS
+  }
   if (nparts == 1 && T >= kFinRingMinTokens && ring_slots >= 2 && ring_vpt <= 5) {
     auto rows = reinterpret_cast<const __nv_bfloat16*>(parts[0]);
     static int sms = 0;

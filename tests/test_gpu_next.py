@@ -108,15 +108,19 @@ def test_norm_quantize_into_permuted_workspace_equals_gathered_linear(T, H, I, E
     assert not scales.cpu().numpy()[pad].any()
 
 
-@pytest.mark.parametrize("nparts,H", [(8, 5120), (4, 256), (1, 1024)])
-def test_expert_tp_tail_finalize(nparts, H):
-    rng = np.random.default_rng(nparts * H)
-    T, K = 6, 4
+@pytest.mark.parametrize("nparts,H,T", [(8, 5120, 6), (4, 256, 6), (1, 1024, 6),
+                                        # many tokens: the persistent kernel that streams every
+                                        # route's part rows through a shared-memory ring
+                                        (8, 5120, 1024), (3, 2048, 1100), (2, 4096, 1030)])
+def test_expert_tp_tail_finalize(nparts, H, T):
+    rng = np.random.default_rng(nparts * H + T)
+    K = 4
     P = T * K + 3
     parts = [inputs._to_bf16_bits(rng.standard_normal((P, H)) / np.sqrt(nparts)) for _ in range(nparts)]
     gamma = inputs._to_bf16_bits(rng.standard_normal(H) * 0.5)
     e2p = rng.permutation(P)[: T * K].reshape(T, K).astype(np.int32)
     e2p[2, 1] = -1
+    e2p[5, :] = -1  # a token with no route: a zero row
     w = rng.random((T, K)).astype(np.float32)
     summed = sum(codecs.bf16_bits_to_f64(p).astype(np.float32) for p in parts)
     rows = codecs.round_to_bf16(summed.astype(np.float64))
@@ -126,6 +130,9 @@ def test_expert_tp_tail_finalize(nparts, H):
                                     bf16_dev(gamma), 1e-6)
     torch.cuda.synchronize()
     assert rel_l2(bf16_host_f64(got), want["out"]) < 2e-3
+    # per element: at most one bf16 step from the correctly rounded value
+    rms = np.sqrt(np.mean(want["out"] ** 2))
+    assert (np.abs(bf16_host_f64(got) - want["out_bf16"]) <= np.abs(want["out_bf16"]) * 2.0**-7 + 1e-4 * rms).all()
     if nparts == 1:
         one = B.post_expert_finalize(dev_parts[0], torch.from_numpy(e2p).to(DEV), torch.from_numpy(w).to(DEV),
                                      bf16_dev(gamma), 1e-6)
