@@ -151,6 +151,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait with acquire at cluster scope, for an mbarrier that the
+// other CTA of a cluster arrives on (release at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  int32_t* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, MOE_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // mbar_wait by every lane of a converged warp, with one outcome for all of
 // them (false if any lane gave up), so that a warp-converged issue loop stays
 // converged.
@@ -214,6 +244,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+
+// The pair form of the same load: the box lands in this CTA's shared memory
+// and its bytes complete on an mbarrier of either CTA of the pair (`bar` is a
+// shared::cluster address, e.g. from mapa), so that one CTA's barrier can
+// count both CTAs' halves of a stage.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+// The shared::cluster address of the variable at local shared offset `addr`
+// in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
 }
 
 // The same loads with an L2 eviction policy (a createpolicy value): data
@@ -383,6 +433,87 @@ __device__ __forceinline__ void tc_commit_f(uint32_t bar) {
     tc_commit(bar);
 }
 
+// ---------------------------------------------------------------------------
+// The pair form (cta_group::2): two CTAs of a cluster, on two SMs, share one
+// MMA of M = 256 (A rows 0-127 from rank 0's shared memory, 128-255 from rank
+// 1's, the same offsets); each CTA's tensor memory holds its 128 rows of the
+// accumulator. Tensor memory is allocated and freed by one warp of each CTA
+// together; rank 0 issues the copies, MMAs and commits. Every tcgen05
+// instruction of a kernel that uses the pair form takes cta_group::2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs: release what this CTA wrote, acquire the peer's.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Issued by lane 0 of a converged warp (the predicate is set inside the asm).
+#define MOE_PAIR_PRED \
+  "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+__device__ __forceinline__ void pair_copy_atom(uint32_t taddr, uint64_t desc) {
+  asm volatile(MOE_PAIR_PRED "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+__device__ __forceinline__ void pair_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t acc) {
+  asm volatile(MOE_PAIR_PRED
+               ".reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+               " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+               : "memory");
+}
+// Commit to this CTA's mbarrier.
+__device__ __forceinline__ void pair_commit(uint32_t bar) {
+  asm volatile(MOE_PAIR_PRED "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                   bar)
+               : "memory");
+}
+// Commit to the mbarrier at the same offset in both CTAs of the pair.
+__device__ __forceinline__ void pair_commit_both(uint32_t bar) {
+  asm volatile(MOE_PAIR_PRED
+               "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+               " [%0], %1;\n\t}" ::"r"(bar),
+               "h"((uint16_t)3)
+               : "memory");
+}
+#undef MOE_PAIR_PRED
+// Arrive (release at cluster scope) on the mbarrier at local offset `bar` in
+// the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
+      "r"(rank)
+      : "memory");
+}
+// The same arrive without release semantics: for a hand-off that orders no
+// memory, only tensor-memory reads that tcgen05.wait::ld has already
+// completed (a release at cluster scope costs the arriving thread about
+// 0.7 us).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar, uint32_t rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
+      "r"(rank)
+      : "memory");
+}
+
 // Instruction descriptor for kind::mxf4nvf4: A and B e2m1 (format 1) in bits
 // [7,10) and [10,13), both K-major, N >> 3 in [17,23), scale type ue4m3 (0)
 // in bit 23, M >> 4 in [24,29), scale-factor ids 0, dense K = 64.
@@ -527,6 +658,21 @@ inline CUresult encode_rows_map(CUtensorMap* map, const void* base, uint64_t row
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+
+// Scale-atom arrays as a 2D uint8 tensor of 128-byte rows (4 rows per
+// 512-byte atom), boxes of box_rows rows, no swizzle: a TMA tensor load of
+// 16 rows brings the 4 atoms of a K = 256 stage.
+inline CUresult encode_atoms_map(CUtensorMap* map, const void* base, uint64_t bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {128u, bytes / 128u};
+  const cuuint64_t strides[1] = {128u};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
 
 // Packed fp32x2 arithmetic (one instruction for two lanes of the pair):
 // d = a * b + c and d = a * b, each element rounded as its scalar form.

@@ -285,33 +285,6 @@ int launch_fp4_mma_rate(int n, int sf_copies, int mpc, int ctas_per_sm, int ring
   return MOE_OK;
 }
 
-// Cluster helpers and the cta_group::2 forms of the copy, MMA and commit
-// (issued by lane 0 of a converged warp) for the pair-form probe below.
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-#define MOE_PAIR_PRED "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-__device__ __forceinline__ void pair_copy_atom(uint32_t taddr, uint64_t desc) {
-  asm volatile(MOE_PAIR_PRED "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(desc) : "memory");
-}
-__device__ __forceinline__ void pair_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                         uint32_t acc) {
-  asm volatile(MOE_PAIR_PRED ".reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
-               " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
-               "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
-               : "memory");
-}
-__device__ __forceinline__ void pair_commit(uint32_t bar) {
-  asm volatile(MOE_PAIR_PRED "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-               : "memory");
-}
-#undef MOE_PAIR_PRED
 
 // The pair form (cta_group::2) of the same MMA stream: clusters of two CTAs,
 // one CTA per SM. Both CTAs fill their operand tiles and allocate tensor
@@ -354,10 +327,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32, 1) fp4_mma_pair_
   }
   __syncwarp();
   cluster_sync_all();  // both CTAs' operands and barriers are ready
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  tmem_alloc_pair(smem_u32(&tmem_slot), ncols);
+  tmem_relinquish_pair();
   tc_fence_before();
   __syncwarp();
   tc_fence_after();
@@ -402,7 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32, 1) fp4_mma_pair_
   __syncwarp();
   cluster_sync_all();  // the peer's tensor memory and shared memory are no longer read
   tc_fence_after();
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  tmem_dealloc_pair(tmem, ncols);
 }
 
 static_assert(rate_tmem_cols(128, 1, 4, 3) <= 256 && rate_tmem_cols(128, 0, 16, 3) <= 256 &&
