@@ -52,12 +52,13 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the roofline kernel, from one ncu capture of it on this workload's batch,
 # and the SHA-256 of the kernel sources it was taken on (gemm.cu,
-# common.cuh, layout.cuh in that order): once those change, traffic is null.
+# gemm_pair.cu, common.cuh, layout.cuh in that order): once those change,
+# traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_309_184 + 5_178_880,
-                  "sources": "2f0cc9c5dd0b680af0bfe378567e0e3caa11e0b2ba7cf6a9f0108fb595c8fb28"},
-    "prefill_t8192_zipf": {"kernel": "grouped_gemm_kernel<1, 128>", "bytes": 1_721_852_672 + 84_444_160,
-                           "sources": "2f0cc9c5dd0b680af0bfe378567e0e3caa11e0b2ba7cf6a9f0108fb595c8fb28"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_349_376 + 5_096_448,
+                  "sources": "f63d411526d9fdad91fde209e35d04143fc5af3f42f8356f73afe317afa7e77c"},
+    "prefill_t8192_zipf": {"kernel": "gemm1_pair_kernel", "bytes": 1_722_235_904 + 83_933_184,
+                           "sources": "f63d411526d9fdad91fde209e35d04143fc5af3f42f8356f73afe317afa7e77c"},
 }
 
 
@@ -70,7 +71,7 @@ def _traffic(workload: str, kernel: str):
     if t is None or not kernel.startswith(t["kernel"]):
         return None
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "layout.cuh"):
+    for f in ("gemm.cu", "gemm_pair.cu", "common.cuh", "layout.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_route_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return t["bytes"] if h.hexdigest() == t["sources"] else None
@@ -499,11 +500,16 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
                 "algorithmic_bytes": n_touch * w13_bytes, "launch_ms": gemm1_ms}
     else:
         ach = gemm1_flops / (gemm1_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": f"grouped_gemm_kernel<1, {tile}> (GEMM1 + SwiGLU + requant)",
+        # 128-row tiles with H and 2I multiples of 256 run GEMM1 in the pair form
+        pair = tile == 128 and H % 256 == 0 and (2 * I) % 256 == 0
+        g1_kernel = "gemm1_pair_kernel" if pair else f"grouped_gemm_kernel<1, {tile}>"
+        roof = {"bound": "tensor", "kernel": g1_kernel + (" (GEMM1 + SwiGLU + requant, tcgen05 cta_group::2 over "
+                                                          "two-CTA clusters)" if pair else
+                                                          " (GEMM1 + SwiGLU + requant)"),
                 "achieved": ach, "peak": fp4_peak["tflops"], "unit": "TFLOP/s", "frac": ach / fp4_peak["tflops"],
                 "peak_kind": "measured dense NVFP4 (burst): " + fp4_peak["how"],
                 "frac_of_bf16x6": ach / (pk["bf16"] * FP4_PER_BF16),
-                "traffic": _traffic(w.name, f"grouped_gemm_kernel<1, {tile}>"),
+                "traffic": _traffic(w.name, g1_kernel),
                 "algorithmic_flops": gemm1_flops, "launch_ms": gemm1_ms,
                 "gemm2": {"achieved": gemm2_flops / (gemm2_ms * 1e-3) / 1e12,
                           "frac": gemm2_flops / (gemm2_ms * 1e-3) / 1e12 / fp4_peak["tflops"],

@@ -969,12 +969,12 @@ static bool gemm2_side(GemmParams& p, CUtensorMap* ta, CUtensorMap* tb, const vo
   return true;
 }
 
-bool gemm1_pair_fits(int tile_m, int H, int I, int max_tiles);
+bool gemm_pair_fits(int tile_m, int K, int rows_w, int max_tiles);
 cudaError_t launch_gemm1_pair(const CUtensorMap& tmW, const CUtensorMap& tmA, const uint8_t* w_sf,
                               const uint8_t* a_sf, const float* g1_alphas, const float* g1_scale_c,
-                              const float* a2_gscale, const int32_t* tile_expert, const int32_t* totals,
-                              uint8_t* hq, uint8_t* hq_sf, int E, int H, int I, int max_tiles, int32_t* status,
-                              cudaStream_t stream, bool pdl);
+                              const float* a2_gscale, const int32_t* tile_expert, const int32_t* tile_row_limit,
+                              const int32_t* totals, uint8_t* hq, uint8_t* hq_sf, int E, int H, int I,
+                              int max_tiles, int32_t* status, cudaStream_t stream, bool pdl);
 
 int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas,
                  const float* g1_scale_c, const float* a2_gscale, const int32_t* tile_expert,
@@ -991,10 +991,10 @@ int launch_gemm1(const void* p_w13, const void* p_w13_sf, const float* g1_alphas
   }
   // 128-row route tiles whose K and 2I are multiples of 256 (the prefill
   // shapes): the pair form (gemm_pair.cu), 0.637 against 0.695 ms at T = 8192
-  if (gemm1_pair_fits(tile_m, H, I, max_tiles)) {
+  if (gemm_pair_fits(tile_m, H, 2 * I, max_tiles)) {
     if (launch_gemm1_pair(maps[0], maps[1], reinterpret_cast<const uint8_t*>(p_w13_sf), a_sf, g1_alphas, g1_scale_c,
-                          a2_gscale, tile_expert, totals, h_codes, h_sf, E, H, I, max_tiles, status, stream,
-                          pdl) != cudaSuccess) {
+                          a2_gscale, tile_expert, tile_row_limit, totals, h_codes, h_sf, E, H, I, max_tiles, status,
+                          stream, pdl) != cudaSuccess) {
       *why = "GEMM1 (pair form) launch failed";
       return MOE_ERR_CUDA;
     }
@@ -1030,11 +1030,15 @@ int launch_gemm2(const void* p_w2, const void* p_w2_sf, const float* g2_alphas,
   }
   maps[0] = maps[2];
   maps[1] = maps[3];
+  const int rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
+  // (GEMM2 in the pair form of gemm_pair.cu, measured: 0.457 against 0.432 ms
+  // at T = 8192; its 8-stage units expose the accumulator hand-back that the
+  // second CTA per SM of this kernel hides)
   p.tile_expert = tile_expert;
   p.tile_row_limit = tile_row_limit;
   p.totals = totals;
   p.rows = reinterpret_cast<__nv_bfloat16*>(rows);
-  p.rows32 = (reinterpret_cast<uintptr_t>(rows) % 32 == 0 && (size_t)H * 2 % 32 == 0) ? 1 : 0;
+  p.rows32 = rows32;
   p.row_ss = row_ss;
   p.ss_gamma = reinterpret_cast<const __nv_bfloat16*>(ss_gamma);
   p.ss_wbn = ss_wbn;

@@ -46,18 +46,19 @@ static_assert(256 + kStages * 48 <= (int)kTmemCols, "pair GEMM1 tensor memory");
 static_assert(kSmem <= 232448, "pair GEMM1 shared memory");
 }  // namespace gpair
 
-struct PairGemm1Params {
-  const uint8_t* w_sf;   // prepared w13 scale atoms [E][2I/128][H/64][512]
-  const uint8_t* a_sf;   // route scale atoms [tiles][H/64][512]
+struct PairGemmParams {
+  const uint8_t* w_sf;   // prepared weight scale atoms [E][rows_w/128][K/64][512]
+  const uint8_t* a_sf;   // route operand scale atoms [tiles][K/64][512]
   const float* s0;       // g1_alphas
   const float* s1;       // g1_scale_c
   const float* a2_gscale;
   const int32_t* tile_expert;
+  const int32_t* tile_row_limit;
   const int32_t* totals;
   uint8_t* hq;           // intermediate codes [P][I/2]
   uint8_t* hq_sf;        // intermediate scale atoms [tiles][I/64][512]
   int32_t* status;
-  int H, I, max_tiles, num_experts;
+  int K, rows_w, I, max_tiles, num_experts;  // contraction length, weight rows per expert
 };
 
 // The pair-start route tiles (the first tile of each expert's consecutive
@@ -100,8 +101,8 @@ __device__ __forceinline__ int build_pair_starts(const int32_t* tile_expert, int
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
     gemm1_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmWsf, const __grid_constant__ CUtensorMap tmAsf,
-                      const PairGemm1Params p) {
+                     const __grid_constant__ CUtensorMap tmWsf, const __grid_constant__ CUtensorMap tmAsf,
+                     const PairGemmParams p) {
   using namespace gpair;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];   // rank 0: both CTAs' halves of the stage landed
@@ -153,8 +154,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
   if (tid == 0) pdl_trigger();
   const uint32_t tmem = tmem_slot;
   const int npairs = npairs_s;
-  const int KC = p.H / 64, nks = p.H / 256;
-  const int tw = (2 * p.I) / 256;  // units per pair (256 weight rows each)
+  const int KC = p.K / 64, nks = p.K / 256;
+  const int tw = p.rows_w / 256;  // units per pair (256 weight rows each)
   const int n_units = npairs * tw;
   const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   // unit u: pair u / tw (weight tile fastest, so that the clusters working
@@ -180,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool stop = false;
-      const int wrows_per_e = 2 * p.I / 128;  // 128-row weight tiles per expert
+      const int wrows_per_e = p.rows_w / 128;  // 128-row weight tiles per expert
       for (int u = cl; u < n_units && !stop; u += ncl) {
         int w, e, mine;
         bool bad;
@@ -193,7 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
           const int t0 = starts[u / tw];
           peer = (t0 + 1 < ntiles && __ldcg(p.tile_expert + t0 + 1) == __ldcg(p.tile_expert + t0)) ? t0 + 1 : -1;
         }
-        const int wrow = e * 2 * p.I + 256 * w + 128 * (int)rank;
+        const int wrow = e * p.rows_w + 256 * w + 128 * (int)rank;
         // atom rows (128 bytes, 4 per atom) of the two weight halves and of the route tile, at K step 0
         const int wsf_row0 = ((e * wrows_per_e + 2 * w) * KC) * 4, wsf_row1 = wsf_row0 + KC * 4;
         const int asf_row = mine >= 0 ? mine * KC * 4 : 0;
@@ -359,40 +360,50 @@ static int even_sm_count() {
   return n & ~1;
 }
 
-// Whether the pair form takes a GEMM1 of this shape.
-bool gemm1_pair_fits(int tile_m, int H, int I, int max_tiles) {
-  return tile_m == 128 && H % 256 == 0 && (2 * I) % 256 == 0 && max_tiles <= gpair::kMaxPairs && max_tiles > 0;
+// Whether the pair form takes a GEMM1 of this shape: 128-row route tiles,
+// K (= H) and the weight rows per expert (2I) multiples of 256.
+bool gemm_pair_fits(int tile_m, int K, int rows_w, int max_tiles) {
+  return tile_m == 128 && K % 256 == 0 && rows_w % 256 == 0 && max_tiles <= gpair::kMaxPairs && max_tiles > 0;
 }
+
+static cudaError_t launch_gemm_pair(const CUtensorMap& tmW, const CUtensorMap& tmA, PairGemmParams& p, int E,
+                                    cudaStream_t stream, bool pdl) {
+  CUtensorMap tmWsf, tmAsf;
+  const uint64_t kc_bytes = (uint64_t)(p.K / 64) * kAtomBytes;
+  p.num_experts = E;
+  if (encode_atoms_map(&tmWsf, p.w_sf, (uint64_t)E * (p.rows_w / 128) * kc_bytes, 16) != CUDA_SUCCESS ||
+      encode_atoms_map(&tmAsf, p.a_sf, (uint64_t)p.max_tiles * kc_bytes, 16) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  auto kern = gemm1_pair_kernel;
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)gpair::kSmem);
+  if (err != cudaSuccess) return err;
+  return launch_kernel(kern, dim3(even_sm_count()), dim3(gpair::kThreads), gpair::kSmem, stream, pdl, tmW, tmA,
+                       tmWsf, tmAsf, p);
+}
+
 
 cudaError_t launch_gemm1_pair(const CUtensorMap& tmW, const CUtensorMap& tmA, const uint8_t* w_sf,
                               const uint8_t* a_sf, const float* g1_alphas, const float* g1_scale_c,
-                              const float* a2_gscale, const int32_t* tile_expert, const int32_t* totals,
-                              uint8_t* hq, uint8_t* hq_sf, int E, int H, int I, int max_tiles, int32_t* status,
-                              cudaStream_t stream, bool pdl) {
-  CUtensorMap tmWsf, tmAsf;
-  const uint64_t kc_bytes = (uint64_t)(H / 64) * kAtomBytes;
-  if (encode_atoms_map(&tmWsf, w_sf, (uint64_t)E * (2 * I / 128) * kc_bytes, 16) != CUDA_SUCCESS ||
-      encode_atoms_map(&tmAsf, a_sf, (uint64_t)max_tiles * kc_bytes, 16) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  PairGemm1Params p{};
+                              const float* a2_gscale, const int32_t* tile_expert, const int32_t* tile_row_limit,
+                              const int32_t* totals, uint8_t* hq, uint8_t* hq_sf, int E, int H, int I,
+                              int max_tiles, int32_t* status, cudaStream_t stream, bool pdl) {
+  PairGemmParams p{};
   p.w_sf = w_sf;
   p.a_sf = a_sf;
   p.s0 = g1_alphas;
   p.s1 = g1_scale_c;
   p.a2_gscale = a2_gscale;
   p.tile_expert = tile_expert;
+  p.tile_row_limit = tile_row_limit;
   p.totals = totals;
   p.hq = hq;
   p.hq_sf = hq_sf;
   p.status = status;
-  p.H = H;
+  p.K = H;
+  p.rows_w = 2 * I;
   p.I = I;
   p.max_tiles = max_tiles;
-  p.num_experts = E;
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gemm1_pair_kernel), (int)gpair::kSmem);
-  if (err != cudaSuccess) return err;
-  return launch_kernel(gemm1_pair_kernel, dim3(even_sm_count()), dim3(gpair::kThreads), gpair::kSmem, stream, pdl,
-                       tmW, tmA, tmWsf, tmAsf, p);
+  return launch_gemm_pair(tmW, tmA, p, E, stream, pdl);
 }
 
 }  // namespace moe
