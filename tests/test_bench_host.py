@@ -11,7 +11,7 @@ import bench  # noqa: E402
 
 def _digest():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "layout.cuh"):
+    for f in ("gemm.cu", "gemm_pair.cu", "common.cuh", "layout.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_route_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -25,3 +25,11 @@ def test_traffic_only_for_unchanged_sources(monkeypatch):
     assert bench._traffic("decode_b64_zipf", "grouped_gemm_kernel<3, 32>") is None
     monkeypatch.setattr(bench, "NCU_TRAFFIC", {"decode_b8": dict(entry, sources="0" * 64)})
     assert bench._traffic("decode_b8", "grouped_gemm_kernel<3, 32>") is None
+
+
+def test_recorded_traffic_matches_the_sources():
+    """The committed captures were taken on the committed kernel sources, so
+    the bench line carries their traffic (not null)."""
+    for name, t in bench.NCU_TRAFFIC.items():
+        assert t["sources"] == _digest(), name
+        assert bench._traffic(name, t["kernel"]) == t["bytes"]

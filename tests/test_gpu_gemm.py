@@ -485,6 +485,66 @@ def test_gemm1_intermediate_and_end_to_end(small_cases, idx, record_property):
     assert err < OUT_BAR, f"out rel-L2 {err:.3g}; gpu {finite_summary(got['out'])}"
 
 
+def _pairing_ids(T, layout):
+    """topk_ids [T, 2] from (expert, first token, last token + 1) runs of each
+    route slot: every token routes slot 0 and slot 1 to distinct experts."""
+    ids = np.full((T, 2), -1, np.int32)
+    for slot, runs in enumerate(layout):
+        for e, t0, t1 in runs:
+            ids[t0:t1, slot] = e
+    return ids
+
+
+@pytest.mark.parametrize("case", ["odd_and_even_tiles", "lone_tiles_only"])
+def test_pair_gemm1_tile_pairing(case, record_property):
+    """GEMM1 at 128-row tiles with H and 2I multiples of 256 runs as 256-row
+    MMAs over a pair of consecutive route tiles of one expert. Expert tile
+    counts 3 (a pair and a lone last tile), 2 (one pair, the second tile full
+    or one row), 1 (a lone partial tile) and 0, against the oracle."""
+    T, H, I, E = 300, 512, 256, 6
+    w = _workload(T, H, I, E, 2, "uniform", 128)
+    raw = inputs.make_layer(w)
+    batch = inputs.make_batch(w)
+    if case == "odd_and_even_tiles":
+        # expert 0: 300 routes (3 tiles), expert 1: 256 (2 full tiles),
+        # expert 2: 43 (1 tile), expert 5: 1; experts 3 and 4: none
+        batch["topk_ids"] = _pairing_ids(T, [[(0, 0, 300)], [(1, 0, 256), (2, 256, 299), (5, 299, 300)]])
+    else:
+        # every expert has at most one tile: each pair's second tile is absent
+        batch["topk_ids"] = _pairing_ids(T, [[(0, 0, 100), (1, 100, 200), (2, 200, 300)],
+                                             [(3, 0, 120), (4, 120, 250), (5, 250, 300)]])
+    a1, a2 = 4.0, 1e-3
+    ref = olayer.moe_layer(batch["x"], batch["topk_ids"], batch["topk_weights"], raw, a1, a2, raw["gamma"],
+                           1e-6, 128, return_intermediate=True)
+    got = run_gpu(Prepared(raw), batch, 128, a1, a2)
+    assert got["status"] == 0
+    assert np.array_equal(got["e2p"], ref["meta"]["expanded_to_permuted"])
+    e2p = got["e2p"].reshape(-1)
+    live = e2p >= 0
+    sf_match = np.mean(got["hq_sf"][e2p[live]] == ref["routes"]["hq_sf"][live])
+    code_match = np.mean(canon_codes(codecs.unpack_nibbles(got["hq_codes"][e2p[live]])) ==
+                         canon_codes(ref["routes"]["hq_codes"][live]))
+    assert sf_match > 0.99 and code_match > 0.99, (sf_match, code_match)
+    err_rows = rel_l2(got["rows"][e2p[live]], ref["routes"]["rows_bf16"][live])
+    err = rel_l2(got["out"], ref["out"])
+    for k, v in (("sf_match", sf_match), ("code_match", code_match), ("rows_rel_l2", err_rows), ("out_rel_l2", err)):
+        record_property(k, float(v))
+    assert err_rows < OUT_BAR and err < OUT_BAR, (err_rows, err)
+
+
+def test_pair_gemm1_without_routes():
+    """No route at all (every id -1) at the pair form's shapes: no tile, no
+    unit; the launch completes with a clean status and a zero output."""
+    T, H, I, E = 40, 512, 256, 4
+    w = _workload(T, H, I, E, 2, "uniform", 128)
+    raw = inputs.make_layer(w)
+    batch = inputs.make_batch(w)
+    batch["topk_ids"] = np.full((T, 2), -1, np.int32)
+    got = run_gpu(Prepared(raw), batch, 128, 4.0, 1e-3, export=False)
+    assert got["status"] == 0
+    assert not got["out"].any()
+
+
 @pytest.mark.parametrize("idx", range(len(SMALL)))
 @pytest.mark.parametrize("wbn", [True, False])
 def test_fused_sums_of_squares_and_streaming_finalize(small_cases, idx, wbn, record_property):
