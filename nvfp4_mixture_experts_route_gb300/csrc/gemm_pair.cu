@@ -40,7 +40,7 @@ constexpr uint32_t kBox = 128 * 128;                     // 128 rows x 128 bytes
 constexpr uint32_t kSfa = 4 * kAtomBytes;                // a route tile's 4 atoms of a stage
 constexpr uint32_t kSfb = 8 * kAtomBytes;                // both weight halves' 4 atoms
 constexpr int kMaxPairs = 1024;                          // route tiles a launch may hold
-constexpr uint32_t kSmem = 1024 + kStages * (2 * kBox + kSfa + kSfb) + kMaxPairs * 4;
+constexpr uint32_t kSmem = 1024 + kStages * (2 * kBox + kSfa + kSfb) + kMaxPairs * 8;  // + pair list and experts
 constexpr uint32_t kTmemCols = 512;
 static_assert(256 + kStages * 48 <= (int)kTmemCols, "pair GEMM1 tensor memory");
 static_assert(kSmem <= 232448, "pair GEMM1 shared memory");
@@ -63,10 +63,14 @@ struct PairGemmParams {
 
 // The pair-start route tiles (the first tile of each expert's consecutive
 // pairs) in ascending order, by one warp: a tile starts a pair when its
-// distance from the first tile of its expert's run is even. Every lane
-// loads its tiles' experts first (kMaxPairs / 32 of them at most), so that
-// the scan waits for one round of loads, not one per 32 tiles.
-__device__ __forceinline__ int build_pair_starts(const int32_t* tile_expert, int ntiles, int* starts, int lane) {
+// distance from the first tile of its expert's run is even. starts[i] is the
+// tile, with kHasPeer set when the next tile belongs to the same expert;
+// experts[i] its expert. Every lane loads its tiles' experts first
+// (kMaxPairs / 32 of them at most), so that the scan waits for one round of
+// loads, not one per 32 tiles, and the units read only shared memory after.
+constexpr int kHasPeer = 1 << 30;
+__device__ __forceinline__ int build_pair_starts(const int32_t* tile_expert, int ntiles, int* starts, int* experts,
+                                                 int lane) {
   constexpr int kPer = gpair::kMaxPairs / 32;
   int ex[kPer];
 #pragma unroll
@@ -89,9 +93,17 @@ __device__ __forceinline__ int build_pair_starts(const int32_t* tile_expert, int
     const uint32_t upto = lane == 31 ? rs : (rs & ((2u << lane) - 1u));
     const int start = upto ? base + (31 - __clz(upto)) : carry_start;
     const bool ps = valid && ((t - start) & 1) == 0;
+    // the expert of tile t + 1 (lane 31: the first tile of the next 32)
+    int e_next = __shfl_down_sync(0xFFFFFFFFu, e, 1);
+    const int e_wrap = __shfl_sync(0xFFFFFFFFu, i + 1 < kPer ? ex[i + 1 < kPer ? i + 1 : i] : -2, 0);
+    if (lane == 31) e_next = e_wrap;
+    const bool peer = t + 1 < ntiles && e_next == e;
     const uint32_t pm = __ballot_sync(0xFFFFFFFFu, ps);
     const int at = count + __popc(pm & ((1u << lane) - 1u));
-    if (ps) starts[at] = t;
+    if (ps) {
+      starts[at] = t | (peer ? kHasPeer : 0);
+      experts[at] = e;
+    }
     count += __popc(pm);
     carry_start = __shfl_sync(0xFFFFFFFFu, start, 31);
     prev_e = __shfl_sync(0xFFFFFFFFu, e, 31);
@@ -121,6 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
   const uint32_t sSFA = sA + kStages * kBox;    // route scale atoms
   const uint32_t sSFB = sSFA + kStages * kSfa;  // weight scale atoms (both halves)
   int* starts = reinterpret_cast<int*>(dsmem + (sSFB + kStages * kSfb - smem_u32(dsmem)));
+  int* experts = starts + kMaxPairs;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -140,7 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
   pdl_wait();
   const int ntiles = min(max(__ldcg(p.totals), 0), p.max_tiles);
   if (warp == 2) {
-    const int n = build_pair_starts(p.tile_expert, ntiles, starts, lane);
+    const int n = build_pair_starts(p.tile_expert, ntiles, starts, experts, lane);
     if (lane == 0) npairs_s = n;
   }
   if (warp == 1) {
@@ -163,13 +176,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
   // An expert id outside [0, E) (a corrupt routing table) reads as expert 0
   // for the loads, so that every address stays in range and every role
   // still walks the same stages, and the unit's results are not stored.
-  auto unit_tiles = [&](int u, int& w, int& e, int& mine, bool& bad) {
+  auto unit_tiles = [&](int u, int& w, int& e, int& mine, int& peer, bool& bad) {
     const int pi = u / tw;
     w = u - pi * tw;
-    const int t0 = starts[pi];
-    e = __ldcg(p.tile_expert + t0);
-    const int t1 = (t0 + 1 < ntiles && __ldcg(p.tile_expert + t0 + 1) == e) ? t0 + 1 : -1;
-    mine = rank == 0 ? t0 : t1;
+    const int v = starts[pi];
+    const int t0 = v & (kHasPeer - 1);
+    peer = (v & kHasPeer) ? t0 + 1 : -1;  // rank 1's tile
+    e = experts[pi];
+    mine = rank == 0 ? t0 : peer;
     bad = e < 0 || e >= p.num_experts;
     if (bad) e = 0;
   };
@@ -183,17 +197,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
       bool stop = false;
       const int wrows_per_e = p.rows_w / 128;  // 128-row weight tiles per expert
       for (int u = cl; u < n_units && !stop; u += ncl) {
-        int w, e, mine;
+        int w, e, mine, peer;
         bool bad;
-        unit_tiles(u, w, e, mine, bad);
+        unit_tiles(u, w, e, mine, peer, bad);
         if (bad && rank == 0) record_status(p.status, MOE_ERR_INVALID_ROUTE);
         // rank 0 expects both halves' bytes; rank 1's route half is absent
         // when its tile is (an odd last tile of the expert)
-        int peer = -1;
-        if (rank == 0) {
-          const int t0 = starts[u / tw];
-          peer = (t0 + 1 < ntiles && __ldcg(p.tile_expert + t0 + 1) == __ldcg(p.tile_expert + t0)) ? t0 + 1 : -1;
-        }
         const int wrow = e * p.rows_w + 256 * w + 128 * (int)rank;
         // atom rows (128 bytes, 4 per atom) of the two weight halves and of the route tile, at K step 0
         const int wsf_row0 = ((e * wrows_per_e + 2 * w) * KC) * 4, wsf_row1 = wsf_row0 + KC * 4;
@@ -292,9 +301,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
       const bool ok = mbar_wait_warp(smem_u32(&accf_bar), uc & 1, &abort_flag, p.status);
       if (!ok) break;
       tc_fence_after();
-      int w, e, mine;
+      int w, e, mine, peer;
       bool bad;
-      unit_tiles(u, w, e, mine, bad);
+      unit_tiles(u, w, e, mine, peer, bad);
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
       uint32_t acc[4][32];
 #pragma unroll
