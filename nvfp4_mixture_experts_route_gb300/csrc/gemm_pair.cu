@@ -270,14 +270,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::kThreads, 1)
           tc_fence_after();
           const uint32_t fa = t_sfa + s * 16, fbc = t_sfb + s * 32;
           const uint64_t sad = sfa_desc0 + ((s * kSfa) >> 4), sbd = sfb_desc0 + ((s * kSfb) >> 4);
-  #pragma unroll
+#pragma unroll
           for (int j = 0; j < 4; ++j) {
             pair_copy_atom(fa + 4 * j, sad + j * (kAtomBytes >> 4));
             pair_copy_atom(fbc + 8 * j, sbd + j * (kAtomBytes >> 4));
             pair_copy_atom(fbc + 8 * j + 4, sbd + (4 + j) * (kAtomBytes >> 4));
           }
           const uint64_t ad = a_desc0 + ((s * kBox) >> 4), wd = w_desc0 + ((s * kBox) >> 4);
-  #pragma unroll
+#pragma unroll
           for (int j = 0; j < 4; ++j)  // A = route rows, B = weight rows; 32 bytes (K = 64) per step
             pair_mma(tmem, ad + ((32 * j) >> 4), wd + ((32 * j) >> 4), idesc, fa + 4 * j, fbc + 8 * j,
                      (ks | j) != 0);
