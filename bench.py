@@ -55,10 +55,10 @@ FP4_PER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate
 # gemm_pair.cu, common.cuh, layout.cuh in that order): once those change,
 # traffic is null.
 NCU_TRAFFIC = {
-    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_349_376 + 5_096_448,
-                  "sources": "f63d411526d9fdad91fde209e35d04143fc5af3f42f8356f73afe317afa7e77c"},
-    "prefill_t8192_zipf": {"kernel": "gemm1_pair_kernel", "bytes": 1_722_235_904 + 83_933_184,
-                           "sources": "f63d411526d9fdad91fde209e35d04143fc5af3f42f8356f73afe317afa7e77c"},
+    "decode_b8": {"kernel": "grouped_gemm_kernel<3, 32>", "bytes": 945_302_272 + 5_205_760,
+                  "sources": "8d1187bbfbdb9ebbff0bb9ff741af60e593d16feae5b5d7864421a978982a952"},
+    "prefill_t8192_zipf": {"kernel": "gemm1_pair_kernel", "bytes": 1_722_032_896 + 84_068_352,
+                           "sources": "8d1187bbfbdb9ebbff0bb9ff741af60e593d16feae5b5d7864421a978982a952"},
 }
 
 
