@@ -157,6 +157,11 @@ def _quant_case(T, H, E, K, tile, g, seed=0, scale=1.0):
     (300, 512, 8, 8, 256, 2.0, 1.0),          # two scale atoms per tile
     (256, 5120, 16, 8, 128, 3.0, 1.0),        # full row width: ten 32-block chunks per token
     (16, 256, 4, 2, 128, 1e-3, 1e-5),         # scales in the e4m3 subnormals / zero
+    # prefill-sized batches: many tokens per route tile, a ragged last chunk,
+    # K < 8, the decode tile size, subnormal scales
+    (1100, 5120, 128, 8, 128, 618.8201293945312, 1.0),
+    (1030, 1152, 16, 3, 32, 3.0, 100.0),
+    (2048, 256, 8, 8, 256, 1e-3, 1e-5),
 ])
 def test_quantize_permute_bit_exact(T, H, E, K, tile, g, scale):
     x, r, codes, scales, _ = _quant_case(T, H, E, K, tile, g, scale=scale)
