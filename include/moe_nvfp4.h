@@ -180,7 +180,9 @@ typedef struct moe_route {
   const int32_t* totals;               /* [2] */
   const int32_t* expanded_to_permuted; /* [T, K]; read by the input quantizer, which
                                           quantizes each token once and writes it to
-                                          the rows of its routes */
+                                          the rows of its routes; an entry outside
+                                          [-1, max_padded_rows) is skipped and
+                                          recorded as MOE_ERR_INVALID_ROUTE in status */
 } moe_route;
 
 /* Kernels moe_nvfp4_experts enqueues for this route-tile size: 2 (the

@@ -16,7 +16,7 @@ size_t route_smem_bytes(int E);
 int route_kernel_count(int T, int K, int E);
 cudaError_t launch_quantize_permute(const void*, const void*, const void*, const float*,
                                     const int32_t*, const int32_t*, const int32_t*, int, int, int,
-                                    int, int, int, uint8_t*, uint8_t*, int32_t*, cudaStream_t);
+                                    int, int, int, uint8_t*, uint8_t*, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_act_scales_io(int, uint8_t*, uint8_t*, int, int, int, cudaStream_t);
 bool route_quantize_fits(int T, int K, int E);
 cudaError_t launch_route_quantize(const int32_t*, int, int, int, int, int, int, int32_t*, int32_t*, int32_t*,
@@ -279,7 +279,6 @@ int moe_experts_workspace_size(int T, int K, int E, int H, int I, int tile_m, si
 int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const float* a1_gscale,
                          const moe_route* r, int T, int H, int I, int E, int K, int tile_m,
                          void* ws, size_t ws_bytes, int32_t* status, void* stream) {
-  (void)status;
   WsLayout L;
   int rc = ws_layout(T, K, E, H, I, tile_m, &L);
   if (rc) return rc;
@@ -298,7 +297,7 @@ int moe_experts_quantize(const void* x, const void* a, const void* a_sf, const f
   cudaError_t err = moe::launch_quantize_permute(
       x, x ? nullptr : a, x ? nullptr : a_sf, a1_gscale, r->expanded_to_permuted, r->tile_row_limit,
       r->totals, T, K, H, tile_m, L.P, L.MT + kDoneExtra, base + L.a_codes, base + L.a_sf,
-      reinterpret_cast<int32_t*>(base + L.done), as_stream(stream));
+      reinterpret_cast<int32_t*>(base + L.done), status, as_stream(stream));
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_quantize");
 }
 

@@ -43,10 +43,13 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
   }
 }
 
-// Token work item (a warp, token t, chunk j): lane l quantizes block
-// b = 32 j + l of the token once and writes its 8 code bytes to the row of
-// each of the token's routes; the first lane of each quad writes the quad's
-// 4 scale bytes (blocks 4m..4m+3, contiguous in the scale atom). Lanes k and
+// Token work item (a warp, token t, chunk j): lane l quantizes the BPL
+// adjacent blocks from b = 32 BPL j + BPL l of the token once and writes
+// their 8 BPL code bytes to the row of each of the token's routes with one
+// store; the first lane of each 4-block group writes the group's 4 scale
+// bytes (contiguous in the scale atom). Two blocks per lane (the standalone
+// kernel) halve the per-route lookups, address arithmetic and store
+// instructions per byte, which bound it at one block per lane. Lanes k and
 // k + 32 of the item first look up route k's permuted row (expanded_to_
 // permuted) and the offset of that row's scale bytes for block 0, so the
 // per-block work is a shuffle and the stores. Padding work item (a warp,
@@ -56,14 +59,17 @@ __device__ __forceinline__ void quantize_block16(const float (&v)[16], float g, 
 // every product, so padding-row codes are never written. The padding items
 // come first, then the token items. Reads x once; writes each route row once.
 //
+// A route row outside [-1, P) is skipped and recorded in *status as
+// MOE_ERR_INVALID_ROUTE (by the token's first chunk item).
 // e2p and tile_row_limit may point to global or shared memory (the fused
 // routing + quantization kernel keeps its own copy of the routing there);
 // n_tiles is the number of route tiles in use.
+template <int BPL>
 __device__ __forceinline__ void quantize_permute_items(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale, const int32_t* e2p,
-    const int32_t* tile_row_limit, int n_tiles, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done) {
+    const int32_t* tile_row_limit, int n_tiles, int T, int K, int H, int tile_m, int P, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done, int32_t* status) {
   // the per-tile GEMM1 completion counters and the unit ticket of the
   // one-launch expert GEMMs that follow
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_done; i += gridDim.x * blockDim.x) done[i] = 0;
@@ -87,10 +93,12 @@ __device__ __forceinline__ void quantize_permute_items(
       }
     }
   }
-  // Tokens: one warp per (token, chunk of 32 blocks). nb is a multiple of 8,
-  // so a quad's four lanes are all in range or all out of it.
-  const int nchunks = (nb + 31) / 32;
+  // Tokens: one warp per (token, chunk of 32 BPL blocks), lane l taking the
+  // BPL adjacent blocks b0 = 32 BPL j + BPL l, ... . nb is a multiple of 8,
+  // so a lane's blocks, and a quad's lanes, are all in range or all out of it.
+  const int nchunks = (nb + 32 * BPL - 1) / (32 * BPL);
   constexpr unsigned kFull = 0xFFFFFFFFu;
+  constexpr int kQuadLanes = 4 / BPL;  // lanes holding one 4-block group
   const size_t group_step = (size_t)S * kAtomBytes;  // scale bytes between consecutive 4-block groups
   for (int w = warp0; w < T * nchunks; w += nwarps) {
     const int t = w / nchunks, j = w - t * nchunks;
@@ -99,48 +107,76 @@ __device__ __forceinline__ void quantize_permute_items(
     size_t s_lo = 0, s_hi = 0;
     if (lane < K) {
       p_lo = e2p[(size_t)t * K + lane];
+      if (p_lo < -1 || p_lo >= P) {
+        if (j == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
+        p_lo = -1;
+      }
       if (p_lo >= 0) s_lo = act_sf_offset(p_lo, 0, tile_m, ng, S);
     }
     if (lane + 32 < K) {
       p_hi = e2p[(size_t)t * K + lane + 32];
+      if (p_hi < -1 || p_hi >= P) {
+        if (j == 0) record_status(status, MOE_ERR_INVALID_ROUTE);
+        p_hi = -1;
+      }
       if (p_hi >= 0) s_hi = act_sf_offset(p_hi, 0, tile_m, ng, S);
     }
-    const int b = 32 * j + lane;
-    const bool on = b < nb;  // every lane stays for the warp-wide shuffles
-    uint2 q = make_uint2(0u, 0u);
-    uint32_t sfc = 0;
-    if (on && x != nullptr) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 16 * b);
-      const uint4 u0 = src[0], u1 = src[1];
-      const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
-      const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
-      float v[16];
+    const int b0 = 32 * BPL * j + BPL * lane;
+    const bool on = b0 < nb;  // every lane stays for the warp-wide shuffles
+    uint32_t q[2 * BPL];      // the lane's code words, block i in q[2i], q[2i+1]
+    uint32_t sf_mine = 0;     // its scale bytes, block i in byte i
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f0 = __bfloat1622float2(h0[i]);
-        const float2 f1 = __bfloat1622float2(h1[i]);
-        v[2 * i] = f0.x;
-        v[2 * i + 1] = f0.y;
-        v[8 + 2 * i] = f1.x;
-        v[8 + 2 * i + 1] = f1.y;
+    for (int i = 0; i < 2 * BPL; ++i) q[i] = 0u;
+    if (on && x != nullptr) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + 16 * b0);
+      uint4 u[2 * BPL];
+#pragma unroll
+      for (int i = 0; i < 2 * BPL; ++i) u[i] = src[i];
+#pragma unroll
+      for (int i = 0; i < BPL; ++i) {
+        const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u[2 * i]);
+        const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u[2 * i + 1]);
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f0 = __bfloat1622float2(h0[e]);
+          const float2 f1 = __bfloat1622float2(h1[e]);
+          v[2 * e] = f0.x;
+          v[2 * e + 1] = f0.y;
+          v[8 + 2 * e] = f1.x;
+          v[8 + 2 * e + 1] = f1.y;
+        }
+        uint32_t sfc;
+        quantize_block16(v, g, q[2 * i], q[2 * i + 1], sfc);
+        sf_mine |= sfc << (8 * i);
       }
-      quantize_block16(v, g, q.x, q.y, sfc);
     } else if (on) {
-      q = *reinterpret_cast<const uint2*>(a_in + (size_t)t * (H / 2) + 8 * b);
-      sfc = a_sf_in[(size_t)t * nb + b];
+#pragma unroll
+      for (int i = 0; i < BPL; ++i) {
+        const uint2 c = *reinterpret_cast<const uint2*>(a_in + (size_t)t * (H / 2) + 8 * (b0 + i));
+        q[2 * i] = c.x;
+        q[2 * i + 1] = c.y;
+        sf_mine |= (uint32_t)a_sf_in[(size_t)t * nb + b0 + i] << (8 * i);
+      }
     }
-    // the quad's four scale bytes, block 4 * (b / 4) in the low byte
-    const int base = lane & ~3;
-    const uint32_t sf4 = __shfl_sync(kFull, sfc, base) | (__shfl_sync(kFull, sfc, base + 1) << 8) |
-                         (__shfl_sync(kFull, sfc, base + 2) << 16) | (__shfl_sync(kFull, sfc, base + 3) << 24);
-    const size_t sf_b = (size_t)(b >> 2) * group_step;
+    // the quad's four scale bytes, block 4 * (b0 / 4) in the low byte
+    const int base = lane & ~(kQuadLanes - 1);
+    uint32_t sf4 = 0;
+#pragma unroll
+    for (int r = 0; r < kQuadLanes; ++r) sf4 |= __shfl_sync(kFull, sf_mine, base + r) << (8 * BPL * r);
+    const size_t sf_b = (size_t)(b0 >> 2) * group_step;
+    const bool quad_first = (lane & (kQuadLanes - 1)) == 0;
     for (int k = 0; k < K; ++k) {
       const int p = __shfl_sync(kFull, k < 32 ? p_lo : p_hi, k & 31);
       if (p < 0) continue;  // the same p in every lane
       const size_t so = __shfl_sync(kFull, k < 32 ? s_lo : s_hi, k & 31);
       if (on) {
-        *reinterpret_cast<uint2*>(codes + (size_t)p * (H / 2) + 8 * b) = q;
-        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(scales + so + sf_b) = sf4;
+        uint8_t* dst = codes + (size_t)p * (H / 2) + 8 * b0;
+        if constexpr (BPL == 2)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+        else
+          *reinterpret_cast<uint2*>(dst) = make_uint2(q[0], q[1]);
+        if (quad_first) *reinterpret_cast<uint32_t*>(scales + so + sf_b) = sf4;
       }
     }
   }
@@ -150,12 +186,12 @@ __global__ void __launch_bounds__(256) quantize_permute_kernel(
     const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ a_in,
     const uint8_t* __restrict__ a_sf_in, const float* __restrict__ gscale,
     const int32_t* __restrict__ e2p, const int32_t* __restrict__ tile_row_limit,
-    const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done) {
+    const int32_t* __restrict__ totals, int T, int K, int H, int tile_m, int P, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, int32_t* __restrict__ done, int n_done, int32_t* status) {
   pdl_wait();
   pdl_trigger();
-  quantize_permute_items(x, a_in, a_sf_in, gscale, e2p, tile_row_limit, totals[0], T, K, H, tile_m, codes, scales,
-                         done, n_done);
+  quantize_permute_items<2>(x, a_in, a_sf_in, gscale, e2p, tile_row_limit, totals[0], T, K, H, tile_m, P, codes,
+                            scales, done, n_done, status);
 }
 
 // Steps a2 and a1 in one kernel, for few routes (T*K <= kFusedMaxRoutes,
@@ -189,8 +225,8 @@ __global__ void __launch_bounds__(256) route_quantize_kernel(
   // push CTA 0's copy out before this grid lets them launch.
   if (writer) __threadfence();
   pdl_trigger();
-  quantize_permute_items(x, a_in, a_sf_in, gscale, e2p_s, limit_s, totals_s[0], T, K, H, tile_m, codes, scales, done,
-                         MT + 1);
+  quantize_permute_items<1>(x, a_in, a_sf_in, gscale, e2p_s, limit_s, totals_s[0], T, K, H, tile_m, P, codes,
+                            scales, done, MT + 1, status);
 }
 
 // Scale atoms <-> row-major scales [rows, K/16].
@@ -220,19 +256,18 @@ cudaError_t launch_quantize_permute(const void* x, const void* a, const void* a_
                                     const float* a1_gscale, const int32_t* e2p,
                                     const int32_t* tile_row_limit, const int32_t* totals, int T,
                                     int K, int H, int tile_m, int P, int n_done, uint8_t* codes,
-                                    uint8_t* scales, int32_t* done, cudaStream_t stream) {
-  (void)P;
+                                    uint8_t* scales, int32_t* done, int32_t* status, cudaStream_t stream) {
   // per route tile a GEMM1 counter, then the unit ticket
   const int MT = n_done - 1;
   // enough warps for one padding item each (one global read then one store
   // per lane), and one warp per token item
   const long long pad_threads = (long long)MT * (H / 64) * 32,
-                  tok_threads = (long long)T * ((H / 16 + 31) / 32) * 32;
+                  tok_threads = (long long)T * ((H / 16 + 63) / 64) * 32;
   const int grid = grid_for(pad_threads > tok_threads ? pad_threads : tok_threads, 256);
   return launch_kernel(quantize_permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const uint8_t*>(a),
                        reinterpret_cast<const uint8_t*>(a_sf), a1_gscale, e2p, tile_row_limit, totals,
-                       T, K, H, tile_m, codes, scales, done, n_done);
+                       T, K, H, tile_m, P, codes, scales, done, n_done, status);
 }
 
 size_t route_quantize_smem(int T, int K, int E, int MT) {

@@ -1,5 +1,7 @@
 """GPU parity of the routing, input-quantization, weight-preparation and
 finalize kernels against the CPU oracle, through the C ABI."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -174,6 +176,34 @@ def test_quantize_permute_bit_exact(T, H, E, K, tile, g, scale):
     assert np.array_equal(scales[live], want_sf[p2t[live]])
     assert np.array_equal(canon_packed(codes[live]), canon_packed(want_packed[p2t[live]]))
     assert not scales[pad].any()  # padding rows: zero scales (their codes are not written)
+
+
+@pytest.mark.parametrize("T", [300, 1100])  # warps per token chunk; staged rows (1024 tokens and more)
+def test_quantize_skips_route_rows_out_of_range(T):
+    H, E, K, tile, g = 1024, 16, 4, 64, 3.0
+    x, r, codes0, scales0, ws = _quant_case(T, H, E, K, tile, g)
+    P, _ = B.route_sizes(T, K, E, tile)
+    e2p = r.expanded_to_permuted.clone()
+    bad = [(5, 1, P), (T - 1, 3, P + 1000), (T // 2, 0, -7)]
+    victims = [int(e2p[t, k].item()) for t, k, _ in bad]
+    for t, k, v in bad:
+        e2p[t, k] = v
+    ws.fill_(0x5A)  # rows that are never written keep this byte
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.experts_quantize(dataclasses.replace(r, expanded_to_permuted=e2p), ws, x=bf16_dev(x),
+                       a1_gscale=torch.tensor([g], dtype=torch.float32, device=DEV), T=T, H=H, I=128, E=E, K=K,
+                       status=status)
+    codes, scales = B.experts_export(0, ws, T=T, H=H, I=128, E=E, K=K, tile_m=tile)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    codes, scales = codes.cpu().numpy(), scales.cpu().numpy()
+    p2t = r.permuted_to_token.cpu().numpy()
+    total = int(r.totals[1].item())
+    live = np.setdiff1d(np.nonzero(p2t[:total] >= 0)[0], victims)
+    assert np.array_equal(codes[live], codes0[live]) and np.array_equal(scales[live], scales0[live])
+    assert (codes[victims] == 0x5A).all() and (scales[victims] == 0x5A).all()
+    pad = np.nonzero(p2t[:total] < 0)[0]
+    assert not scales[pad].any()
 
 
 @pytest.mark.parametrize("T", [12, 260])
