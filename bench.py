@@ -429,13 +429,15 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         torch.cuda.synchronize()
         fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
 
-    # e2e: the public serving call NvFp4MoE.replay_host: one CUDA graph per
-    # step whose inputs are the layer's pinned host buffer (x, topk_ids and
-    # topk_weights, laid out by input_layout) and whose output lands in
-    # pinned host memory. At decode sizes it is zero-copy (the step's kernels
-    # read the inputs and the finalize writes the output over the host link
-    # themselves); otherwise one copy in, routing, expert body and finalize,
-    # one copy out. Either way the transfers are inside the timed region.
+    # e2e: the public pipelined serving call from pinned host memory,
+    # NvFp4MoE.submit_host on alternating slots (inputs x, topk_ids and
+    # topk_weights laid out by input_layout, output in pinned host memory):
+    # per step one copy in, the step's graph (routing, expert body, finalize)
+    # and one copy out, on three streams ordered by events, so a step's copies
+    # overlap its neighbours' kernels; every step's transfers are inside the
+    # timed region. (Measured against the zero-copy NvFp4MoE.replay_host,
+    # whose kernels read and write the pinned buffers themselves: equal at
+    # b=8, 2 % slower at b=64, far slower at prefill sizes, where it copies.)
     # One weight copy: a step streams the touched experts' weights (far
     # larger than L2) from HBM anyway. --no-graph times the eager public call
     # (NvFp4MoE.forward) with two copies around it.
@@ -449,23 +451,35 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
     in_h[offs["topk_weights"]:offs["topk_weights"] + T * K * 4].copy_(
         torch.from_numpy(batch["topk_weights"].view(np.uint8).reshape(-1)))
     gb = moe.graph_buffers(T, K)
+    pipelined = args.graph
+    if pipelined:
+        for slot in moe.host_pipeline(T, K)["slots"]:
+            slot["host_inputs"].copy_(in_h)
 
     def e2e_step(i):
-        if args.graph:
-            moe.replay_host(T, K)
+        if pipelined:
+            moe.submit_host(T, K, i % 2)
         else:
             gb["inputs"].copy_(in_h, non_blocking=True)
             out_h.copy_(moe.forward(gb["x"], gb["topk_ids"], gb["topk_weights"])[0], non_blocking=True)
 
+    if pipelined:
+        moe.pipeline_begin(T, K)
     for i in range(args.warmup):
         e2e_step(i)
+    if pipelined:
+        moe.pipeline_join(T, K)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
+    if pipelined:
+        moe.pipeline_begin(T, K)
     for i in range(args.steps):
         e2e_step(i)
+    if pipelined:
+        moe.pipeline_join(T, K)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
@@ -534,8 +548,8 @@ def measure_workload(args, w, layer: Layer, world, rank, dev, fp4_peak) -> dict:
         "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": in_h.numel(),
                 "d2h_bytes_per_step": out_h.numel() * 2,
-                "transfer": ("zero-copy: the kernels read the pinned inputs and write the pinned output"
-                             if args.graph and moe.zero_copy(T, K) else "one copy in, one copy out")},
+                "transfer": ("pipelined: per step one copy in and one copy out, on their own streams beside "
+                             "the step's graph, two slots" if pipelined else "one copy in, one copy out")},
         "gpu_launches": launches_per_step * args.steps,
     }
     if tensor_bound:

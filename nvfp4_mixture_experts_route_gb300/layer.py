@@ -205,3 +205,92 @@ class NvFp4MoE:
             g["graph"] = graph
         g["graph"].replay()
         return g["out"]
+
+    # -- pipelined serving from pinned host memory --------------------------
+    def host_pipeline(self, T: int, K: int, depth: int = 2) -> dict:
+        """Slots of the pipelined serving call for (T, K): ``depth`` sets of
+        pinned ``host_inputs`` (bytes laid out by ``input_layout``) and
+        ``host_out`` bf16 [T, H], each with its own device buffers and step
+        graph, and three streams (copy in, step, copy out)."""
+        key = ("pipe", T, K, depth)
+        if key not in self._buffers:
+            offs, nbytes = self.input_layout(T, K)
+            dev = self.device
+            slots = []
+            for _ in range(depth):
+                flat = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+                s = {
+                    "host_inputs": torch.zeros(nbytes, dtype=torch.uint8).pin_memory(),
+                    "host_out": torch.empty((T, self.H), dtype=torch.bfloat16).pin_memory(),
+                    "inputs": flat,
+                    "x": flat[offs["x"]:offs["x"] + T * self.H * 2].view(torch.bfloat16).view(T, self.H),
+                    "topk_ids": flat[offs["topk_ids"]:offs["topk_ids"] + T * K * 4].view(torch.int32).view(T, K),
+                    "topk_weights": flat[offs["topk_weights"]:offs["topk_weights"] + T * K * 4]
+                    .view(torch.float32).view(T, K),
+                    "out": torch.empty((T, self.H), dtype=torch.bfloat16, device=dev),
+                    "graph": None,
+                    "used": False,
+                    "in_ready": torch.cuda.Event(),
+                    "computed": torch.cuda.Event(),
+                    "out_ready": torch.cuda.Event(),
+                }
+                s["topk_ids"].fill_(-1)
+                slots.append(s)
+            self._buffers[key] = {"slots": slots, "copy_in": torch.cuda.Stream(dev),
+                                  "step": torch.cuda.Stream(dev), "copy_out": torch.cuda.Stream(dev)}
+        return self._buffers[key]
+
+    def pipeline_begin(self, T: int, K: int, depth: int = 2) -> None:
+        """Order the pipeline's streams after the work already on the current
+        stream (call once before a run of ``submit_host``)."""
+        p = self.host_pipeline(T, K, depth)
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream(self.device))
+        for st in (p["copy_in"], p["step"], p["copy_out"]):
+            st.wait_event(ev)
+
+    def submit_host(self, T: int, K: int, slot: int, depth: int = 2) -> torch.cuda.Event:
+        """Enqueue one serving step on slot ``slot`` of ``host_pipeline``: the
+        copy of its ``host_inputs`` to the device, the step (one graph replay:
+        routing, expert body, finalize), and the copy of its output to
+        ``host_out``, each on its own stream, ordered by events. Consecutive
+        steps on alternating slots overlap one step's copies with the
+        neighbouring steps' kernels. Returns the event after which ``host_out``
+        of this slot holds the result. Fill ``host_inputs`` before the call,
+        and wait for the slot's previous event before refilling it or reading
+        its ``host_out``."""
+        p = self.host_pipeline(T, K, depth)
+        s = p["slots"][slot]
+        cin, stp, cout = p["copy_in"], p["step"], p["copy_out"]
+        if s["used"]:
+            cin.wait_event(s["computed"])  # the slot's device inputs were read by its last step
+        with torch.cuda.stream(cin):
+            s["inputs"].copy_(s["host_inputs"], non_blocking=True)
+            s["in_ready"].record(cin)
+        stp.wait_event(s["in_ready"])
+        if s["used"]:
+            stp.wait_event(s["out_ready"])  # the slot's device output was copied out
+        with torch.cuda.stream(stp):
+            if s["graph"] is None:
+                self.forward(s["x"], s["topk_ids"], s["topk_weights"], out=s["out"])  # warm-up, outside capture
+                stp.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    self.forward(s["x"], s["topk_ids"], s["topk_weights"], out=s["out"])
+                s["graph"] = graph
+            s["graph"].replay()
+            s["computed"].record(stp)
+        cout.wait_event(s["computed"])
+        with torch.cuda.stream(cout):
+            s["host_out"].copy_(s["out"], non_blocking=True)
+            s["out_ready"].record(cout)
+        s["used"] = True
+        return s["out_ready"]
+
+    def pipeline_join(self, T: int, K: int, depth: int = 2) -> None:
+        """Make the current stream wait for every step submitted so far."""
+        p = self.host_pipeline(T, K, depth)
+        cur = torch.cuda.current_stream(self.device)
+        for s in p["slots"]:
+            if s["used"]:
+                cur.wait_event(s["out_ready"])

@@ -966,6 +966,50 @@ def test_zero_copy_serving_step_matches_device_step():
         assert torch.equal(got, want)
 
 
+@pytest.mark.parametrize("T,tile", [(300, 128), (4, 32)])
+def test_pipelined_serving_call_matches_eager(T, tile):
+    """NvFp4MoE.submit_host on alternating slots (copy in, step graph and
+    copy out on three streams) gives each step the eager forward's output of
+    that step's batch bit for bit, with six different batches in flight two
+    at a time and every slot refilled only after its previous step's event."""
+    import dataclasses
+
+    from nvfp4_mixture_experts_route_gb300.layer import NvFp4MoE
+
+    w = dataclasses.replace(inputs.WORKLOADS["tiny_t4"], T=T, tile_m=tile)
+    raw = inputs.make_layer(w)
+    moe = NvFp4MoE(raw, 1.0, 1.0, raw["gamma"], tile_m=w.tile_m)
+    offs, _ = moe.input_layout(w.T, w.K)
+    slots = moe.host_pipeline(w.T, w.K)["slots"]
+    batches = [inputs.make_batch(w, seed=seed) for seed in range(6)]
+    want = []
+    for batch in batches:
+        x = bf16_dev(batch["x"])
+        ids = torch.from_numpy(batch["topk_ids"]).to("cuda")
+        tw = torch.from_numpy(batch["topk_weights"]).to("cuda")
+        want.append(moe.forward(x, ids, tw)[0].cpu())
+    got, events = [None] * len(batches), []
+    moe.pipeline_begin(w.T, w.K)
+    for i, batch in enumerate(batches):
+        slot = slots[i % 2]
+        if i >= 2:
+            events[i - 2].synchronize()
+            got[i - 2] = slot["host_out"].clone()
+        hi = slot["host_inputs"]
+        hi[offs["x"]:offs["x"] + w.T * w.H * 2].copy_(torch.from_numpy(batch["x"].view(np.uint8).reshape(-1)))
+        hi[offs["topk_ids"]:offs["topk_ids"] + w.T * w.K * 4].copy_(
+            torch.from_numpy(batch["topk_ids"].view(np.uint8).reshape(-1)))
+        hi[offs["topk_weights"]:offs["topk_weights"] + w.T * w.K * 4].copy_(
+            torch.from_numpy(batch["topk_weights"].view(np.uint8).reshape(-1)))
+        events.append(moe.submit_host(w.T, w.K, i % 2))
+    moe.pipeline_join(w.T, w.K)
+    torch.cuda.synchronize()
+    for i in (len(batches) - 2, len(batches) - 1):
+        got[i] = slots[i % 2]["host_out"].clone()
+    for i in range(len(batches)):
+        assert torch.equal(got[i], want[i]), i
+
+
 @pytest.mark.parametrize("name", ["decode_b8", "decode_b64_zipf", "prefill_t8192_zipf"])
 def test_timed_launch_path_matches_split_path(full, name):
     """The routed body then the plain finalize (for decode tiles the routing
@@ -1004,6 +1048,16 @@ def test_timed_launch_path_matches_split_path(full, name):
     host = moe.replay_host(w.T, w.K)
     torch.cuda.synchronize()
     assert np.array_equal(bf16_host_f64(host), split["out"])
+    # the pipelined serving call (bench.py's e2e form for larger steps)
+    for slot in moe.host_pipeline(w.T, w.K)["slots"]:
+        slot["host_inputs"].copy_(hb["host_inputs"])
+    moe.pipeline_begin(w.T, w.K)
+    for i in range(3):
+        moe.submit_host(w.T, w.K, i % 2)
+    moe.pipeline_join(w.T, w.K)
+    torch.cuda.synchronize()
+    for slot in moe.host_pipeline(w.T, w.K)["slots"]:
+        assert np.array_equal(bf16_host_f64(slot["host_out"]), split["out"])
     status, fused = _fused_rows(prep, batch, w.tile_m, a1, a2, calls=1)
     assert status == 0 and np.array_equal(fused[0], split["rows"])
     # The layer through the whole-block call (the norm's sums of squares
