@@ -302,6 +302,7 @@ def test_tp_slice_layout_identity_on_gpu():
     (1024, 8, 5120, 1.0, 1.0),
     (1500, 6, 2048, 0.5, 1e2),
     (1030, 8, 4096, 1.0, 1.0),
+    (1024, 40, 512, 1.0, 1.0),  # more than 32 routes per token
 ])
 @pytest.mark.parametrize("wbn", [True, False])
 def test_finalize_parity(T, K, H, gamma_sd, scale, wbn):

@@ -108,13 +108,14 @@ def test_norm_quantize_into_permuted_workspace_equals_gathered_linear(T, H, I, E
     assert not scales.cpu().numpy()[pad].any()
 
 
-@pytest.mark.parametrize("nparts,H,T", [(8, 5120, 6), (4, 256, 6), (1, 1024, 6),
-                                        # many tokens: the persistent kernel that streams every
-                                        # route's part rows through a shared-memory ring
-                                        (8, 5120, 1024), (3, 2048, 1100), (2, 4096, 1030)])
-def test_expert_tp_tail_finalize(nparts, H, T):
+@pytest.mark.parametrize("nparts,H,T,K", [(8, 5120, 6, 4), (4, 256, 6, 4), (1, 1024, 6, 4),
+                                          # many tokens: the persistent kernel that streams every
+                                          # route's part rows through a shared-memory ring
+                                          (8, 5120, 1024, 4), (3, 2048, 1100, 4), (2, 4096, 1030, 4),
+                                          # more than 32 routes per token
+                                          (2, 512, 1024, 36)])
+def test_expert_tp_tail_finalize(nparts, H, T, K):
     rng = np.random.default_rng(nparts * H + T)
-    K = 4
     P = T * K + 3
     parts = [inputs._to_bf16_bits(rng.standard_normal((P, H)) / np.sqrt(nparts)) for _ in range(nparts)]
     gamma = inputs._to_bf16_bits(rng.standard_normal(H) * 0.5)
