@@ -258,7 +258,10 @@ class NvFp4MoE:
         neighbouring steps' kernels. Returns the event after which ``host_out``
         of this slot holds the result. Fill ``host_inputs`` before the call,
         and wait for the slot's previous event before refilling it or reading
-        its ``host_out``."""
+        its ``host_out``. The steps share the layer's workspace for (T, K)
+        with ``forward``, ``replay`` and ``replay_host``: between
+        ``pipeline_begin`` and ``pipeline_join`` make no other call of this
+        layer for the same shape."""
         p = self.host_pipeline(T, K, depth)
         s = p["slots"][slot]
         cin, stp, cout = p["copy_in"], p["step"], p["copy_out"]
